@@ -1,0 +1,127 @@
+"""CPU oracle of the speculative-decoding verify step -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline / reference arm
+may import this package. The product path (the CUDA library and its binding) never does, and
+this package imports nothing from it.
+
+The arithmetic lives in ``spec_oracle.c`` (plain single-threaded C in double precision); this
+module only compiles it with gcc and marshals numpy arrays through ctypes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libspec_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32 = 0
+BF16 = 1
+
+# error codes of spec_oracle.c
+OK, ERR_ROW, ERR_TOKEN, ERR_PARENT, ERR_ARG, ERR_MEM = 0, -1, -2, -3, -4, -5
+
+
+def build(force: bool = False) -> str:
+    """Compile spec_oracle.c into libspec_oracle.so (no fast-math, no FMA contraction, so
+    the same doubles come out on x86-64 and aarch64)."""
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared",
+                               "-ffp-contract=off", "-fno-fast-math", "-Wall", "-Wextra",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i64, dbl, i32 = ctypes.c_void_p, ctypes.c_long, ctypes.c_double, ctypes.c_int
+            lib.oracle_probs.argtypes = [vp, i32, i64, i64, dbl, vp]
+            lib.oracle_argmax.argtypes = [vp, i32, i64, i64, vp]
+            lib.oracle_verify_chain.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, dbl, vp,
+                                                vp, vp]
+            lib.oracle_verify_tree.argtypes = [vp, i32, vp, vp, i64, i64, i64, vp, vp, vp]
+            for f in (lib.oracle_probs, lib.oracle_argmax, lib.oracle_verify_chain,
+                      lib.oracle_verify_tree):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+def _logits(a: np.ndarray, dtype: int) -> np.ndarray:
+    want = np.uint16 if dtype == BF16 else np.float32
+    if a.dtype != want:
+        raise TypeError(f"logits dtype {a.dtype} does not match dtype flag {dtype}")
+    return np.ascontiguousarray(a)
+
+
+def probs(logits: np.ndarray, dtype: int, temperature: float):
+    """[..., V] logits -> float64 probabilities (NaN rows for invalid rows), return code."""
+    lg = _logits(logits, dtype)
+    V = lg.shape[-1]
+    rows = lg.size // V
+    out = np.empty(lg.shape, dtype=np.float64)
+    rc = _load().oracle_probs(_ptr(lg), dtype, rows, V, float(temperature), _ptr(out))
+    return out, rc
+
+
+def argmax(logits: np.ndarray, dtype: int):
+    lg = _logits(logits, dtype)
+    V = lg.shape[-1]
+    rows = lg.size // V
+    out = np.empty(lg.shape[:-1], dtype=np.int32)
+    rc = _load().oracle_argmax(_ptr(lg), dtype, rows, V, _ptr(out))
+    return out, rc
+
+
+def verify_chain(target, draft, dtype, tokens, uniforms, temperature):
+    """Returns (accept_len [B], out_tokens [B, gamma+1], margin [B], rc)."""
+    tg = _logits(target, dtype)
+    B, g1, V = tg.shape
+    gamma = g1 - 1
+    if draft is None:
+        dr = None
+    else:
+        dr = _logits(draft, dtype)
+        assert dr.shape == (B, gamma, V)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, gamma)
+    uni = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, gamma + 1)
+    acc = np.empty(B, dtype=np.int32)
+    out = np.empty((B, gamma + 1), dtype=np.int32)
+    mg = np.empty(B, dtype=np.float64)
+    dptr = _ptr(dr) if dr is not None and dr.size else None
+    rc = _load().oracle_verify_chain(_ptr(tg), dptr, dtype, _ptr(tok), _ptr(uni), B, gamma, V,
+                                     float(temperature), _ptr(acc), _ptr(out), _ptr(mg))
+    return acc, out, mg, rc
+
+
+def verify_tree(target, dtype, parents, tokens):
+    """Returns (accept_len [B], path_nodes [B, N], out_tokens [B, N], rc)."""
+    tg = _logits(target, dtype)
+    B, N, V = tg.shape
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+    acc = np.empty(B, dtype=np.int32)
+    path = np.empty((B, N), dtype=np.int32)
+    out = np.empty((B, N), dtype=np.int32)
+    rc = _load().oracle_verify_tree(_ptr(tg), dtype, _ptr(par), _ptr(tok), B, N, V, _ptr(acc),
+                                    _ptr(path), _ptr(out))
+    return acc, path, out, rc

@@ -1,0 +1,349 @@
+/*
+ * spec_oracle.c -- CPU oracle of the speculative-decoding verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY. The tests, the smoke check and the benchmark's CPU-baseline leg
+ * load this file's library; the product path (the CUDA library and its Python binding) never
+ * does. It shares no code, header, table or constant with the CUDA library.
+ *
+ * Plain, slow, single-threaded C in double precision, written as the method reads, one step
+ * after another, so that it can be checked against the pages by eye:
+ *
+ *   "Fast Inference from Transformers via Speculative Decoding" (Leviathan, Kalman, Matias;
+ *   pith.science review, sections "The pith", "Core claim", "What carries the argument",
+ *   "Desk Editor's Note", "Referee Report: Significance", "Circularity Check") describes the
+ *   step: a draft model proposes gamma tokens, the target model scores all of them in one
+ *   parallel pass, the longest prefix that passes a rejection-sampling test on the target's
+ *   own probabilities is accepted, and a distribution-preserving correction makes the output
+ *   an exact sample of the target.
+ *
+ *   The precise rule (the standard one that makes that claim true, and the one this build
+ *   takes): p = softmax(target logits / T), q = softmax(draft logits / T); draft token x_i is
+ *   accepted while u_i <= p_i(x_i) / q_i(x_i); at the first rejection n the emitted token is
+ *   drawn from norm(max(0, p_n - q_n)); if all gamma drafts pass, one more token is drawn
+ *   from p_gamma.
+ *
+ *   "Falcon: Faster and Parallel Inference of Large Language Models through Enhanced
+ *   Semi-Autoregressive Drafting and Custom-Designed Decoding Tree" (pith.science review,
+ *   sections "What carries the argument", "Core claim", Figure 3 "SAR decoding tree
+ *   attention", Figure 4 "greedy (temperature=0)") verifies a tree of drafts in one pass
+ *   under greedy decoding: a node survives when its token equals the target's argmax at its
+ *   parent and its parent survives; the deepest surviving node's root path is accepted.
+ *
+ * Readings taken where the pages are silent (each is also listed in the design notes):
+ *   - accept on equality (u <= ratio); uniforms lie strictly in (0,1);
+ *   - q(x) = 0: ratio = +inf if p(x) > 0, else 0 (so a token neither model allows is rejected);
+ *   - inverse CDF: the first index whose inclusive running sum strictly exceeds u * S;
+ *   - a residual whose sum is exactly 0 falls back to p_n;
+ *   - T = 0: p and q are one-hot at the lowest-index argmax; the draft logits are not used
+ *     (x_i is accepted iff it equals the target argmax, the correction and the bonus token
+ *     are target argmaxes);
+ *   - a logits row is invalid if it holds NaN or +inf or has no finite entry (-inf entries,
+ *     i.e. masked tokens, are allowed); a draft token outside [0, V) is invalid; an invalid
+ *     batch row reports accept_len = -1 and all its out_tokens = -1;
+ *   - tree: parents[0] = -1 and 0 <= parents[i] < i; node 0 is the committed root; ties in
+ *     depth go to the smallest node index; the bonus token is the argmax at the deepest
+ *     accepted node.
+ *
+ * Margins: for every draw the oracle reports how close it was to a decision boundary, so
+ * tests can separate draws that any correct fp32 implementation must reproduce from the
+ * rare ones that rounding may legitimately flip:
+ *   decision margin  |u_i - ratio_i| / max(ratio_i, 1e-300)
+ *   CDF margin       min(c_k - t, t - c_{k-1}) / S at the chosen index k, t = u * S
+ * A batch row's margin is the minimum over its draws (+inf when it made none, e.g. T = 0).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+#define ORC_OK 0
+#define ORC_ERR_ROW (-1)    /* NaN / +inf / no finite logit in a row      */
+#define ORC_ERR_TOKEN (-2)  /* draft or node token outside [0, V)          */
+#define ORC_ERR_PARENT (-3) /* tree parent index not in [0, i), or root != -1 */
+#define ORC_ERR_ARG (-4)    /* bad sizes or temperature                    */
+#define ORC_ERR_MEM (-5)
+
+/* ------------------------------------------------------------------ logits access */
+
+/* Value of element idx of a logits tensor, as a double. bf16 is widened exactly: its 16 bits
+ * are the upper half of the fp32 with the same value. */
+static double logit_at(const void *base, int dtype, size_t idx) {
+  if (dtype == ORC_F32) return (double)((const float *)base)[idx];
+  uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* 1 if the row [off, off+V) has no NaN, no +inf and at least one finite value. */
+static int row_valid(const void *base, int dtype, size_t off, long V) {
+  int any_finite = 0;
+  for (long k = 0; k < V; ++k) {
+    double v = logit_at(base, dtype, off + (size_t)k);
+    if (isnan(v) || v == INFINITY) return 0;
+    if (isfinite(v)) any_finite = 1;
+  }
+  return any_finite;
+}
+
+/* Lowest index holding the row maximum. */
+static long argmax_row(const void *base, int dtype, size_t off, long V) {
+  long best = 0;
+  double bv = logit_at(base, dtype, off);
+  for (long k = 1; k < V; ++k) {
+    double v = logit_at(base, dtype, off + (size_t)k);
+    if (v > bv) { bv = v; best = k; }
+  }
+  return best;
+}
+
+/* Temperature softmax of one (valid) row: p[k] = exp((l[k]-m)/T) / sum_j exp((l[j]-m)/T),
+ * m = max_k l[k], sums in index order. T == 0: one-hot at the lowest-index argmax. */
+static void softmax_row(const void *base, int dtype, size_t off, long V, double T, double *p) {
+  if (T == 0.0) {
+    long g = argmax_row(base, dtype, off, V);
+    for (long k = 0; k < V; ++k) p[k] = 0.0;
+    p[g] = 1.0;
+    return;
+  }
+  double m = -INFINITY;
+  for (long k = 0; k < V; ++k) {
+    double v = logit_at(base, dtype, off + (size_t)k);
+    if (v > m) m = v;
+  }
+  double Z = 0.0;
+  for (long k = 0; k < V; ++k) {
+    p[k] = exp((logit_at(base, dtype, off + (size_t)k) - m) / T);
+    Z += p[k];
+  }
+  for (long k = 0; k < V; ++k) p[k] /= Z;
+}
+
+/* Inverse-CDF draw from the unnormalised weights r[0..V): the first k whose inclusive running
+ * sum c_k strictly exceeds t = u * S, S = sum r (index order). If rounding leaves no such k,
+ * the last k with r[k] > 0. Writes the CDF margin. */
+static long inverse_cdf(const double *r, long V, double u, double *margin) {
+  double S = 0.0;
+  for (long k = 0; k < V; ++k) S += r[k];
+  double t = u * S;
+  double c = 0.0;
+  for (long k = 0; k < V; ++k) {
+    double prev = c;
+    c += r[k];
+    if (c > t) {
+      double a = c - t, b = t - prev;
+      *margin = (a < b ? a : b) / S;
+      return k;
+    }
+  }
+  *margin = 0.0;
+  for (long k = V - 1; k >= 0; --k)
+    if (r[k] > 0.0) return k;
+  return V - 1;
+}
+
+/* ------------------------------------------------------------------ public: probabilities */
+
+/* out[rows, V] = temperature softmax of each logits row (one-hot at the argmax for T == 0).
+ * Invalid rows are filled with NaN. Returns 0, or ORC_ERR_ROW if any row was invalid. */
+int oracle_probs(const void *logits, int dtype, long rows, long V, double T, double *out) {
+  if (rows < 0 || V < 1 || !(T >= 0.0) || isinf(T)) return ORC_ERR_ARG;
+  int rc = ORC_OK;
+  for (long r = 0; r < rows; ++r) {
+    size_t off = (size_t)r * (size_t)V;
+    if (!row_valid(logits, dtype, off, V)) {
+      for (long k = 0; k < V; ++k) out[off + (size_t)k] = NAN;
+      rc = ORC_ERR_ROW;
+      continue;
+    }
+    softmax_row(logits, dtype, off, V, T, out + off);
+  }
+  return rc;
+}
+
+/* Lowest-index argmax of each row; -1 for an invalid row. */
+int oracle_argmax(const void *logits, int dtype, long rows, long V, int32_t *out) {
+  if (rows < 0 || V < 1) return ORC_ERR_ARG;
+  int rc = ORC_OK;
+  for (long r = 0; r < rows; ++r) {
+    size_t off = (size_t)r * (size_t)V;
+    if (!row_valid(logits, dtype, off, V)) { out[r] = -1; rc = ORC_ERR_ROW; continue; }
+    out[r] = (int32_t)argmax_row(logits, dtype, off, V);
+  }
+  return rc;
+}
+
+/* ------------------------------------------------------------------ public: chain verify */
+
+static void fail_row(int32_t *accept_len, int32_t *out_tokens, long b, long gamma) {
+  accept_len[b] = -1;
+  for (long j = 0; j <= gamma; ++j) out_tokens[b * (gamma + 1) + j] = -1;
+}
+
+/*
+ * Batched chain verify.
+ *   target   [B, gamma+1, V] logits of the target at positions 0..gamma
+ *   draft    [B, gamma, V]   logits of the draft at positions 0..gamma-1 (unused at T == 0)
+ *   tokens   [B, gamma]      draft tokens x_0..x_{gamma-1}
+ *   uniforms [B, gamma+1]    u_0..u_{gamma-1} acceptance tests, u_gamma the final draw
+ * Outputs: accept_len[B] = n (number of accepted drafts), out_tokens[B, gamma+1] =
+ * x_0..x_{n-1}, then the correction (n < gamma) or bonus (n == gamma) token, then -1;
+ * margin[B] (may be NULL). Returns 0 or the first error code met.
+ */
+int oracle_verify_chain(const void *target, const void *draft, int dtype, const int32_t *tokens,
+                        const float *uniforms, long B, long gamma, long V, double T,
+                        int32_t *accept_len, int32_t *out_tokens, double *margin) {
+  if (B < 0 || gamma < 0 || V < 1 || !(T >= 0.0) || isinf(T)) return ORC_ERR_ARG;
+  double *p = (double *)malloc(sizeof(double) * (size_t)V);
+  double *q = (double *)malloc(sizeof(double) * (size_t)V);
+  double *r = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!p || !q || !r) { free(p); free(q); free(r); return ORC_ERR_MEM; }
+  int rc = ORC_OK;
+  for (long b = 0; b < B; ++b) {
+    const size_t trow0 = (size_t)b * (size_t)(gamma + 1);
+    const size_t drow0 = (size_t)b * (size_t)gamma;
+    const int32_t *x = tokens + (size_t)b * (size_t)gamma;
+    const float *u = uniforms + (size_t)b * (size_t)(gamma + 1);
+    if (margin) margin[b] = INFINITY;
+
+    /* validate the whole batch row before any decision */
+    int err = ORC_OK;
+    for (long i = 0; i <= gamma && !err; ++i)
+      if (!row_valid(target, dtype, (trow0 + (size_t)i) * (size_t)V, V)) err = ORC_ERR_ROW;
+    if (T > 0.0)
+      for (long i = 0; i < gamma && !err; ++i)
+        if (!row_valid(draft, dtype, (drow0 + (size_t)i) * (size_t)V, V)) err = ORC_ERR_ROW;
+    for (long i = 0; i < gamma && !err; ++i)
+      if (x[i] < 0 || x[i] >= V) err = ORC_ERR_TOKEN;
+    if (err) {
+      fail_row(accept_len, out_tokens, b, gamma);
+      if (rc == ORC_OK) rc = err;
+      continue;
+    }
+
+    long n = gamma;
+    long token;
+    if (T == 0.0) {
+      /* greedy: accept x_i iff it is the target argmax at position i */
+      for (long i = 0; i < gamma; ++i) {
+        long g = argmax_row(target, dtype, (trow0 + (size_t)i) * (size_t)V, V);
+        if (x[i] != g) { n = i; break; }
+      }
+      token = argmax_row(target, dtype, (trow0 + (size_t)n) * (size_t)V, V);
+    } else {
+      double mg = INFINITY;
+      for (long i = 0; i < gamma; ++i) {
+        softmax_row(target, dtype, (trow0 + (size_t)i) * (size_t)V, V, T, p);
+        softmax_row(draft, dtype, (drow0 + (size_t)i) * (size_t)V, V, T, q);
+        double px = p[x[i]], qx = q[x[i]];
+        double ratio = (qx > 0.0) ? px / qx : (px > 0.0 ? INFINITY : 0.0);
+        double ui = (double)u[i];
+        if (isfinite(ratio)) {
+          double m = fabs(ui - ratio) / (ratio > 1e-300 ? ratio : 1e-300);
+          if (m < mg) mg = m;
+        }
+        if (ui > ratio) { n = i; break; } /* first rejection ends the step */
+      }
+      if (n < gamma) {
+        /* p and q still hold position n: residual max(0, p - q) */
+        double S = 0.0;
+        for (long k = 0; k < V; ++k) {
+          double d = p[k] - q[k];
+          r[k] = d > 0.0 ? d : 0.0;
+          S += r[k];
+        }
+        if (S == 0.0)
+          for (long k = 0; k < V; ++k) r[k] = p[k];
+      } else {
+        softmax_row(target, dtype, (trow0 + (size_t)gamma) * (size_t)V, V, T, r);
+      }
+      double cm;
+      token = inverse_cdf(r, V, (double)u[gamma], &cm);
+      if (cm < mg) mg = cm;
+      if (margin) margin[b] = mg;
+    }
+
+    accept_len[b] = (int32_t)n;
+    int32_t *o = out_tokens + (size_t)b * (size_t)(gamma + 1);
+    for (long j = 0; j < n; ++j) o[j] = x[j];
+    o[n] = (int32_t)token;
+    for (long j = n + 1; j <= gamma; ++j) o[j] = -1;
+  }
+  free(p); free(q); free(r);
+  return rc;
+}
+
+/* ------------------------------------------------------------------ public: tree verify */
+
+/*
+ * Batched greedy tree verify.
+ *   target   [B, N, V]  target logits at every node
+ *   parents  [B, N]     parents[b,0] = -1, 0 <= parents[b,i] < i
+ *   tokens   [B, N]     node tokens (node 0's is unused)
+ * A node is accepted iff it is the root, or its parent is accepted and its token equals the
+ * target argmax at its parent. d* = deepest accepted node (smallest index on ties).
+ * Outputs: accept_len[B] = depth(d*); path_nodes[B, N] = root..d*, then -1;
+ * out_tokens[B, N] = tokens of path nodes 1..depth, then argmax at d* (bonus), then -1.
+ */
+int oracle_verify_tree(const void *target, int dtype, const int32_t *parents,
+                       const int32_t *tokens, long B, long N, long V, int32_t *accept_len,
+                       int32_t *path_nodes, int32_t *out_tokens) {
+  if (B < 0 || N < 1 || V < 1) return ORC_ERR_ARG;
+  long *g = (long *)malloc(sizeof(long) * (size_t)N);
+  int *acc = (int *)malloc(sizeof(int) * (size_t)N);
+  long *depth = (long *)malloc(sizeof(long) * (size_t)N);
+  long *path = (long *)malloc(sizeof(long) * (size_t)N);
+  if (!g || !acc || !depth || !path) {
+    free(g); free(acc); free(depth); free(path);
+    return ORC_ERR_MEM;
+  }
+  int rc = ORC_OK;
+  for (long b = 0; b < B; ++b) {
+    const int32_t *par = parents + (size_t)b * (size_t)N;
+    const int32_t *tok = tokens + (size_t)b * (size_t)N;
+    int32_t *pn = path_nodes + (size_t)b * (size_t)N;
+    int32_t *ot = out_tokens + (size_t)b * (size_t)N;
+    for (long j = 0; j < N; ++j) { pn[j] = -1; ot[j] = -1; }
+
+    int err = ORC_OK;
+    if (par[0] != -1) err = ORC_ERR_PARENT;
+    for (long i = 1; i < N && !err; ++i)
+      if (par[i] < 0 || par[i] >= i) err = ORC_ERR_PARENT;
+    for (long i = 1; i < N && !err; ++i)
+      if (tok[i] < 0 || tok[i] >= V) err = ORC_ERR_TOKEN;
+    for (long j = 0; j < N && !err; ++j)
+      if (!row_valid(target, dtype, ((size_t)b * (size_t)N + (size_t)j) * (size_t)V, V))
+        err = ORC_ERR_ROW;
+    if (err) {
+      accept_len[b] = -1;
+      if (rc == ORC_OK) rc = err;
+      continue;
+    }
+
+    for (long j = 0; j < N; ++j)
+      g[j] = argmax_row(target, dtype, ((size_t)b * (size_t)N + (size_t)j) * (size_t)V, V);
+    acc[0] = 1;
+    depth[0] = 0;
+    for (long i = 1; i < N; ++i) {
+      long pa = par[i];
+      acc[i] = acc[pa] && (long)tok[i] == g[pa];
+      depth[i] = depth[pa] + 1;
+    }
+    long best = 0;
+    for (long i = 1; i < N; ++i)
+      if (acc[i] && depth[i] > depth[best]) best = i;
+
+    long D = depth[best];
+    long v = best;
+    for (long j = D; j >= 0; --j) { path[j] = v; v = (j > 0) ? par[v] : -1; }
+    for (long j = 0; j <= D; ++j) pn[j] = (int32_t)path[j];
+    for (long j = 0; j < D; ++j) ot[j] = tok[path[j + 1]];
+    ot[D] = (int32_t)g[best];
+    accept_len[b] = (int32_t)D;
+  }
+  free(g); free(acc); free(depth); free(path);
+  return rc;
+}
