@@ -48,7 +48,12 @@
  * tests can separate draws that any correct fp32 implementation must reproduce from the
  * rare ones that rounding may legitimately flip:
  *   decision margin  |u_i - ratio_i| / max(ratio_i, 1e-300)
- *   CDF margin       min(c_k - t, t - c_{k-1}) / S at the chosen index k, t = u * S
+ *   CDF margin       min(c_k - t, t - c_{k-1}) / P at the chosen index k, t = u * S, where P
+ *                    is the scale of the operands the CDF is built from: P = sum of p_n over
+ *                    the indices where r > 0 (for the bonus draw r = p_gamma, so P = S = 1).
+ *                    The residual r = max(0, p_n - q_n) is a difference of two unit-mass
+ *                    distributions; rounding in p and q moves its CDF by an amount that scales
+ *                    with P, not with the residual's own mass S, which can be far smaller.
  * A batch row's margin is the minimum over its draws (+inf when it made none, e.g. T = 0).
  */
 #include <math.h>
@@ -124,8 +129,8 @@ static void softmax_row(const void *base, int dtype, size_t off, long V, double 
 
 /* Inverse-CDF draw from the unnormalised weights r[0..V): the first k whose inclusive running
  * sum c_k strictly exceeds t = u * S, S = sum r (index order). If rounding leaves no such k,
- * the last k with r[k] > 0. Writes the CDF margin. */
-static long inverse_cdf(const double *r, long V, double u, double *margin) {
+ * the last k with r[k] > 0. Writes the CDF margin relative to `scale` (see Margins above). */
+static long inverse_cdf(const double *r, long V, double u, double scale, double *margin) {
   double S = 0.0;
   for (long k = 0; k < V; ++k) S += r[k];
   double t = u * S;
@@ -135,7 +140,7 @@ static long inverse_cdf(const double *r, long V, double u, double *margin) {
     c += r[k];
     if (c > t) {
       double a = c - t, b = t - prev;
-      *margin = (a < b ? a : b) / S;
+      *margin = (a < b ? a : b) / scale;
       return k;
     }
   }
@@ -247,21 +252,26 @@ int oracle_verify_chain(const void *target, const void *draft, int dtype, const 
         }
         if (ui > ratio) { n = i; break; } /* first rejection ends the step */
       }
+      double scale = 1.0;
       if (n < gamma) {
         /* p and q still hold position n: residual max(0, p - q) */
         double S = 0.0;
+        scale = 0.0;
         for (long k = 0; k < V; ++k) {
           double d = p[k] - q[k];
           r[k] = d > 0.0 ? d : 0.0;
           S += r[k];
+          if (r[k] > 0.0) scale += p[k];
         }
-        if (S == 0.0)
+        if (S == 0.0) {
           for (long k = 0; k < V; ++k) r[k] = p[k];
+          scale = 1.0;
+        }
       } else {
         softmax_row(target, dtype, (trow0 + (size_t)gamma) * (size_t)V, V, T, r);
       }
       double cm;
-      token = inverse_cdf(r, V, (double)u[gamma], &cm);
+      token = inverse_cdf(r, V, (double)u[gamma], scale, &cm);
       if (cm < mg) mg = cm;
       if (margin) margin[b] = mg;
     }
