@@ -1,0 +1,527 @@
+"""Benchmark of the verify step on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  chain verify  B=64, gamma=5, V=32000, bf16, T=1   (softmax statistics, acceptance ballot,
+                                                     correction/bonus draw, emit)
+  tree verify   B=32 trees of 64 nodes, V=32000, bf16, greedy (argmax, path, bonus)
+  probs         the chain's 384 target rows -> fp32 probabilities, T=1
+Metric: verified positions per second (chain positions B*(gamma+1) plus tree nodes B*N), and
+achieved HBM GB/s against the measured copy bandwidth.
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier and
+torch.cuda.synchronize() on both sides, CUDA events on the launching stream, max over ranks.
+Inputs rotate over 3 copies, so every buffer is reused only after more than 4x the L2 size of
+other traffic. Per-kernel durations come from event pairs around every 8th step's launches.
+`e2e` repeats the step through the same C entry points with inputs in pinned host memory:
+host-to-device copies of the step's inputs and device-to-host copies of all its outputs are
+inside the timed region.
+
+--impl reference times the CPU oracle (test infrastructure, single-threaded C, fp64) on a
+bounded row sample of the same workload each step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified positions/sec and achieved HBM GB/s (% of GB300 peak) on 1 GPU"
+UNIT = "positions/s"
+L2_BYTES = 129e6
+ROT = 3
+EVENT_EVERY = 8
+WORKLOAD = ("verify step: chain B=64 gamma=5 V=32000 bf16 T=1 + tree B=32 N=64 V=32000 bf16 "
+            "greedy + probs 384x32000 bf16->fp32 T=1")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed-offset", type=int, default=0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_init(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if _cuda_ok() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def _cuda_ok():
+    import torch
+    return torch.cuda.is_available()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device="cpu"):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world, device="cpu"):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ workload
+
+def make_inputs(seed_offset=0):
+    from workloads import chain_32k, tree_32k
+    ci = chain_32k(seed=2 + 100 * seed_offset)
+    ti = tree_32k(seed=4 + 100 * seed_offset)
+    return ci, ti
+
+
+def step_bytes(ci, ti):
+    """Algorithmic bytes of one step per kernel: every logit read once, small int/fp32 arrays
+    read or written once, the probabilities written once."""
+    B, g, V = ci.B, ci.gamma, ci.V
+    chain = (ci.target.nbytes + ci.draft.nbytes + ci.tokens.nbytes + ci.uniforms.nbytes
+             + 4 * B + 4 * B * (g + 1))
+    tree = ti.target.nbytes + ti.parents.nbytes + ti.tokens.nbytes + 4 * ti.B * (2 * ti.N + 1)
+    probs = ci.target.nbytes + 4 * ci.target.size
+    return {"chain": chain, "tree": tree, "probs": probs}
+
+
+def positions(ci, ti):
+    return ci.B * (ci.gamma + 1) + ti.B * ti.N
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_78_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """dram read+write bytes per launch of `kernel` from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return d["per_launch_bytes"].get(kernel)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        self.path = tempfile.mktemp(suffix=".csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Runner:
+    """Pre-marshalled C calls of one step on device buffers (copy `k` of each input)."""
+
+    def __init__(self, ci, ti, device):
+        import torch
+        import speculative_decoding_verification_78_gb300 as sv
+        from speculative_decoding_verification_78_gb300._binding import load_library
+        self.torch, self.sv = torch, sv
+        self.lib = load_library()
+        self.ci, self.ti = ci, ti
+        dev = device
+
+        def d(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+            return torch.from_numpy(a).to(dev)
+
+        self.d = d
+        self.copies = []
+        for _ in range(ROT):
+            self.copies.append(dict(ct=d(ci.target), cd=d(ci.draft), tt=d(ti.target)))
+        self.tok, self.uni = d(ci.tokens), d(ci.uniforms)
+        self.par, self.ttok = d(ti.parents), d(ti.tokens)
+        B, g, V = ci.B, ci.gamma, ci.V
+        self.acc = torch.empty(B, dtype=torch.int32, device=dev)
+        self.out = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+        self.tacc = torch.empty(ti.B, dtype=torch.int32, device=dev)
+        self.tpath = torch.empty((ti.B, ti.N), dtype=torch.int32, device=dev)
+        self.tout = torch.empty((ti.B, ti.N), dtype=torch.int32, device=dev)
+        self.probs = [torch.empty(ci.target.shape, dtype=torch.float32, device=dev)
+                      for _ in range(ROT)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws_c = sv.new_workspace(B, 2 * g + 1, V, sv.SPEC_BF16, dev)
+        self.ws_t = sv.new_workspace(ti.B, ti.N, ti.V, sv.SPEC_BF16, dev)
+        rows = B * (g + 1)
+        self.ws_p = sv.new_workspace(rows, 1, V, sv.SPEC_BF16, dev)
+        self.stream = torch.cuda.current_stream(dev)
+        vp = ctypes.c_void_p
+        sp = vp(self.stream.cuda_stream)
+        self.args = []
+        for k in range(ROT):
+            c = self.copies[k]
+            pk = self.copies[(k + 1) % ROT]["ct"]   # probs reads a copy not touched this step
+            chain = (vp(c["ct"].data_ptr()), vp(c["cd"].data_ptr()), sv.SPEC_BF16,
+                     vp(self.tok.data_ptr()), vp(self.uni.data_ptr()), B, g, V,
+                     ctypes.c_float(ci.temperature), vp(self.acc.data_ptr()),
+                     vp(self.out.data_ptr()), vp(self.status.data_ptr()),
+                     vp(self.ws_c.data_ptr()), self.ws_c.numel(), sp)
+            tree = (vp(c["tt"].data_ptr()), sv.SPEC_BF16, vp(self.par.data_ptr()),
+                    vp(self.ttok.data_ptr()), ti.B, ti.N, ti.V, vp(self.tacc.data_ptr()),
+                    vp(self.tpath.data_ptr()), vp(self.tout.data_ptr()),
+                    vp(self.status.data_ptr()), vp(self.ws_t.data_ptr()), self.ws_t.numel(), sp)
+            probs = (vp(pk.data_ptr()), sv.SPEC_BF16, rows, V, ctypes.c_float(1.0),
+                     vp(self.probs[k].data_ptr()), vp(self.status.data_ptr()),
+                     vp(self.ws_p.data_ptr()), self.ws_p.numel(), sp)
+            self.args.append((chain, tree, probs))
+
+    def step(self, i, evs=None):
+        chain, tree, probs = self.args[i % ROT]
+        lib = self.lib
+        if evs is None:
+            rc = lib.spec_verify_chain(*chain) | lib.spec_verify_tree(*tree) | \
+                lib.spec_probs(*probs)
+        else:
+            evs[0].record(self.stream)
+            rc = lib.spec_verify_chain(*chain)
+            evs[1].record(self.stream)
+            rc |= lib.spec_verify_tree(*tree)
+            evs[2].record(self.stream)
+            rc |= lib.spec_probs(*probs)
+            evs[3].record(self.stream)
+        if rc:
+            raise RuntimeError(f"verify call failed: {rc}")
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import oracle  # noqa: F401  (only for the cpu_baseline leg below)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    ci, ti = make_inputs(args.seed_offset + rank)
+    r = Runner(ci, ti, device)
+    for i in range(args.warmup):
+        r.step(i)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0, "device-side error in warm-up"
+
+    K = args.steps
+    nev = (K + EVENT_EVERY - 1) // EVENT_EVERY
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nev)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    host0 = time.perf_counter()
+    t0.record(r.stream)
+    for i in range(K):
+        r.step(i, evs[i // EVENT_EVERY] if i % EVENT_EVERY == 0 else None)
+    t1.record(r.stream)
+    host_issue = time.perf_counter() - host0
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    elapsed = t0.elapsed_time(t1) * 1e-3
+    elapsed = max_over_ranks(elapsed, world, device)
+    assert int(r.status.item()) == 0, "device-side error in timed steps"
+
+    per_kernel = {"chain": [], "tree": [], "probs": []}
+    for e in evs:
+        per_kernel["chain"].append(e[0].elapsed_time(e[1]) * 1e-3)
+        per_kernel["tree"].append(e[1].elapsed_time(e[2]) * 1e-3)
+        per_kernel["probs"].append(e[2].elapsed_time(e[3]) * 1e-3)
+    avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
+    nbytes = step_bytes(ci, ti)
+    peak, peak_kind = measured_peak()
+    rows = {}
+    for k in ("chain", "tree", "probs"):
+        gbs = nbytes[k] / avg[k] / 1e9
+        rows[k] = {"us_per_launch": avg[k] * 1e6, "algorithmic_bytes": nbytes[k],
+                   "GBps": gbs, "frac_of_peak": gbs / peak}
+    rows["chain"]["verified_positions"] = ci.B * (ci.gamma + 1)
+    rows["tree"]["verified_positions"] = ti.B * ti.N
+    dom = max(("chain", "tree", "probs"), key=lambda k: avg[k])
+    kname = {"chain": "verify_kernel<bf16, chain-sample>", "tree": "verify_kernel<bf16, tree>",
+             "probs": "verify_kernel<bf16, probs>"}[dom]
+    pos_total = sum_over_ranks(positions(ci, ti) * K, world, device)
+    value = pos_total / elapsed
+    step_total_bytes = sum(nbytes.values())
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": elapsed / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world * (ci.B + ti.B),
+                   "positions_per_step": positions(ci, ti) * world,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"inputs rotated over {ROT} copies (>4x L2 of traffic between reuses)"},
+        "achieved_GBps": step_total_bytes * world * K / elapsed / 1e9 / world,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": rows[dom]["GBps"],
+                     "peak": peak, "unit": "GB/s", "frac": rows[dom]["GBps"] / peak,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": ncu_traffic(dom), "algorithmic_bytes": nbytes[dom]},
+        "rows": rows,
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+        "host_issue_us_per_step": host_issue / K * 1e6,
+        "emitted_tokens_per_step": int((r.acc.cpu().numpy() + 1).sum()),
+    }
+    out["e2e"] = e2e(r, ci, ti, args.e2e_steps, world, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(ci, ti, budget_s=10.0)
+    return out
+
+
+def e2e(r, ci, ti, steps, world, device):
+    """The step through the same C entry points with HOST inputs: H2D copies of the step's
+    inputs from pinned memory and D2H copies of all outputs are timed."""
+    import torch
+    pin = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+                     if a.dtype == np.uint16 else torch.from_numpy(a)).pin_memory()
+    h_ct, h_cd, h_tt = pin(ci.target), pin(ci.draft), pin(ti.target)
+    h_tok, h_uni, h_par, h_ttok = pin(ci.tokens), pin(ci.uniforms), pin(ti.parents), \
+        pin(ti.tokens)
+    o_acc = torch.empty_like(r.acc, device="cpu").pin_memory()
+    o_out = torch.empty_like(r.out, device="cpu").pin_memory()
+    o_tacc = torch.empty_like(r.tacc, device="cpu").pin_memory()
+    o_tpath = torch.empty_like(r.tpath, device="cpu").pin_memory()
+    o_tout = torch.empty_like(r.tout, device="cpu").pin_memory()
+    o_pr = torch.empty_like(r.probs[0], device="cpu").pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in (h_ct, h_cd, h_tt, h_tok, h_uni, h_par,
+                                                     h_ttok))
+    bo = sum(t.numel() * t.element_size() for t in (o_acc, o_out, o_tacc, o_tpath, o_tout, o_pr))
+
+    def one(i):
+        k = i % ROT
+        c = r.copies[k]
+        c["ct"].copy_(h_ct, non_blocking=True)
+        c["cd"].copy_(h_cd, non_blocking=True)
+        c["tt"].copy_(h_tt, non_blocking=True)
+        r.tok.copy_(h_tok, non_blocking=True)
+        r.uni.copy_(h_uni, non_blocking=True)
+        r.par.copy_(h_par, non_blocking=True)
+        r.ttok.copy_(h_ttok, non_blocking=True)
+        lib = r.lib
+        chain, tree, probs = r.args[k]
+        # probs reads this step's freshly copied target rows
+        probs = (ctypes.c_void_p(c["ct"].data_ptr()),) + probs[1:]
+        rc = lib.spec_verify_chain(*chain) | lib.spec_verify_tree(*tree) | lib.spec_probs(*probs)
+        if rc:
+            raise RuntimeError(f"verify call failed: {rc}")
+        o_acc.copy_(r.acc, non_blocking=True)
+        o_out.copy_(r.out, non_blocking=True)
+        o_tacc.copy_(r.tacc, non_blocking=True)
+        o_tpath.copy_(r.tpath, non_blocking=True)
+        o_tout.copy_(r.tout, non_blocking=True)
+        o_pr.copy_(r.probs[k], non_blocking=True)
+
+    for i in range(5):
+        one(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        one(i)
+    t1.record()
+    torch.cuda.synchronize()
+    el = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world, device)
+    pos = sum_over_ranks(positions(ci, ti) * steps, world, device)
+    return {"value": pos / el, "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "steps": steps, "ms_per_step": el / steps * 1e3}
+
+
+# ------------------------------------------------------------------ the oracle
+
+def oracle_step(ci, ti, crow, trow, prow):
+    """One bounded sample of the step on the CPU oracle: chain rows crow, tree rows trow, probs
+    rows prow (numpy index arrays). Returns the positions verified."""
+    import oracle
+    from workloads import BF16
+    oracle.verify_chain(ci.target[crow], ci.draft[crow], BF16, ci.tokens[crow],
+                        ci.uniforms[crow], ci.temperature)
+    oracle.verify_tree(ti.target[trow], BF16, ti.parents[trow], ti.tokens[trow])
+    flat = ci.target.reshape(-1, ci.V)
+    oracle.probs(flat[prow], BF16, 1.0)
+    return len(crow) * (ci.gamma + 1) + len(trow) * ti.N
+
+
+def cpu_baseline(ci, ti, budget_s=10.0):
+    """The oracle as it stands, single-threaded, on whole steps of the same workload, repeated
+    until about budget_s seconds of CPU work."""
+    crow, trow = np.arange(ci.B), np.arange(ti.B)
+    prow = np.arange(ci.B * (ci.gamma + 1))
+    pos, n = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        pos += oracle_step(ci, ti, crow, trow, prow)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} full steps of the same workload (chain 64 rows, tree 32 rows, probs "
+                      f"384 rows) in {el:.1f} s on one host core, fp64 C oracle"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    ci, ti = make_inputs(args.seed_offset)
+    # size each step's row sample so that warm-up + timed steps take about 2 minutes
+    full = time.perf_counter()
+    oracle_step(ci, ti, np.arange(4), np.arange(2), np.arange(24))
+    t_small = time.perf_counter() - full          # 1/16 of a full step
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    frac = min(1.0, per_step_budget / (16 * t_small))
+    nc = max(1, int(round(ci.B * frac)))
+    nt = max(1, int(round(ti.B * frac)))
+    npb = max(1, int(round(ci.B * (ci.gamma + 1) * frac)))
+
+    def rows(i):
+        return ((np.arange(nc) + i * nc) % ci.B, (np.arange(nt) + i * nt) % ti.B,
+                (np.arange(npb) + i * npb) % (ci.B * (ci.gamma + 1)))
+
+    for i in range(args.warmup):
+        oracle_step(ci, ti, *rows(i))
+    pos = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        pos += oracle_step(ci, ti, *rows(i + args.warmup))
+    el = time.perf_counter() - t0
+    value = pos / el
+    sample = (f"each step: {nc}/{ci.B} chain rows, {nt}/{ti.B} tree rows, {npb}/"
+              f"{ci.B * (ci.gamma + 1)} probs rows of the same workload, one host core")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": ci.B + ti.B,
+                       "positions_per_step": positions(ci, ti), "parallelism": "single"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out))
+        return
+    rank, world, local = dist_init(args.gpus)
+    out = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 speculative-decoding verify library (libspec_verify.so).
+ *
+ * The operation. Speculative decoding lets a cheap draft model propose gamma tokens and has the
+ * large target model score all of them in one parallel pass; a rejection-sampling test on the
+ * target's own probabilities accepts the longest passing prefix and a distribution-preserving
+ * correction makes every emitted token an exact sample of the target ("Fast Inference from
+ * Transformers via Speculative Decoding", Leviathan, Kalman, Matias; pith.science review,
+ * sections "The pith", "Core claim", "What carries the argument", "Desk Editor's Note",
+ * "Circularity Check"). Falcon verifies a tree of drafts in one pass under greedy decoding
+ * ("Falcon: Faster and Parallel Inference of Large Language Models through Enhanced
+ * Semi-Autoregressive Drafting and Custom-Designed Decoding Tree", pith.science review,
+ * "What carries the argument", Figure 3, Figure 4). This library is that verify step and
+ * nothing else: the draft and target models are the caller's.
+ *
+ * Common rules for every entry point
+ *   - All pointers except `stream` and `workspace`'s host-side size are DEVICE pointers on the
+ *     current CUDA device. The caller owns every buffer; the library allocates nothing, frees
+ *     nothing and keeps no state except cached device attributes.
+ *   - Logits are row-major, contiguous, fp32 (SPEC_F32) or bf16 (SPEC_BF16) whose base address
+ *     is aligned to the element size. Rows need not be 16-byte aligned (an unaligned row is read
+ *     with scalar loads at its ends).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are stream-ordered and
+ *     asynchronous: they enqueue work and return; nothing synchronises with the host.
+ *   - Return value: SPEC_OK, or a negative SPEC_ERR_* code found on the host before anything
+ *     was enqueued (SPEC_ERR_LAUNCH: the launch itself failed, cudaGetLastError).
+ *   - Device-side problems found in the data (a non-finite logit row, a token outside [0, V),
+ *     a bad tree parent) never trap: the affected batch row reports accept_len = -1 with all
+ *     its output tokens -1, and *status receives the first such code (atomic compare-and-swap
+ *     from 0). *status is never cleared by the library: zero it before a call whose errors you
+ *     want to see.
+ *   - A logits row is valid when it holds no NaN and no +inf and at least one finite value;
+ *     -inf entries (masked tokens) are allowed and get probability 0.
+ *   - Workspace: a caller-owned device buffer of at least spec_workspace_bytes(...) bytes,
+ *     16-byte aligned, ZERO-FILLED before its first use (cudaMemset or spec_workspace_init).
+ *     Every call leaves it zero-filled again, so it can be reused by later calls on the same
+ *     stream; two calls that may run at the same time need two workspaces.
+ *   - Results are deterministic: the same inputs give bit-identical outputs on the same GPU.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+/* host-side return codes */
+#define SPEC_OK 0
+#define SPEC_ERR_NULL (-1)      /* a required pointer is NULL                                */
+#define SPEC_ERR_SHAPE (-2)     /* B, gamma, N, V or rows out of range (see limits below)     */
+#define SPEC_ERR_TEMP (-3)      /* temperature not 0 and not in [FLT_MIN, FLT_MAX]             */
+#define SPEC_ERR_DTYPE (-4)     /* dtype not SPEC_F32 / SPEC_BF16                             */
+#define SPEC_ERR_WORKSPACE (-5) /* workspace smaller than spec_workspace_bytes(...)            */
+#define SPEC_ERR_ALIGN (-6)     /* a pointer is not aligned to its element size (16 for the
+                                   workspace)                                                */
+#define SPEC_ERR_LAUNCH (-7)    /* the kernel launch failed (e.g. no sm_103a device)          */
+/* device-side codes, written to *status */
+#define SPEC_ERR_NONFINITE (-20) /* a logits row has NaN or +inf, or no finite entry          */
+#define SPEC_ERR_TOKEN (-21)     /* a draft / node token is outside [0, V)                    */
+#define SPEC_ERR_PARENT (-22)    /* parents[b,0] != -1 or parents[b,i] not in [0, i)          */
+
+/* limits */
+#define SPEC_MAX_V (1 << 20)   /* vocabulary size                                            */
+#define SPEC_MAX_GAMMA 255     /* draft length of the chain                                  */
+#define SPEC_MAX_NODES 1024    /* nodes per candidate tree                                   */
+
+/*
+ * Bytes of workspace needed by a call over B batch rows of `rows_per_b` logits rows of V
+ * elements: rows_per_b = 2*gamma+1 for spec_verify_chain (any temperature), N for
+ * spec_verify_tree, 1 for spec_probs (with B = rows). Returns 0 for invalid arguments.
+ */
+size_t spec_workspace_bytes(int B, int rows_per_b, int V, int dtype);
+
+/* Zero-fills a workspace on `stream` (a cudaMemsetAsync). */
+int spec_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Chain verification (rejection sampling), batched over B independent steps.
+ *
+ *   p_i = softmax(target_logits[b, i, :] / T)   for i = 0..gamma
+ *   q_i = softmax(draft_logits[b, i, :] / T)    for i = 0..gamma-1
+ *   x_i = draft_tokens[b, i]; draft x_i is accepted while u_i <= p_i(x_i) / q_i(x_i)
+ *         (u_i = uniforms[b, i]); q_i(x_i) = 0 counts as +inf if p_i(x_i) > 0, else as 0.
+ *   n   = index of the first rejection, or gamma if all pass.
+ *   The emitted token at position n is drawn with u = uniforms[b, gamma] by inverse CDF
+ *   (the first k whose running sum strictly exceeds u * S) from
+ *     r = max(0, p_n - q_n)   if n < gamma (r = p_n if that sums to 0), or
+ *     r = p_gamma             if n == gamma (the bonus token).
+ *   T == 0 is greedy decoding: x_i is accepted iff it is the lowest-index argmax of target
+ *   row i, and the emitted token is the argmax of target row n; draft_logits is not read
+ *   (may be NULL) and neither is uniforms (may be NULL).
+ *
+ *   target_logits [B, gamma+1, V]   dtype
+ *   draft_logits  [B, gamma, V]     dtype (unused at T == 0)
+ *   draft_tokens  [B, gamma]        int32 (may be NULL when gamma == 0)
+ *   uniforms      [B, gamma+1]      fp32 in (0, 1) (unused at T == 0)
+ *   accept_len    [B]               int32 out: n, or -1 for an invalid batch row
+ *   out_tokens    [B, gamma+1]      int32 out: x_0..x_{n-1}, the drawn token, then -1
+ *   status        [1]               int32 device word, see the common rules
+ * Limits: 1 <= V <= SPEC_MAX_V, 0 <= gamma <= SPEC_MAX_GAMMA, B >= 0 (B == 0 does nothing),
+ * temperature == 0 or FLT_MIN <= temperature <= FLT_MAX.
+ */
+int spec_verify_chain(const void *target_logits, const void *draft_logits, int dtype,
+                      const int32_t *draft_tokens, const float *uniforms, int B, int gamma, int V,
+                      float temperature, int32_t *accept_len, int32_t *out_tokens,
+                      int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Greedy tree verification, batched over B candidate trees of N nodes.
+ *
+ *   g_j = lowest-index argmax of target_logits[b, j, :]
+ *   node 0 is the committed root and is accepted; node i > 0 is accepted iff its parent is
+ *   accepted and node_tokens[b, i] == g_{parents[b, i]}.
+ *   d* = the deepest accepted node (the smallest index among equally deep ones).
+ *
+ *   target_logits [B, N, V]   dtype
+ *   parents       [B, N]      int32, parents[b, 0] = -1, 0 <= parents[b, i] < i
+ *   node_tokens   [B, N]      int32 (node 0's entry is not read)
+ *   accept_len    [B]         int32 out: depth of d* (accepted draft tokens), or -1
+ *   path_nodes    [B, N]      int32 out: root .. d* (depth+1 entries), then -1
+ *   out_tokens    [B, N]      int32 out: tokens of path nodes 1..depth, then g_{d*} (the bonus
+ *                             token), then -1
+ * Limits: 1 <= N <= SPEC_MAX_NODES, 1 <= V <= SPEC_MAX_V, B >= 0.
+ */
+int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parents,
+                     const int32_t *node_tokens, int B, int N, int V, int32_t *accept_len,
+                     int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Temperature softmax of `rows` logits rows into fp32 probabilities:
+ *   out_probs[r, k] = exp((l[r,k] - max_k l[r,k]) / T) / sum_j exp((l[r,j] - max l[r]) / T)
+ * T == 0 gives the one-hot vector at the lowest-index argmax. An invalid row is written as NaN
+ * and reported through *status (SPEC_ERR_NONFINITE).
+ *
+ *   logits    [rows, V]   dtype
+ *   out_probs [rows, V]   fp32 out (4-byte aligned)
+ * Limits: 1 <= V <= SPEC_MAX_V, rows >= 0, temperature as for spec_verify_chain.
+ */
+int spec_probs(const void *logits, int dtype, int rows, int V, float temperature,
+               float *out_probs, int32_t *status, void *workspace, size_t workspace_bytes,
+               void *stream);
+
+/* Static text for any SPEC_* code ("unknown status" otherwise). */
+const char *spec_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

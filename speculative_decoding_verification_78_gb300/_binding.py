@@ -1,0 +1,209 @@
+"""ctypes binding of libspec_verify.so: the C entry points under the same names.
+
+Argument marshalling only: every step of the verify path runs in the library's CUDA kernels.
+torch is used for device memory and streams. There is no fallback: when the library is
+missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libspec_verify.so")
+
+SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_OK = 0
+SPEC_ERR_NULL, SPEC_ERR_SHAPE, SPEC_ERR_TEMP, SPEC_ERR_DTYPE = -1, -2, -3, -4
+SPEC_ERR_WORKSPACE, SPEC_ERR_ALIGN, SPEC_ERR_LAUNCH = -5, -6, -7
+SPEC_ERR_NONFINITE, SPEC_ERR_TOKEN, SPEC_ERR_PARENT = -20, -21, -22
+SPEC_MAX_V, SPEC_MAX_GAMMA, SPEC_MAX_NODES = 1 << 20, 255, 1024
+
+# every symbol include/spec_verify.h declares
+EXPORTS = ("spec_workspace_bytes", "spec_workspace_init", "spec_verify_chain",
+           "spec_verify_tree", "spec_probs", "spec_status_string")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {spec_status_string(code)} ({code})")
+
+
+def load_library():
+    """Loads libspec_verify.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                              "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.spec_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        lib.spec_workspace_bytes.restype = sz
+        lib.spec_workspace_init.argtypes = [vp, sz, vp]
+        lib.spec_workspace_init.restype = i32
+        lib.spec_verify_chain.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, f32, vp, vp, vp,
+                                          vp, sz, vp]
+        lib.spec_verify_chain.restype = i32
+        lib.spec_verify_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz,
+                                         vp]
+        lib.spec_verify_tree.restype = i32
+        lib.spec_probs.argtypes = [vp, i32, i32, i32, f32, vp, vp, vp, sz, vp]
+        lib.spec_probs.restype = i32
+        lib.spec_status_string.argtypes = [i32]
+        lib.spec_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------------ marshalling helpers
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"expected a torch.Tensor, got {type(t)}")
+    if t.numel() and not t.is_cuda:
+        raise ValueError("device tensor expected (the library takes device pointers)")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def dtype_flag(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype in (torch.bfloat16, torch.int16) or str(t.dtype) == "torch.uint16":
+        return SPEC_BF16
+    raise TypeError(f"logits must be float32 or bfloat16 (got {t.dtype})")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+# ------------------------------------------------------------------ the C entry points
+
+def spec_workspace_bytes(B: int, rows_per_b: int, V: int, dtype: int) -> int:
+    return int(load_library().spec_workspace_bytes(B, rows_per_b, V, dtype))
+
+
+def spec_workspace_init(workspace: torch.Tensor, stream=None) -> int:
+    return load_library().spec_workspace_init(_ptr(workspace), _nbytes(workspace), _stream(stream))
+
+
+def spec_verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperature,
+                      accept_len, out_tokens, status, workspace, stream=None) -> int:
+    """target_logits [B, gamma+1, V], draft_logits [B, gamma, V] (fp32 or bf16), draft_tokens
+    [B, gamma] int32, uniforms [B, gamma+1] fp32; outputs accept_len [B], out_tokens
+    [B, gamma+1] int32; status [1] int32; workspace uint8 (zero-filled once)."""
+    B, g1, V = target_logits.shape
+    return load_library().spec_verify_chain(
+        _ptr(target_logits), _ptr(draft_logits), dtype_flag(target_logits), _ptr(draft_tokens),
+        _ptr(uniforms), B, g1 - 1, V, float(temperature), _ptr(accept_len), _ptr(out_tokens),
+        _ptr(status), _ptr(workspace), _nbytes(workspace), _stream(stream))
+
+
+def spec_verify_tree(target_logits, parents, node_tokens, accept_len, path_nodes, out_tokens,
+                     status, workspace, stream=None) -> int:
+    """target_logits [B, N, V]; parents, node_tokens [B, N] int32; outputs accept_len [B],
+    path_nodes [B, N], out_tokens [B, N] int32."""
+    B, N, V = target_logits.shape
+    return load_library().spec_verify_tree(
+        _ptr(target_logits), dtype_flag(target_logits), _ptr(parents), _ptr(node_tokens), B, N,
+        V, _ptr(accept_len), _ptr(path_nodes), _ptr(out_tokens), _ptr(status), _ptr(workspace),
+        _nbytes(workspace), _stream(stream))
+
+
+def spec_probs(logits, temperature, out_probs, status, workspace, stream=None) -> int:
+    """logits [..., V] -> out_probs [..., V] fp32."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V if V else 0
+    return load_library().spec_probs(
+        _ptr(logits), dtype_flag(logits), rows, V, float(temperature), _ptr(out_probs),
+        _ptr(status), _ptr(workspace), _nbytes(workspace), _stream(stream))
+
+
+def spec_status_string(code: int) -> str:
+    try:
+        return load_library().spec_status_string(int(code)).decode()
+    except ImportError:
+        return f"status {code}"
+
+
+# ------------------------------------------------------------------ conveniences (allocation)
+
+def new_workspace(B: int, rows_per_b: int, V: int, dtype: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace tensor large enough for the given call shape."""
+    n = spec_workspace_bytes(B, rows_per_b, V, dtype)
+    if n == 0:
+        raise SpecError(SPEC_ERR_SHAPE, "spec_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def check(code: int, where: str) -> None:
+    if code != SPEC_OK:
+        raise SpecError(code, where)
+
+
+def verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperature,
+                 workspace=None, stream=None):
+    """Allocates the outputs and runs spec_verify_chain. Returns (accept_len, out_tokens,
+    status) device tensors."""
+    B, g1, V = target_logits.shape
+    dev = target_logits.device
+    if workspace is None:
+        workspace = new_workspace(B, 2 * (g1 - 1) + 1, V, dtype_flag(target_logits), dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty((B, g1), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    check(spec_verify_chain(target_logits, draft_logits, draft_tokens, uniforms, temperature,
+                            acc, out, st, workspace, stream), "spec_verify_chain")
+    return acc, out, st
+
+
+def verify_tree(target_logits, parents, node_tokens, workspace=None, stream=None):
+    """Allocates the outputs and runs spec_verify_tree. Returns (accept_len, path_nodes,
+    out_tokens, status) device tensors."""
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    if workspace is None:
+        workspace = new_workspace(B, N, V, dtype_flag(target_logits), dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    out = torch.empty((B, N), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    check(spec_verify_tree(target_logits, parents, node_tokens, acc, path, out, st, workspace,
+                           stream), "spec_verify_tree")
+    return acc, path, out, st
+
+
+def probs(logits, temperature, workspace=None, stream=None):
+    """Allocates the output and runs spec_probs. Returns (probs fp32, status)."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    dev = logits.device
+    if workspace is None:
+        workspace = new_workspace(rows, 1, V, dtype_flag(logits), dev)
+    out = torch.empty(logits.shape, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    check(spec_probs(logits, temperature, out, st, workspace, stream), "spec_probs")
+    return out, st

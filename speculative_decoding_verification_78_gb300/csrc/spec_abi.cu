@@ -1,0 +1,231 @@
+// spec_abi.cu -- the extern "C" entry points of libspec_verify.so: argument checks on the host,
+// workspace layout, launch configuration, and dispatch to the kernel instances.
+#include <cuda_runtime.h>
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "spec_launch.h"
+#include "spec_verify.h"
+
+using namespace specv;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];   // cached multiprocessor counts (0 = not queried yet)
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < kMaxDevices) g_sm_count[dev] = n;
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int elem_size(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
+
+// units per logits row: one unit is 32 lanes x 8 vectors of 16 bytes
+int chunks_per_row(int V, int dtype) {
+  const int epv = 16 / elem_size(dtype);
+  const long long nv = V / epv;
+  const long long c = (nv + kUnitVecs - 1) / kUnitVecs;
+  return c < 1 ? 1 : static_cast<int>(c);
+}
+
+struct Layout {
+  size_t count, part, xlogit, total;
+};
+
+// workspace: [control words | per-batch-row counters | unit partials | draft-token logits]
+Layout layout(long long B, long long R, long long C) {
+  Layout L;
+  L.count = 256;
+  L.part = L.count + align256(static_cast<size_t>(B) * 4);
+  L.xlogit = L.part + align256(static_cast<size_t>(B * R * C) * 8);
+  L.total = L.xlogit + align256(static_cast<size_t>(B * R) * 4);
+  return L;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool temp_ok(float T) { return T == 0.f || (T >= FLT_MIN && T <= FLT_MAX); }
+
+// Fills the workspace pointers and unit counts of p; returns SPEC_OK or SPEC_ERR_WORKSPACE.
+int plan(Params &p, int dtype, void *ws, size_t ws_bytes) {
+  p.C = chunks_per_row(p.V, dtype);
+  const Layout L = layout(p.B, p.R, p.C);
+  if (ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  char *w = static_cast<char *>(ws);
+  p.ws_ctl = reinterpret_cast<unsigned *>(w);
+  p.ws_count = reinterpret_cast<unsigned *>(w + L.count);
+  p.ws_part = reinterpret_cast<uint2 *>(w + L.part);
+  p.ws_xlogit = reinterpret_cast<float *>(w + L.xlogit);
+  p.units = static_cast<long long>(p.B) * p.R * p.C;
+  p.groups = (p.units + kWarps - 1) / kWarps;
+  return SPEC_OK;
+}
+
+// persistent grid: two CTAs of 512 threads per SM, never more CTAs than groups
+int grid_for(const Params &p) {
+  const long long cap = 2LL * (sm_count() > 0 ? sm_count() : 1);
+  long long g = p.groups < cap ? p.groups : cap;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
+Params blank() {
+  Params p{};
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_bytes(int B, int rows_per_b, int V, int dtype) {
+  if (B < 0 || rows_per_b < 1 || V < 1 || V > SPEC_MAX_V) return 0;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return 0;
+  return layout(B, rows_per_b, chunks_per_row(V, dtype)).total;
+}
+
+int spec_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+  if (!workspace) return SPEC_ERR_NULL;
+  if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
+}
+
+int spec_verify_chain(const void *target_logits, const void *draft_logits, int dtype,
+                      const int32_t *draft_tokens, const float *uniforms, int B, int gamma, int V,
+                      float temperature, int32_t *accept_len, int32_t *out_tokens,
+                      int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (B < 0 || gamma < 0 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V)
+    return SPEC_ERR_SHAPE;
+  if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
+  const bool greedy = temperature == 0.f;
+  if (!target_logits || !accept_len || !out_tokens || !status || !workspace) return SPEC_ERR_NULL;
+  if (gamma > 0 && !draft_tokens) return SPEC_ERR_NULL;
+  if (!greedy && (!uniforms || (gamma > 0 && !draft_logits))) return SPEC_ERR_NULL;
+  const int es = elem_size(dtype);
+  if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)) ||
+      (draft_tokens && !aligned(draft_tokens, 4)) || (uniforms && !aligned(uniforms, 4)) ||
+      !aligned(accept_len, 4) || !aligned(out_tokens, 4) || !aligned(status, 4) ||
+      !aligned(workspace, 16))
+    return SPEC_ERR_ALIGN;
+  if (B == 0) return SPEC_OK;
+
+  Params p = blank();
+  p.tgt = target_logits;
+  p.drf = greedy ? nullptr : draft_logits;
+  p.tokens = draft_tokens;
+  p.uniforms = greedy ? nullptr : uniforms;
+  p.accept_len = accept_len;
+  p.out_tokens = out_tokens;
+  p.status = status;
+  p.B = B;
+  p.gamma = gamma;
+  p.N = 0;
+  p.V = V;
+  p.Rt = gamma + 1;
+  p.Rd = greedy ? 0 : gamma;
+  p.R = p.Rt + p.Rd;
+  p.c2 = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  const int rc = plan(p, dtype, workspace, workspace_bytes);
+  if (rc != SPEC_OK) return rc;
+  const int nseg = (V + kSeg - 1) / kSeg;
+  const size_t smem = greedy ? sizeof(int) * 2 * p.R : sizeof(float) * (2 * p.R + nseg);
+  const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
+                                     smem, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parents,
+                     const int32_t *node_tokens, int B, int N, int V, int32_t *accept_len,
+                     int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (B < 0 || N < 1 || N > SPEC_MAX_NODES || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_SHAPE;
+  if (!target_logits || !parents || !node_tokens || !accept_len || !path_nodes || !out_tokens ||
+      !status || !workspace)
+    return SPEC_ERR_NULL;
+  if (!aligned(target_logits, elem_size(dtype)) || !aligned(parents, 4) ||
+      !aligned(node_tokens, 4) || !aligned(accept_len, 4) || !aligned(path_nodes, 4) ||
+      !aligned(out_tokens, 4) || !aligned(status, 4) || !aligned(workspace, 16))
+    return SPEC_ERR_ALIGN;
+  if (B == 0) return SPEC_OK;
+
+  Params p = blank();
+  p.tgt = target_logits;
+  p.tokens = node_tokens;
+  p.parents = parents;
+  p.accept_len = accept_len;
+  p.out_tokens = out_tokens;
+  p.path_nodes = path_nodes;
+  p.status = status;
+  p.B = B;
+  p.N = N;
+  p.V = V;
+  p.Rt = N;
+  p.Rd = 0;
+  p.R = N;
+  const int rc = plan(p, dtype, workspace, workspace_bytes);
+  if (rc != SPEC_OK) return rc;
+  const size_t smem = sizeof(int) * 9 * static_cast<size_t>(N);
+  const cudaError_t e = launch_tree(dtype, p, grid_for(p), smem, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+int spec_probs(const void *logits, int dtype, int rows, int V, float temperature,
+               float *out_probs, int32_t *status, void *workspace, size_t workspace_bytes,
+               void *stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (rows < 0 || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_SHAPE;
+  if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
+  if (!logits || !out_probs || !status || !workspace) return SPEC_ERR_NULL;
+  if (!aligned(logits, elem_size(dtype)) || !aligned(out_probs, 4) || !aligned(status, 4) ||
+      !aligned(workspace, 16))
+    return SPEC_ERR_ALIGN;
+  if (rows == 0) return SPEC_OK;
+  const bool greedy = temperature == 0.f;
+  Params p = blank();
+  p.tgt = logits;
+  p.out_probs = out_probs;
+  p.status = status;
+  p.B = rows;
+  p.V = V;
+  p.Rt = 1;
+  p.Rd = 0;
+  p.R = 1;
+  p.c2 = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  const int rc = plan(p, dtype, workspace, workspace_bytes);
+  if (rc != SPEC_OK) return rc;
+  const cudaError_t e = launch_probs(greedy ? kProbsGreedy : kProbs, dtype, p, grid_for(p), 0,
+                                     static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+const char *spec_status_string(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_NULL: return "a required pointer is NULL";
+    case SPEC_ERR_SHAPE: return "B, gamma, N, V or rows out of range";
+    case SPEC_ERR_TEMP: return "temperature must be 0 or a finite value >= FLT_MIN";
+    case SPEC_ERR_DTYPE: return "dtype must be SPEC_F32 or SPEC_BF16";
+    case SPEC_ERR_WORKSPACE: return "workspace smaller than spec_workspace_bytes()";
+    case SPEC_ERR_ALIGN: return "pointer not aligned to its element size (workspace: 16 bytes)";
+    case SPEC_ERR_LAUNCH: return "kernel launch failed";
+    case SPEC_ERR_NONFINITE: return "a logits row holds NaN or +inf, or no finite value";
+    case SPEC_ERR_TOKEN: return "a draft or node token is outside [0, V)";
+    case SPEC_ERR_PARENT: return "a tree parent index is invalid";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/spec_verify.h
+declares, sizes workspaces, and rejects bad arguments on the host before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_78_gb300 import build as b
+    b.build()
+    import speculative_decoding_verification_78_gb300 as sv
+    return sv.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    import speculative_decoding_verification_78_gb300 as sv
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+    assert sorted(sv.EXPORTS) == names
+
+
+def test_status_strings(lib):
+    import speculative_decoding_verification_78_gb300 as sv
+    for code in (sv.SPEC_OK, sv.SPEC_ERR_NULL, sv.SPEC_ERR_SHAPE, sv.SPEC_ERR_TEMP,
+                 sv.SPEC_ERR_DTYPE, sv.SPEC_ERR_WORKSPACE, sv.SPEC_ERR_ALIGN, sv.SPEC_ERR_LAUNCH,
+                 sv.SPEC_ERR_NONFINITE, sv.SPEC_ERR_TOKEN, sv.SPEC_ERR_PARENT):
+        assert sv.spec_status_string(code) != "unknown status"
+    assert sv.spec_status_string(12345) == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    import speculative_decoding_verification_78_gb300 as sv
+    a = sv.spec_workspace_bytes(64, 11, 32000, sv.SPEC_BF16)
+    b = sv.spec_workspace_bytes(64, 11, 32000, sv.SPEC_F32)
+    assert 0 < a < b                      # bf16 rows are half as many units
+    assert a % 256 == 0
+    assert sv.spec_workspace_bytes(64, 11, 0, sv.SPEC_BF16) == 0
+    assert sv.spec_workspace_bytes(64, 11, sv.SPEC_MAX_V + 1, sv.SPEC_BF16) == 0
+    assert sv.spec_workspace_bytes(64, 11, 100, 7) == 0
+    # grows with the batch and the rows per batch row
+    assert sv.spec_workspace_bytes(128, 11, 32000, 1) > a
+    assert sv.spec_workspace_bytes(64, 21, 32000, 1) > a
+
+
+FAKE = 0x100000          # a 256-byte aligned fake device address: never dereferenced here
+
+
+def _chain(lib, **kw):
+    a = dict(t=FAKE, d=FAKE, dtype=1, tok=FAKE, uni=FAKE, B=4, g=3, V=1000, T=1.0, acc=FAKE,
+             out=FAKE, st=FAKE, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.spec_verify_chain(vp(a["t"]), vp(a["d"]), a["dtype"], vp(a["tok"]), vp(a["uni"]),
+                                 a["B"], a["g"], a["V"], a["T"], vp(a["acc"]), vp(a["out"]),
+                                 vp(a["st"]), vp(a["ws"]), a["wsb"], None)
+
+
+def test_chain_host_validation(lib):
+    import speculative_decoding_verification_78_gb300 as sv
+    assert _chain(lib, dtype=3) == sv.SPEC_ERR_DTYPE
+    assert _chain(lib, V=0) == sv.SPEC_ERR_SHAPE
+    assert _chain(lib, V=sv.SPEC_MAX_V + 1) == sv.SPEC_ERR_SHAPE
+    assert _chain(lib, g=-1) == sv.SPEC_ERR_SHAPE
+    assert _chain(lib, g=sv.SPEC_MAX_GAMMA + 1) == sv.SPEC_ERR_SHAPE
+    assert _chain(lib, B=-1) == sv.SPEC_ERR_SHAPE
+    assert _chain(lib, T=-1.0) == sv.SPEC_ERR_TEMP
+    assert _chain(lib, T=float("nan")) == sv.SPEC_ERR_TEMP
+    assert _chain(lib, T=float("inf")) == sv.SPEC_ERR_TEMP
+    assert _chain(lib, T=1e-40) == sv.SPEC_ERR_TEMP        # below FLT_MIN
+    assert _chain(lib, t=0) == sv.SPEC_ERR_NULL
+    assert _chain(lib, d=0) == sv.SPEC_ERR_NULL
+    assert _chain(lib, uni=0) == sv.SPEC_ERR_NULL
+    assert _chain(lib, tok=0) == sv.SPEC_ERR_NULL
+    assert _chain(lib, st=0) == sv.SPEC_ERR_NULL
+    assert _chain(lib, ws=0) == sv.SPEC_ERR_NULL
+    assert _chain(lib, t=FAKE + 1) == sv.SPEC_ERR_ALIGN     # bf16 needs 2-byte alignment
+    assert _chain(lib, dtype=0, t=FAKE + 2) == sv.SPEC_ERR_ALIGN
+    assert _chain(lib, ws=FAKE + 8) == sv.SPEC_ERR_ALIGN
+    assert _chain(lib, acc=FAKE + 2) == sv.SPEC_ERR_ALIGN
+    need = sv.spec_workspace_bytes(4, 7, 1000, 1)
+    assert _chain(lib, wsb=need - 1) == sv.SPEC_ERR_WORKSPACE
+    # empty batch: nothing to do, nothing launched
+    assert _chain(lib, B=0) == sv.SPEC_OK
+    # greedy needs neither draft logits nor uniforms; gamma = 0 needs no tokens
+    assert _chain(lib, T=0.0, d=0, uni=0, wsb=need - 1) == sv.SPEC_ERR_WORKSPACE
+    assert _chain(lib, g=0, tok=0, d=0, wsb=8) == sv.SPEC_ERR_WORKSPACE
+
+
+def test_tree_and_probs_host_validation(lib):
+    import speculative_decoding_verification_78_gb300 as sv
+    vp = ctypes.c_void_p
+
+    def tree(**kw):
+        a = dict(t=FAKE, dtype=1, par=FAKE, tok=FAKE, B=2, N=64, V=1000, acc=FAKE, path=FAKE,
+                 out=FAKE, st=FAKE, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return lib.spec_verify_tree(vp(a["t"]), a["dtype"], vp(a["par"]), vp(a["tok"]), a["B"],
+                                    a["N"], a["V"], vp(a["acc"]), vp(a["path"]), vp(a["out"]),
+                                    vp(a["st"]), vp(a["ws"]), a["wsb"], None)
+
+    assert tree(N=0) == sv.SPEC_ERR_SHAPE
+    assert tree(N=sv.SPEC_MAX_NODES + 1) == sv.SPEC_ERR_SHAPE
+    assert tree(par=0) == sv.SPEC_ERR_NULL
+    assert tree(path=0) == sv.SPEC_ERR_NULL
+    assert tree(dtype=-1) == sv.SPEC_ERR_DTYPE
+    assert tree(tok=FAKE + 2) == sv.SPEC_ERR_ALIGN
+    assert tree(wsb=100) == sv.SPEC_ERR_WORKSPACE
+    assert tree(B=0) == sv.SPEC_OK
+
+    def pr(**kw):
+        a = dict(t=FAKE, dtype=0, rows=3, V=100, T=1.0, out=FAKE, st=FAKE, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return lib.spec_probs(vp(a["t"]), a["dtype"], a["rows"], a["V"], a["T"], vp(a["out"]),
+                              vp(a["st"]), vp(a["ws"]), a["wsb"], None)
+
+    assert pr(V=0) == sv.SPEC_ERR_SHAPE
+    assert pr(rows=-2) == sv.SPEC_ERR_SHAPE
+    assert pr(T=-0.5) == sv.SPEC_ERR_TEMP
+    assert pr(out=0) == sv.SPEC_ERR_NULL
+    assert pr(out=FAKE + 1) == sv.SPEC_ERR_ALIGN
+    assert pr(wsb=16) == sv.SPEC_ERR_WORKSPACE
+    assert pr(rows=0) == sv.SPEC_OK
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import speculative_decoding_verification_78_gb300._binding as bnd
+    monkeypatch.setattr(bnd, "_lib", None)
+    monkeypatch.setattr(bnd, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        bnd.load_library()

@@ -1,0 +1,328 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle on the same
+seeded inputs and the same uniforms.
+
+Accept lengths, emitted tokens and tree paths must be bit-exact, except for chain draws whose
+oracle margin to a decision or CDF boundary is below 1e-5 relative (counted, reported, and
+bounded). Tree and greedy results have no such exemption: argmax compares identical stored
+values. Probabilities must agree within 1e-5 absolute (fp32 logits) and 2e-3 (bf16 logits).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from golden_io import chain_cases, tree_cases
+from gpu_util import compare_chain, dev, run_chain, run_tree
+from workloads import (BF16, F32, ChainInputs, TreeInputs, bf16_to_f32, chain_128k, chain_32k,
+                       chain_tiny, f32_to_bf16, make_uniforms, sweep_152k, tree_32k, tree_shape)
+
+pytestmark = pytest.mark.gpu
+
+PROB_TOL = {F32: 1e-5, BF16: 2e-3}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_78_gb300 as sv
+    sv.load_library()
+
+
+# --------------------------------------------------------------------------- golden fixtures
+
+
+@pytest.mark.parametrize("case", chain_cases(), ids=lambda c: c["name"])
+def test_golden_chain(case):
+    ci = ChainInputs(case["name"], case["target"], case["draft"], F32, case["tokens"],
+                     case["uniforms"], case["T"])
+    acc, out, st = run_chain(ci)
+    assert st == 0
+    np.testing.assert_array_equal(acc, case["accept_len"])
+    np.testing.assert_array_equal(out, case["out_tokens"])
+
+
+@pytest.mark.parametrize("case", tree_cases(), ids=lambda c: c["name"])
+def test_golden_tree(case):
+    ti = TreeInputs(case["name"], case["target"], F32, case["parents"], case["tokens"])
+    acc, path, out, st = run_tree(ti)
+    assert st == 0
+    np.testing.assert_array_equal(acc, case["accept_len"])
+    np.testing.assert_array_equal(path, case["path_nodes"])
+    np.testing.assert_array_equal(out, case["out_tokens"])
+
+
+# --------------------------------------------------------------------------- the workloads
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_chain_tiny_1000_steps(orc, offset):
+    """1000 B=1 steps batched, gamma=4, V=1000 fp32 (with offset=1 every row starts 4 bytes
+    past a 16-byte boundary)."""
+    ci = chain_tiny()
+    gpu = run_chain(ci, offset_elems=offset)
+    assert gpu[2] == 0
+    flagged, fdiff, oa = compare_chain(orc, ci, gpu)
+    assert 0 < oa.mean() < 4
+
+
+def test_chain_32k_bf16(orc):
+    ci = chain_32k()
+    gpu = run_chain(ci)
+    assert gpu[2] == 0
+    compare_chain(orc, ci, gpu)
+
+
+@pytest.mark.parametrize("sigma", [0.25, 1.0, 4.0])
+def test_chain_128k_bf16_sigma_sweep(orc, sigma):
+    """Full-size call (B=256, gamma=8, V=128256, bf16, T=0.7); the oracle checks every row for
+    sigma = 1 and a 64-row sample otherwise."""
+    ci = chain_128k(sigma=sigma)
+    gpu = run_chain(ci)
+    assert gpu[2] == 0
+    rows = None if sigma == 1.0 else np.arange(0, ci.B, 4)
+    compare_chain(orc, ci, gpu, rows=rows)
+
+
+@pytest.mark.parametrize("B,gamma", [(1, 3), (1, 7), (16, 3), (16, 7), (128, 3), (128, 7)])
+def test_sweep_152k_fp32(orc, B, gamma):
+    ci = sweep_152k(B=B, gamma=gamma)
+    gpu = run_chain(ci)
+    assert gpu[2] == 0
+    rows = None if B <= 16 else np.arange(0, B, B // 16)
+    compare_chain(orc, ci, gpu, rows=rows)
+
+
+def test_sweep_152k_fp32_largest(orc):
+    """B=1024, gamma=7, V=152064 fp32: 9.3 GB of logits in one call; 16 rows checked."""
+    ci = sweep_152k(B=1024, gamma=7)
+    gpu = run_chain(ci)
+    assert gpu[2] == 0
+    compare_chain(orc, ci, gpu, rows=np.arange(0, 1024, 64))
+    del ci
+
+
+def test_tree_32k_bf16(orc):
+    ti = tree_32k()
+    acc, path, out, st = run_tree(ti)
+    ra, rp, ro, rc = orc.verify_tree(ti.target, BF16, ti.parents, ti.tokens)
+    assert st == 0 and rc == 0
+    np.testing.assert_array_equal(acc, ra)
+    np.testing.assert_array_equal(path, rp)
+    np.testing.assert_array_equal(out, ro)
+    assert acc.max() >= 2
+
+
+# --------------------------------------------------------------------------- probabilities
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("V,T", [(32000, 1.0), (1001, 0.7), (5, 100.0), (4097, 0.01),
+                                 (3000, 0.0)])
+def test_probs(orc, dtype, V, T):
+    import speculative_decoding_verification_78_gb300 as sv
+    rng = np.random.default_rng(V)
+    x = (rng.standard_normal((37, V)) * 3).astype(np.float32)
+    x[::5, ::7] = -np.inf      # masked entries
+    lg = f32_to_bf16(x) if dtype == BF16 else x
+    for off in (0, 1):
+        pr, st = sv.probs(dev(lg, off), T)
+        torch.cuda.synchronize()
+        po, rc = orc.probs(lg, dtype, T)
+        assert int(st.item()) == 0 and rc == 0
+        err = np.abs(pr.cpu().numpy().astype(np.float64) - po).max()
+        assert err <= PROB_TOL[dtype], err
+        assert err <= 2e-6     # what the kernel actually reaches (fp32 arithmetic)
+
+
+def test_probs_invalid_rows():
+    import speculative_decoding_verification_78_gb300 as sv
+    x = np.zeros((4, 300), np.float32)
+    x[0, 7] = np.nan
+    x[1, 0] = np.inf
+    x[2, :] = -np.inf
+    pr, st = sv.probs(dev(x), 1.0)
+    p = pr.cpu().numpy()
+    assert int(st.item()) == sv.SPEC_ERR_NONFINITE
+    assert np.all(np.isnan(p[:3])) and np.allclose(p[3], 1 / 300)
+
+
+# --------------------------------------------------------------------------- edge cases
+
+
+def _chain_from(tgt, drf, tok, u, T, dtype=F32, name="edge"):
+    return ChainInputs(name, tgt, drf, dtype, np.asarray(tok, np.int32), np.asarray(u, np.float32),
+                       T)
+
+
+def test_gamma_zero_and_vocab_one(orc):
+    rng = np.random.default_rng(0)
+    for V in (1, 2, 7, 300):
+        tgt = (rng.standard_normal((50, 1, V)) * 2).astype(np.float32)
+        ci = _chain_from(tgt, np.zeros((50, 0, V), np.float32), np.zeros((50, 0)),
+                         make_uniforms(rng, (50, 1)), 1.0)
+        gpu = run_chain(ci)
+        assert gpu[2] == 0 and np.all(gpu[0] == 0)
+        compare_chain(orc, ci, gpu)
+    # V = 1: every draft is token 0 with p = q = 1, always accepted, bonus 0
+    tgt = np.zeros((3, 4, 1), np.float32)
+    ci = _chain_from(tgt, np.zeros((3, 3, 1), np.float32), np.zeros((3, 3)),
+                     np.full((3, 4), 0.999, np.float32), 1.0)
+    acc, out, st = run_chain(ci)
+    assert st == 0 and np.all(acc == 3) and np.all(out == 0)
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+@pytest.mark.parametrize("V,offset", [(1001, 0), (1001, 1), (4099, 3), (257, 0)])
+def test_ragged_vocab_and_unaligned_rows(orc, dtype, V, offset):
+    ci = chain_32k(seed=11, B=40, gamma=3, V=V, dtype=dtype, peaked=5)
+    gpu = run_chain(ci, offset_elems=offset)
+    assert gpu[2] == 0
+    compare_chain(orc, ci, gpu)
+
+
+@pytest.mark.parametrize("T", [0.01, 0.3, 100.0])
+def test_temperatures(orc, T):
+    ci = chain_32k(seed=12, B=48, gamma=4, V=5000, temperature=T)
+    gpu = run_chain(ci)
+    assert gpu[2] == 0
+    compare_chain(orc, ci, gpu)
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_greedy_chain_with_ties(orc, dtype):
+    """T = 0 with small-integer logits (many exact ties, also across units far apart)."""
+    rng = np.random.default_rng(3)
+    B, g, V = 64, 6, 9000
+    x = rng.integers(-4, 4, size=(B, g + 1, V)).astype(np.float32)
+    x[:, :, [17, 4000, 8999]] = 9.0          # equal maxima in different units: lowest wins
+    x[::3, :, 17] = 0.0                      # ... or the next one
+    tgt = f32_to_bf16(x) if dtype == BF16 else x
+    greedy = np.argmax(x, axis=2)
+    tok = np.where(rng.random((B, g)) < 0.8, greedy[:, :g], rng.integers(0, V, (B, g)))
+    ci = _chain_from(tgt, tgt[:, :g].copy(), tok, make_uniforms(rng, (B, g + 1)), 0.0, dtype)
+    acc, out, st = run_chain(ci)
+    oa, oo, _, rc = orc.verify_chain(tgt, None, dtype, ci.tokens, ci.uniforms, 0.0)
+    assert st == 0 and rc == 0
+    np.testing.assert_array_equal(acc, oa)
+    np.testing.assert_array_equal(out, oo)
+
+
+def test_all_accept_and_first_reject(orc):
+    rng = np.random.default_rng(4)
+    B, g, V = 32, 5, 3000
+    t = (rng.standard_normal((B, g + 1, V)) * 2).astype(np.float32)
+    tok = rng.integers(0, V, (B, g)).astype(np.int32)
+    # draft == target: every ratio is 1, all drafts accepted
+    ci = _chain_from(t, t[:, :g].copy(), tok, make_uniforms(rng, (B, g + 1)), 1.0)
+    acc, out, st = run_chain(ci)
+    assert st == 0 and np.all(acc == g)
+    compare_chain(orc, ci, (acc, out, st))
+    # the target gives the first draft token probability 0: rejected at position 0
+    t2 = t.copy()
+    t2[np.arange(B), 0, tok[:, 0]] = -np.inf
+    ci2 = _chain_from(t2, t[:, :g].copy(), tok, ci.uniforms, 1.0)
+    acc2, out2, st2 = run_chain(ci2)
+    assert st2 == 0 and np.all(acc2 == 0)
+    assert np.all(out2[:, 0] != tok[:, 0])
+    compare_chain(orc, ci2, (acc2, out2, st2))
+
+
+def test_long_draft_gamma_40(orc):
+    ci = chain_32k(seed=13, B=8, gamma=40, V=2000, peaked=3)
+    # a near-copy draft so that acceptance runs past 32 positions
+    ci.draft = ci.target[:, :40].copy()
+    gpu = run_chain(ci)
+    assert gpu[2] == 0
+    compare_chain(orc, ci, gpu)
+    assert gpu[0].max() > 32
+
+
+def test_largest_vocab(orc):
+    rng = np.random.default_rng(5)
+    V = 1 << 20
+    t = (rng.standard_normal((2, 2, V)) * 2).astype(np.float32)
+    d = t[:, :1] + (rng.standard_normal((2, 1, V)) * 0.5).astype(np.float32)
+    ci = _chain_from(t, d, rng.integers(0, V, (2, 1)), make_uniforms(rng, (2, 2)), 1.0)
+    gpu = run_chain(ci)
+    assert gpu[2] == 0
+    compare_chain(orc, ci, gpu)
+
+
+def test_invalid_rows_report_and_isolate(orc):
+    import speculative_decoding_verification_78_gb300 as sv
+    ci = chain_32k(seed=14, B=6, gamma=3, V=700, dtype=F32)
+    ci.target[1, 3, 5] = np.nan          # NaN in the bonus row: the whole step is invalid
+    ci.draft[2, 0, 9] = np.inf
+    ci.target[3, 1, :] = -np.inf         # no finite value
+    ci.tokens[4, 2] = 700                # token out of range
+    acc, out, st = run_chain(ci)
+    oa, oo, _, _ = orc.verify_chain(ci.target, ci.draft, F32, ci.tokens, ci.uniforms, 1.0)
+    assert st in (sv.SPEC_ERR_NONFINITE, sv.SPEC_ERR_TOKEN)
+    assert list(acc[1:5]) == [-1, -1, -1, -1] and np.all(out[1:5] == -1)
+    np.testing.assert_array_equal(acc, oa)
+    for b in (0, 5):
+        np.testing.assert_array_equal(out[b], oo[b])
+
+
+def test_tree_shapes_and_errors(orc):
+    import speculative_decoding_verification_78_gb300 as sv
+    rng = np.random.default_rng(6)
+    V = 600
+    for N, kind in [(1, "root"), (9, "chain"), (12, "star"), (64, "rule"), (1024, "random"),
+                    (300, "chain")]:
+        B = 6
+        if kind == "root":
+            par = np.full((B, 1), -1, np.int32)
+        elif kind == "chain":
+            par = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+        elif kind == "star":
+            par = np.tile(np.array([-1] + [0] * (N - 1), np.int32), (B, 1))
+        elif kind == "rule":
+            par = np.stack([tree_shape(rng, N) for _ in range(B)])
+        else:
+            par = np.stack([np.array([-1] + [int(rng.integers(0, i)) for i in range(1, N)])
+                            for _ in range(B)]).astype(np.int32)
+        x = rng.integers(-3, 3, size=(B, N, V)).astype(np.float32)
+        tgt = f32_to_bf16(x)
+        g = np.argmax(bf16_to_f32(tgt), axis=2)
+        tok = np.where(rng.random((B, N)) < 0.85, np.take_along_axis(g, np.maximum(par, 0), 1),
+                       rng.integers(0, V, (B, N))).astype(np.int32)
+        if kind == "star":
+            tok[:, 1:] = g[:, :1]          # duplicate siblings, all accepted: node 1 wins
+        ti = TreeInputs(kind, tgt, BF16, par, tok)
+        acc, path, out, st = run_tree(ti)
+        ra, rp, ro, rc = orc.verify_tree(tgt, BF16, par, tok)
+        assert st == 0 and rc == 0, kind
+        np.testing.assert_array_equal(acc, ra)
+        np.testing.assert_array_equal(path, rp)
+        np.testing.assert_array_equal(out, ro)
+    # invalid parents / tokens / rows: reported per row, others unaffected
+    par = np.tile(np.array([-1, 0, 0, 1], np.int32), (5, 1))
+    tgt = np.zeros((5, 4, 50), np.float32)
+    tok = np.zeros((5, 4), np.int32)
+    par[1, 0] = 0
+    par[2, 3] = 3
+    tok[3, 2] = 50
+    tgt[4, 2, 1] = np.nan
+    ti = TreeInputs("bad", tgt, F32, par, tok)
+    acc, path, out, st = run_tree(ti)
+    ra, rp, ro, _ = orc.verify_tree(tgt, F32, par, tok)
+    assert st in (sv.SPEC_ERR_PARENT, sv.SPEC_ERR_TOKEN, sv.SPEC_ERR_NONFINITE)
+    assert list(acc) == [2, -1, -1, -1, -1]
+    np.testing.assert_array_equal(acc, ra)
+    np.testing.assert_array_equal(path[0], rp[0])
+
+
+def test_deterministic_and_workspace_reuse(orc):
+    import speculative_decoding_verification_78_gb300 as sv
+    ci = chain_32k(seed=15, B=32, gamma=5, V=8000)
+    ws = sv.new_workspace(ci.B, 2 * ci.gamma + 1, ci.V, sv.SPEC_BF16)
+    first = run_chain(ci, workspace=ws)
+    for _ in range(3):
+        again = run_chain(ci, workspace=ws)
+        assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
+    # control words and per-batch-row counters are zero again after every call
+    ctl = ws[:256 + 4 * ci.B].view(torch.int32).cpu().numpy()
+    assert np.all(ctl == 0), "workspace counters not reset"
+    compare_chain(orc, ci, first)
