@@ -32,9 +32,9 @@
  *   - A logits row is valid when it holds no NaN and no +inf and at least one finite value;
  *     -inf entries (masked tokens) are allowed and get probability 0.
  *   - Workspace: a caller-owned device buffer of at least spec_workspace_bytes(...) bytes,
- *     16-byte aligned, ZERO-FILLED before its first use (cudaMemset or spec_workspace_init).
- *     Every call leaves it zero-filled again, so it can be reused by later calls on the same
- *     stream; two calls that may run at the same time need two workspaces.
+ *     16-byte aligned. It is scratch: every call overwrites the parts it uses before reading
+ *     them, so it needs no initialisation and holds nothing between calls. Calls on one
+ *     stream may share a workspace; two calls that may run at the same time need two.
  *   - Results are deterministic: the same inputs give bit-identical outputs on the same GPU.
  */
 #ifndef SPEC_VERIFY_H
@@ -76,7 +76,7 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
  */
 size_t spec_workspace_bytes(int B, int rows_per_b, int V, int dtype);
 
-/* Zero-fills a workspace on `stream` (a cudaMemsetAsync). */
+/* Zero-fills a workspace on `stream` (a cudaMemsetAsync). Optional: no call requires it. */
 int spec_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
 
 /*

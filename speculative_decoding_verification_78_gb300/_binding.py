@@ -114,7 +114,7 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, uniforms, tempe
                       accept_len, out_tokens, status, workspace, stream=None) -> int:
     """target_logits [B, gamma+1, V], draft_logits [B, gamma, V] (fp32 or bf16), draft_tokens
     [B, gamma] int32, uniforms [B, gamma+1] fp32; outputs accept_len [B], out_tokens
-    [B, gamma+1] int32; status [1] int32; workspace uint8 (zero-filled once)."""
+    [B, gamma+1] int32; status [1] int32; workspace uint8 (scratch, no initialisation)."""
     B, g1, V = target_logits.shape
     return load_library().spec_verify_chain(
         _ptr(target_logits), _ptr(draft_logits), dtype_flag(target_logits), _ptr(draft_tokens),
@@ -152,11 +152,11 @@ def spec_status_string(code: int) -> str:
 # ------------------------------------------------------------------ conveniences (allocation)
 
 def new_workspace(B: int, rows_per_b: int, V: int, dtype: int, device=None) -> torch.Tensor:
-    """A zero-filled workspace tensor large enough for the given call shape."""
+    """A workspace tensor large enough for the given call shape (scratch; never needs zeroing)."""
     n = spec_workspace_bytes(B, rows_per_b, V, dtype)
     if n == 0:
         raise SpecError(SPEC_ERR_SHAPE, "spec_workspace_bytes")
-    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def check(code: int, where: str) -> None:

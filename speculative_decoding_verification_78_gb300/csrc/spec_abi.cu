@@ -38,14 +38,13 @@ int chunks_per_row(int V, int dtype) {
 }
 
 struct Layout {
-  size_t count, part, xlogit, total;
+  size_t part, xlogit, total;
 };
 
-// workspace: [control words | per-batch-row counters | unit partials | draft-token logits]
+// workspace: [unit partials | draft-token logits], each part 256-byte aligned
 Layout layout(long long B, long long R, long long C) {
   Layout L;
-  L.count = 256;
-  L.part = L.count + align256(static_cast<size_t>(B) * 4);
+  L.part = 0;
   L.xlogit = L.part + align256(static_cast<size_t>(B * R * C) * 8);
   L.total = L.xlogit + align256(static_cast<size_t>(B * R) * 4);
   return L;
@@ -55,26 +54,65 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool temp_ok(float T) { return T == 0.f || (T >= FLT_MIN && T <= FLT_MAX); }
 
-// Fills the workspace pointers and unit counts of p; returns SPEC_OK or SPEC_ERR_WORKSPACE.
+// Fills the workspace pointers and unit counts of p; returns SPEC_OK, SPEC_ERR_WORKSPACE, or
+// SPEC_ERR_SHAPE when the call has 2^31 - 64 units or more (unit ids are 32-bit on the device).
 int plan(Params &p, int dtype, void *ws, size_t ws_bytes) {
   p.C = chunks_per_row(p.V, dtype);
+  const long long units = static_cast<long long>(p.B) * p.R * p.C;
+  if (units >= (1LL << 31) - 64) return SPEC_ERR_SHAPE;
   const Layout L = layout(p.B, p.R, p.C);
   if (ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
   char *w = static_cast<char *>(ws);
-  p.ws_ctl = reinterpret_cast<unsigned *>(w);
-  p.ws_count = reinterpret_cast<unsigned *>(w + L.count);
   p.ws_part = reinterpret_cast<uint2 *>(w + L.part);
   p.ws_xlogit = reinterpret_cast<float *>(w + L.xlogit);
-  p.units = static_cast<long long>(p.B) * p.R * p.C;
-  p.groups = (p.units + kWarps - 1) / kWarps;
+  p.units = static_cast<int>(units);
+  p.upb = p.R * p.C;
   return SPEC_OK;
 }
 
-// persistent grid: two CTAs of 512 threads per SM, never more CTAs than groups
+// stream kernel grid: at most two CTAs of 512 threads per SM (all resident at once), never
+// more CTAs than groups of kWarps units
 int grid_for(const Params &p) {
   const long long cap = 2LL * (sm_count() > 0 ? sm_count() : 1);
-  long long g = p.groups < cap ? p.groups : cap;
+  const long long groups = (static_cast<long long>(p.units) + kWarps - 1) / kWarps;
+  long long g = groups < cap ? groups : cap;
   return g < 1 ? 1 : static_cast<int>(g);
+}
+
+// Finishing plan for chain sampling. Single-unit rows with gamma <= 31: one warp per batch row.
+// Otherwise one cluster of S CTAs per batch row, S chosen so that the draw's pass over the
+// stopping rows fills about two CTAs per SM, with at least 8 residual segments per CTA.
+FinishPlan chain_sample_plan(const Params &p) {
+  FinishPlan f{};
+  if (p.C == 1 && p.V <= kWarpTailMaxV && p.gamma <= 31) {
+    f.warp_tail = true;
+    f.cluster = 1;
+    f.grid = (p.B + kWarps - 1) / kWarps;
+    f.smem = 0;
+    return f;
+  }
+  const int nseg = (p.V + kSeg - 1) / kSeg;
+  const int sms = sm_count() > 0 ? sm_count() : 1;
+  int S = (2 * sms + p.B - 1) / p.B;
+  int cap = nseg / 8;
+  if (cap < 1) cap = 1;
+  if (cap > kMaxCluster) cap = kMaxCluster;
+  if (S > cap) S = cap;
+  if (S < 1) S = 1;
+  f.warp_tail = false;
+  f.cluster = S;
+  f.grid = p.B * S;
+  f.smem = sizeof(float) * (2 * static_cast<size_t>(p.R) + nseg);
+  return f;
+}
+
+FinishPlan cta_plan(int rows, size_t smem) {
+  FinishPlan f{};
+  f.grid = rows;
+  f.cluster = 1;
+  f.smem = smem;
+  f.warp_tail = false;
+  return f;
 }
 
 Params blank() {
@@ -139,10 +177,10 @@ int spec_verify_chain(const void *target_logits, const void *draft_logits, int d
   p.c2 = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const int nseg = (V + kSeg - 1) / kSeg;
-  const size_t smem = greedy ? sizeof(int) * 2 * p.R : sizeof(float) * (2 * p.R + nseg);
+  const FinishPlan f = greedy ? cta_plan(B, sizeof(int) * (2 * static_cast<size_t>(p.R) + gamma))
+                              : chain_sample_plan(p);
   const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
-                                     smem, static_cast<cudaStream_t>(stream));
+                                     f, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -177,8 +215,9 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
   p.R = N;
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const size_t smem = sizeof(int) * 9 * static_cast<size_t>(N);
-  const cudaError_t e = launch_tree(dtype, p, grid_for(p), smem, static_cast<cudaStream_t>(stream));
+  const FinishPlan f = cta_plan(B, sizeof(int) * 6 * static_cast<size_t>(N));
+  const cudaError_t e = launch_tree(dtype, p, grid_for(p), f,
+                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -206,8 +245,8 @@ int spec_probs(const void *logits, int dtype, int rows, int V, float temperature
   p.c2 = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const cudaError_t e = launch_probs(greedy ? kProbsGreedy : kProbs, dtype, p, grid_for(p), 0,
-                                     static_cast<cudaStream_t>(stream));
+  const cudaError_t e = launch_probs(greedy ? kProbsGreedy : kProbs, dtype, p, grid_for(p),
+                                     cta_plan(rows, 0), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 

@@ -1,25 +1,27 @@
 // spec_device.cuh -- device code of the GB300 verify kernels (sm_103a).
 //
-// One persistent kernel template serves every entry point. The logits of a call are cut into
-// work units: one unit = one warp's share of one logits row, 32 lanes x 8 x 16-byte vectors
-// (4 KB), read once from HBM with coalesced, L1-bypassing 128-bit loads. A unit reduces to one
-// 8-byte partial: (row max, sum of exp2((l - max) * log2(e)/T)) for the softmax statistics, or
-// (max value, lowest index) for greedy argmax. CTAs of 16 warps take groups of 16 consecutive
-// units (batch-row-major order) from a global counter; the CTA that completes the last unit of
-// a batch row (an atomic per-row arrival count) runs that row's tail with all 512 threads:
+// Each call runs two kernels. The stream kernel cuts the call's logits into units (one warp's
+// share of one row: up to 32 lanes x 8 x 16-byte vectors = 4 KB of the row's 16-byte aligned
+// interior), reads every unit exactly once with coalesced, L1-bypassing 128-bit loads and
+// reduces it to one 8-byte partial: (max, sum of exp2((l - max) * log2(e)/T)) for softmax
+// statistics, or (max value, lowest index) for greedy argmax. The finishing kernel, a
+// programmatic dependent launch, combines the partials of each batch row and produces the
+// outputs:
 //
-//   chain, T > 0  acceptance test of every draft with one warp ballot, then the correction /
-//                 bonus draw as a block-wide prefix scan over the one target (and draft) row
-//                 the step stopped at, re-read from L2 right after it was streamed;
+//   chain, T > 0  acceptance of every draft with one warp ballot, then the correction / bonus
+//                 draw: an inverse CDF over max(0, p_n - q_n) (or p_gamma) as a prefix scan
+//                 over segment sums of the one target and draft row the step stopped at,
+//                 re-read from L2 and split over the CTAs of a thread-block cluster;
 //   chain, T = 0  argmax comparison of every draft token, then the greedy correction token;
 //   tree          accepted flags and depths of all nodes by pointer jumping, deepest node,
 //                 path and bonus token;
 //   probs         one write pass of the normalised probabilities of the row.
 //
-// No CTA ever waits for another: completion is detected with atomics, so any grid size is
-// safe. Partials written by other SMs are read with ld.global.cg (L2), never through L1.
+// No CTA ever waits for another CTA of its own grid except through the hardware cluster
+// barrier. Data written by other CTAs is read with ld.global.cg (L2), never through L1.
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -30,10 +32,11 @@ namespace specv {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kVPL = 8;                   // 16-byte vectors per lane in one unit
-constexpr int kUnitVecs = 32 * kVPL;      // vectors per unit (4 KB)
-constexpr int kSeg = 256;                 // residual segment: 32 lanes x 8 elements
-constexpr int kSegIter = 2;               // segments per warp per pass-A iteration
+constexpr int kVPL = 8;                     // 16-byte vectors per lane in one unit
+constexpr int kUnitVecs = 32 * kVPL;        // vectors per unit (4 KB)
+constexpr int kSeg = 256;                   // residual segment: 32 lanes x 8 elements
+constexpr int kWarpTailMaxV = 2048;         // rows this short get warp-level chain finishing
+constexpr int kMaxCluster = 8;              // CTAs per batch row in the chain finisher
 
 enum Mode : int { kChainSample = 0, kChainGreedy = 1, kTree = 2, kProbs = 3, kProbsGreedy = 4 };
 
@@ -48,14 +51,13 @@ struct Params {
   int32_t *path_nodes;       // tree: [B, N]
   float *out_probs;          // probs: [B, V]
   int32_t *status;
-  unsigned *ws_ctl;          // [0] next group to hand out, [1] CTAs finished
-  unsigned *ws_count;        // [B] units finished per batch row
   uint2 *ws_part;            // [B*R*C] one partial per unit
   float *ws_xlogit;          // [B*R] logit at the row's draft token (chain sampling)
-  long long units;           // B*R*C
-  long long groups;          // ceil(units / kWarps)
+  int units;                 // B*R*C (< 2^31, checked on the host)
+  int upb;                   // units per batch row, R*C
   int B, gamma, N, V;
   int Rt, Rd, R, C;          // rows per batch row: target, draft, total; units per row
+  int S;                     // chain sampling: CTAs per batch row (cluster size) when finishing
   float c2;                  // log2(e) / T
 };
 
@@ -71,16 +73,17 @@ template <> struct Elem<uint16_t> {   // bf16 bit patterns
   static constexpr uint32_t kNegInfWord = 0xff80ff80u;
 };
 
-// volatile: the load sits behind a bounds guard and must never be speculated past it
+// 128-bit streaming load that does not allocate in L1 (every logit is read once). volatile:
+// the load sits behind a bounds guard and must never be speculated past it.
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p));
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
   return r;
 }
 
-__device__ __forceinline__ uint4 ld_vec(const void *p) {   // L1-cached (tail re-reads)
+__device__ __forceinline__ uint4 ld_vec(const void *p) {   // L1-cached (re-reads)
   return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
@@ -158,14 +161,29 @@ __device__ __forceinline__ RowGeom row_geom(const E *row, int V) {
 }
 
 template <typename E>
-__device__ __forceinline__ const E *row_ptr(const Params &p, long long b, int r) {
+__device__ __forceinline__ const E *row_ptr(const Params &p, int b, int r) {
   if (r < p.Rt)
     return static_cast<const E *>(p.tgt) + (static_cast<long long>(b) * p.Rt + r) * p.V;
   return static_cast<const E *>(p.drf) + (static_cast<long long>(b) * p.Rd + (r - p.Rt)) * p.V;
 }
 
-// Loads one unit into registers: kVPL vectors per lane (out-of-row slots hold -inf), plus the
-// row's head/tail scalar for this lane when the unit is chunk 0 (else -inf).
+struct UnitId {
+  int b, r, chunk;
+};
+
+// unit -> (batch row, row, chunk), 32-bit unsigned division only
+__device__ __forceinline__ UnitId unit_id(const Params &p, int unit) {
+  UnitId u;
+  const unsigned uu = static_cast<unsigned>(unit);
+  u.b = static_cast<int>(uu / static_cast<unsigned>(p.upb));
+  const unsigned rem = uu - static_cast<unsigned>(u.b) * static_cast<unsigned>(p.upb);
+  u.r = static_cast<int>(rem / static_cast<unsigned>(p.C));
+  u.chunk = static_cast<int>(rem - static_cast<unsigned>(u.r) * static_cast<unsigned>(p.C));
+  return u;
+}
+
+// Loads one unit straight into registers: vectors j*32+lane of chunk `chunk` (-inf beyond the
+// row's interior), plus this lane's head/tail scalar when the unit is chunk 0.
 template <typename E>
 __device__ __forceinline__ void load_unit(const E *row, const RowGeom &g, int chunk, int lane,
                                           uint4 (&buf)[kVPL], float &ex_head, float &ex_tail) {
@@ -241,12 +259,9 @@ __device__ __forceinline__ void warp_stat_merge(float &m, float &s, float c2) {
 }
 
 template <typename E>
-__device__ __forceinline__ void unit_stats(const E *row, const RowGeom &g, int chunk, int lane,
+__device__ __forceinline__ void unit_stats(const uint4 (&buf)[kVPL], float eh, float et,
                                            float c2, float &m_out, float &s_out) {
   constexpr int kEPV = Elem<E>::kPerVec;
-  uint4 buf[kVPL];
-  float eh, et;
-  load_unit<E>(row, g, chunk, lane, buf, eh, et);
   const float m = unit_lane_max<E>(buf, eh, et);
   float s = 0.f;
   if (m != -INFINITY) {
@@ -279,31 +294,62 @@ __device__ __forceinline__ void arg_merge(float &v, int &i, float v2, int i2) {
   }
 }
 
-// Unit argmax: (value, lowest index) over the unit's elements; value NaN when the unit holds
-// NaN or +inf; value -inf (index INT_MAX) when it holds no element above -inf.
+// NaN-propagating maximum of one vector.
 template <typename E>
-__device__ __forceinline__ void unit_argmax(const E *row, const RowGeom &g, int chunk, int lane,
-                                            float &v_out, int &i_out) {
+__device__ __forceinline__ float vec_max(const uint4 &v) {
+  if constexpr (sizeof(E) == 2) {
+    const uint32_t w = bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w));
+    return fmax_nan(bf_lo(w), bf_hi(w));
+  } else {
+    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+}
+
+// Unit argmax: (value, lowest index) over the unit's elements; value NaN when the unit holds
+// NaN or +inf; value -inf (index INT_MAX) when it holds no element above -inf. Lanes holding
+// the warp maximum locate it through their per-vector maxima: first vector, then element.
+template <typename E>
+__device__ __forceinline__ void unit_argmax(const uint4 (&buf)[kVPL], float eh, float et,
+                                            const RowGeom &g, int chunk, int lane, float &v_out,
+                                            int &i_out) {
   constexpr int kEPV = Elem<E>::kPerVec;
-  uint4 buf[kVPL];
-  float eh, et;
-  load_unit<E>(row, g, chunk, lane, buf, eh, et);
-  float wm = unit_lane_max<E>(buf, eh, et);
+  float vm[kVPL];
+#pragma unroll
+  for (int j = 0; j < kVPL; ++j) vm[j] = vec_max<E>(buf[j]);
+  float lm = fmax_nan(eh, et);
+#pragma unroll
+  for (int j = 0; j < kVPL; ++j) lm = fmax_nan(lm, vm[j]);
+  float wm = lm;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) wm = fmax_nan(wm, __shfl_xor_sync(0xffffffffu, wm, off));
   int idx = 0x7fffffff;
   if (wm != wm || wm == INFINITY) {
     wm = __int_as_float(0x7fc00000);
   } else if (wm != -INFINITY) {
-    // smallest index in this lane holding wm: scan from the highest index down
-    if (et == wm) idx = g.h + g.nv * kEPV + lane;
-    const int v0 = chunk * kUnitVecs + lane;
+    if (lm == wm) {
+      if (eh == wm) {
+        idx = lane;                                   // head elements precede every vector
+      } else {
+        int js = kVPL;
 #pragma unroll
-    for (int j = kVPL - 1; j >= 0; --j)
+        for (int j = kVPL - 1; j >= 0; --j)
+          if (vm[j] == wm) js = j;
+        if (js < kVPL) {
+          uint4 t = buf[0];
 #pragma unroll
-      for (int e = kEPV - 1; e >= 0; --e)
-        if (vec_elem<E>(buf[j], e) == wm) idx = g.h + (v0 + j * 32) * kEPV + e;
-    if (eh == wm) idx = lane;
+          for (int j = 1; j < kVPL; ++j)
+            if (j == js) t = buf[j];
+          int e0 = kEPV - 1;
+#pragma unroll
+          for (int e = kEPV - 1; e >= 0; --e)
+            if (vec_elem<E>(t, e) == wm) e0 = e;
+          idx = g.h + (chunk * kUnitVecs + js * 32 + lane) * kEPV + e0;
+        } else {
+          idx = g.h + g.nv * kEPV + lane;             // the tail element
+        }
+      }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, off));
   }
@@ -344,7 +390,7 @@ __device__ __forceinline__ int block_max_int(int v, int *red) {
 // ------------------------------------------------------------------ residual / bonus draw
 
 // r(k) for the draw: max(0, p(k) - q(k)) when Q is given, else p(k); every operation rounded
-// explicitly so that pass A and pass C produce identical values.
+// explicitly so that every pass produces identical values.
 __device__ __forceinline__ float resid(float pt, float qd, bool hasq, float Mt, float iZt,
                                       float Md, float iZd, float c2) {
   const float p = __fmul_rn(ex2_shift(pt, Mt, c2), iZt);
@@ -353,69 +399,151 @@ __device__ __forceinline__ float resid(float pt, float qd, bool hasq, float Mt, 
   return fmaxf(__fsub_rn(p, q), 0.f);
 }
 
-// The 8 elements [k0, k0+8) of a row as fp32 (-inf beyond V).
+// The 8 elements [k0, k0+8) of a row, still encoded (bf16: w[0] holds 8 halves; fp32: w[0],
+// w[1] hold 4 words each); -inf beyond V.
 template <typename E>
-__device__ __forceinline__ void load8(const E *row, int k0, int V, bool vec_ok, float (&x)[8]) {
+__device__ __forceinline__ void load8_raw(const E *row, int k0, int V, bool vec_ok,
+                                          uint4 (&w)[2]) {
   if (vec_ok && k0 + 8 <= V) {
-    if constexpr (sizeof(E) == 2) {
-      const uint4 v = ld_vec(row + k0);
-      x[0] = bf_lo(v.x); x[1] = bf_hi(v.x); x[2] = bf_lo(v.y); x[3] = bf_hi(v.y);
-      x[4] = bf_lo(v.z); x[5] = bf_hi(v.z); x[6] = bf_lo(v.w); x[7] = bf_hi(v.w);
-    } else {
-      const uint4 a = ld_vec(row + k0);
-      const uint4 b = ld_vec(row + k0 + 4);
-      x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
-      x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
-      x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
-      x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
-    }
+    w[0] = ld_vec(row + k0);
+    if constexpr (sizeof(E) == 4) w[1] = ld_vec(row + k0 + 4);
   } else {
+    uint32_t h[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = (k0 + e < V) ? ld_elem<E>(row + k0 + e) : -INFINITY;
+    for (int e = 0; e < 8; ++e) {
+      if constexpr (sizeof(E) == 2)
+        h[e] = (k0 + e < V) ? static_cast<uint32_t>(__ldg(row + k0 + e)) : 0xff80u;
+      else
+        h[e] = (k0 + e < V) ? __float_as_uint(__ldg(row + k0 + e)) : 0xff800000u;
+    }
+    if constexpr (sizeof(E) == 2) {
+      w[0] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                        h[6] | (h[7] << 16));
+    } else {
+      w[0] = make_uint4(h[0], h[1], h[2], h[3]);
+      w[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
   }
 }
 
-// Inverse-CDF draw over r (see resid) with uniform u: the first k whose running sum strictly
-// exceeds u * S. Returns -1 when Q is given and S == 0 (the caller then retries without Q).
-// All threads of the CTA call it; the result is returned to every thread.
 template <typename E>
-__device__ int draw_token(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
-                          float c2, int V, float u, float *segsum, TailShared &sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool hasq = Q != nullptr;
-  const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) & 15u) == 0) &&
-                      (!hasq || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
-  const int nseg = (V + kSeg - 1) / kSeg;
+__device__ __forceinline__ float raw8_elem(const uint4 (&w)[2], int e) {
+  if constexpr (sizeof(E) == 2) return vec_elem<uint16_t>(w[0], e);
+  else return vec_elem<float>(e < 4 ? w[0] : w[1], e & 3);
+}
 
-  // pass A: per-segment sums of r (each warp takes kSegIter segments per iteration)
-  for (int s0 = warp * kSegIter; s0 < nseg; s0 += kWarps * kSegIter) {
-    float pt[kSegIter][8], qd[kSegIter][8];
+// Segment sum over this lane's 8 elements of segment `seg` (sequential), and the 8 values.
+template <typename E>
+__device__ __forceinline__ float lane_resid(const E *P, const E *Q, int seg, int lane, int V,
+                                            bool vec_ok, float Mt, float iZt, float Md,
+                                            float iZd, float c2, float (&r)[8]) {
+  const int k0 = seg * kSeg + lane * 8;
+  uint4 wp[2], wq[2];
+  load8_raw<E>(P, k0, V, vec_ok, wp);
+  if (Q) load8_raw<E>(Q, k0, V, vec_ok, wq);
+  float ls = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    r[e] = resid(raw8_elem<E>(wp, e), Q ? raw8_elem<E>(wq, e) : -INFINITY, Q != nullptr, Mt,
+                 iZt, Md, iZd, c2);
+    ls = __fadd_rn(ls, r[e]);
+  }
+  return ls;
+}
+
+// Within one segment whose exclusive prefix is `base`: the first element whose running sum
+// strictly exceeds t, or (mode 1 / no crossing) the last element with r > 0. One warp; the
+// token is returned to every lane.
+__device__ __forceinline__ int segment_pick(const float (&r)[8], float ls, int k0, float base,
+                                            float t, int mode, int lane) {
+  int lastpos = -1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (r[e] > 0.f) lastpos = k0 + e;
+  int tok = -1;
+  if (mode == 0) {
+    float li = ls;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, li, off);
+      if (lane >= off) li = __fadd_rn(li, y);
+    }
+    const float lup = __shfl_up_sync(0xffffffffu, li, 1);
+    const float lex = (lane == 0) ? base : __fadd_rn(base, lup);
+    const float lin = __fadd_rn(base, li);
+    const unsigned cross = __ballot_sync(0xffffffffu, lin > t);
+    if (cross) {
+      const int cl = __ffs(cross) - 1;
+      if (lane == cl) {
+        float acc = lex;
+        for (int e = 0; e < 8; ++e) {
+          const float nxt = __fadd_rn(acc, r[e]);
+          if (nxt > t) { tok = k0 + e; break; }
+          acc = nxt;
+        }
+        if (tok < 0) tok = lastpos;
+      }
+      tok = __shfl_sync(0xffffffffu, tok, cl);
+    }
+  }
+  if (tok < 0) {
+    const unsigned has = __ballot_sync(0xffffffffu, lastpos >= 0);
+    const int hl = has ? 31 - __clz(has) : 0;
+    tok = __shfl_sync(0xffffffffu, lastpos, hl);
+  }
+  return tok;
+}
+
+// Pass A of the CTA-wide draw: the sum of r over each segment in [lo, hi) (kSeg elements,
+// 8 per lane, sequential within a lane, then a fixed xor tree over the warp) into
+// out[seg - out_base]. Each warp takes kSegIter segments per iteration with all their loads
+// in flight together.
+template <typename E>
+__device__ void segment_sums(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
+                             float c2, int V, int lo, int hi, float *out, int out_base) {
+  constexpr int kSegIter = (sizeof(E) == 2) ? 4 : 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) & 15u) == 0) &&
+                      (!Q || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
+  for (int s0 = lo + warp * kSegIter; s0 < hi; s0 += kWarps * kSegIter) {
+    uint4 wp[kSegIter][2], wq[kSegIter][2];
 #pragma unroll
     for (int t = 0; t < kSegIter; ++t) {
-      const int k0 = (s0 + t) * kSeg + lane * 8;
-      load8<E>(P, k0, V, vec_ok, pt[t]);
-      if (hasq) load8<E>(Q, k0, V, vec_ok, qd[t]);
-      else
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qd[t][e] = -INFINITY;
+      const int k0 = (s0 + t < hi) ? (s0 + t) * kSeg + lane * 8 : V;
+      load8_raw<E>(P, k0, V, vec_ok, wp[t]);
+      if (Q) load8_raw<E>(Q, k0, V, vec_ok, wq[t]);
     }
 #pragma unroll
     for (int t = 0; t < kSegIter; ++t) {
       float ls = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ls = __fadd_rn(ls, resid(pt[t][e], qd[t][e], hasq, Mt, iZt, Md, iZd, c2));
+      for (int e = 0; e < 8; ++e)
+        ls = __fadd_rn(ls, resid(raw8_elem<E>(wp[t], e), Q ? raw8_elem<E>(wq[t], e) : -INFINITY,
+                                 Q != nullptr, Mt, iZt, Md, iZd, c2));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xffffffffu, ls, off));
-      if (lane == 0 && s0 + t < nseg) segsum[s0 + t] = ls;
+      if (lane == 0 && s0 + t < hi) out[s0 + t - out_base] = ls;
     }
   }
-  __syncthreads();
+}
 
-  // pass B: exclusive scan of the segment sums over the CTA (fixed association)
-  const int K = (nseg + kThreads - 1) / kThreads;
-  const int lo = threadIdx.x * K, hi = min(nseg, lo + K);
+// Passes B and C of the draw within one vocabulary slice [lo*kSeg, (lo+nl)*kSeg): segsum[0..nl)
+// holds the slice's segment sums (shared memory), `base` the running sum before the slice and
+// `t` the target u*S. An exclusive scan of the segment sums (fixed association) finds the
+// segment where the running sum first exceeds t; warp 0 rescans it. mode 0: that element (or,
+// if rounding leaves no crossing in the slice, the slice's last element with r > 0); mode 1:
+// the last element with r > 0. All threads call it; every thread gets the token.
+template <typename E>
+__device__ int pick_in_slice(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
+                             float c2, int V, const float *segsum, int nl, int lo, float base,
+                             float t, int mode, TailShared &sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) & 15u) == 0) &&
+                      (!Q || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
+  const int K = (nl + kThreads - 1) / kThreads;
+  const int tl = threadIdx.x * K, th = min(nl, tl + K);
   float local = 0.f;
-  for (int j = lo; j < hi; ++j) local = __fadd_rn(local, segsum[j]);
+  for (int j = tl; j < th; ++j) local = __fadd_rn(local, segsum[j]);
   float incl_w = local;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -425,164 +553,265 @@ __device__ int draw_token(const E *P, const E *Q, float Mt, float iZt, float Md,
   if (lane == 31) sh.warp_tot[warp] = incl_w;
   __syncthreads();
   if (threadIdx.x == 0) {
-    float o = 0.f;
-    sh.off[0] = 0.f;
+    float o = base;
+    sh.off[0] = base;
     for (int w = 0; w < kWarps; ++w) {
       o = __fadd_rn(o, sh.warp_tot[w]);
       sh.off[w + 1] = o;
     }
-    sh.total = o;
-    sh.target = __fmul_rn(u, o);
     sh.seg = -1;
-    sh.mode = 0;
+    sh.mode = mode;
+    sh.base = base;
   }
   __syncthreads();
-  const float S = sh.total;
-  if (hasq && S == 0.f) return -1;    // uniform across the CTA
-  const float t_target = sh.target;
-  const float up = __shfl_up_sync(0xffffffffu, incl_w, 1);
-  const float excl = (lane == 0) ? sh.off[warp] : __fadd_rn(sh.off[warp], up);
-  const float incl = __fadd_rn(sh.off[warp], incl_w);
-  if (lo < hi && excl <= t_target && t_target < incl) {
-    float acc = excl;
-    int found = -1, lastpos = -1;
-    float lastbase = excl;
-    for (int j = lo; j < hi; ++j) {
-      const float nxt = __fadd_rn(acc, segsum[j]);
-      if (segsum[j] > 0.f) { lastpos = j; lastbase = acc; }
-      if (nxt > t_target) { found = j; break; }
-      acc = nxt;
+  if (mode == 0) {
+    const float up = __shfl_up_sync(0xffffffffu, incl_w, 1);
+    const float excl = (lane == 0) ? sh.off[warp] : __fadd_rn(sh.off[warp], up);
+    const float incl = __fadd_rn(sh.off[warp], incl_w);
+    if (tl < th && excl <= t && t < incl) {
+      float acc = excl;
+      int found = -1, lastpos = -1;
+      float lastbase = excl;
+      for (int j = tl; j < th; ++j) {
+        const float nxt = __fadd_rn(acc, segsum[j]);
+        if (segsum[j] > 0.f) { lastpos = j; lastbase = acc; }
+        if (nxt > t) { found = j; break; }
+        acc = nxt;
+      }
+      if (found >= 0) { sh.seg = found; sh.base = acc; sh.mode = 0; }
+      else { sh.seg = lastpos; sh.base = lastbase; sh.mode = 1; }
     }
-    if (found >= 0) { sh.seg = found; sh.base = acc; sh.mode = 0; }
-    else { sh.seg = lastpos; sh.base = lastbase; sh.mode = 1; }
   }
   __syncthreads();
   if (sh.seg < 0) {
-    // t_target >= S after rounding: the last segment holding mass, its last positive element
     int last = -1;
-    for (int j = lo; j < hi; ++j)
+    for (int j = tl; j < th; ++j)
       if (segsum[j] > 0.f) last = j;
     last = block_max_int(last, sh.red_i);
-    if (threadIdx.x == 0) { sh.seg = last; sh.mode = 1; sh.base = 0.f; }
+    if (threadIdx.x == 0) { sh.seg = last; sh.mode = 1; }
     __syncthreads();
   }
-
-  // pass C: warp 0 rescans the chosen segment
   if (warp == 0) {
-    const int seg = max(sh.seg, 0);   // sh.seg >= 0 whenever S > 0; never index before the row
-    const int k0 = seg * kSeg + lane * 8;
-    float pt[8], qd[8], r[8];
-    load8<E>(P, k0, V, vec_ok, pt);
-    if (hasq) load8<E>(Q, k0, V, vec_ok, qd);
-    else
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qd[e] = -INFINITY;
-    float ls = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      r[e] = resid(pt[e], qd[e], hasq, Mt, iZt, Md, iZd, c2);
-      ls = __fadd_rn(ls, r[e]);
-    }
-    int lastpos = -1;
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (r[e] > 0.f) lastpos = k0 + e;
-    int tok = -1;
-    if (sh.mode == 0) {
-      float li = ls;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, li, off);
-        if (lane >= off) li = __fadd_rn(li, y);
-      }
-      const float lup = __shfl_up_sync(0xffffffffu, li, 1);
-      const float lex = (lane == 0) ? sh.base : __fadd_rn(sh.base, lup);
-      const float lin = __fadd_rn(sh.base, li);
-      const unsigned cross = __ballot_sync(0xffffffffu, lin > t_target);
-      if (cross) {
-        const int cl = __ffs(cross) - 1;
-        if (lane == cl) {
-          float acc = lex;
-          for (int e = 0; e < 8; ++e) {
-            const float nxt = __fadd_rn(acc, r[e]);
-            if (nxt > t_target) { tok = k0 + e; break; }
-            acc = nxt;
-          }
-          if (tok < 0) tok = lastpos;
-        }
-        tok = __shfl_sync(0xffffffffu, tok, cl);
-      }
-    }
-    if (tok < 0) {
-      const unsigned has = __ballot_sync(0xffffffffu, lastpos >= 0);
-      const int hl = has ? 31 - __clz(has) : 0;
-      tok = __shfl_sync(0xffffffffu, lastpos, hl);
-      if (tok < 0) tok = V - 1;   // unreachable when S > 0
-    }
+    const int seg = lo + max(sh.seg, 0);   // never index before the slice
+    float r[8];
+    const float ls = lane_resid<E>(P, Q, seg, lane, V, vec_ok, Mt, iZt, Md, iZd, c2, r);
+    int tok = segment_pick(r, ls, seg * kSeg + lane * 8, sh.base, t, sh.mode, lane);
+    if (tok < 0) tok = V - 1;   // unreachable when the slice holds mass
     if (lane == 0) sh.token = tok;
   }
   __syncthreads();
   return sh.token;
 }
 
-// ------------------------------------------------------------------ tails
-
+// CTA-wide inverse-CDF draw over the whole row: the first k whose running sum strictly exceeds
+// u * S. Returns -1 when Q is given and S == 0. segsum: shared memory, ceil(V/kSeg) floats.
 template <typename E>
-__device__ void fail_chain_row(const Params &p, int b) {
-  const int g1 = p.gamma + 1;
-  for (int j = threadIdx.x; j < g1; j += kThreads) p.out_tokens[(long long)b * g1 + j] = -1;
-  if (threadIdx.x == 0) p.accept_len[b] = -1;
-}
-
-template <typename E>
-__device__ void tail_chain_sample(const Params &p, int b, float *smem, TailShared &sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int R = p.R, gamma = p.gamma;
-  float *rowM = smem;
-  float *rowZ = smem + R;
-  float *segsum = smem + 2 * R;
-  const float c2 = p.c2;
-
-  // combine the unit partials of every row of this step
-  for (int r = warp; r < R; r += kWarps) {
-    const uint2 *part = p.ws_part + (static_cast<long long>(b) * R + r) * p.C;
-    float m = -INFINITY, s = 0.f;
-    for (int c = lane; c < p.C; c += 32) {
-      const uint2 v = ldcg_u2(part + c);
-      stat_merge(m, s, __uint_as_float(v.x), __uint_as_float(v.y), c2);
-    }
-    warp_stat_merge(m, s, c2);
-    if (lane == 0) { rowM[r] = m; rowZ[r] = s; }
+__device__ int draw_token_cta(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
+                              float c2, int V, float u, float *segsum, TailShared &sh) {
+  const int nseg = (V + kSeg - 1) / kSeg;
+  segment_sums<E>(P, Q, Mt, iZt, Md, iZd, c2, V, 0, nseg, segsum, 0);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int j = 0; j < nseg; ++j) tot = __fadd_rn(tot, segsum[j]);
+    sh.total = tot;
   }
   __syncthreads();
+  const float S = sh.total;
+  if (Q && S == 0.f) return -1;
+  const float t = __fmul_rn(u, S);
+  // t >= S after rounding leaves no crossing: pick_in_slice then takes the last r > 0
+  return pick_in_slice<E>(P, Q, Mt, iZt, Md, iZd, c2, V, segsum, nseg, 0, 0.f, t,
+                          t < S ? 0 : 1, sh);
+}
 
-  // acceptance: one lane per draft position, first rejection by ballot
+// Warp-wide draw for rows of at most kWarpTailMaxV elements (<= 8 segments).
+template <typename E>
+__device__ int draw_token_warp(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
+                               float c2, int V, float u) {
+  constexpr int kMaxSeg = kWarpTailMaxV / kSeg;
+  const int lane = threadIdx.x & 31;
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) & 15u) == 0) &&
+                      (!Q || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
+  const int nseg = (V + kSeg - 1) / kSeg;
+  float ss[kMaxSeg];
+#pragma unroll
+  for (int s = 0; s < kMaxSeg; ++s) {
+    ss[s] = 0.f;
+    if (s < nseg) {
+      float r[8];
+      float ls = lane_resid<E>(P, Q, s, lane, V, vec_ok, Mt, iZt, Md, iZd, c2, r);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xffffffffu, ls, off));
+      ss[s] = ls;
+    }
+  }
+  float S = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMaxSeg; ++s) S = __fadd_rn(S, ss[s]);
+  if (Q && S == 0.f) return -1;
+  const float t = __fmul_rn(u, S);
+  int seg = -1, mode = 0, lastseg = -1;
+  float base = 0.f, acc = 0.f, lastbase = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMaxSeg; ++s) {
+    if (seg < 0 && s < nseg) {
+      const float nxt = __fadd_rn(acc, ss[s]);
+      if (ss[s] > 0.f) { lastseg = s; lastbase = acc; }
+      if (nxt > t) { seg = s; base = acc; }
+      acc = nxt;
+    }
+  }
+  if (seg < 0) { seg = max(lastseg, 0); base = lastbase; mode = 1; }
+  float r[8];
+  const float ls = lane_resid<E>(P, Q, seg, lane, V, vec_ok, Mt, iZt, Md, iZd, c2, r);
+  const int tok = segment_pick(r, ls, seg * kSeg + lane * 8, base, t, mode, lane);
+  return tok < 0 ? V - 1 : tok;
+}
+
+// ------------------------------------------------------------------ finishing helpers
+
+__device__ __forceinline__ void fail_chain_row(const Params &p, int b, int tid, int nthreads) {
+  const int g1 = p.gamma + 1;
+  for (int j = tid; j < g1; j += nthreads) p.out_tokens[static_cast<long long>(b) * g1 + j] = -1;
+  if (tid == 0) p.accept_len[b] = -1;
+}
+
+// the acceptance test u <= p_i(x_i)/q_i(x_i), with
+// p_i(x_i)/q_i(x_i) = 2^(((lt - ld) + (Md - Mt)) * c2) * Zd / Zt
+__device__ __forceinline__ bool rejects(float u, float lt, float ld, float Mt, float Zt, float Md,
+                                        float Zd, float c2) {
+  const float d = __fadd_rn(__fsub_rn(lt, ld), __fsub_rn(Md, Mt));
+  const float ratio = __fmul_rn(ex2(__fmul_rn(d, c2)), __fdiv_rn(Zd, Zt));
+  return !(u <= ratio);
+}
+
+__device__ __forceinline__ bool stats_ok(float m, float z) {
+  return isfinite(m) && isfinite(z) && z > 0.f;
+}
+
+// argmax of a row is usable when it is finite (no NaN/+inf seen, some element above -inf)
+__device__ __forceinline__ bool arg_ok(float v) { return v == v && v != -INFINITY; }
+
+// Combines the unit partials of rows r = warp, warp + kWarps, ... of batch row b into per-row
+// statistics. The loads for four rows per warp (two partials per lane each) are issued before
+// any is combined, so this costs one round trip when C <= 64.
+__device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float *rowM,
+                                                   float *rowZ) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint2 *base = p.ws_part + static_cast<long long>(b) * p.R * p.C;
+  for (int r0 = warp; r0 < p.R; r0 += 4 * kWarps) {
+    uint2 v[4][2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + q * kWarps;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int c = lane + 32 * t;
+        v[q][t] = (r < p.R && c < p.C) ? ldcg_u2(base + static_cast<long long>(r) * p.C + c)
+                                       : make_uint2(0xff800000u, 0u);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + q * kWarps;
+      if (r < p.R) {
+        float m = -INFINITY, s = 0.f;
+        stat_merge(m, s, __uint_as_float(v[q][0].x), __uint_as_float(v[q][0].y), p.c2);
+        stat_merge(m, s, __uint_as_float(v[q][1].x), __uint_as_float(v[q][1].y), p.c2);
+        for (int c = lane + 64; c < p.C; c += 32) {
+          const uint2 w = ldcg_u2(base + static_cast<long long>(r) * p.C + c);
+          stat_merge(m, s, __uint_as_float(w.x), __uint_as_float(w.y), p.c2);
+        }
+        warp_stat_merge(m, s, p.c2);
+        if (lane == 0) { rowM[r] = m; rowZ[r] = s; }
+      }
+    }
+  }
+}
+
+// Same for greedy argmax partials: g[r] = lowest index of the row maximum, ok[r] = the row is
+// usable (finite maximum, no NaN / +inf seen).
+__device__ __forceinline__ void combine_rows_arg(const Params &p, int b, int *g, int *ok) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint2 *base = p.ws_part + static_cast<long long>(b) * p.R * p.C;
+  for (int r0 = warp; r0 < p.R; r0 += 4 * kWarps) {
+    uint2 v[4][2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + q * kWarps;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int c = lane + 32 * t;
+        v[q][t] = (r < p.R && c < p.C) ? ldcg_u2(base + static_cast<long long>(r) * p.C + c)
+                                       : make_uint2(0xff800000u, 0x7fffffffu);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = r0 + q * kWarps;
+      if (r < p.R) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        arg_merge(bv, bi, __uint_as_float(v[q][0].x), static_cast<int>(v[q][0].y));
+        arg_merge(bv, bi, __uint_as_float(v[q][1].x), static_cast<int>(v[q][1].y));
+        for (int c = lane + 64; c < p.C; c += 32) {
+          const uint2 w = ldcg_u2(base + static_cast<long long>(r) * p.C + c);
+          arg_merge(bv, bi, __uint_as_float(w.x), static_cast<int>(w.y));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
+          const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
+          arg_merge(bv, bi, v2, i2);
+        }
+        if (lane == 0) { g[r] = bi; ok[r] = arg_ok(bv) ? 1 : 0; }
+      }
+    }
+  }
+}
+
+// Chain sampling, whole CTA: combines the statistics of every row of batch row b (rowM/rowZ in
+// shared memory), copies the drafts to xs (shared memory) and runs the acceptance test of every
+// draft with one warp ballot per 32 positions. Returns 0 with *n = the number of accepted
+// drafts (on every thread), or a device error code (a non-finite row, a token outside [0, V)).
+__device__ inline int chain_accept(const Params &p, int b, float *rowM, float *rowZ, int *xs,
+                                   TailShared &sh, int *n_out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int R = p.R, gamma = p.gamma;
+  const float c2 = p.c2;
+  const float *ub = p.uniforms + static_cast<long long>(b) * (gamma + 1);
+  const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
+  const float *xl = p.ws_xlogit + static_cast<long long>(b) * R;
+  // one round trip: warp 0 fetches the first 32 positions' inputs, every thread a share of the
+  // drafts, every warp the unit partials of its rows
+  float ui = 0.f, lti = 0.f, ldi = 0.f;
+  if (warp == 0 && lane < gamma) {
+    ui = ub[lane];
+    lti = ldcg_f(xl + lane);
+    ldi = ldcg_f(xl + gamma + 1 + lane);
+  }
+  for (int i = threadIdx.x; i < gamma; i += kThreads) xs[i] = x[i];
+  combine_rows_stats(p, b, rowM, rowZ);
+  __syncthreads();
   if (warp == 0) {
     int err = 0;
-    for (int r = lane; r < R; r += 32) {
-      const float m = rowM[r], z = rowZ[r];
-      if (!(isfinite(m) && isfinite(z) && z > 0.f)) err = SPEC_ERR_NONFINITE;
-    }
-    const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
+    for (int r = lane; r < R; r += 32)
+      if (!stats_ok(rowM[r], rowZ[r])) err = SPEC_ERR_NONFINITE;
     for (int i = lane; i < gamma; i += 32)
-      if (x[i] < 0 || x[i] >= p.V) err = err ? err : SPEC_ERR_TOKEN;
+      if (xs[i] < 0 || xs[i] >= p.V) err = err ? err : SPEC_ERR_TOKEN;
     const unsigned any_err = __ballot_sync(0xffffffffu, err != 0);
     int n = gamma;
     if (any_err) {
       err = __shfl_sync(0xffffffffu, err, __ffs(any_err) - 1);
     } else {
-      const float *u = p.uniforms + static_cast<long long>(b) * (gamma + 1);
-      const float *xl = p.ws_xlogit + static_cast<long long>(b) * R;
       for (int i0 = 0; i0 < gamma; i0 += 32) {
         const int i = i0 + lane;
         bool rej = false;
         if (i < gamma) {
+          if (i0 > 0) { ui = ub[i]; lti = ldcg_f(xl + i); ldi = ldcg_f(xl + gamma + 1 + i); }
           const int rd = gamma + 1 + i;
-          const float lt = ldcg_f(xl + i), ld = ldcg_f(xl + rd);
-          // p_i(x)/q_i(x) = 2^(((lt - ld) + (Md - Mt)) * c2) * Zd / Zt
-          const float d = __fadd_rn(__fsub_rn(lt, ld), __fsub_rn(rowM[rd], rowM[i]));
-          const float ratio = __fmul_rn(ex2(__fmul_rn(d, c2)), __fdiv_rn(rowZ[rd], rowZ[i]));
-          rej = !(u[i] <= ratio);
+          rej = rejects(ui, lti, ldi, rowM[i], rowZ[i], rowM[rd], rowZ[rd], c2);
         }
         const unsigned rb = __ballot_sync(0xffffffffu, rej);
         if (rb) { n = i0 + __ffs(rb) - 1; break; }
@@ -591,71 +820,88 @@ __device__ void tail_chain_sample(const Params &p, int b, float *smem, TailShare
     if (lane == 0) { sh.n = n; sh.err = err; }
   }
   __syncthreads();
-  if (sh.err) {
-    if (threadIdx.x == 0) set_status(p.status, sh.err);
-    fail_chain_row<E>(p, b);
+  *n_out = sh.n;
+  return sh.err;
+}
+
+// out_tokens[b] = x_0..x_{n-1}, tok, then -1; accept_len[b] = n. x: the step's drafts.
+__device__ __forceinline__ void emit_chain(const Params &p, int b, int n, int tok, const int *x,
+                                           int tid, int nthreads) {
+  const int g1 = p.gamma + 1;
+  int32_t *o = p.out_tokens + static_cast<long long>(b) * g1;
+  for (int j = tid; j < g1; j += nthreads) o[j] = (j < n) ? x[j] : (j == n ? tok : -1);
+  if (tid == 0) p.accept_len[b] = n;
+}
+
+// Chain sampling, one warp, for steps whose rows are single units (gamma <= 31, V <=
+// kWarpTailMaxV): lane i holds the statistics of rows i and i + 32 (m0/z0, m1/z1) and the
+// logits at draft token x_i of target row i (lti) and draft row i (ldi).
+template <typename E>
+__device__ void tail_chain_sample_regs(const Params &p, int b, float m0, float z0, float m1,
+                                       float z1, float lti, float ldi) {
+  const int lane = threadIdx.x & 31;
+  const int R = p.R, gamma = p.gamma;
+  const float c2 = p.c2;
+  const float *ub = p.uniforms + static_cast<long long>(b) * (gamma + 1);
+  const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
+  int xi = 0;
+  float ui = 0.f;
+  if (lane < gamma) {
+    xi = x[lane];
+    ui = ub[lane];
+  }
+  const float u = ub[gamma];
+  int err = 0;
+  if ((lane < R && !stats_ok(m0, z0)) || (lane + 32 < R && !stats_ok(m1, z1)))
+    err = SPEC_ERR_NONFINITE;
+  if (lane < gamma && (xi < 0 || xi >= p.V)) err = err ? err : SPEC_ERR_TOKEN;
+  const unsigned any_err = __ballot_sync(0xffffffffu, err != 0);
+  if (any_err) {
+    err = __shfl_sync(0xffffffffu, err, __ffs(any_err) - 1);
+    if (lane == 0) set_status(p.status, err);
+    fail_chain_row(p, b, lane, 32);
     return;
   }
-  const int n = sh.n;
+  // statistics of draft row gamma+1+lane (held by lane gamma+1+lane, or lane gamma+1+lane-32)
+  const int rd = gamma + 1 + lane;
+  const float dmA = __shfl_sync(0xffffffffu, m0, rd & 31);
+  const float dzA = __shfl_sync(0xffffffffu, z0, rd & 31);
+  const float dmB = __shfl_sync(0xffffffffu, m1, rd & 31);
+  const float dzB = __shfl_sync(0xffffffffu, z1, rd & 31);
+  const float Md_i = rd < 32 ? dmA : dmB, Zd_i = rd < 32 ? dzA : dzB;
+  const bool rej = lane < gamma && rejects(ui, lti, ldi, m0, z0, Md_i, Zd_i, c2);
+  const unsigned rb = __ballot_sync(0xffffffffu, rej);
+  const int n = rb ? __ffs(rb) - 1 : gamma;
+  const float Mt = __shfl_sync(0xffffffffu, m0, n);
+  const float Zt = __shfl_sync(0xffffffffu, z0, n);
+  const int rn = gamma + 1 + n;
+  const float mA = __shfl_sync(0xffffffffu, m0, rn & 31), zA = __shfl_sync(0xffffffffu, z0, rn & 31);
+  const float mB = __shfl_sync(0xffffffffu, m1, rn & 31), zB = __shfl_sync(0xffffffffu, z1, rn & 31);
+  const float Md = rn < 32 ? mA : mB, Zd = rn < 32 ? zA : zB;
   const E *P = row_ptr<E>(p, b, n);
-  const E *Q = (n < gamma) ? row_ptr<E>(p, b, gamma + 1 + n) : nullptr;
-  const float Mt = rowM[n], iZt = __frcp_rn(rowZ[n]);
-  const float Md = Q ? rowM[gamma + 1 + n] : 0.f, iZd = Q ? __frcp_rn(rowZ[gamma + 1 + n]) : 0.f;
-  const float u = p.uniforms[static_cast<long long>(b) * (gamma + 1) + gamma];
-  int tok = draw_token<E>(P, Q, Mt, iZt, Md, iZd, c2, p.V, u, segsum, sh);
-  if (tok < 0) tok = draw_token<E>(P, nullptr, Mt, iZt, 0.f, 0.f, c2, p.V, u, segsum, sh);
-
-  const int g1 = gamma + 1;
-  int32_t *o = p.out_tokens + static_cast<long long>(b) * g1;
-  const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
-  for (int j = threadIdx.x; j < g1; j += kThreads) o[j] = (j < n) ? x[j] : (j == n ? tok : -1);
-  if (threadIdx.x == 0) p.accept_len[b] = n;
+  const E *Q = (n < gamma) ? row_ptr<E>(p, b, rn) : nullptr;
+  const float iZt = __frcp_rn(Zt), iZd = Q ? __frcp_rn(Zd) : 0.f;
+  int tok = draw_token_warp<E>(P, Q, Mt, iZt, Q ? Md : 0.f, iZd, c2, p.V, u);
+  if (tok < 0) tok = draw_token_warp<E>(P, nullptr, Mt, iZt, 0.f, 0.f, c2, p.V, u);
+  emit_chain(p, b, n, tok, x, lane, 32);
 }
 
-// combine argmax partials of row (b, r) with one warp; returns (value, index) on all lanes
-__device__ __forceinline__ void warp_row_argmax(const Params &p, long long b, int r, float &v,
-                                                int &i) {
-  const int lane = threadIdx.x & 31;
-  const uint2 *part = p.ws_part + (b * p.R + r) * p.C;
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  for (int c = lane; c < p.C; c += 32) {
-    const uint2 w = ldcg_u2(part + c);
-    arg_merge(bv, bi, __uint_as_float(w.x), static_cast<int>(w.y));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
-    const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
-    arg_merge(bv, bi, v2, i2);
-  }
-  v = bv;
-  i = bi;
-}
-
-// argmax of a row is usable when it is finite (no NaN/+inf seen, some element above -inf)
-__device__ __forceinline__ bool arg_ok(float v) { return v == v && v != -INFINITY; }
-
-template <typename E>
-__device__ void tail_chain_greedy(const Params &p, int b, float *smem, TailShared &sh) {
+__device__ inline void tail_chain_greedy(const Params &p, int b, float *smem, TailShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = p.R, gamma = p.gamma;
   int *g = reinterpret_cast<int *>(smem);
   int *gok = g + R;
-  for (int r = warp; r < R; r += kWarps) {
-    float v;
-    int i;
-    warp_row_argmax(p, b, r, v, i);
-    if (lane == 0) { g[r] = i; gok[r] = arg_ok(v); }
-  }
+  int *xs = gok + R;
+  const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
+  for (int i = threadIdx.x; i < gamma; i += kThreads) xs[i] = x[i];
+  combine_rows_arg(p, b, g, gok);
   __syncthreads();
   if (warp == 0) {
     int err = 0;
     for (int r = lane; r < R; r += 32)
       if (!gok[r]) err = SPEC_ERR_NONFINITE;
-    const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
     for (int i = lane; i < gamma; i += 32)
-      if (x[i] < 0 || x[i] >= p.V) err = err ? err : SPEC_ERR_TOKEN;
+      if (xs[i] < 0 || xs[i] >= p.V) err = err ? err : SPEC_ERR_TOKEN;
     const unsigned any_err = __ballot_sync(0xffffffffu, err != 0);
     int n = gamma;
     if (any_err) {
@@ -663,7 +909,7 @@ __device__ void tail_chain_greedy(const Params &p, int b, float *smem, TailShare
     } else {
       for (int i0 = 0; i0 < gamma; i0 += 32) {
         const int i = i0 + lane;
-        const bool rej = (i < gamma) && (x[i] != g[i]);
+        const bool rej = (i < gamma) && (xs[i] != g[i]);
         const unsigned rb = __ballot_sync(0xffffffffu, rej);
         if (rb) { n = i0 + __ffs(rb) - 1; break; }
       }
@@ -673,43 +919,32 @@ __device__ void tail_chain_greedy(const Params &p, int b, float *smem, TailShare
   __syncthreads();
   if (sh.err) {
     if (threadIdx.x == 0) set_status(p.status, sh.err);
-    fail_chain_row<E>(p, b);
+    fail_chain_row(p, b, threadIdx.x, kThreads);
     return;
   }
-  const int n = sh.n, g1 = gamma + 1;
-  int32_t *o = p.out_tokens + static_cast<long long>(b) * g1;
-  const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
-  for (int j = threadIdx.x; j < g1; j += kThreads) o[j] = (j < n) ? x[j] : (j == n ? g[n] : -1);
-  if (threadIdx.x == 0) p.accept_len[b] = n;
+  emit_chain(p, b, sh.n, g[sh.n], xs, threadIdx.x, kThreads);
 }
 
-template <typename E>
-__device__ void tail_tree(const Params &p, int b, float *smem, TailShared &sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared &sh) {
   const int N = p.N;
   int *g = reinterpret_cast<int *>(smem);
   int *par = g + N;
   int *tok = par + N;
-  int *anc = tok + N;      // [2][N]
-  int *acc = anc + 2 * N;  // [2][N]
-  int *dep = acc + 2 * N;  // [2][N]
+  int *anc = tok + N;
+  int *acc = anc + N;
+  int *dep = acc + N;
   const long long bN = static_cast<long long>(b) * N;
   if (threadIdx.x == 0) sh.err = 0;
-  __syncthreads();
-  for (int r = warp; r < N; r += kWarps) {
-    float v;
-    int i;
-    warp_row_argmax(p, b, r, v, i);
-    if (lane == 0) {
-      g[r] = i;
-      if (!arg_ok(v)) atomicCAS(&sh.err, 0, SPEC_ERR_NONFINITE);
-    }
-  }
+  // one round trip: parents and tokens, and the argmax partials of every node
   for (int j = threadIdx.x; j < N; j += kThreads) {
-    const int pj = p.parents[bN + j];
-    const int tj = (j == 0) ? 0 : p.tokens[bN + j];
-    par[j] = pj;
-    tok[j] = tj;
+    par[j] = p.parents[bN + j];
+    tok[j] = (j == 0) ? 0 : p.tokens[bN + j];
+  }
+  combine_rows_arg(p, b, g, anc);   // anc[] holds the row-usable flags until reused below
+  __syncthreads();
+  for (int j = threadIdx.x; j < N; j += kThreads) {
+    if (!anc[j]) atomicCAS(&sh.err, 0, SPEC_ERR_NONFINITE);
+    const int pj = par[j], tj = tok[j];
     if (j == 0 ? (pj != -1) : (pj < 0 || pj >= j)) atomicCAS(&sh.err, 0, SPEC_ERR_PARENT);
     else if (j > 0 && (tj < 0 || tj >= p.V)) atomicCAS(&sh.err, 0, SPEC_ERR_TOKEN);
   }
@@ -729,22 +964,31 @@ __device__ void tail_tree(const Params &p, int b, float *smem, TailShared &sh) {
     dep[j] = (j == 0) ? 0 : 1;
   }
   __syncthreads();
-  int cur = 0;
+  constexpr int kPer = (SPEC_MAX_NODES + kThreads - 1) / kThreads;
   for (int span = 1; span < N; span <<= 1) {
-    const int nxt = cur ^ 1;
-    for (int j = threadIdx.x; j < N; j += kThreads) {
-      const int a = anc[cur * N + j];
-      anc[nxt * N + j] = anc[cur * N + a];
-      acc[nxt * N + j] = acc[cur * N + j] & acc[cur * N + a];
-      dep[nxt * N + j] = dep[cur * N + j] + dep[cur * N + a];
+    int na[kPer], nc[kPer], nd[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int j = threadIdx.x + q * kThreads;
+      if (j < N) {
+        const int a = anc[j];
+        na[q] = anc[a];
+        nc[q] = acc[j] & acc[a];
+        nd[q] = dep[j] + dep[a];
+      }
     }
     __syncthreads();
-    cur = nxt;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int j = threadIdx.x + q * kThreads;
+      if (j < N) { anc[j] = na[q]; acc[j] = nc[q]; dep[j] = nd[q]; }
+    }
+    __syncthreads();
   }
   // deepest accepted node, smallest index among equals
   int key = -1;
   for (int j = threadIdx.x; j < N; j += kThreads)
-    if (acc[cur * N + j]) key = max(key, (dep[cur * N + j] << 11) | (2047 - j));
+    if (acc[j]) key = max(key, (dep[j] << 11) | (2047 - j));
   key = block_max_int(key, sh.red_i);
   const int best = 2047 - (key & 2047);
   const int D = key >> 11;
@@ -766,18 +1010,27 @@ __device__ void tail_tree(const Params &p, int b, float *smem, TailShared &sh) {
 
 // probabilities of one row (b = row index): one write pass
 template <typename E, bool kGreedy>
-__device__ void tail_probs(const Params &p, int b, float *smem, TailShared &sh) {
+__device__ void tail_probs(const Params &p, int b, TailShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int V = p.V;
   const float c2 = p.c2;
   if (warp == 0) {
+    const uint2 *part = p.ws_part + static_cast<long long>(b) * p.C;
     if (kGreedy) {
-      float v;
-      int i;
-      warp_row_argmax(p, b, 0, v, i);
-      if (lane == 0) { sh.err = arg_ok(v) ? 0 : SPEC_ERR_NONFINITE; sh.token = i; }
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int c = lane; c < p.C; c += 32) {
+        const uint2 w = ldcg_u2(part + c);
+        arg_merge(bv, bi, __uint_as_float(w.x), static_cast<int>(w.y));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
+        arg_merge(bv, bi, v2, i2);
+      }
+      if (lane == 0) { sh.err = arg_ok(bv) ? 0 : SPEC_ERR_NONFINITE; sh.token = bi; }
     } else {
-      const uint2 *part = p.ws_part + static_cast<long long>(b) * p.C;
       float m = -INFINITY, s = 0.f;
       for (int c = lane; c < p.C; c += 32) {
         const uint2 v = ldcg_u2(part + c);
@@ -785,7 +1038,7 @@ __device__ void tail_probs(const Params &p, int b, float *smem, TailShared &sh) 
       }
       warp_stat_merge(m, s, c2);
       if (lane == 0) {
-        sh.err = (isfinite(m) && isfinite(s) && s > 0.f) ? 0 : SPEC_ERR_NONFINITE;
+        sh.err = stats_ok(m, s) ? 0 : SPEC_ERR_NONFINITE;
         sh.base = m;
         sh.total = s;
       }
@@ -798,109 +1051,256 @@ __device__ void tail_probs(const Params &p, int b, float *smem, TailShared &sh) 
   float *out = p.out_probs + static_cast<long long>(b) * V;
   const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(b) * V;
   if (err && threadIdx.x == 0) set_status(p.status, err);
+  auto val = [&](float l) -> float { return __fmul_rn(ex2_shift(l, M, c2), iZ); };
+  const bool vec = !err && !kGreedy && ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) &&
+                   ((reinterpret_cast<uintptr_t>(out) & 15u) == 0);
+  if (vec) {
+    // 8 elements per thread and step (one or two 16-byte loads, two 16-byte stores), with the
+    // loads of kPV steps in flight together
+    constexpr int kPV = 4;
+    const int n8 = V / 8;
+    for (int q0 = threadIdx.x; q0 < n8; q0 += kPV * kThreads) {
+      uint4 w[kPV][2];
+#pragma unroll
+      for (int t = 0; t < kPV; ++t) {
+        const int q = q0 + t * kThreads;
+        if (q < n8) {
+          w[t][0] = ld_vec(row + 8 * q);
+          if constexpr (sizeof(E) == 4) w[t][1] = ld_vec(row + 8 * q + 4);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kPV; ++t) {
+        const int q = q0 + t * kThreads;
+        if (q < n8) {
+          float4 *o4 = reinterpret_cast<float4 *>(out + 8 * q);
+          o4[0] = make_float4(val(raw8_elem<E>(w[t], 0)), val(raw8_elem<E>(w[t], 1)),
+                              val(raw8_elem<E>(w[t], 2)), val(raw8_elem<E>(w[t], 3)));
+          o4[1] = make_float4(val(raw8_elem<E>(w[t], 4)), val(raw8_elem<E>(w[t], 5)),
+                              val(raw8_elem<E>(w[t], 6)), val(raw8_elem<E>(w[t], 7)));
+        }
+      }
+    }
+    for (int k = 8 * n8 + threadIdx.x; k < V; k += kThreads) out[k] = val(ld_elem<E>(row + k));
+    return;
+  }
+  auto sval = [&](int k) -> float {
+    if (err) return __int_as_float(0x7fc00000);
+    if (kGreedy) return (k == g) ? 1.f : 0.f;
+    return val(ld_elem<E>(row + k));
+  };
   // 4-element groups aligned to 16 bytes of the output row
   const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(out) >> 2) & 3u);
   const int h = min(V, (4 - mis) & 3);
   const int ng = (V - h) / 4;
-  auto val = [&](int k) -> float {
-    if (err) return __int_as_float(0x7fc00000);
-    if (kGreedy) return (k == g) ? 1.f : 0.f;
-    return __fmul_rn(ex2_shift(ld_elem<E>(row + k), M, c2), iZ);
-  };
-  for (int k = threadIdx.x; k < h; k += kThreads) out[k] = val(k);
+  for (int k = threadIdx.x; k < h; k += kThreads) out[k] = sval(k);
   float4 *o4 = reinterpret_cast<float4 *>(out + h);
   for (int q = threadIdx.x; q < ng; q += kThreads) {
     const int k = h + 4 * q;
-    o4[q] = make_float4(val(k), val(k + 1), val(k + 2), val(k + 3));
+    o4[q] = make_float4(sval(k), sval(k + 1), sval(k + 2), sval(k + 3));
   }
-  for (int k = h + 4 * ng + threadIdx.x; k < V; k += kThreads) out[k] = val(k);
+  for (int k = h + 4 * ng + threadIdx.x; k < V; k += kThreads) out[k] = sval(k);
 }
 
-// ------------------------------------------------------------------ the kernel
+// ------------------------------------------------------------------ the kernels
+//
+// Every call runs two kernels on its stream. The stream kernel reads every logit once and
+// writes one partial per unit; the finishing kernel, launched as a programmatic dependent of
+// the stream kernel (so its launch overlaps the stream kernel's last wave), waits for the
+// stream kernel's results and turns them into outputs.
 
+// The stream kernel: warp w of the grid reduces units w, w + W, w + 2W, ... (W warps in all),
+// each to one 8-byte partial. For chain sampling it also records the logit at each row's draft
+// token, taken from the registers of the lane that loaded it (or, for a head/tail element,
+// loaded by chunk 0). No barriers, atomics or fences: the finishing kernel starts only after
+// this grid has completed.
 template <typename E, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) verify_kernel(Params p) {
-  extern __shared__ float smem[];
-  __shared__ TailShared sh;
-  __shared__ int s_tail[kWarps];
-  __shared__ int s_ntail;
-  __shared__ long long s_group;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long upb = static_cast<long long>(p.R) * p.C;   // units per batch row
+__global__ void __launch_bounds__(kThreads, 2) stream_kernel(Params p) {
+  constexpr int kEPV = Elem<E>::kPerVec;
   constexpr bool kStats = (MODE == kChainSample || MODE == kProbs);
-
-  long long group = blockIdx.x;
-  while (group < p.groups) {
-    const long long unit = group * kWarps + warp;
-    if (unit < p.units) {
-      const long long b = unit / upb;
-      const long long rem = unit - b * upb;
-      const int r = static_cast<int>(rem / p.C);
-      const int chunk = static_cast<int>(rem - static_cast<long long>(r) * p.C);
-      const E *row = row_ptr<E>(p, b, r);
-      const RowGeom geo = row_geom<E>(row, p.V);
-      if constexpr (MODE == kChainSample) {
-        // chunk 0 also fetches the logit at this row's draft token (target rows < gamma and
-        // every draft row), so the tail does not wait on a scattered load
-        if (chunk == 0 && lane == 0 && r != p.gamma) {
-          const int i = (r < p.Rt) ? r : r - p.Rt;
-          const int x = p.tokens[b * p.gamma + i];
-          const float xl = (x >= 0 && x < p.V) ? ld_elem<E>(row + x) : 0.f;
-          p.ws_xlogit[b * p.R + r] = xl;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int W = gridDim.x * kWarps;
+  for (int unit = blockIdx.x * kWarps + (threadIdx.x >> 5); unit < p.units; unit += W) {
+    const UnitId u = unit_id(p, unit);
+    // the draft token of this row, fetched before the unit's data so both loads overlap
+    int x = -1;
+    if constexpr (MODE == kChainSample) {
+      if (u.r != p.gamma) {
+        const int i = (u.r < p.Rt) ? u.r : u.r - p.Rt;
+        x = __ldg(p.tokens + static_cast<long long>(u.b) * p.gamma + i);
+      }
+    }
+    const E *row = row_ptr<E>(p, u.b, u.r);
+    const RowGeom g = row_geom<E>(row, p.V);
+    uint4 buf[kVPL];
+    float eh, et;
+    load_unit<E>(row, g, u.chunk, lane, buf, eh, et);
+    uint2 part;
+    if constexpr (kStats) {
+      float m, s;
+      unit_stats<E>(buf, eh, et, p.c2, m, s);
+      part = make_uint2(__float_as_uint(m), __float_as_uint(s));
+    } else {
+      float v;
+      int i;
+      unit_argmax<E>(buf, eh, et, g, u.chunk, lane, v, i);
+      part = make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
+    }
+    if (lane == 0) p.ws_part[unit] = part;
+    if constexpr (MODE == kChainSample) {
+      if (x >= 0 && x < p.V) {
+        float *dst = p.ws_xlogit + static_cast<long long>(u.b) * p.R + u.r;
+        const int rel = x - g.h;
+        const int vx = rel >= 0 ? rel / kEPV : -1;
+        const int v0 = u.chunk * kUnitVecs;
+        if (rel >= 0 && vx < g.nv) {
+          if (vx >= v0 && vx < v0 + kUnitVecs) {
+            // slot (vx - v0) = j*32 + owner lane: pick vector j, then element e
+            const int js = (vx - v0) >> 5, owner = (vx - v0) & 31, e = rel - vx * kEPV;
+            uint4 t = buf[0];
+#pragma unroll
+            for (int j = 1; j < kVPL; ++j)
+              if (j == js) t = buf[j];
+            const float val = __shfl_sync(0xffffffffu, vec_elem<E>(t, e), owner);
+            if (lane == 0) *dst = val;
+          }
+        } else if (u.chunk == 0 && lane == 0) {
+          *dst = ld_elem<E>(row + x);
         }
       }
-      uint2 part;
-      if constexpr (kStats) {
-        float m, s;
-        unit_stats<E>(row, geo, chunk, lane, p.c2, m, s);
-        part = make_uint2(__float_as_uint(m), __float_as_uint(s));
-      } else {
-        float v;
-        int i;
-        unit_argmax<E>(row, geo, chunk, lane, v, i);
-        part = make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
-      }
-      if (lane == 0) p.ws_part[unit] = part;
-      __threadfence();
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const long long u0 = group * kWarps;
-      const long long u1 = min(u0 + kWarps, p.units);
-      int nt = 0;
-      for (long long b = u0 / upb; b <= (u1 - 1) / upb; ++b) {
-        const long long lo = max(u0, b * upb), hi = min(u1, (b + 1) * upb);
-        const unsigned add = static_cast<unsigned>(hi - lo);
-        const unsigned old = atomicAdd(p.ws_count + b, add);
-        if (old + add == static_cast<unsigned>(upb)) s_tail[nt++] = static_cast<int>(b);
-      }
-      s_ntail = nt;
-      __threadfence();
-    }
-    __syncthreads();
-    const int ntail = s_ntail;
-    for (int t = 0; t < ntail; ++t) {
-      const int b = s_tail[t];
-      if constexpr (MODE == kChainSample) tail_chain_sample<E>(p, b, smem, sh);
-      else if constexpr (MODE == kChainGreedy) tail_chain_greedy<E>(p, b, smem, sh);
-      else if constexpr (MODE == kTree) tail_tree<E>(p, b, smem, sh);
-      else if constexpr (MODE == kProbs) tail_probs<E, false>(p, b, smem, sh);
-      else tail_probs<E, true>(p, b, smem, sh);
-      __syncthreads();
-      if (threadIdx.x == 0) p.ws_count[b] = 0;   // leave the workspace zeroed
-    }
-    if (threadIdx.x == 0) s_group = static_cast<long long>(atomicAdd(p.ws_ctl, 1u)) + gridDim.x;
-    __syncthreads();
-    group = s_group;
   }
+}
+
+// Waits until the stream kernel of this call has completed and its writes are visible.
+__device__ __forceinline__ void wait_stream_kernel() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Finishing kernel for chain sampling: one thread-block cluster of S CTAs per batch row (S = the
+// cluster size, blockIdx.x = b * S + rank). Every CTA of the cluster combines the row's
+// partials and decides acceptance (cheap, redundant); CTA `rank` then sums the residual (or
+// bonus) weights over its slice of the vocabulary into shared memory. The slice totals are
+// exchanged through distributed shared memory after a cluster barrier; the CTA whose slice
+// holds the crossing draws the token from its own segment sums and writes the outputs.
+template <typename E>
+__global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
+  namespace cg = cooperative_groups;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float *rowM = reinterpret_cast<float *>(smem_raw);
+  float *rowZ = rowM + p.R;
+  float *segsum = rowZ + p.R;
+  __shared__ TailShared sh;
+  __shared__ int xs[SPEC_MAX_GAMMA];
+  __shared__ float s_total;
+  __shared__ float s_pre[kMaxCluster + 1];
+  cg::cluster_group cl = cg::this_cluster();
+  const int S = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int b = blockIdx.x / S;
+  wait_stream_kernel();
+  int n = 0;
+  const int err = chain_accept(p, b, rowM, rowZ, xs, sh, &n);
+  if (err) {   // the same on every CTA of the cluster: all of them leave here
+    if (rank == 0) {
+      if (threadIdx.x == 0) set_status(p.status, err);
+      fail_chain_row(p, b, threadIdx.x, kThreads);
+    }
+    return;
+  }
+  const int gamma = p.gamma;
+  const E *P = row_ptr<E>(p, b, n);
+  const E *Q = (n < gamma) ? row_ptr<E>(p, b, gamma + 1 + n) : nullptr;
+  const float Mt = rowM[n], iZt = __frcp_rn(rowZ[n]);
+  const float Md = Q ? rowM[gamma + 1 + n] : 0.f, iZd = Q ? __frcp_rn(rowZ[gamma + 1 + n]) : 0.f;
+  const float u = p.uniforms[static_cast<long long>(b) * (gamma + 1) + gamma];
+  const int nseg = (p.V + kSeg - 1) / kSeg;
+  const int K = (nseg + S - 1) / S;
+  const int lo = min(nseg, rank * K), hi = min(nseg, lo + K), nl = hi - lo;
+  segment_sums<E>(P, Q, Mt, iZt, Md, iZd, p.c2, p.V, lo, hi, segsum, lo);
+  __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned done = atomicAdd(p.ws_ctl + 1, 1u);
-    if (done == gridDim.x - 1) {
-      p.ws_ctl[0] = 0u;
-      p.ws_ctl[1] = 0u;
-    }
+    float tot = 0.f;
+    for (int j = 0; j < nl; ++j) tot = __fadd_rn(tot, segsum[j]);
+    s_total = tot;
   }
+  cl.sync();   // every slice total written
+  if (threadIdx.x == 0) {
+    float acc = 0.f;
+    for (int r = 0; r < S; ++r) {
+      s_pre[r] = acc;
+      acc = __fadd_rn(acc, *cl.map_shared_rank(&s_total, r));
+    }
+    s_pre[S] = acc;
+  }
+  cl.sync();   // every CTA has read its peers' totals; shared memory is private again
+  const float Sall = s_pre[S];
+  int tok = -1;
+  if (Q && Sall == 0.f) {
+    // the residual vanished: draw from p_n alone, on the first CTA of the cluster
+    if (rank != 0) return;
+    tok = draw_token_cta<E>(P, nullptr, Mt, iZt, 0.f, 0.f, p.c2, p.V, u, segsum, sh);
+  } else {
+    const float t = __fmul_rn(u, Sall);
+    int owner = -1, mode = 0;
+    for (int r = 0; r < S; ++r)
+      if (owner < 0 && s_pre[r + 1] > t) owner = r;
+    if (owner < 0) {   // t >= S after rounding: the last slice holding mass
+      mode = 1;
+      for (int r = 0; r < S; ++r)
+        if (s_pre[r + 1] > s_pre[r]) owner = r;
+      owner = max(owner, 0);
+    }
+    if (rank != owner) return;
+    tok = pick_in_slice<E>(P, Q, Mt, iZt, Md, iZd, p.c2, p.V, segsum, nl, lo, s_pre[rank], t,
+                           mode, sh);
+  }
+  emit_chain(p, b, n, tok, xs, threadIdx.x, kThreads);
+}
+
+// Finishing kernel for chain sampling when every row is a single unit (gamma <= 31, V <=
+// kWarpTailMaxV): one warp per batch row; lane i holds rows i and i + 32 and the draft-token
+// logits of position i.
+template <typename E>
+__global__ void __launch_bounds__(kThreads, 2) finish_chain_sample_warp(Params p) {
+  wait_stream_kernel();
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (b >= p.B) return;
+  const int R = p.R, gamma = p.gamma;
+  const uint2 *part = p.ws_part + static_cast<long long>(b) * R;   // C == 1
+  const float *xl = p.ws_xlogit + static_cast<long long>(b) * R;
+  float m0 = 0.f, z0 = 1.f, m1 = 0.f, z1 = 1.f, lti = 0.f, ldi = 0.f;
+  if (lane < R) {
+    const uint2 v = ldcg_u2(part + lane);
+    m0 = __uint_as_float(v.x);
+    z0 = __uint_as_float(v.y);
+  }
+  if (lane + 32 < R) {
+    const uint2 v = ldcg_u2(part + lane + 32);
+    m1 = __uint_as_float(v.x);
+    z1 = __uint_as_float(v.y);
+  }
+  if (lane < gamma) {
+    lti = ldcg_f(xl + lane);
+    ldi = ldcg_f(xl + gamma + 1 + lane);
+  }
+  tail_chain_sample_regs<E>(p, b, m0, z0, m1, z1, lti, ldi);
+}
+
+// Finishing kernel for greedy chains, trees and probabilities: one CTA per batch row.
+template <typename E, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) finish_cta(Params p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float *scratch = reinterpret_cast<float *>(smem_raw);
+  __shared__ TailShared sh;
+  wait_stream_kernel();
+  const int b = blockIdx.x;
+  if constexpr (MODE == kChainGreedy) tail_chain_greedy(p, b, scratch, sh);
+  else if constexpr (MODE == kTree) tail_tree(p, b, scratch, sh);
+  else if constexpr (MODE == kProbs) tail_probs<E, false>(p, b, sh);
+  else tail_probs<E, true>(p, b, sh);
 }
 
 }  // namespace specv

@@ -1,22 +1,26 @@
-// spec_kernels_probs.cu -- instances of the verify kernel for the probability helper.
+// spec_kernels_probs.cu -- kernel instances for the probability helper.
 #include "spec_launch.h"
 
 namespace specv {
 
-cudaError_t launch_probs(int mode, int dtype, const Params &p, int grid, size_t smem,
+namespace {
+
+template <typename E, int MODE>
+cudaError_t probs(const Params &p, int grid, const FinishPlan &f, cudaStream_t stream) {
+  cudaError_t e = launch_stream<E, MODE>(p, grid, stream);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(finish_cta<E, MODE>, p, f.grid, 1, f.smem, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_probs(int mode, int dtype, const Params &p, int grid, const FinishPlan &f,
                          cudaStream_t stream) {
-  if (mode == kProbs) {
-    if (dtype == SPEC_BF16)
-      verify_kernel<uint16_t, kProbs><<<grid, kThreads, smem, stream>>>(p);
-    else
-      verify_kernel<float, kProbs><<<grid, kThreads, smem, stream>>>(p);
-  } else {
-    if (dtype == SPEC_BF16)
-      verify_kernel<uint16_t, kProbsGreedy><<<grid, kThreads, smem, stream>>>(p);
-    else
-      verify_kernel<float, kProbsGreedy><<<grid, kThreads, smem, stream>>>(p);
-  }
-  return cudaGetLastError();
+  if (mode == kProbs)
+    return dtype == SPEC_BF16 ? probs<uint16_t, kProbs>(p, grid, f, stream)
+                              : probs<float, kProbs>(p, grid, f, stream);
+  return dtype == SPEC_BF16 ? probs<uint16_t, kProbsGreedy>(p, grid, f, stream)
+                            : probs<float, kProbsGreedy>(p, grid, f, stream);
 }
 
 }  // namespace specv

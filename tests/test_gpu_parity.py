@@ -315,14 +315,17 @@ def test_tree_shapes_and_errors(orc):
 
 
 def test_deterministic_and_workspace_reuse(orc):
+    """The workspace is scratch: whatever it holds before a call (here garbage bytes, then the
+    previous call's leftovers) does not change the result."""
     import speculative_decoding_verification_78_gb300 as sv
     ci = chain_32k(seed=15, B=32, gamma=5, V=8000)
     ws = sv.new_workspace(ci.B, 2 * ci.gamma + 1, ci.V, sv.SPEC_BF16)
+    ws.fill_(0xA5)
     first = run_chain(ci, workspace=ws)
-    for _ in range(3):
+    for k in range(3):
+        if k == 1:
+            ws.fill_(0xFF)   # NaN bit patterns everywhere
         again = run_chain(ci, workspace=ws)
         assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
-    # control words and per-batch-row counters are zero again after every call
-    ctl = ws[:256 + 4 * ci.B].view(torch.int32).cpu().numpy()
-    assert np.all(ctl == 0), "workspace counters not reset"
+        assert again[2] == 0
     compare_chain(orc, ci, first)
