@@ -10,8 +10,11 @@ achieved HBM GB/s against the measured copy bandwidth.
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream, max over ranks.
-Inputs rotate over 3 copies, so every buffer is reused only after more than 4x the L2 size of
-other traffic. Per-kernel durations come from event pairs around every 8th step's launches.
+Each call's two kernel launches are captured once in a CUDA graph (per input copy) exactly as
+the C entry point enqueues them; a step replays the chain, tree and probs graphs, so the timed
+region measures the GPU work rather than Python's launch rate. Inputs rotate over 3 copies, so
+every buffer is reused only after more than 4x the L2 size of other traffic. Per-call durations
+come from event pairs around every 8th step's graph launches.
 `e2e` repeats the step through the same C entry points with inputs in pinned host memory:
 host-to-device copies of the step's inputs and device-to-host copies of all its outputs are
 inside the timed region.
@@ -43,6 +46,7 @@ UNIT = "positions/s"
 L2_BYTES = 129e6
 ROT = 3
 EVENT_EVERY = 8
+KINDS = ("chain", "tree", "probs")
 WORKLOAD = ("verify step: chain B=64 gamma=5 V=32000 bf16 T=1 + tree B=32 N=64 V=32000 bf16 "
             "greedy + probs 384x32000 bf16->fp32 T=1")
 
@@ -112,6 +116,14 @@ def make_inputs(seed_offset=0):
     return ci, ti
 
 
+def config_for(world):
+    """The JSON line's config: the workload, its batch over all replicas, and how L2 reuse is
+    avoided between timed steps."""
+    return {"workload": WORKLOAD, "global_batch": world * (64 + 32),
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": f"inputs rotated over {ROT} copies (>4x L2 of traffic between reuses)"}
+
+
 def step_bytes(ci, ti):
     """Algorithmic bytes of one step per kernel: every logit read once, small int/fp32 arrays
     read or written once, the probabilities written once."""
@@ -121,6 +133,26 @@ def step_bytes(ci, ti):
     tree = ti.target.nbytes + ti.parents.nbytes + ti.tokens.nbytes + 4 * ti.B * (2 * ti.N + 1)
     probs = ci.target.nbytes + 4 * ci.target.size
     return {"chain": chain, "tree": tree, "probs": probs}
+
+
+def launch_shapes(ci, ti):
+    """Per call of the step: the kernels it launches (from the library's own launch plan)."""
+    import speculative_decoding_verification_78_gb300 as sv
+    out = {}
+    for kind, code, B, rows, V, T, mode in (
+            ("chain", sv.SPEC_CALL_CHAIN, ci.B, 2 * ci.gamma + 1, ci.V, ci.temperature,
+             "chain-sample"),
+            ("tree", sv.SPEC_CALL_TREE, ti.B, ti.N, ti.V, 0.0, "tree"),
+            ("probs", sv.SPEC_CALL_PROBS, ci.B * (ci.gamma + 1), 1, ci.V, 1.0, "probs")):
+        k, grid, cluster = sv.spec_launch_shape(code, B, rows, V, sv.SPEC_BF16, T)
+        if k == 1:
+            names = f"fused_kernel<bf16, {mode}> ({grid} CTAs, clusters of {cluster})"
+        else:
+            fin = {"chain-sample": "finish_chain_sample<bf16>", "tree": "finish_cta<bf16, tree>",
+                   "probs": "finish_probs<bf16>"}[mode]
+            names = f"stream_kernel<bf16, {mode}> + {fin} ({grid} CTAs)"
+        out[kind] = {"launches": k, "kernels": names}
+    return out
 
 
 def positions(ci, ti):
@@ -255,7 +287,7 @@ class Runner:
         self.ws_t = sv.new_workspace(ti.B, ti.N, ti.V, sv.SPEC_BF16, dev)
         rows = B * (g + 1)
         self.ws_p = sv.new_workspace(rows, 1, V, sv.SPEC_BF16, dev)
-        self.stream = torch.cuda.current_stream(dev)
+        self.stream = torch.cuda.Stream(dev)
         vp = ctypes.c_void_p
         sp = vp(self.stream.cuda_stream)
         self.args = []
@@ -276,33 +308,58 @@ class Runner:
                      vp(self.ws_p.data_ptr()), self.ws_p.numel(), sp)
             self.args.append((chain, tree, probs))
 
-    def step(self, i, evs=None):
-        chain, tree, probs = self.args[i % ROT]
+    def call(self, kind, k):
+        chain, tree, probs = self.args[k]
         lib = self.lib
-        if evs is None:
-            rc = lib.spec_verify_chain(*chain) | lib.spec_verify_tree(*tree) | \
-                lib.spec_probs(*probs)
-        else:
-            evs[0].record(self.stream)
+        if kind == "chain":
             rc = lib.spec_verify_chain(*chain)
-            evs[1].record(self.stream)
-            rc |= lib.spec_verify_tree(*tree)
-            evs[2].record(self.stream)
-            rc |= lib.spec_probs(*probs)
-            evs[3].record(self.stream)
+        elif kind == "tree":
+            rc = lib.spec_verify_tree(*tree)
+        else:
+            rc = lib.spec_probs(*probs)
         if rc:
-            raise RuntimeError(f"verify call failed: {rc}")
+            raise RuntimeError(f"{kind} call failed: {rc}")
+
+    def capture(self):
+        """One CUDA graph per (call, input copy): each holds that call's two kernel launches
+        exactly as the C entry point enqueues them."""
+        torch = self.torch
+        self.graphs = {}
+        with torch.cuda.stream(self.stream):
+            for k in range(ROT):
+                for kind in KINDS:
+                    self.call(kind, k)
+        torch.cuda.synchronize()
+        for k in range(ROT):
+            for kind in KINDS:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    self.call(kind, k)
+                self.graphs[kind, k] = g
+        torch.cuda.synchronize()
+
+    def step(self, i, evs=None):
+        k = i % ROT
+        if evs is None:
+            for kind in KINDS:
+                self.graphs[kind, k].replay()
+        else:
+            for j, kind in enumerate(KINDS):
+                evs[j].record(self.stream)
+                self.graphs[kind, k].replay()
+            evs[len(KINDS)].record(self.stream)
 
 
 def run_ours(args, rank, world, local):
     import torch
-    import oracle  # noqa: F401  (only for the cpu_baseline leg below)
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     ci, ti = make_inputs(args.seed_offset + rank)
     r = Runner(ci, ti, device)
-    for i in range(args.warmup):
-        r.step(i)
+    r.capture()
+    with torch.cuda.stream(r.stream):
+        for i in range(args.warmup):
+            r.step(i)
     torch.cuda.synchronize()
     assert int(r.status.item()) == 0, "device-side error in warm-up"
 
@@ -315,10 +372,11 @@ def run_ours(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     host0 = time.perf_counter()
-    t0.record(r.stream)
-    for i in range(K):
-        r.step(i, evs[i // EVENT_EVERY] if i % EVENT_EVERY == 0 else None)
-    t1.record(r.stream)
+    with torch.cuda.stream(r.stream):
+        t0.record(r.stream)
+        for i in range(K):
+            r.step(i, evs[i // EVENT_EVERY] if i % EVENT_EVERY == 0 else None)
+        t1.record(r.stream)
     host_issue = time.perf_counter() - host0
     torch.cuda.synchronize()
     barrier(world)
@@ -343,8 +401,8 @@ def run_ours(args, rank, world, local):
     rows["chain"]["verified_positions"] = ci.B * (ci.gamma + 1)
     rows["tree"]["verified_positions"] = ti.B * ti.N
     dom = max(("chain", "tree", "probs"), key=lambda k: avg[k])
-    kname = {"chain": "verify_kernel<bf16, chain-sample>", "tree": "verify_kernel<bf16, tree>",
-             "probs": "verify_kernel<bf16, probs>"}[dom]
+    shapes = launch_shapes(ci, ti)
+    kname = shapes[dom]["kernels"]
     pos_total = sum_over_ranks(positions(ci, ti) * K, world, device)
     value = pos_total / elapsed
     step_total_bytes = sum(nbytes.values())
@@ -352,10 +410,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": elapsed / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": world * (ci.B + ti.B),
-                   "positions_per_step": positions(ci, ti) * world,
-                   "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": f"inputs rotated over {ROT} copies (>4x L2 of traffic between reuses)"},
+        "config": dict(config_for(world), positions_per_step=positions(ci, ti) * world),
         "achieved_GBps": step_total_bytes * world * K / elapsed / 1e9 / world,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": rows[dom]["GBps"],
                      "peak": peak, "unit": "GB/s", "frac": rows[dom]["GBps"] / peak,
@@ -363,7 +418,8 @@ def run_ours(args, rank, world, local):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "traffic": ncu_traffic(dom), "algorithmic_bytes": nbytes[dom]},
         "rows": rows,
-        "gpu_launches": 3 * K,
+        "gpu_launches": sum(v["launches"] for v in shapes.values()) * K,
+        "launch_shapes": shapes,
         "clocks": clk,
         "host_issue_us_per_step": host_issue / K * 1e6,
         "emitted_tokens_per_step": int((r.acc.cpu().numpy() + 1).sum()),
@@ -417,14 +473,16 @@ def e2e(r, ci, ti, steps, world, device):
         o_tout.copy_(r.tout, non_blocking=True)
         o_pr.copy_(r.probs[k], non_blocking=True)
 
-    for i in range(5):
-        one(i)
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for i in range(steps):
-        one(i)
-    t1.record()
+    # copies and kernels on the one stream the C calls were given
+    with torch.cuda.stream(r.stream):
+        for i in range(5):
+            one(i)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(r.stream)
+        for i in range(steps):
+            one(i)
+        t1.record(r.stream)
     torch.cuda.synchronize()
     el = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world, device)
     pos = sum_over_ranks(positions(ci, ti) * steps, world, device)
@@ -497,8 +555,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": ci.B + ti.B,
-                       "positions_per_step": positions(ci, ti), "parallelism": "single"},
+            "config": dict(config_for(1), positions_per_step=positions(ci, ti)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -149,6 +149,24 @@ int spec_probs(const void *logits, int dtype, int rows, int V, float temperature
 /* Static text for any SPEC_* code ("unknown status" otherwise). */
 const char *spec_status_string(int code);
 
+/*
+ * The kernel launches a call of the given shape makes on the current device; it enqueues
+ * nothing and touches no memory (for tests and profiling; the pages have no counterpart).
+ *   kind        SPEC_CALL_CHAIN (rows_per_b = 2*gamma+1, any temperature), SPEC_CALL_TREE
+ *               (rows_per_b = N) or SPEC_CALL_PROBS (B = rows, rows_per_b = 1)
+ *   kernels[0]  1: one fused kernel (one thread-block cluster per batch row does the whole
+ *               call); 2: a stream kernel over all rows, then a finishing kernel
+ *   grid[0]     CTAs of the launch that finishes the call
+ *   cluster[0]  its thread-block cluster size (1 = no cluster)
+ * Returns SPEC_OK or SPEC_ERR_NULL / SHAPE / DTYPE / TEMP. The shape depends on the device's
+ * multiprocessor count.
+ */
+#define SPEC_CALL_CHAIN 0
+#define SPEC_CALL_TREE 1
+#define SPEC_CALL_PROBS 2
+int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float temperature,
+                      int *kernels, int *grid, int *cluster);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,8 @@ SPEC_MAX_V, SPEC_MAX_GAMMA, SPEC_MAX_NODES = 1 << 20, 255, 1024
 
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_workspace_bytes", "spec_workspace_init", "spec_verify_chain",
-           "spec_verify_tree", "spec_probs", "spec_status_string")
+           "spec_verify_tree", "spec_probs", "spec_status_string", "spec_launch_shape")
+SPEC_CALL_CHAIN, SPEC_CALL_TREE, SPEC_CALL_PROBS = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +63,8 @@ def load_library():
         lib.spec_probs.restype = i32
         lib.spec_status_string.argtypes = [i32]
         lib.spec_status_string.restype = ctypes.c_char_p
+        lib.spec_launch_shape.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp]
+        lib.spec_launch_shape.restype = i32
         _lib = lib
         return lib
 
@@ -140,6 +143,17 @@ def spec_probs(logits, temperature, out_probs, status, workspace, stream=None) -
     return load_library().spec_probs(
         _ptr(logits), dtype_flag(logits), rows, V, float(temperature), _ptr(out_probs),
         _ptr(status), _ptr(workspace), _nbytes(workspace), _stream(stream))
+
+
+def spec_launch_shape(kind: int, B: int, rows_per_b: int, V: int, dtype: int,
+                      temperature: float = 1.0):
+    """(kernels, grid, cluster) of a call of this shape on the current device."""
+    k, g, c = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = load_library().spec_launch_shape(kind, B, rows_per_b, V, dtype, float(temperature),
+                                          ctypes.byref(k), ctypes.byref(g), ctypes.byref(c))
+    if rc != SPEC_OK:
+        raise SpecError(rc, "spec_launch_shape")
+    return k.value, g.value, c.value
 
 
 def spec_status_string(code: int) -> str:

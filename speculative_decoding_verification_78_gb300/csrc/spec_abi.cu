@@ -54,24 +54,32 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool temp_ok(float T) { return T == 0.f || (T >= FLT_MIN && T <= FLT_MAX); }
 
-// Fills the workspace pointers and unit counts of p; returns SPEC_OK, SPEC_ERR_WORKSPACE, or
-// SPEC_ERR_SHAPE when the call has 2^31 - 64 units or more (unit ids are 32-bit on the device).
-int plan(Params &p, int dtype, void *ws, size_t ws_bytes) {
+// Fills the unit counts of p; returns SPEC_OK, or SPEC_ERR_SHAPE when the call has 2^31 - 64
+// units or more (unit ids are 32-bit on the device).
+int plan_units(Params &p, int dtype) {
   p.C = chunks_per_row(p.V, dtype);
   const long long units = static_cast<long long>(p.B) * p.R * p.C;
   if (units >= (1LL << 31) - 64) return SPEC_ERR_SHAPE;
-  const Layout L = layout(p.B, p.R, p.C);
-  if (ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
-  char *w = static_cast<char *>(ws);
-  p.ws_part = reinterpret_cast<uint2 *>(w + L.part);
-  p.ws_xlogit = reinterpret_cast<float *>(w + L.xlogit);
   p.units = static_cast<int>(units);
   p.upb = p.R * p.C;
   return SPEC_OK;
 }
 
-// stream kernel grid: at most two CTAs of 512 threads per SM (all resident at once), never
-// more CTAs than groups of kWarps units
+// plan_units, then the workspace pointers; SPEC_ERR_WORKSPACE when the workspace is too small.
+int plan(Params &p, int dtype, void *ws, size_t ws_bytes) {
+  const int rc = plan_units(p, dtype);
+  if (rc != SPEC_OK) return rc;
+  const Layout L = layout(p.B, p.R, p.C);
+  if (ws_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  char *w = static_cast<char *>(ws);
+  p.ws_part = reinterpret_cast<uint2 *>(w + L.part);
+  p.ws_xlogit = reinterpret_cast<float *>(w + L.xlogit);
+  return SPEC_OK;
+}
+
+// Stream kernel grid: two CTAs of 512 threads per SM (all resident at once), never more CTAs
+// than groups of kWarps units. (Trimming the grid so that the last round of loads is full was
+// measured slower: fewer loads in flight.)
 int grid_for(const Params &p) {
   const long long cap = 2LL * (sm_count() > 0 ? sm_count() : 1);
   const long long groups = (static_cast<long long>(p.units) + kWarps - 1) / kWarps;
@@ -80,8 +88,9 @@ int grid_for(const Params &p) {
 }
 
 // Finishing plan for chain sampling. Single-unit rows with gamma <= 31: one warp per batch row.
-// Otherwise one cluster of S CTAs per batch row, S chosen so that the draw's pass over the
-// stopping rows fills about two CTAs per SM, with at least 8 residual segments per CTA.
+// Otherwise one cluster of S CTAs per batch row: S is the largest power of two (at most 8) for
+// which all B*S CTAs are resident at once (two per SM) and every CTA gets at least 8 residual
+// segments.
 FinishPlan chain_sample_plan(const Params &p) {
   FinishPlan f{};
   if (p.C == 1 && p.V <= kWarpTailMaxV && p.gamma <= 31) {
@@ -93,17 +102,47 @@ FinishPlan chain_sample_plan(const Params &p) {
   }
   const int nseg = (p.V + kSeg - 1) / kSeg;
   const int sms = sm_count() > 0 ? sm_count() : 1;
-  int S = (2 * sms + p.B - 1) / p.B;
   int cap = nseg / 8;
-  if (cap < 1) cap = 1;
   if (cap > kMaxCluster) cap = kMaxCluster;
-  if (S > cap) S = cap;
-  if (S < 1) S = 1;
+  const int fit = (2 * sms) / p.B;
+  if (cap > fit) cap = fit;
+  int S = 1;
+  while (2 * S <= cap) S *= 2;
   f.warp_tail = false;
+  f.fused = false;
   f.cluster = S;
   f.grid = p.B * S;
   f.smem = sizeof(float) * (2 * static_cast<size_t>(p.R) + nseg);
   return f;
+}
+
+// The fused single-kernel plan (one cluster of S CTAs per batch row), when it applies: at most
+// kFusedMaxRows rows per batch row, at least one full unit per row and CTA, and enough batch rows
+// that B*S CTAs keep every SM streaming. S is the largest power of two (at most 8) for which
+// the B*S CTAs are all resident at once (two per SM). Fills p.fper / p.fU.
+bool fused_plan(Params &p, int dtype, int mode, FinishPlan &f) {
+  if (p.R > kFusedMaxRows) return false;
+  const int sms = sm_count() > 0 ? sm_count() : 1;
+  const int nvmax = p.V / (16 / elem_size(dtype));
+  if (nvmax < kUnitVecs) return false;
+  int S = 1;
+  while (2 * S <= kMaxCluster && static_cast<long long>(p.B) * 2 * S <= 2LL * sms &&
+         nvmax / (2 * S) >= kUnitVecs)
+    S *= 2;
+  if (static_cast<long long>(p.B) * S < sms) return false;
+  p.fper = (nvmax + S - 1) / S;
+  p.fU = (p.fper + kUnitVecs - 1) / kUnitVecs;
+  const size_t R = static_cast<size_t>(p.R);
+  const size_t nseg = (static_cast<size_t>(p.V) + kSeg - 1) / kSeg;
+  size_t fin = 6 * R;                                       // tree
+  if (mode == kChainSample) fin = 3 * R + nseg;             // rowM, rowZ, xlf, segsum
+  if (mode == kChainGreedy) fin = 2 * R + p.gamma;          // g, gok, xs
+  f.fused = true;
+  f.warp_tail = false;
+  f.grid = p.B * S;
+  f.cluster = S;
+  f.smem = 8 * kWarps * R + 8 * R + 4 * R + 4 * fin;
+  return true;
 }
 
 FinishPlan cta_plan(int rows, size_t smem) {
@@ -119,6 +158,57 @@ Params blank() {
   Params p{};
   return p;
 }
+
+float c2_of(float T) {
+  return T == 0.f ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+}
+
+// Row geometry of each kind of call (no pointers).
+void chain_shape(Params &p, int B, int gamma, int V, float T) {
+  const bool greedy = T == 0.f;
+  p.B = B;
+  p.gamma = gamma;
+  p.N = 0;
+  p.V = V;
+  p.Rt = gamma + 1;
+  p.Rd = greedy ? 0 : gamma;
+  p.R = p.Rt + p.Rd;
+  p.c2 = c2_of(T);
+}
+
+void tree_shape(Params &p, int B, int N, int V) {
+  p.B = B;
+  p.N = N;
+  p.V = V;
+  p.Rt = N;
+  p.Rd = 0;
+  p.R = N;
+}
+
+void probs_shape(Params &p, int rows, int V, float T) {
+  p.B = rows;
+  p.V = V;
+  p.Rt = 1;
+  p.Rd = 0;
+  p.R = 1;
+  p.c2 = c2_of(T);
+}
+
+// The launch plan of each kind of call (after plan_units).
+FinishPlan chain_finish(Params &p, int dtype, bool greedy) {
+  FinishPlan f{};
+  if (fused_plan(p, dtype, greedy ? kChainGreedy : kChainSample, f)) return f;
+  return greedy ? cta_plan(p.B, sizeof(int) * (2 * static_cast<size_t>(p.R) + p.gamma))
+                : chain_sample_plan(p);
+}
+
+FinishPlan tree_finish(Params &p, int dtype) {
+  FinishPlan f{};
+  if (fused_plan(p, dtype, kTree, f)) return f;
+  return cta_plan(p.B, sizeof(int) * 6 * static_cast<size_t>(p.N));
+}
+
+FinishPlan probs_finish(const Params &p) { return cta_plan(grid_for(p), 0); }
 
 }  // namespace
 
@@ -160,6 +250,7 @@ int spec_verify_chain(const void *target_logits, const void *draft_logits, int d
   if (B == 0) return SPEC_OK;
 
   Params p = blank();
+  chain_shape(p, B, gamma, V, temperature);
   p.tgt = target_logits;
   p.drf = greedy ? nullptr : draft_logits;
   p.tokens = draft_tokens;
@@ -167,18 +258,9 @@ int spec_verify_chain(const void *target_logits, const void *draft_logits, int d
   p.accept_len = accept_len;
   p.out_tokens = out_tokens;
   p.status = status;
-  p.B = B;
-  p.gamma = gamma;
-  p.N = 0;
-  p.V = V;
-  p.Rt = gamma + 1;
-  p.Rd = greedy ? 0 : gamma;
-  p.R = p.Rt + p.Rd;
-  p.c2 = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const FinishPlan f = greedy ? cta_plan(B, sizeof(int) * (2 * static_cast<size_t>(p.R) + gamma))
-                              : chain_sample_plan(p);
+  const FinishPlan f = chain_finish(p, dtype, greedy);
   const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
                                      f, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
@@ -200,6 +282,7 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
   if (B == 0) return SPEC_OK;
 
   Params p = blank();
+  tree_shape(p, B, N, V);
   p.tgt = target_logits;
   p.tokens = node_tokens;
   p.parents = parents;
@@ -207,17 +290,10 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
   p.out_tokens = out_tokens;
   p.path_nodes = path_nodes;
   p.status = status;
-  p.B = B;
-  p.N = N;
-  p.V = V;
-  p.Rt = N;
-  p.Rd = 0;
-  p.R = N;
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const FinishPlan f = cta_plan(B, sizeof(int) * 6 * static_cast<size_t>(N));
-  const cudaError_t e = launch_tree(dtype, p, grid_for(p), f,
-                                    static_cast<cudaStream_t>(stream));
+  const FinishPlan f = tree_finish(p, dtype);
+  const cudaError_t e = launch_tree(dtype, p, grid_for(p), f, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -234,20 +310,51 @@ int spec_probs(const void *logits, int dtype, int rows, int V, float temperature
   if (rows == 0) return SPEC_OK;
   const bool greedy = temperature == 0.f;
   Params p = blank();
+  probs_shape(p, rows, V, temperature);
   p.tgt = logits;
   p.out_probs = out_probs;
   p.status = status;
-  p.B = rows;
-  p.V = V;
-  p.Rt = 1;
-  p.Rd = 0;
-  p.R = 1;
-  p.c2 = greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
   const cudaError_t e = launch_probs(greedy ? kProbsGreedy : kProbs, dtype, p, grid_for(p),
-                                     cta_plan(rows, 0), static_cast<cudaStream_t>(stream));
+                                     probs_finish(p), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float temperature,
+                      int *kernels, int *grid, int *cluster) {
+  if (!kernels || !grid || !cluster) return SPEC_ERR_NULL;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (B < 1 || rows_per_b < 1 || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_SHAPE;
+  Params p = blank();
+  FinishPlan f{};
+  if (kind == SPEC_CALL_CHAIN) {
+    if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
+    if ((rows_per_b & 1) == 0 || (rows_per_b - 1) / 2 > SPEC_MAX_GAMMA) return SPEC_ERR_SHAPE;
+    chain_shape(p, B, (rows_per_b - 1) / 2, V, temperature);
+    const int rc = plan_units(p, dtype);
+    if (rc != SPEC_OK) return rc;
+    f = chain_finish(p, dtype, temperature == 0.f);
+  } else if (kind == SPEC_CALL_TREE) {
+    if (rows_per_b > SPEC_MAX_NODES) return SPEC_ERR_SHAPE;
+    tree_shape(p, B, rows_per_b, V);
+    const int rc = plan_units(p, dtype);
+    if (rc != SPEC_OK) return rc;
+    f = tree_finish(p, dtype);
+  } else if (kind == SPEC_CALL_PROBS) {
+    if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
+    if (rows_per_b != 1) return SPEC_ERR_SHAPE;
+    probs_shape(p, B, V, temperature);
+    const int rc = plan_units(p, dtype);
+    if (rc != SPEC_OK) return rc;
+    f = probs_finish(p);
+  } else {
+    return SPEC_ERR_SHAPE;
+  }
+  *kernels = f.fused ? 1 : 2;
+  *grid = f.grid;
+  *cluster = f.cluster;
+  return SPEC_OK;
 }
 
 const char *spec_status_string(int code) {

@@ -15,7 +15,7 @@
 //   chain, T = 0  argmax comparison of every draft token, then the greedy correction token;
 //   tree          accepted flags and depths of all nodes by pointer jumping, deepest node,
 //                 path and bonus token;
-//   probs         one write pass of the normalised probabilities of the row.
+//   probs         one write pass of the normalised probabilities, unit by unit.
 //
 // No CTA ever waits for another CTA of its own grid except through the hardware cluster
 // barrier. Data written by other CTAs is read with ld.global.cg (L2), never through L1.
@@ -37,6 +37,8 @@ constexpr int kUnitVecs = 32 * kVPL;        // vectors per unit (4 KB)
 constexpr int kSeg = 256;                   // residual segment: 32 lanes x 8 elements
 constexpr int kWarpTailMaxV = 2048;         // rows this short get warp-level chain finishing
 constexpr int kMaxCluster = 8;              // CTAs per batch row in the chain finisher
+static_assert(SPEC_MAX_GAMMA < kThreads, "one draft token per thread");
+static_assert(kMaxCluster <= 32, "one cluster rank per lane");
 
 enum Mode : int { kChainSample = 0, kChainGreedy = 1, kTree = 2, kProbs = 3, kProbsGreedy = 4 };
 
@@ -57,7 +59,8 @@ struct Params {
   int upb;                   // units per batch row, R*C
   int B, gamma, N, V;
   int Rt, Rd, R, C;          // rows per batch row: target, draft, total; units per row
-  int S;                     // chain sampling: CTAs per batch row (cluster size) when finishing
+  int fper;                  // fused kernel: interior vectors per CTA slice of a row
+  int fU;                    // fused kernel: units per CTA slice of a row, ceil(fper / kUnitVecs)
   float c2;                  // log2(e) / T
 };
 
@@ -182,24 +185,32 @@ __device__ __forceinline__ UnitId unit_id(const Params &p, int unit) {
   return u;
 }
 
-// Loads one unit straight into registers: vectors j*32+lane of chunk `chunk` (-inf beyond the
-// row's interior), plus this lane's head/tail scalar when the unit is chunk 0.
+// Loads one span of a row straight into registers: interior vectors vb + j*32 + lane below ve
+// (at most kUnitVecs of them; -inf beyond), plus this lane's head/tail scalar when `scalars`.
 template <typename E>
-__device__ __forceinline__ void load_unit(const E *row, const RowGeom &g, int chunk, int lane,
-                                          uint4 (&buf)[kVPL], float &ex_head, float &ex_tail) {
-  const int v0 = chunk * kUnitVecs + lane;
+__device__ __forceinline__ void load_span(const E *row, const RowGeom &g, int vb, int ve,
+                                          bool scalars, int lane, uint4 (&buf)[kVPL],
+                                          float &ex_head, float &ex_tail) {
+  const int v0 = vb + lane;
   const uint32_t ni = Elem<E>::kNegInfWord;
 #pragma unroll
   for (int j = 0; j < kVPL; ++j) {
     const int v = v0 + j * 32;
-    buf[j] = (v < g.nv) ? ld_stream(g.vecs + v) : make_uint4(ni, ni, ni, ni);
+    buf[j] = (v < ve) ? ld_stream(g.vecs + v) : make_uint4(ni, ni, ni, ni);
   }
   ex_head = -INFINITY;
   ex_tail = -INFINITY;
-  if (chunk == 0) {
+  if (scalars) {
     if (lane < g.h) ex_head = ld_elem<E>(row + lane);
     if (lane < g.tl) ex_tail = ld_elem<E>(row + g.h + g.nv * Elem<E>::kPerVec + lane);
   }
+}
+
+// One unit of the stream kernel: chunk `chunk` of the row (its head/tail scalars with chunk 0).
+template <typename E>
+__device__ __forceinline__ void load_unit(const E *row, const RowGeom &g, int chunk, int lane,
+                                          uint4 (&buf)[kVPL], float &ex_head, float &ex_tail) {
+  load_span<E>(row, g, chunk * kUnitVecs, g.nv, chunk == 0, lane, buf, ex_head, ex_tail);
 }
 
 // NaN-propagating maximum of a lane's unit values.
@@ -311,7 +322,7 @@ __device__ __forceinline__ float vec_max(const uint4 &v) {
 // the warp maximum locate it through their per-vector maxima: first vector, then element.
 template <typename E>
 __device__ __forceinline__ void unit_argmax(const uint4 (&buf)[kVPL], float eh, float et,
-                                            const RowGeom &g, int chunk, int lane, float &v_out,
+                                            const RowGeom &g, int vb, int lane, float &v_out,
                                             int &i_out) {
   constexpr int kEPV = Elem<E>::kPerVec;
   float vm[kVPL];
@@ -344,7 +355,7 @@ __device__ __forceinline__ void unit_argmax(const uint4 (&buf)[kVPL], float eh, 
 #pragma unroll
           for (int e = kEPV - 1; e >= 0; --e)
             if (vec_elem<E>(t, e) == wm) e0 = e;
-          idx = g.h + (chunk * kUnitVecs + js * 32 + lane) * kEPV + e0;
+          idx = g.h + (vb + js * 32 + lane) * kEPV + e0;
         } else {
           idx = g.h + g.nv * kEPV + lane;             // the tail element
         }
@@ -355,6 +366,33 @@ __device__ __forceinline__ void unit_argmax(const uint4 (&buf)[kVPL], float eh, 
   }
   v_out = wm;
   i_out = idx;
+}
+
+// The logit at token x (0 <= x < V) if the span [vb, ve) of interior vectors (or, with
+// `scalars`, the row's head/tail elements) holds it: taken from the register of the lane that
+// loaded it (a shuffle), or re-read for a head/tail element. Returns whether this span holds x
+// (the same on every lane); *val is valid on lane 0.
+template <typename E>
+__device__ __forceinline__ bool span_logit(const E *row, const RowGeom &g, int vb, int ve,
+                                           bool scalars, int x, int lane,
+                                           const uint4 (&buf)[kVPL], float *val) {
+  constexpr int kEPV = Elem<E>::kPerVec;
+  const int rel = x - g.h;
+  const int vx = rel >= 0 ? rel / kEPV : -1;
+  if (rel >= 0 && vx < g.nv) {
+    if (vx < vb || vx >= ve) return false;
+    // slot (vx - vb) = j*32 + owner lane: pick vector j, then element e
+    const int js = (vx - vb) >> 5, owner = (vx - vb) & 31, e = rel - vx * kEPV;
+    uint4 t = buf[0];
+#pragma unroll
+    for (int j = 1; j < kVPL; ++j)
+      if (j == js) t = buf[j];
+    *val = __shfl_sync(0xffffffffu, vec_elem<E>(t, e), owner);
+    return true;
+  }
+  if (!scalars) return false;
+  if (lane == 0) *val = ld_elem<E>(row + x);
+  return true;
 }
 
 // ------------------------------------------------------------------ block helpers
@@ -552,16 +590,20 @@ __device__ int pick_in_slice(const E *P, const E *Q, float Mt, float iZt, float 
   }
   if (lane == 31) sh.warp_tot[warp] = incl_w;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float o = base;
-    sh.off[0] = base;
-    for (int w = 0; w < kWarps; ++w) {
-      o = __fadd_rn(o, sh.warp_tot[w]);
-      sh.off[w + 1] = o;
+  if (warp == 0) {   // warp offsets: base + inclusive scan of the warp totals
+    float v = (lane < kWarps) ? sh.warp_tot[lane] : 0.f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v = __fadd_rn(v, y);
     }
-    sh.seg = -1;
-    sh.mode = mode;
-    sh.base = base;
+    if (lane < kWarps) sh.off[lane + 1] = __fadd_rn(base, v);
+    if (lane == 0) {
+      sh.off[0] = base;
+      sh.seg = -1;
+      sh.mode = mode;
+      sh.base = base;
+    }
   }
   __syncthreads();
   if (mode == 0) {
@@ -719,9 +761,16 @@ __device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float
         float m = -INFINITY, s = 0.f;
         stat_merge(m, s, __uint_as_float(v[q][0].x), __uint_as_float(v[q][0].y), p.c2);
         stat_merge(m, s, __uint_as_float(v[q][1].x), __uint_as_float(v[q][1].y), p.c2);
-        for (int c = lane + 64; c < p.C; c += 32) {
-          const uint2 w = ldcg_u2(base + static_cast<long long>(r) * p.C + c);
-          stat_merge(m, s, __uint_as_float(w.x), __uint_as_float(w.y), p.c2);
+        // partials beyond the first 64: four loads in flight per lane, merged in index order
+        const uint2 *pr = base + static_cast<long long>(r) * p.C;
+        for (int c0 = lane + 64; c0 < p.C; c0 += 128) {
+          uint2 w[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            w[t] = (c0 + 32 * t < p.C) ? ldcg_u2(pr + c0 + 32 * t) : make_uint2(0xff800000u, 0u);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            stat_merge(m, s, __uint_as_float(w[t].x), __uint_as_float(w[t].y), p.c2);
         }
         warp_stat_merge(m, s, p.c2);
         if (lane == 0) { rowM[r] = m; rowZ[r] = s; }
@@ -755,9 +804,16 @@ __device__ __forceinline__ void combine_rows_arg(const Params &p, int b, int *g,
         int bi = 0x7fffffff;
         arg_merge(bv, bi, __uint_as_float(v[q][0].x), static_cast<int>(v[q][0].y));
         arg_merge(bv, bi, __uint_as_float(v[q][1].x), static_cast<int>(v[q][1].y));
-        for (int c = lane + 64; c < p.C; c += 32) {
-          const uint2 w = ldcg_u2(base + static_cast<long long>(r) * p.C + c);
-          arg_merge(bv, bi, __uint_as_float(w.x), static_cast<int>(w.y));
+        const uint2 *pr = base + static_cast<long long>(r) * p.C;
+        for (int c0 = lane + 64; c0 < p.C; c0 += 128) {
+          uint2 w[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            w[t] = (c0 + 32 * t < p.C) ? ldcg_u2(pr + c0 + 32 * t)
+                                       : make_uint2(0xff800000u, 0x7fffffffu);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            arg_merge(bv, bi, __uint_as_float(w[t].x), static_cast<int>(w[t].y));
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -775,24 +831,33 @@ __device__ __forceinline__ void combine_rows_arg(const Params &p, int b, int *g,
 // shared memory), copies the drafts to xs (shared memory) and runs the acceptance test of every
 // draft with one warp ballot per 32 positions. Returns 0 with *n = the number of accepted
 // drafts (on every thread), or a device error code (a non-finite row, a token outside [0, V)).
-__device__ inline int chain_accept(const Params &p, int b, float *rowM, float *rowZ, int *xs,
-                                   TailShared &sh, int *n_out) {
+//
+// kFused: the row statistics are already in rowM/rowZ and the draft-token logits in xl_smem
+// (shared memory), gathered by the cluster; otherwise both come from the stream kernel's
+// workspace.
+template <bool kFused>
+__device__ inline int chain_accept(const Params &p, int b, float *rowM, float *rowZ,
+                                   const float *xl_smem, int *xs, TailShared &sh, int *n_out) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = p.R, gamma = p.gamma;
   const float c2 = p.c2;
   const float *ub = p.uniforms + static_cast<long long>(b) * (gamma + 1);
   const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
-  const float *xl = p.ws_xlogit + static_cast<long long>(b) * R;
+  const float *xl = kFused ? xl_smem : p.ws_xlogit + static_cast<long long>(b) * R;
+  auto ldx = [&](int i) -> float { return kFused ? xl[i] : ldcg_f(xl + i); };
   // one round trip: warp 0 fetches the first 32 positions' inputs, every thread a share of the
   // drafts, every warp the unit partials of its rows
   float ui = 0.f, lti = 0.f, ldi = 0.f;
   if (warp == 0 && lane < gamma) {
     ui = ub[lane];
-    lti = ldcg_f(xl + lane);
-    ldi = ldcg_f(xl + gamma + 1 + lane);
+    lti = ldx(lane);
+    ldi = ldx(gamma + 1 + lane);
   }
-  for (int i = threadIdx.x; i < gamma; i += kThreads) xs[i] = x[i];
-  combine_rows_stats(p, b, rowM, rowZ);
+  // gamma <= SPEC_MAX_GAMMA < kThreads: one draft per thread, kept in a register until the
+  // partial loads below have been issued (a shared store would wait for it)
+  const int xv = (static_cast<int>(threadIdx.x) < gamma) ? x[threadIdx.x] : 0;
+  if (!kFused) combine_rows_stats(p, b, rowM, rowZ);
+  if (static_cast<int>(threadIdx.x) < gamma) xs[threadIdx.x] = xv;
   __syncthreads();
   if (warp == 0) {
     int err = 0;
@@ -809,7 +874,7 @@ __device__ inline int chain_accept(const Params &p, int b, float *rowM, float *r
         const int i = i0 + lane;
         bool rej = false;
         if (i < gamma) {
-          if (i0 > 0) { ui = ub[i]; lti = ldcg_f(xl + i); ldi = ldcg_f(xl + gamma + 1 + i); }
+          if (i0 > 0) { ui = ub[i]; lti = ldx(i); ldi = ldx(gamma + 1 + i); }
           const int rd = gamma + 1 + i;
           rej = rejects(ui, lti, ldi, rowM[i], rowZ[i], rowM[rd], rowZ[rd], c2);
         }
@@ -886,6 +951,9 @@ __device__ void tail_chain_sample_regs(const Params &p, int b, float m0, float z
   emit_chain(p, b, n, tok, x, lane, 32);
 }
 
+// Greedy chain: smem holds g[R] (row argmaxes), gok[R] (row usable), xs[gamma]. kFused: g and
+// gok were filled by the caller; otherwise they are gathered here from the unit partials.
+template <bool kFused>
 __device__ inline void tail_chain_greedy(const Params &p, int b, float *smem, TailShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = p.R, gamma = p.gamma;
@@ -893,8 +961,9 @@ __device__ inline void tail_chain_greedy(const Params &p, int b, float *smem, Ta
   int *gok = g + R;
   int *xs = gok + R;
   const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
-  for (int i = threadIdx.x; i < gamma; i += kThreads) xs[i] = x[i];
-  combine_rows_arg(p, b, g, gok);
+  const int xv = (static_cast<int>(threadIdx.x) < gamma) ? x[threadIdx.x] : 0;
+  if (!kFused) combine_rows_arg(p, b, g, gok);
+  if (static_cast<int>(threadIdx.x) < gamma) xs[threadIdx.x] = xv;
   __syncthreads();
   if (warp == 0) {
     int err = 0;
@@ -925,6 +994,9 @@ __device__ inline void tail_chain_greedy(const Params &p, int b, float *smem, Ta
   emit_chain(p, b, sh.n, g[sh.n], xs, threadIdx.x, kThreads);
 }
 
+// Greedy tree (any N up to SPEC_MAX_NODES): smem holds g[N], then par, tok, anc, acc, dep
+// (N ints each). kFused: g and the row-usable flags (in anc) were filled by the caller.
+template <bool kFused>
 __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared &sh) {
   const int N = p.N;
   int *g = reinterpret_cast<int *>(smem);
@@ -940,7 +1012,7 @@ __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared
     par[j] = p.parents[bN + j];
     tok[j] = (j == 0) ? 0 : p.tokens[bN + j];
   }
-  combine_rows_arg(p, b, g, anc);   // anc[] holds the row-usable flags until reused below
+  if (!kFused) combine_rows_arg(p, b, g, anc);   // anc[] holds the row-usable flags until reused
   __syncthreads();
   for (int j = threadIdx.x; j < N; j += kThreads) {
     if (!anc[j]) atomicCAS(&sh.err, 0, SPEC_ERR_NONFINITE);
@@ -1008,98 +1080,165 @@ __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared
   }
 }
 
-// probabilities of one row (b = row index): one write pass
-template <typename E, bool kGreedy>
-__device__ void tail_probs(const Params &p, int b, TailShared &sh) {
+// Greedy tree verification for trees of at most 64 nodes: all warps combine the argmax
+// partials into shared memory, then warp 0 holds nodes lane and lane + 32 in registers and does
+// the rest with shuffles (no block barriers): accepted flags and depths by pointer jumping, the
+// deepest accepted node by a warp maximum, and the path by walking parents back from it.
+// smem holds g[N] and the row-usable flags okf[N]; kFused: filled by the caller.
+template <bool kFused>
+__device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int V = p.V;
-  const float c2 = p.c2;
-  if (warp == 0) {
-    const uint2 *part = p.ws_part + static_cast<long long>(b) * p.C;
-    if (kGreedy) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int c = lane; c < p.C; c += 32) {
-        const uint2 w = ldcg_u2(part + c);
-        arg_merge(bv, bi, __uint_as_float(w.x), static_cast<int>(w.y));
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
-        arg_merge(bv, bi, v2, i2);
-      }
-      if (lane == 0) { sh.err = arg_ok(bv) ? 0 : SPEC_ERR_NONFINITE; sh.token = bi; }
-    } else {
-      float m = -INFINITY, s = 0.f;
-      for (int c = lane; c < p.C; c += 32) {
-        const uint2 v = ldcg_u2(part + c);
-        stat_merge(m, s, __uint_as_float(v.x), __uint_as_float(v.y), c2);
-      }
-      warp_stat_merge(m, s, c2);
-      if (lane == 0) {
-        sh.err = stats_ok(m, s) ? 0 : SPEC_ERR_NONFINITE;
-        sh.base = m;
-        sh.total = s;
-      }
+  const int N = p.N;
+  int *g = reinterpret_cast<int *>(smem);
+  int *okf = g + N;
+  const long long bN = static_cast<long long>(b) * N;
+  int par0 = -1, par1 = -1, tok0 = 0, tok1 = 0;
+  if (warp == 0) {   // issued before the partial loads, used after them
+    if (lane < N) {
+      par0 = p.parents[bN + lane];
+      tok0 = (lane == 0) ? 0 : p.tokens[bN + lane];
+    }
+    if (lane + 32 < N) {
+      par1 = p.parents[bN + lane + 32];
+      tok1 = p.tokens[bN + lane + 32];
     }
   }
+  if (!kFused) combine_rows_arg(p, b, g, okf);
   __syncthreads();
-  const int err = sh.err;
-  const float M = sh.base, iZ = __frcp_rn(sh.total);
-  const int g = sh.token;
-  float *out = p.out_probs + static_cast<long long>(b) * V;
-  const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(b) * V;
-  if (err && threadIdx.x == 0) set_status(p.status, err);
-  auto val = [&](float l) -> float { return __fmul_rn(ex2_shift(l, M, c2), iZ); };
-  const bool vec = !err && !kGreedy && ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) &&
-                   ((reinterpret_cast<uintptr_t>(out) & 15u) == 0);
-  if (vec) {
-    // 8 elements per thread and step (one or two 16-byte loads, two 16-byte stores), with the
-    // loads of kPV steps in flight together
-    constexpr int kPV = 4;
-    const int n8 = V / 8;
-    for (int q0 = threadIdx.x; q0 < n8; q0 += kPV * kThreads) {
-      uint4 w[kPV][2];
+  if (warp != 0) return;   // no block barrier follows
+  const int j0 = lane, j1 = lane + 32;
+  const bool in0 = j0 < N, in1 = j1 < N;
+  auto code = [&](int j, bool in, int par, int tok, int what) -> bool {
+    if (!in) return false;
+    if (what == 0) return okf[j] == 0;
+    if (what == 1) return j == 0 ? (par != -1) : (par < 0 || par >= j);
+    return j > 0 && (tok < 0 || tok >= p.V);
+  };
+  int err = 0;
+  const int codes[3] = {SPEC_ERR_NONFINITE, SPEC_ERR_PARENT, SPEC_ERR_TOKEN};
 #pragma unroll
-      for (int t = 0; t < kPV; ++t) {
-        const int q = q0 + t * kThreads;
-        if (q < n8) {
-          w[t][0] = ld_vec(row + 8 * q);
-          if constexpr (sizeof(E) == 4) w[t][1] = ld_vec(row + 8 * q + 4);
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kPV; ++t) {
-        const int q = q0 + t * kThreads;
-        if (q < n8) {
-          float4 *o4 = reinterpret_cast<float4 *>(out + 8 * q);
-          o4[0] = make_float4(val(raw8_elem<E>(w[t], 0)), val(raw8_elem<E>(w[t], 1)),
-                              val(raw8_elem<E>(w[t], 2)), val(raw8_elem<E>(w[t], 3)));
-          o4[1] = make_float4(val(raw8_elem<E>(w[t], 4)), val(raw8_elem<E>(w[t], 5)),
-                              val(raw8_elem<E>(w[t], 6)), val(raw8_elem<E>(w[t], 7)));
-        }
-      }
-    }
-    for (int k = 8 * n8 + threadIdx.x; k < V; k += kThreads) out[k] = val(ld_elem<E>(row + k));
+  for (int w = 0; w < 3; ++w) {
+    const bool bad = code(j0, in0, par0, tok0, w) || code(j1, in1, par1, tok1, w);
+    if (!err && __any_sync(0xffffffffu, bad)) err = codes[w];
+  }
+  int32_t *pn = p.path_nodes + bN;
+  int32_t *ot = p.out_tokens + bN;
+  if (err) {
+    if (in0) { pn[j0] = -1; ot[j0] = -1; }
+    if (in1) { pn[j1] = -1; ot[j1] = -1; }
+    if (lane == 0) { set_status(p.status, err); p.accept_len[b] = -1; }
     return;
   }
-  auto sval = [&](int k) -> float {
-    if (err) return __int_as_float(0x7fc00000);
-    if (kGreedy) return (k == g) ? 1.f : 0.f;
-    return val(ld_elem<E>(row + k));
-  };
-  // 4-element groups aligned to 16 bytes of the output row
-  const int mis = static_cast<int>((reinterpret_cast<uintptr_t>(out) >> 2) & 3u);
-  const int h = min(V, (4 - mis) & 3);
-  const int ng = (V - h) / 4;
-  for (int k = threadIdx.x; k < h; k += kThreads) out[k] = sval(k);
-  float4 *o4 = reinterpret_cast<float4 *>(out + h);
-  for (int q = threadIdx.x; q < ng; q += kThreads) {
-    const int k = h + 4 * q;
-    o4[q] = make_float4(sval(k), sval(k + 1), sval(k + 2), sval(k + 3));
+  // anc: the node reached so far; pk = (hops << 1) | (every node on the way matched)
+  int anc0 = 0, anc1 = 0, pk0 = 1, pk1 = 1;
+  if (in0 && j0 > 0) { anc0 = par0; pk0 = 2 | (tok0 == g[par0] ? 1 : 0); }
+  if (in1) { anc1 = par1; pk1 = 2 | (tok1 == g[par1] ? 1 : 0); }
+  auto join = [](int a, int c) { return ((((a >> 1) + (c >> 1))) << 1) | (a & c & 1); };
+  for (int span = 1; span < N; span <<= 1) {
+    const int sA = anc0 & 31, sB = anc1 & 31;
+    const int aA0 = __shfl_sync(0xffffffffu, anc0, sA), aA1 = __shfl_sync(0xffffffffu, anc1, sA);
+    const int kA0 = __shfl_sync(0xffffffffu, pk0, sA), kA1 = __shfl_sync(0xffffffffu, pk1, sA);
+    const int aB0 = __shfl_sync(0xffffffffu, anc0, sB), aB1 = __shfl_sync(0xffffffffu, anc1, sB);
+    const int kB0 = __shfl_sync(0xffffffffu, pk0, sB), kB1 = __shfl_sync(0xffffffffu, pk1, sB);
+    const bool hA = anc0 >= 32, hB = anc1 >= 32;
+    pk0 = join(pk0, hA ? kA1 : kA0);
+    pk1 = join(pk1, hB ? kB1 : kB0);
+    anc0 = hA ? aA1 : aA0;
+    anc1 = hB ? aB1 : aB0;
   }
-  for (int k = h + 4 * ng + threadIdx.x; k < V; k += kThreads) out[k] = sval(k);
+  int key = -1;
+  if (in0 && (pk0 & 1)) key = ((pk0 >> 1) << 11) | (2047 - j0);
+  if (in1 && (pk1 & 1)) key = max(key, ((pk1 >> 1) << 11) | (2047 - j1));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, off));
+  const int best = 2047 - (key & 2047);
+  const int D = key >> 11;
+  if (in0 && j0 > D) { pn[j0] = -1; ot[j0] = -1; }
+  if (in1 && j1 > D) { pn[j1] = -1; ot[j1] = -1; }
+  int v = best;
+  for (int d = D; d >= 0; --d) {   // warp-uniform walk from the deepest node to the root
+    const int src = v & 31;
+    const int t0 = __shfl_sync(0xffffffffu, tok0, src), t1 = __shfl_sync(0xffffffffu, tok1, src);
+    const int q0 = __shfl_sync(0xffffffffu, par0, src), q1 = __shfl_sync(0xffffffffu, par1, src);
+    if (lane == 0) {
+      pn[d] = v;
+      if (d > 0) ot[d - 1] = (v >= 32) ? t1 : t0;
+    }
+    v = (v >= 32) ? q1 : q0;
+  }
+  if (lane == 0) {
+    ot[D] = g[best];
+    p.accept_len[b] = D;
+  }
+}
+
+// The correction / bonus draw of chain sampling over a thread-block cluster of S CTAs (S = 1:
+// no cluster), after acceptance gave n: CTA `rank` sums r(k) = max(0, p_n(k) - q_n(k)) (or
+// p_gamma(k)) over its slice of 256-element segments into segsum (shared memory); the slice
+// totals are exchanged through distributed shared memory between two cluster barriers; the CTA
+// whose slice holds u * S picks the token and writes the outputs. Every CTA of the cluster calls
+// it; CTAs other than the writer return from it early.
+template <typename E>
+__device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, const float *rowZ,
+                             const int *xs, float *segsum, TailShared &sh, float &s_total,
+                             float *s_pre) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int S = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int gamma = p.gamma;
+  const E *P = row_ptr<E>(p, b, n);
+  const E *Q = (n < gamma) ? row_ptr<E>(p, b, gamma + 1 + n) : nullptr;
+  const float Mt = rowM[n], iZt = __frcp_rn(rowZ[n]);
+  const float Md = Q ? rowM[gamma + 1 + n] : 0.f, iZd = Q ? __frcp_rn(rowZ[gamma + 1 + n]) : 0.f;
+  const float u = p.uniforms[static_cast<long long>(b) * (gamma + 1) + gamma];
+  const int nseg = (p.V + kSeg - 1) / kSeg;
+  const int K = (nseg + S - 1) / S;
+  const int lo = min(nseg, rank * K), hi = min(nseg, lo + K), nl = hi - lo;
+  segment_sums<E>(P, Q, Mt, iZt, Md, iZd, p.c2, p.V, lo, hi, segsum, lo);
+  __syncthreads();
+  if (threadIdx.x < 32) {   // slice total: strided lane sums, then a fixed xor tree
+    float tot = 0.f;
+    for (int j = threadIdx.x; j < nl; j += 32) tot = __fadd_rn(tot, segsum[j]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot = __fadd_rn(tot, __shfl_xor_sync(0xffffffffu, tot, off));
+    if (threadIdx.x == 0) s_total = tot;
+  }
+  cl.sync();   // every slice total written
+  if (threadIdx.x < 32) {   // lane r reads rank r's total; inclusive scan in rank order
+    const int r = threadIdx.x;
+    float v = (r < S) ? *cl.map_shared_rank(&s_total, r) : 0.f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, v, off);
+      if (r >= off) v = __fadd_rn(v, y);
+    }
+    if (r < S) s_pre[r + 1] = v;
+    if (r == 0) s_pre[0] = 0.f;
+  }
+  cl.sync();   // every CTA has read its peers' totals; shared memory is private again
+  const float Sall = s_pre[S];
+  int tok = -1;
+  if (Q && Sall == 0.f) {
+    // the residual vanished: draw from p_n alone, on the first CTA of the cluster
+    if (rank != 0) return;
+    tok = draw_token_cta<E>(P, nullptr, Mt, iZt, 0.f, 0.f, p.c2, p.V, u, segsum, sh);
+  } else {
+    const float t = __fmul_rn(u, Sall);
+    int owner = -1, mode = 0;
+    for (int r = 0; r < S; ++r)
+      if (owner < 0 && s_pre[r + 1] > t) owner = r;
+    if (owner < 0) {   // t >= S after rounding: the last slice holding mass
+      mode = 1;
+      for (int r = 0; r < S; ++r)
+        if (s_pre[r + 1] > s_pre[r]) owner = r;
+      owner = max(owner, 0);
+    }
+    if (rank != owner) return;
+    tok = pick_in_slice<E>(P, Q, Mt, iZt, Md, iZd, p.c2, p.V, segsum, nl, lo, s_pre[rank], t,
+                           mode, sh);
+  }
+  emit_chain(p, b, n, tok, xs, threadIdx.x, kThreads);
 }
 
 // ------------------------------------------------------------------ the kernels
@@ -1112,13 +1251,15 @@ __device__ void tail_probs(const Params &p, int b, TailShared &sh) {
 // The stream kernel: warp w of the grid reduces units w, w + W, w + 2W, ... (W warps in all),
 // each to one 8-byte partial. For chain sampling it also records the logit at each row's draft
 // token, taken from the registers of the lane that loaded it (or, for a head/tail element,
-// loaded by chunk 0). No barriers, atomics or fences: the finishing kernel starts only after
-// this grid has completed.
+// loaded by chunk 0). No barriers, atomics or fences: the finishing kernel reads the partials
+// only after this grid has completed.
 template <typename E, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) stream_kernel(Params p) {
-  constexpr int kEPV = Elem<E>::kPerVec;
   constexpr bool kStats = (MODE == kChainSample || MODE == kProbs);
+  // The finishing kernel may be scheduled as soon as every CTA of this grid is running; this
+  // grid itself reads nothing before the kernel ahead of it on the stream has completed.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int W = gridDim.x * kWarps;
   for (int unit = blockIdx.x * kWarps + (threadIdx.x >> 5); unit < p.units; unit += W) {
@@ -1144,37 +1285,26 @@ __global__ void __launch_bounds__(kThreads, 2) stream_kernel(Params p) {
     } else {
       float v;
       int i;
-      unit_argmax<E>(buf, eh, et, g, u.chunk, lane, v, i);
+      unit_argmax<E>(buf, eh, et, g, u.chunk * kUnitVecs, lane, v, i);
       part = make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
     }
     if (lane == 0) p.ws_part[unit] = part;
     if constexpr (MODE == kChainSample) {
       if (x >= 0 && x < p.V) {
-        float *dst = p.ws_xlogit + static_cast<long long>(u.b) * p.R + u.r;
-        const int rel = x - g.h;
-        const int vx = rel >= 0 ? rel / kEPV : -1;
-        const int v0 = u.chunk * kUnitVecs;
-        if (rel >= 0 && vx < g.nv) {
-          if (vx >= v0 && vx < v0 + kUnitVecs) {
-            // slot (vx - v0) = j*32 + owner lane: pick vector j, then element e
-            const int js = (vx - v0) >> 5, owner = (vx - v0) & 31, e = rel - vx * kEPV;
-            uint4 t = buf[0];
-#pragma unroll
-            for (int j = 1; j < kVPL; ++j)
-              if (j == js) t = buf[j];
-            const float val = __shfl_sync(0xffffffffu, vec_elem<E>(t, e), owner);
-            if (lane == 0) *dst = val;
-          }
-        } else if (u.chunk == 0 && lane == 0) {
-          *dst = ld_elem<E>(row + x);
-        }
+        const int vb = u.chunk * kUnitVecs;
+        float val = 0.f;
+        if (span_logit<E>(row, g, vb, vb + kUnitVecs, u.chunk == 0, x, lane, buf, &val) &&
+            lane == 0)
+          p.ws_xlogit[static_cast<long long>(u.b) * p.R + u.r] = val;
       }
     }
   }
 }
 
-// Waits until the stream kernel of this call has completed and its writes are visible.
+// Lets the next kernel on the stream (the next call's stream kernel) be scheduled early, then
+// waits until the stream kernel of this call has completed and its writes are visible.
 __device__ __forceinline__ void wait_stream_kernel() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
@@ -1201,7 +1331,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   const int b = blockIdx.x / S;
   wait_stream_kernel();
   int n = 0;
-  const int err = chain_accept(p, b, rowM, rowZ, xs, sh, &n);
+  const int err = chain_accept<false>(p, b, rowM, rowZ, nullptr, xs, sh, &n);
   if (err) {   // the same on every CTA of the cluster: all of them leave here
     if (rank == 0) {
       if (threadIdx.x == 0) set_status(p.status, err);
@@ -1209,54 +1339,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
     }
     return;
   }
-  const int gamma = p.gamma;
-  const E *P = row_ptr<E>(p, b, n);
-  const E *Q = (n < gamma) ? row_ptr<E>(p, b, gamma + 1 + n) : nullptr;
-  const float Mt = rowM[n], iZt = __frcp_rn(rowZ[n]);
-  const float Md = Q ? rowM[gamma + 1 + n] : 0.f, iZd = Q ? __frcp_rn(rowZ[gamma + 1 + n]) : 0.f;
-  const float u = p.uniforms[static_cast<long long>(b) * (gamma + 1) + gamma];
-  const int nseg = (p.V + kSeg - 1) / kSeg;
-  const int K = (nseg + S - 1) / S;
-  const int lo = min(nseg, rank * K), hi = min(nseg, lo + K), nl = hi - lo;
-  segment_sums<E>(P, Q, Mt, iZt, Md, iZd, p.c2, p.V, lo, hi, segsum, lo);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int j = 0; j < nl; ++j) tot = __fadd_rn(tot, segsum[j]);
-    s_total = tot;
-  }
-  cl.sync();   // every slice total written
-  if (threadIdx.x == 0) {
-    float acc = 0.f;
-    for (int r = 0; r < S; ++r) {
-      s_pre[r] = acc;
-      acc = __fadd_rn(acc, *cl.map_shared_rank(&s_total, r));
-    }
-    s_pre[S] = acc;
-  }
-  cl.sync();   // every CTA has read its peers' totals; shared memory is private again
-  const float Sall = s_pre[S];
-  int tok = -1;
-  if (Q && Sall == 0.f) {
-    // the residual vanished: draw from p_n alone, on the first CTA of the cluster
-    if (rank != 0) return;
-    tok = draw_token_cta<E>(P, nullptr, Mt, iZt, 0.f, 0.f, p.c2, p.V, u, segsum, sh);
-  } else {
-    const float t = __fmul_rn(u, Sall);
-    int owner = -1, mode = 0;
-    for (int r = 0; r < S; ++r)
-      if (owner < 0 && s_pre[r + 1] > t) owner = r;
-    if (owner < 0) {   // t >= S after rounding: the last slice holding mass
-      mode = 1;
-      for (int r = 0; r < S; ++r)
-        if (s_pre[r + 1] > s_pre[r]) owner = r;
-      owner = max(owner, 0);
-    }
-    if (rank != owner) return;
-    tok = pick_in_slice<E>(P, Q, Mt, iZt, Md, iZd, p.c2, p.V, segsum, nl, lo, s_pre[rank], t,
-                           mode, sh);
-  }
-  emit_chain(p, b, n, tok, xs, threadIdx.x, kThreads);
+  cluster_draw<E>(p, b, n, rowM, rowZ, xs, segsum, sh, s_total, s_pre);
 }
 
 // Finishing kernel for chain sampling when every row is a single unit (gamma <= 31, V <=
@@ -1289,7 +1372,310 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample_warp(Params p
   tail_chain_sample_regs<E>(p, b, m0, z0, m1, z1, lti, ldi);
 }
 
-// Finishing kernel for greedy chains, trees and probabilities: one CTA per batch row.
+// Four consecutive elements of a row as fp32 (8 bytes of bf16 or 16 bytes of fp32; p must be
+// aligned to that size).
+template <typename E> __device__ __forceinline__ uint2 ld_quad_raw(const E *p);
+template <> __device__ __forceinline__ uint2 ld_quad_raw<uint16_t>(const uint16_t *p) {
+  return __ldcs(reinterpret_cast<const uint2 *>(p));
+}
+template <typename E> __device__ __forceinline__ float quad_elem(const uint2 &lo, const uint2 &hi,
+                                                                 int e);
+template <> __device__ __forceinline__ float quad_elem<uint16_t>(const uint2 &w, const uint2 &,
+                                                                 int e) {
+  const uint32_t x = (e < 2) ? w.x : w.y;
+  return (e & 1) ? bf_hi(x) : bf_lo(x);
+}
+template <> __device__ __forceinline__ float quad_elem<float>(const uint2 &lo, const uint2 &hi,
+                                                              int e) {
+  const uint32_t x = e == 0 ? lo.x : e == 1 ? lo.y : e == 2 ? hi.x : hi.y;
+  return __uint_as_float(x);
+}
+
+// Finishing kernel for probabilities: the same units as the stream kernel, grid-stride, so the
+// write pass is spread evenly over every SM whatever the number of rows. A warp re-reads its
+// unit (an L2 hit right after the stream pass) in groups of four elements, lane l taking groups
+// l, l + 32, ..., so that each 16-byte store instruction of the warp covers 512 contiguous
+// bytes of output; the row's C partials are combined while those loads are in flight. A row
+// found invalid is written as NaN and reported once, by its chunk 0.
+template <typename E, bool kGreedy>
+__global__ void __launch_bounds__(kThreads, 2) finish_probs(Params p) {
+  constexpr int kEPV = Elem<E>::kPerVec;
+  constexpr int kQuads = kUnitVecs * kEPV / 4 / 32;   // groups of four per lane and unit
+  wait_stream_kernel();
+  const int lane = threadIdx.x & 31;
+  const int W = gridDim.x * kWarps;
+  const int V = p.V;
+  const float c2 = p.c2;
+  for (int unit = blockIdx.x * kWarps + (threadIdx.x >> 5); unit < p.units; unit += W) {
+    const UnitId u = unit_id(p, unit);   // one logits row per batch row: u.b is the row
+    const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(u.b) * V;
+    const RowGeom g = row_geom<E>(row, V);
+    const uint2 *part = p.ws_part + static_cast<long long>(u.b) * p.C;
+    const uint2 w0 = (lane < p.C) ? ldcg_u2(part + lane)
+                                  : make_uint2(0xff800000u, kGreedy ? 0x7fffffffu : 0u);
+    // the unit's interior as groups of four: group q covers elements k0 + 4q .. k0 + 4q + 3
+    const int k0 = g.h + u.chunk * kUnitVecs * kEPV;
+    const int nq = min(kUnitVecs, g.nv - u.chunk * kUnitVecs) * kEPV / 4;
+    const E *rq = row + k0;
+    uint2 lo[kQuads], hi[kQuads];
+#pragma unroll
+    for (int i = 0; i < kQuads; ++i) {
+      const int q = lane + 32 * i;
+      if (q < nq) {
+        if constexpr (sizeof(E) == 2) {
+          lo[i] = ld_quad_raw<uint16_t>(rq + 4 * q);
+        } else {
+          const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(rq + 4 * q));
+          lo[i] = make_uint2(v.x, v.y);
+          hi[i] = make_uint2(v.z, v.w);
+        }
+      }
+    }
+    float eh = -INFINITY, et = -INFINITY;
+    if (u.chunk == 0) {
+      if (lane < g.h) eh = ld_elem<E>(row + lane);
+      if (lane < g.tl) et = ld_elem<E>(row + g.h + g.nv * kEPV + lane);
+    }
+    float M = 0.f, iZ = 0.f;
+    int gi = 0;
+    bool ok;
+    if constexpr (kGreedy) {
+      float bv = __uint_as_float(w0.x);
+      int bi = static_cast<int>(w0.y);
+      for (int c = lane + 32; c < p.C; c += 32) {
+        const uint2 w = ldcg_u2(part + c);
+        arg_merge(bv, bi, __uint_as_float(w.x), static_cast<int>(w.y));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
+        arg_merge(bv, bi, v2, i2);
+      }
+      ok = arg_ok(bv);
+      gi = bi;
+    } else {
+      float m = __uint_as_float(w0.x), s = __uint_as_float(w0.y);
+      for (int c = lane + 32; c < p.C; c += 32) {
+        const uint2 w = ldcg_u2(part + c);
+        stat_merge(m, s, __uint_as_float(w.x), __uint_as_float(w.y), c2);
+      }
+      warp_stat_merge(m, s, c2);
+      ok = stats_ok(m, s);
+      M = m;
+      iZ = __frcp_rn(s);
+    }
+    if (!ok && u.chunk == 0 && lane == 0) set_status(p.status, SPEC_ERR_NONFINITE);
+    auto val = [&](float l, int k) -> float {
+      if (!ok) return __int_as_float(0x7fc00000);
+      if constexpr (kGreedy) return (k == gi) ? 1.f : 0.f;
+      else return __fmul_rn(ex2_shift(l, M, c2), iZ);
+    };
+    float *out = p.out_probs + static_cast<long long>(u.b) * V;
+    float *oq = out + k0;
+    const bool vec_out = ((reinterpret_cast<uintptr_t>(oq) & 15u) == 0);
+#pragma unroll
+    for (int i = 0; i < kQuads; ++i) {
+      const int q = lane + 32 * i;
+      if (q < nq) {
+        const int k = k0 + 4 * q;
+        const float4 y = make_float4(val(quad_elem<E>(lo[i], hi[i], 0), k),
+                                     val(quad_elem<E>(lo[i], hi[i], 1), k + 1),
+                                     val(quad_elem<E>(lo[i], hi[i], 2), k + 2),
+                                     val(quad_elem<E>(lo[i], hi[i], 3), k + 3));
+        if (vec_out) {
+          __stcs(reinterpret_cast<float4 *>(oq + 4 * q), y);
+        } else {
+          __stcs(oq + 4 * q, y.x);
+          __stcs(oq + 4 * q + 1, y.y);
+          __stcs(oq + 4 * q + 2, y.z);
+          __stcs(oq + 4 * q + 3, y.w);
+        }
+      }
+    }
+    if (u.chunk == 0) {
+      if (lane < g.h) __stcs(out + lane, val(eh, lane));
+      const int kt = g.h + g.nv * kEPV + lane;
+      if (lane < g.tl) __stcs(out + kt, val(et, kt));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the fused kernel
+//
+// For batches large enough to fill the GPU with one thread-block cluster of S CTAs per batch
+// row, the whole call is one kernel: CTA `rank` of batch row b streams its slice (interior
+// vectors [rank*fper, (rank+1)*fper), plus the head/tail scalars on rank 0) of every row of b,
+// in units of at most 4 KB per warp, and folds the unit results into one accumulator per warp
+// and row (each warp meets its rows in increasing order, so the folding order is fixed). The
+// warp accumulators are combined per row, exported to the other CTAs of the cluster through
+// distributed shared memory, and every CTA combines the S slices of every row in rank order, so
+// all of them hold identical row results without a trip through global memory. Then:
+//   chain sampling: acceptance ballot and the cluster draw of the correction / bonus token;
+//   greedy chain, tree: rank 0 finishes exactly as the one-CTA finishing kernel does.
+// Rows per batch row are limited (R <= kFusedMaxRows) so that the per-warp accumulators fit
+// in shared memory.
+constexpr int kFusedMaxRows = 128;
+
+template <typename E, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) fused_kernel(Params p) {
+  namespace cg = cooperative_groups;
+  constexpr bool kStats = (MODE == kChainSample);
+  constexpr int kEPV = Elem<E>::kPerVec;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int R = p.R;
+  uint2 *wacc = reinterpret_cast<uint2 *>(smem_raw);   // [kWarps][R] warp accumulators
+  uint2 *rowpart = wacc + kWarps * R;                   // [R] this slice's row results
+  float *xl = reinterpret_cast<float *>(rowpart + R);   // [R] draft-token logits found here
+  float *fin = xl + R;                                  // finishing scratch
+  __shared__ TailShared sh;
+  __shared__ int xs[SPEC_MAX_GAMMA];
+  __shared__ float s_total;
+  __shared__ float s_pre[kMaxCluster + 1];
+  cg::cluster_group cl = cg::this_cluster();
+  const int S = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int b = blockIdx.x / S;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint2 neutral = kStats ? make_uint2(0xff800000u, 0u) : make_uint2(0xff800000u, 0x7fffffffu);
+  for (int r = lane; r < R; r += 32) wacc[warp * R + r] = neutral;
+  __syncwarp();
+  const int per = p.fper, U = p.fU;
+  float am = -INFINITY, as = 0.f;   // stats: (m, s); argmax: (value, -)
+  int ai = 0x7fffffff;              // argmax: index
+  int cur = -1;
+  const int total = R * U;
+  for (int t = warp; t < total; t += kWarps) {
+    const int r = t / U, uc = t - r * U;
+    if (r != cur) {
+      if (cur >= 0 && lane == 0)
+        wacc[warp * R + cur] = kStats ? make_uint2(__float_as_uint(am), __float_as_uint(as))
+                                      : make_uint2(__float_as_uint(am), static_cast<uint32_t>(ai));
+      am = -INFINITY;
+      as = 0.f;
+      ai = 0x7fffffff;
+      cur = r;
+    }
+    int x = -1;   // the draft token of this row, fetched before the data so both loads overlap
+    if constexpr (kStats) {
+      if (r != p.gamma) {
+        const int i = (r < p.Rt) ? r : r - p.Rt;
+        x = __ldg(p.tokens + static_cast<long long>(b) * p.gamma + i);
+      }
+    }
+    const E *row = row_ptr<E>(p, b, r);
+    const RowGeom g = row_geom<E>(row, p.V);
+    const int vb = rank * per + uc * kUnitVecs;
+    const int ve = min(g.nv, min((rank + 1) * per, vb + kUnitVecs));
+    const bool scal = (rank == 0 && uc == 0);
+    uint4 buf[kVPL];
+    float eh, et;
+    load_span<E>(row, g, vb, ve, scal, lane, buf, eh, et);
+    if constexpr (kStats) {
+      float m, s2;
+      unit_stats<E>(buf, eh, et, p.c2, m, s2);
+      stat_merge(am, as, m, s2, p.c2);
+      if (x >= 0 && x < p.V) {
+        float val = 0.f;
+        if (span_logit<E>(row, g, vb, ve, scal, x, lane, buf, &val) && lane == 0) xl[r] = val;
+      }
+    } else {
+      float v;
+      int i;
+      unit_argmax<E>(buf, eh, et, g, vb, lane, v, i);
+      arg_merge(am, ai, v, i);
+    }
+  }
+  if (cur >= 0 && lane == 0)
+    wacc[warp * R + cur] = kStats ? make_uint2(__float_as_uint(am), __float_as_uint(as))
+                                  : make_uint2(__float_as_uint(am), static_cast<uint32_t>(ai));
+  __syncthreads();
+  // this slice's result per row: the kWarps accumulators, combined by a fixed xor tree
+  for (int r = warp; r < R; r += kWarps) {
+    const uint2 w = (lane < kWarps) ? wacc[lane * R + r] : neutral;
+    float v = __uint_as_float(w.x), s2 = __uint_as_float(w.y);
+    int i = static_cast<int>(w.y);
+    if constexpr (kStats) {
+      warp_stat_merge(v, s2, p.c2);
+    } else {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+        const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
+        arg_merge(v, i, v2, i2);
+      }
+    }
+    if (lane == 0)
+      rowpart[r] = kStats ? make_uint2(__float_as_uint(v), __float_as_uint(s2))
+                          : make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
+  }
+  cl.sync();   // every slice's row results written
+  // every CTA: the S slices of each row, read in rank order through distributed shared memory
+  const int N = R;
+  float *rowM = fin, *rowZ = fin + R, *xlf = fin + 2 * R;   // chain sampling
+  int *gi = reinterpret_cast<int *>(fin);                      // greedy: row argmaxes
+  int *gok = (MODE == kTree && N > 64) ? gi + 3 * N : gi + N;  // greedy: row-usable flags
+  for (int r = warp; r < R; r += kWarps) {
+    const uint2 w = (lane < S) ? *cl.map_shared_rank(&rowpart[r], lane) : neutral;
+    float v = __uint_as_float(w.x), s2 = __uint_as_float(w.y);
+    int i = static_cast<int>(w.y);
+    if constexpr (kStats) {
+      warp_stat_merge(v, s2, p.c2);
+      if (lane == 0) { rowM[r] = v; rowZ[r] = s2; }
+    } else {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+        const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
+        arg_merge(v, i, v2, i2);
+      }
+      if (lane == 0) { gi[r] = i; gok[r] = arg_ok(v) ? 1 : 0; }
+    }
+  }
+  if constexpr (kStats) {
+    // the draft-token logit of each row, from the CTA whose slice holds the token
+    for (int r = threadIdx.x; r < R; r += kThreads) {
+      float val = 0.f;
+      if (r != p.gamma) {
+        const int i = (r < p.Rt) ? r : r - p.Rt;
+        const int x = p.tokens[static_cast<long long>(b) * p.gamma + i];
+        if (x >= 0 && x < p.V) {
+          const RowGeom g = row_geom<E>(row_ptr<E>(p, b, r), p.V);
+          const int rel = x - g.h;
+          const int vx = rel >= 0 ? rel / kEPV : -1;
+          const int owner = (rel >= 0 && vx < g.nv) ? vx / per : 0;
+          val = *cl.map_shared_rank(&xl[r], owner);
+        }
+      }
+      xlf[r] = val;
+    }
+  }
+  __syncthreads();
+  if constexpr (kStats) {
+    int n = 0;
+    const int err = chain_accept<true>(p, b, rowM, rowZ, xlf, xs, sh, &n);
+    if (err) {   // the same on every CTA of the cluster
+      cl.sync();   // no CTA leaves while a peer may still read its shared memory
+      if (rank == 0) {
+        if (threadIdx.x == 0) set_status(p.status, err);
+        fail_chain_row(p, b, threadIdx.x, kThreads);
+      }
+      return;
+    }
+    // cluster_draw's first cluster barrier also ends every read of rowpart / xl above
+    cluster_draw<E>(p, b, n, rowM, rowZ, xs, fin + 3 * R, sh, s_total, s_pre);
+  } else {
+    cl.sync();   // no CTA leaves while a peer may still read its shared memory
+    if (rank != 0) return;
+    if constexpr (MODE == kChainGreedy) tail_chain_greedy<true>(p, b, fin, sh);
+    else if (N <= 64) tail_tree_small<true>(p, b, fin);
+    else tail_tree<true>(p, b, fin, sh);
+  }
+}
+
+// Finishing kernel for greedy chains and trees: one CTA per batch row.
 template <typename E, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) finish_cta(Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -1297,10 +1683,9 @@ __global__ void __launch_bounds__(kThreads, 2) finish_cta(Params p) {
   __shared__ TailShared sh;
   wait_stream_kernel();
   const int b = blockIdx.x;
-  if constexpr (MODE == kChainGreedy) tail_chain_greedy(p, b, scratch, sh);
-  else if constexpr (MODE == kTree) tail_tree(p, b, scratch, sh);
-  else if constexpr (MODE == kProbs) tail_probs<E, false>(p, b, sh);
-  else tail_probs<E, true>(p, b, sh);
+  if constexpr (MODE == kChainGreedy) tail_chain_greedy<false>(p, b, scratch, sh);
+  else if (p.N <= 64) tail_tree_small<false>(p, b, scratch);
+  else tail_tree<false>(p, b, scratch, sh);
 }
 
 }  // namespace specv

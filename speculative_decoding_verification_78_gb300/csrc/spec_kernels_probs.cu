@@ -9,7 +9,7 @@ template <typename E, int MODE>
 cudaError_t probs(const Params &p, int grid, const FinishPlan &f, cudaStream_t stream) {
   cudaError_t e = launch_stream<E, MODE>(p, grid, stream);
   if (e != cudaSuccess) return e;
-  return launch_dependent(finish_cta<E, MODE>, p, f.grid, 1, f.smem, stream);
+  return launch_dependent(finish_probs<E, MODE == kProbsGreedy>, p, f.grid, 1, 0, stream);
 }
 
 }  // namespace

@@ -1,8 +1,9 @@
 // spec_launch.h -- internal: launch helpers and the per-translation-unit launchers.
 //
-// Every call enqueues two kernels on the caller's stream: stream_kernel<E, MODE> (a plain
-// launch) and its finishing kernel, launched with programmatic stream serialization so that it
-// may start while the stream kernel drains and waits (griddepcontrol.wait) for its results.
+// Every call enqueues two kernels on the caller's stream, both with programmatic stream
+// serialization: stream_kernel<E, MODE>, then its finishing kernel. Each may be scheduled while
+// the kernel ahead of it drains and waits (griddepcontrol.wait) for that kernel's completion
+// before touching memory the other could write.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -17,6 +18,7 @@ struct FinishPlan {
   int cluster;     // CTAs per cluster (1 = no cluster)
   size_t smem;     // dynamic shared memory per CTA
   bool warp_tail;  // chain sampling with single-unit rows: one warp per batch row
+  bool fused;      // one fused_kernel launch does the whole call (no stream kernel)
 };
 
 template <typename Kernel>
@@ -44,10 +46,12 @@ inline cudaError_t launch_dependent(Kernel kernel, const Params &p, int grid, in
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
+// The stream kernel is itself a programmatic dependent of whatever precedes it on the stream:
+// its launch may overlap the previous kernel's last CTAs, and it waits (griddepcontrol.wait)
+// for that kernel to complete before reading anything.
 template <typename E, int MODE>
 inline cudaError_t launch_stream(const Params &p, int grid, cudaStream_t stream) {
-  stream_kernel<E, MODE><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(stream_kernel<E, MODE>, p, grid, 1, 0, stream);
 }
 
 // Launchers: each enqueues the stream kernel and the finishing kernel of its mode for the

@@ -143,3 +143,26 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(bnd, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         bnd.load_library()
+
+
+def test_launch_shape_host_validation(lib):
+    import speculative_decoding_verification_78_gb300 as sv
+    k, g, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    ref = (ctypes.byref(k), ctypes.byref(g), ctypes.byref(c))
+    assert lib.spec_launch_shape(sv.SPEC_CALL_CHAIN, 4, 11, 1000, sv.SPEC_F32, 1.0, *ref) == 0
+    assert k.value in (1, 2) and g.value >= 1 and c.value >= 1
+    assert lib.spec_launch_shape(sv.SPEC_CALL_CHAIN, 4, 11, 1000, sv.SPEC_F32, 1.0,
+                                 None, None, None) == sv.SPEC_ERR_NULL
+    assert lib.spec_launch_shape(sv.SPEC_CALL_CHAIN, 4, 10, 1000, sv.SPEC_F32, 1.0,
+                                 *ref) == sv.SPEC_ERR_SHAPE          # rows_per_b must be odd
+    assert lib.spec_launch_shape(sv.SPEC_CALL_CHAIN, 4, 11, 1000, 7, 1.0,
+                                 *ref) == sv.SPEC_ERR_DTYPE
+    assert lib.spec_launch_shape(sv.SPEC_CALL_CHAIN, 4, 11, 1000, sv.SPEC_F32, -1.0,
+                                 *ref) == sv.SPEC_ERR_TEMP
+    assert lib.spec_launch_shape(sv.SPEC_CALL_TREE, 4, sv.SPEC_MAX_NODES + 1, 1000, sv.SPEC_F32,
+                                 0.0, *ref) == sv.SPEC_ERR_SHAPE
+    assert lib.spec_launch_shape(sv.SPEC_CALL_PROBS, 4, 2, 1000, sv.SPEC_F32, 1.0,
+                                 *ref) == sv.SPEC_ERR_SHAPE
+    assert lib.spec_launch_shape(sv.SPEC_CALL_PROBS, 4, 1, 1000, sv.SPEC_BF16, 0.0, *ref) == 0
+    assert k.value == 2
+    assert lib.spec_launch_shape(9, 4, 1, 1000, sv.SPEC_F32, 1.0, *ref) == sv.SPEC_ERR_SHAPE

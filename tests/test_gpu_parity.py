@@ -270,7 +270,7 @@ def test_tree_shapes_and_errors(orc):
     rng = np.random.default_rng(6)
     V = 600
     for N, kind in [(1, "root"), (9, "chain"), (12, "star"), (64, "rule"), (1024, "random"),
-                    (300, "chain")]:
+                    (300, "chain"), (33, "random"), (63, "chain"), (65, "random"), (64, "chain")]:
         B = 6
         if kind == "root":
             par = np.full((B, 1), -1, np.int32)
@@ -312,6 +312,26 @@ def test_tree_shapes_and_errors(orc):
     assert list(acc) == [2, -1, -1, -1, -1]
     np.testing.assert_array_equal(acc, ra)
     np.testing.assert_array_equal(path[0], rp[0])
+    assert np.all(path[1:] == -1) and np.all(out[1:] == -1)
+    # one kind of error at a time, in a small (<= 64 nodes) and a large tree: the exact code
+    for N in (4, 80):
+        for what, want in (("parent", sv.SPEC_ERR_PARENT), ("token", sv.SPEC_ERR_TOKEN),
+                           ("row", sv.SPEC_ERR_NONFINITE)):
+            par = np.tile(np.arange(-1, N - 1, dtype=np.int32), (3, 1))
+            tgt = np.zeros((3, N, 50), np.float32)
+            tok = np.zeros((3, N), np.int32)
+            if what == "parent":
+                par[1, N - 1] = N - 1
+            elif what == "token":
+                tok[1, N - 2] = -5
+            else:
+                tgt[1, N - 1, 7] = np.inf
+            acc, path, out, st = run_tree(TreeInputs(what, tgt, F32, par, tok))
+            ra, rp, ro, _ = orc.verify_tree(tgt, F32, par, tok)
+            assert st == want, (N, what, st)
+            np.testing.assert_array_equal(acc, ra)
+            np.testing.assert_array_equal(path, rp)
+            np.testing.assert_array_equal(out, ro)
 
 
 def test_deterministic_and_workspace_reuse(orc):
