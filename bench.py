@@ -10,11 +10,11 @@ achieved HBM GB/s against the measured copy bandwidth.
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream, max over ranks.
-Each call's two kernel launches are captured once in a CUDA graph (per input copy) exactly as
-the C entry point enqueues them; a step replays the chain, tree and probs graphs, so the timed
-region measures the GPU work rather than Python's launch rate. Inputs rotate over 3 copies, so
-every buffer is reused only after more than 4x the L2 size of other traffic. Per-call durations
-come from event pairs around every 8th step's graph launches.
+The launches of a step are captured once per input copy in a CUDA graph, exactly as the C entry
+points enqueue them; a step replays that graph, so the timed region measures the GPU work rather
+than Python's launch rate. Every 8th step instead replays one graph per call with CUDA events
+between them: those give the per-call durations. Inputs rotate over 3 copies, so every buffer is
+reused only after more than 4x the L2 size of other traffic.
 `e2e` repeats the step through the same C entry points with inputs in pinned host memory:
 host-to-device copies of the step's inputs and device-to-host copies of all its outputs are
 inside the timed region.
@@ -145,12 +145,10 @@ def launch_shapes(ci, ti):
             ("tree", sv.SPEC_CALL_TREE, ti.B, ti.N, ti.V, 0.0, "tree"),
             ("probs", sv.SPEC_CALL_PROBS, ci.B * (ci.gamma + 1), 1, ci.V, 1.0, "probs")):
         k, grid, cluster = sv.spec_launch_shape(code, B, rows, V, sv.SPEC_BF16, T)
-        if k == 1:
-            names = f"fused_kernel<bf16, {mode}> ({grid} CTAs, clusters of {cluster})"
-        else:
-            fin = {"chain-sample": "finish_chain_sample<bf16>", "tree": "finish_cta<bf16, tree>",
-                   "probs": "finish_probs<bf16>"}[mode]
-            names = f"stream_kernel<bf16, {mode}> + {fin} ({grid} CTAs)"
+        fin = {"chain-sample": "finish_chain_sample<bf16>", "tree": "finish_cta<bf16, tree>",
+               "probs": "finish_probs<bf16>"}[mode]
+        names = (f"stream_kernel<bf16, {mode}> + {fin} ({grid} CTAs"
+                 + (f", clusters of {cluster})" if cluster > 1 else ")"))
         out[kind] = {"launches": k, "kernels": names}
     return out
 
@@ -321,10 +319,11 @@ class Runner:
             raise RuntimeError(f"{kind} call failed: {rc}")
 
     def capture(self):
-        """One CUDA graph per (call, input copy): each holds that call's two kernel launches
-        exactly as the C entry point enqueues them."""
+        """CUDA graphs per input copy k: one holding a whole step (the chain, tree and probs
+        calls, six kernel launches exactly as the C entry points enqueue them), and one per
+        call for the steps whose per-call durations are sampled with events in between."""
         torch = self.torch
-        self.graphs = {}
+        self.graphs, self.step_graphs = {}, {}
         with torch.cuda.stream(self.stream):
             for k in range(ROT):
                 for kind in KINDS:
@@ -336,13 +335,17 @@ class Runner:
                 with torch.cuda.graph(g, stream=self.stream):
                     self.call(kind, k)
                 self.graphs[kind, k] = g
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for kind in KINDS:
+                    self.call(kind, k)
+            self.step_graphs[k] = g
         torch.cuda.synchronize()
 
     def step(self, i, evs=None):
         k = i % ROT
         if evs is None:
-            for kind in KINDS:
-                self.graphs[kind, k].replay()
+            self.step_graphs[k].replay()
         else:
             for j, kind in enumerate(KINDS):
                 evs[j].record(self.stream)

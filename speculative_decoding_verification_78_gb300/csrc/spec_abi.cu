@@ -109,40 +109,10 @@ FinishPlan chain_sample_plan(const Params &p) {
   int S = 1;
   while (2 * S <= cap) S *= 2;
   f.warp_tail = false;
-  f.fused = false;
   f.cluster = S;
   f.grid = p.B * S;
   f.smem = sizeof(float) * (2 * static_cast<size_t>(p.R) + nseg);
   return f;
-}
-
-// The fused single-kernel plan (one cluster of S CTAs per batch row), when it applies: at most
-// kFusedMaxRows rows per batch row, at least one full unit per row and CTA, and enough batch rows
-// that B*S CTAs keep every SM streaming. S is the largest power of two (at most 8) for which
-// the B*S CTAs are all resident at once (two per SM). Fills p.fper / p.fU.
-bool fused_plan(Params &p, int dtype, int mode, FinishPlan &f) {
-  if (p.R > kFusedMaxRows) return false;
-  const int sms = sm_count() > 0 ? sm_count() : 1;
-  const int nvmax = p.V / (16 / elem_size(dtype));
-  if (nvmax < kUnitVecs) return false;
-  int S = 1;
-  while (2 * S <= kMaxCluster && static_cast<long long>(p.B) * 2 * S <= 2LL * sms &&
-         nvmax / (2 * S) >= kUnitVecs)
-    S *= 2;
-  if (static_cast<long long>(p.B) * S < sms) return false;
-  p.fper = (nvmax + S - 1) / S;
-  p.fU = (p.fper + kUnitVecs - 1) / kUnitVecs;
-  const size_t R = static_cast<size_t>(p.R);
-  const size_t nseg = (static_cast<size_t>(p.V) + kSeg - 1) / kSeg;
-  size_t fin = 6 * R;                                       // tree
-  if (mode == kChainSample) fin = 3 * R + nseg;             // rowM, rowZ, xlf, segsum
-  if (mode == kChainGreedy) fin = 2 * R + p.gamma;          // g, gok, xs
-  f.fused = true;
-  f.warp_tail = false;
-  f.grid = p.B * S;
-  f.cluster = S;
-  f.smem = 8 * kWarps * R + 8 * R + 4 * R + 4 * fin;
-  return true;
 }
 
 FinishPlan cta_plan(int rows, size_t smem) {
@@ -195,16 +165,12 @@ void probs_shape(Params &p, int rows, int V, float T) {
 }
 
 // The launch plan of each kind of call (after plan_units).
-FinishPlan chain_finish(Params &p, int dtype, bool greedy) {
-  FinishPlan f{};
-  if (fused_plan(p, dtype, greedy ? kChainGreedy : kChainSample, f)) return f;
+FinishPlan chain_finish(const Params &p, bool greedy) {
   return greedy ? cta_plan(p.B, sizeof(int) * (2 * static_cast<size_t>(p.R) + p.gamma))
                 : chain_sample_plan(p);
 }
 
-FinishPlan tree_finish(Params &p, int dtype) {
-  FinishPlan f{};
-  if (fused_plan(p, dtype, kTree, f)) return f;
+FinishPlan tree_finish(const Params &p) {
   return cta_plan(p.B, sizeof(int) * 6 * static_cast<size_t>(p.N));
 }
 
@@ -260,7 +226,7 @@ int spec_verify_chain(const void *target_logits, const void *draft_logits, int d
   p.status = status;
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const FinishPlan f = chain_finish(p, dtype, greedy);
+  const FinishPlan f = chain_finish(p, greedy);
   const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
                                      f, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
@@ -292,7 +258,7 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
   p.status = status;
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const FinishPlan f = tree_finish(p, dtype);
+  const FinishPlan f = tree_finish(p);
   const cudaError_t e = launch_tree(dtype, p, grid_for(p), f, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
@@ -334,13 +300,13 @@ int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float t
     chain_shape(p, B, (rows_per_b - 1) / 2, V, temperature);
     const int rc = plan_units(p, dtype);
     if (rc != SPEC_OK) return rc;
-    f = chain_finish(p, dtype, temperature == 0.f);
+    f = chain_finish(p, temperature == 0.f);
   } else if (kind == SPEC_CALL_TREE) {
     if (rows_per_b > SPEC_MAX_NODES) return SPEC_ERR_SHAPE;
     tree_shape(p, B, rows_per_b, V);
     const int rc = plan_units(p, dtype);
     if (rc != SPEC_OK) return rc;
-    f = tree_finish(p, dtype);
+    f = tree_finish(p);
   } else if (kind == SPEC_CALL_PROBS) {
     if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
     if (rows_per_b != 1) return SPEC_ERR_SHAPE;
@@ -351,7 +317,7 @@ int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float t
   } else {
     return SPEC_ERR_SHAPE;
   }
-  *kernels = f.fused ? 1 : 2;
+  *kernels = 2;
   *grid = f.grid;
   *cluster = f.cluster;
   return SPEC_OK;

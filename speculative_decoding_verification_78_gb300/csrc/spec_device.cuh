@@ -59,8 +59,6 @@ struct Params {
   int upb;                   // units per batch row, R*C
   int B, gamma, N, V;
   int Rt, Rd, R, C;          // rows per batch row: target, draft, total; units per row
-  int fper;                  // fused kernel: interior vectors per CTA slice of a row
-  int fU;                    // fused kernel: units per CTA slice of a row, ceil(fper / kUnitVecs)
   float c2;                  // log2(e) / T
 };
 
@@ -831,20 +829,15 @@ __device__ __forceinline__ void combine_rows_arg(const Params &p, int b, int *g,
 // shared memory), copies the drafts to xs (shared memory) and runs the acceptance test of every
 // draft with one warp ballot per 32 positions. Returns 0 with *n = the number of accepted
 // drafts (on every thread), or a device error code (a non-finite row, a token outside [0, V)).
-//
-// kFused: the row statistics are already in rowM/rowZ and the draft-token logits in xl_smem
-// (shared memory), gathered by the cluster; otherwise both come from the stream kernel's
-// workspace.
-template <bool kFused>
-__device__ inline int chain_accept(const Params &p, int b, float *rowM, float *rowZ,
-                                   const float *xl_smem, int *xs, TailShared &sh, int *n_out) {
+__device__ inline int chain_accept(const Params &p, int b, float *rowM, float *rowZ, int *xs,
+                                   TailShared &sh, int *n_out) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = p.R, gamma = p.gamma;
   const float c2 = p.c2;
   const float *ub = p.uniforms + static_cast<long long>(b) * (gamma + 1);
   const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
-  const float *xl = kFused ? xl_smem : p.ws_xlogit + static_cast<long long>(b) * R;
-  auto ldx = [&](int i) -> float { return kFused ? xl[i] : ldcg_f(xl + i); };
+  const float *xl = p.ws_xlogit + static_cast<long long>(b) * R;
+  auto ldx = [&](int i) -> float { return ldcg_f(xl + i); };
   // one round trip: warp 0 fetches the first 32 positions' inputs, every thread a share of the
   // drafts, every warp the unit partials of its rows
   float ui = 0.f, lti = 0.f, ldi = 0.f;
@@ -856,7 +849,7 @@ __device__ inline int chain_accept(const Params &p, int b, float *rowM, float *r
   // gamma <= SPEC_MAX_GAMMA < kThreads: one draft per thread, kept in a register until the
   // partial loads below have been issued (a shared store would wait for it)
   const int xv = (static_cast<int>(threadIdx.x) < gamma) ? x[threadIdx.x] : 0;
-  if (!kFused) combine_rows_stats(p, b, rowM, rowZ);
+  combine_rows_stats(p, b, rowM, rowZ);
   if (static_cast<int>(threadIdx.x) < gamma) xs[threadIdx.x] = xv;
   __syncthreads();
   if (warp == 0) {
@@ -951,9 +944,8 @@ __device__ void tail_chain_sample_regs(const Params &p, int b, float m0, float z
   emit_chain(p, b, n, tok, x, lane, 32);
 }
 
-// Greedy chain: smem holds g[R] (row argmaxes), gok[R] (row usable), xs[gamma]. kFused: g and
-// gok were filled by the caller; otherwise they are gathered here from the unit partials.
-template <bool kFused>
+// Greedy chain: smem holds g[R] (row argmaxes), gok[R] (row usable), xs[gamma], gathered here
+// from the unit partials.
 __device__ inline void tail_chain_greedy(const Params &p, int b, float *smem, TailShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = p.R, gamma = p.gamma;
@@ -962,7 +954,7 @@ __device__ inline void tail_chain_greedy(const Params &p, int b, float *smem, Ta
   int *xs = gok + R;
   const int32_t *x = p.tokens + static_cast<long long>(b) * gamma;
   const int xv = (static_cast<int>(threadIdx.x) < gamma) ? x[threadIdx.x] : 0;
-  if (!kFused) combine_rows_arg(p, b, g, gok);
+  combine_rows_arg(p, b, g, gok);
   if (static_cast<int>(threadIdx.x) < gamma) xs[threadIdx.x] = xv;
   __syncthreads();
   if (warp == 0) {
@@ -995,8 +987,7 @@ __device__ inline void tail_chain_greedy(const Params &p, int b, float *smem, Ta
 }
 
 // Greedy tree (any N up to SPEC_MAX_NODES): smem holds g[N], then par, tok, anc, acc, dep
-// (N ints each). kFused: g and the row-usable flags (in anc) were filled by the caller.
-template <bool kFused>
+// (N ints each).
 __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared &sh) {
   const int N = p.N;
   int *g = reinterpret_cast<int *>(smem);
@@ -1012,7 +1003,7 @@ __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared
     par[j] = p.parents[bN + j];
     tok[j] = (j == 0) ? 0 : p.tokens[bN + j];
   }
-  if (!kFused) combine_rows_arg(p, b, g, anc);   // anc[] holds the row-usable flags until reused
+  combine_rows_arg(p, b, g, anc);   // anc[] holds the row-usable flags until reused below
   __syncthreads();
   for (int j = threadIdx.x; j < N; j += kThreads) {
     if (!anc[j]) atomicCAS(&sh.err, 0, SPEC_ERR_NONFINITE);
@@ -1084,8 +1075,7 @@ __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared
 // partials into shared memory, then warp 0 holds nodes lane and lane + 32 in registers and does
 // the rest with shuffles (no block barriers): accepted flags and depths by pointer jumping, the
 // deepest accepted node by a warp maximum, and the path by walking parents back from it.
-// smem holds g[N] and the row-usable flags okf[N]; kFused: filled by the caller.
-template <bool kFused>
+// smem holds g[N] and the row-usable flags okf[N].
 __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int N = p.N;
@@ -1103,7 +1093,7 @@ __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
       tok1 = p.tokens[bN + lane + 32];
     }
   }
-  if (!kFused) combine_rows_arg(p, b, g, okf);
+  combine_rows_arg(p, b, g, okf);
   __syncthreads();
   if (warp != 0) return;   // no block barrier follows
   const int j0 = lane, j1 = lane + 32;
@@ -1331,7 +1321,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   const int b = blockIdx.x / S;
   wait_stream_kernel();
   int n = 0;
-  const int err = chain_accept<false>(p, b, rowM, rowZ, nullptr, xs, sh, &n);
+  const int err = chain_accept(p, b, rowM, rowZ, xs, sh, &n);
   if (err) {   // the same on every CTA of the cluster: all of them leave here
     if (rank == 0) {
       if (threadIdx.x == 0) set_status(p.status, err);
@@ -1501,180 +1491,6 @@ __global__ void __launch_bounds__(kThreads, 2) finish_probs(Params p) {
   }
 }
 
-// ------------------------------------------------------------------ the fused kernel
-//
-// For batches large enough to fill the GPU with one thread-block cluster of S CTAs per batch
-// row, the whole call is one kernel: CTA `rank` of batch row b streams its slice (interior
-// vectors [rank*fper, (rank+1)*fper), plus the head/tail scalars on rank 0) of every row of b,
-// in units of at most 4 KB per warp, and folds the unit results into one accumulator per warp
-// and row (each warp meets its rows in increasing order, so the folding order is fixed). The
-// warp accumulators are combined per row, exported to the other CTAs of the cluster through
-// distributed shared memory, and every CTA combines the S slices of every row in rank order, so
-// all of them hold identical row results without a trip through global memory. Then:
-//   chain sampling: acceptance ballot and the cluster draw of the correction / bonus token;
-//   greedy chain, tree: rank 0 finishes exactly as the one-CTA finishing kernel does.
-// Rows per batch row are limited (R <= kFusedMaxRows) so that the per-warp accumulators fit
-// in shared memory.
-constexpr int kFusedMaxRows = 128;
-
-template <typename E, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) fused_kernel(Params p) {
-  namespace cg = cooperative_groups;
-  constexpr bool kStats = (MODE == kChainSample);
-  constexpr int kEPV = Elem<E>::kPerVec;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int R = p.R;
-  uint2 *wacc = reinterpret_cast<uint2 *>(smem_raw);   // [kWarps][R] warp accumulators
-  uint2 *rowpart = wacc + kWarps * R;                   // [R] this slice's row results
-  float *xl = reinterpret_cast<float *>(rowpart + R);   // [R] draft-token logits found here
-  float *fin = xl + R;                                  // finishing scratch
-  __shared__ TailShared sh;
-  __shared__ int xs[SPEC_MAX_GAMMA];
-  __shared__ float s_total;
-  __shared__ float s_pre[kMaxCluster + 1];
-  cg::cluster_group cl = cg::this_cluster();
-  const int S = static_cast<int>(cl.num_blocks());
-  const int rank = static_cast<int>(cl.block_rank());
-  const int b = blockIdx.x / S;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const uint2 neutral = kStats ? make_uint2(0xff800000u, 0u) : make_uint2(0xff800000u, 0x7fffffffu);
-  for (int r = lane; r < R; r += 32) wacc[warp * R + r] = neutral;
-  __syncwarp();
-  const int per = p.fper, U = p.fU;
-  float am = -INFINITY, as = 0.f;   // stats: (m, s); argmax: (value, -)
-  int ai = 0x7fffffff;              // argmax: index
-  int cur = -1;
-  const int total = R * U;
-  for (int t = warp; t < total; t += kWarps) {
-    const int r = t / U, uc = t - r * U;
-    if (r != cur) {
-      if (cur >= 0 && lane == 0)
-        wacc[warp * R + cur] = kStats ? make_uint2(__float_as_uint(am), __float_as_uint(as))
-                                      : make_uint2(__float_as_uint(am), static_cast<uint32_t>(ai));
-      am = -INFINITY;
-      as = 0.f;
-      ai = 0x7fffffff;
-      cur = r;
-    }
-    int x = -1;   // the draft token of this row, fetched before the data so both loads overlap
-    if constexpr (kStats) {
-      if (r != p.gamma) {
-        const int i = (r < p.Rt) ? r : r - p.Rt;
-        x = __ldg(p.tokens + static_cast<long long>(b) * p.gamma + i);
-      }
-    }
-    const E *row = row_ptr<E>(p, b, r);
-    const RowGeom g = row_geom<E>(row, p.V);
-    const int vb = rank * per + uc * kUnitVecs;
-    const int ve = min(g.nv, min((rank + 1) * per, vb + kUnitVecs));
-    const bool scal = (rank == 0 && uc == 0);
-    uint4 buf[kVPL];
-    float eh, et;
-    load_span<E>(row, g, vb, ve, scal, lane, buf, eh, et);
-    if constexpr (kStats) {
-      float m, s2;
-      unit_stats<E>(buf, eh, et, p.c2, m, s2);
-      stat_merge(am, as, m, s2, p.c2);
-      if (x >= 0 && x < p.V) {
-        float val = 0.f;
-        if (span_logit<E>(row, g, vb, ve, scal, x, lane, buf, &val) && lane == 0) xl[r] = val;
-      }
-    } else {
-      float v;
-      int i;
-      unit_argmax<E>(buf, eh, et, g, vb, lane, v, i);
-      arg_merge(am, ai, v, i);
-    }
-  }
-  if (cur >= 0 && lane == 0)
-    wacc[warp * R + cur] = kStats ? make_uint2(__float_as_uint(am), __float_as_uint(as))
-                                  : make_uint2(__float_as_uint(am), static_cast<uint32_t>(ai));
-  __syncthreads();
-  // this slice's result per row: the kWarps accumulators, combined by a fixed xor tree
-  for (int r = warp; r < R; r += kWarps) {
-    const uint2 w = (lane < kWarps) ? wacc[lane * R + r] : neutral;
-    float v = __uint_as_float(w.x), s2 = __uint_as_float(w.y);
-    int i = static_cast<int>(w.y);
-    if constexpr (kStats) {
-      warp_stat_merge(v, s2, p.c2);
-    } else {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
-        const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
-        arg_merge(v, i, v2, i2);
-      }
-    }
-    if (lane == 0)
-      rowpart[r] = kStats ? make_uint2(__float_as_uint(v), __float_as_uint(s2))
-                          : make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
-  }
-  cl.sync();   // every slice's row results written
-  // every CTA: the S slices of each row, read in rank order through distributed shared memory
-  const int N = R;
-  float *rowM = fin, *rowZ = fin + R, *xlf = fin + 2 * R;   // chain sampling
-  int *gi = reinterpret_cast<int *>(fin);                      // greedy: row argmaxes
-  int *gok = (MODE == kTree && N > 64) ? gi + 3 * N : gi + N;  // greedy: row-usable flags
-  for (int r = warp; r < R; r += kWarps) {
-    const uint2 w = (lane < S) ? *cl.map_shared_rank(&rowpart[r], lane) : neutral;
-    float v = __uint_as_float(w.x), s2 = __uint_as_float(w.y);
-    int i = static_cast<int>(w.y);
-    if constexpr (kStats) {
-      warp_stat_merge(v, s2, p.c2);
-      if (lane == 0) { rowM[r] = v; rowZ[r] = s2; }
-    } else {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
-        const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
-        arg_merge(v, i, v2, i2);
-      }
-      if (lane == 0) { gi[r] = i; gok[r] = arg_ok(v) ? 1 : 0; }
-    }
-  }
-  if constexpr (kStats) {
-    // the draft-token logit of each row, from the CTA whose slice holds the token
-    for (int r = threadIdx.x; r < R; r += kThreads) {
-      float val = 0.f;
-      if (r != p.gamma) {
-        const int i = (r < p.Rt) ? r : r - p.Rt;
-        const int x = p.tokens[static_cast<long long>(b) * p.gamma + i];
-        if (x >= 0 && x < p.V) {
-          const RowGeom g = row_geom<E>(row_ptr<E>(p, b, r), p.V);
-          const int rel = x - g.h;
-          const int vx = rel >= 0 ? rel / kEPV : -1;
-          const int owner = (rel >= 0 && vx < g.nv) ? vx / per : 0;
-          val = *cl.map_shared_rank(&xl[r], owner);
-        }
-      }
-      xlf[r] = val;
-    }
-  }
-  __syncthreads();
-  if constexpr (kStats) {
-    int n = 0;
-    const int err = chain_accept<true>(p, b, rowM, rowZ, xlf, xs, sh, &n);
-    if (err) {   // the same on every CTA of the cluster
-      cl.sync();   // no CTA leaves while a peer may still read its shared memory
-      if (rank == 0) {
-        if (threadIdx.x == 0) set_status(p.status, err);
-        fail_chain_row(p, b, threadIdx.x, kThreads);
-      }
-      return;
-    }
-    // cluster_draw's first cluster barrier also ends every read of rowpart / xl above
-    cluster_draw<E>(p, b, n, rowM, rowZ, xs, fin + 3 * R, sh, s_total, s_pre);
-  } else {
-    cl.sync();   // no CTA leaves while a peer may still read its shared memory
-    if (rank != 0) return;
-    if constexpr (MODE == kChainGreedy) tail_chain_greedy<true>(p, b, fin, sh);
-    else if (N <= 64) tail_tree_small<true>(p, b, fin);
-    else tail_tree<true>(p, b, fin, sh);
-  }
-}
-
 // Finishing kernel for greedy chains and trees: one CTA per batch row.
 template <typename E, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) finish_cta(Params p) {
@@ -1683,9 +1499,9 @@ __global__ void __launch_bounds__(kThreads, 2) finish_cta(Params p) {
   __shared__ TailShared sh;
   wait_stream_kernel();
   const int b = blockIdx.x;
-  if constexpr (MODE == kChainGreedy) tail_chain_greedy<false>(p, b, scratch, sh);
-  else if (p.N <= 64) tail_tree_small<false>(p, b, scratch);
-  else tail_tree<false>(p, b, scratch, sh);
+  if constexpr (MODE == kChainGreedy) tail_chain_greedy(p, b, scratch, sh);
+  else if (p.N <= 64) tail_tree_small(p, b, scratch);
+  else tail_tree(p, b, scratch, sh);
 }
 
 }  // namespace specv

@@ -7,8 +7,6 @@ namespace {
 
 template <typename E>
 cudaError_t chain_sample(const Params &p, int grid, const FinishPlan &f, cudaStream_t stream) {
-  if (f.fused)
-    return launch_dependent(fused_kernel<E, kChainSample>, p, f.grid, f.cluster, f.smem, stream);
   cudaError_t e = launch_stream<E, kChainSample>(p, grid, stream);
   if (e != cudaSuccess) return e;
   if (f.warp_tail)
@@ -18,8 +16,6 @@ cudaError_t chain_sample(const Params &p, int grid, const FinishPlan &f, cudaStr
 
 template <typename E>
 cudaError_t chain_greedy(const Params &p, int grid, const FinishPlan &f, cudaStream_t stream) {
-  if (f.fused)
-    return launch_dependent(fused_kernel<E, kChainGreedy>, p, f.grid, f.cluster, f.smem, stream);
   cudaError_t e = launch_stream<E, kChainGreedy>(p, grid, stream);
   if (e != cudaSuccess) return e;
   return launch_dependent(finish_cta<E, kChainGreedy>, p, f.grid, 1, f.smem, stream);

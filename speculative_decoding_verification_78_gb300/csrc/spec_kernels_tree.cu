@@ -7,7 +7,6 @@ namespace {
 
 template <typename E>
 cudaError_t tree(const Params &p, int grid, const FinishPlan &f, cudaStream_t stream) {
-  if (f.fused) return launch_dependent(fused_kernel<E, kTree>, p, f.grid, f.cluster, f.smem, stream);
   cudaError_t e = launch_stream<E, kTree>(p, grid, stream);
   if (e != cudaSuccess) return e;
   return launch_dependent(finish_cta<E, kTree>, p, f.grid, 1, f.smem, stream);

@@ -18,7 +18,6 @@ struct FinishPlan {
   int cluster;     // CTAs per cluster (1 = no cluster)
   size_t smem;     // dynamic shared memory per CTA
   bool warp_tail;  // chain sampling with single-unit rows: one warp per batch row
-  bool fused;      // one fused_kernel launch does the whole call (no stream kernel)
 };
 
 template <typename Kernel>
