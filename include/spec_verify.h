@@ -167,6 +167,31 @@ const char *spec_status_string(int code);
 int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float temperature,
                       int *kernels, int *grid, int *cluster);
 
+/*
+ * spec_verify_chain without a workspace argument; the pages have no counterpart. It is for
+ * callers that cannot hand the library device memory of their own: a process whose device
+ * memory is all owned by another framework's caching allocator, or a per-step decode path that
+ * must not allocate (an allocation can synchronise the device and fragments memory over a long
+ * run). The scratch is instead a file-scope device array of SPEC_STATIC_SCRATCH_BYTES inside the
+ * library, one per device, reserved when the library's device code is loaded; the call itself
+ * allocates and frees nothing.
+ *   - Nothing in the array needs to start at any particular value.
+ *   - A call whose spec_workspace_bytes(B, 2*gamma+1, V, dtype) exceeds the array returns
+ *     SPEC_ERR_WORKSPACE before anything is enqueued.
+ *   - The array's device address is looked up (cudaGetSymbolAddress) on the first call made on
+ *     each device, with that device current, and cached; make that first call before any
+ *     stream capture begins.
+ *   - Every call on a device shares the one array: two calls that may run at the same time (on
+ *     different streams, or from different host threads without ordering) race on it and give
+ *     undefined results. Calls ordered on one stream are fine.
+ * Arguments, results and every other rule are those of spec_verify_chain.
+ */
+#define SPEC_STATIC_SCRATCH_BYTES (4u << 20)
+int spec_verify_chain_static(const void *target_logits, const void *draft_logits, int dtype,
+                             const int32_t *draft_tokens, const float *uniforms, int B, int gamma,
+                             int V, float temperature, int32_t *accept_len, int32_t *out_tokens,
+                             int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

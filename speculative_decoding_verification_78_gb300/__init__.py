@@ -6,10 +6,10 @@ softmax helper. This package is its thin Python binding; see _binding.py.
 """
 
 from ._binding import (  # noqa: F401
-    EXPORTS, LIB_PATH, SPEC_BF16, SPEC_ERR_ALIGN, SPEC_ERR_DTYPE, SPEC_ERR_LAUNCH,
-    SPEC_ERR_NONFINITE, SPEC_ERR_NULL, SPEC_ERR_PARENT, SPEC_ERR_SHAPE, SPEC_ERR_TEMP,
-    SPEC_ERR_TOKEN, SPEC_ERR_WORKSPACE, SPEC_F32, SPEC_MAX_GAMMA, SPEC_MAX_NODES, SPEC_MAX_V,
-    SPEC_OK, SPEC_CALL_CHAIN, SPEC_CALL_PROBS, SPEC_CALL_TREE, SpecError, check, dtype_flag,
-    load_library, new_workspace, probs, spec_launch_shape, spec_probs, spec_status_string,
-    spec_verify_chain, spec_verify_tree, spec_workspace_bytes, spec_workspace_init, verify_chain,
-    verify_tree)
+    EXPORTS, LIB_PATH, SPEC_BF16, SPEC_CALL_CHAIN, SPEC_CALL_PROBS, SPEC_CALL_TREE,
+    SPEC_ERR_ALIGN, SPEC_ERR_DTYPE, SPEC_ERR_LAUNCH, SPEC_ERR_NONFINITE, SPEC_ERR_NULL,
+    SPEC_ERR_PARENT, SPEC_ERR_SHAPE, SPEC_ERR_TEMP, SPEC_ERR_TOKEN, SPEC_ERR_WORKSPACE, SPEC_F32,
+    SPEC_MAX_GAMMA, SPEC_MAX_NODES, SPEC_MAX_V, SPEC_OK, SPEC_STATIC_SCRATCH_BYTES, SpecError,
+    check, dtype_flag, load_library, new_workspace, probs, spec_launch_shape, spec_probs,
+    spec_status_string, spec_verify_chain, spec_verify_chain_static, spec_verify_tree,
+    spec_workspace_bytes, spec_workspace_init, verify_chain, verify_tree)

@@ -25,7 +25,9 @@ SPEC_MAX_V, SPEC_MAX_GAMMA, SPEC_MAX_NODES = 1 << 20, 255, 1024
 
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_workspace_bytes", "spec_workspace_init", "spec_verify_chain",
-           "spec_verify_tree", "spec_probs", "spec_status_string", "spec_launch_shape")
+           "spec_verify_tree", "spec_probs", "spec_status_string", "spec_launch_shape",
+           "spec_verify_chain_static")
+SPEC_STATIC_SCRATCH_BYTES = 4 << 20
 SPEC_CALL_CHAIN, SPEC_CALL_TREE, SPEC_CALL_PROBS = 0, 1, 2
 
 _lock = threading.Lock()
@@ -65,6 +67,9 @@ def load_library():
         lib.spec_status_string.restype = ctypes.c_char_p
         lib.spec_launch_shape.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp]
         lib.spec_launch_shape.restype = i32
+        lib.spec_verify_chain_static.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, f32, vp, vp,
+                                                 vp, vp]
+        lib.spec_verify_chain_static.restype = i32
         _lib = lib
         return lib
 
@@ -123,6 +128,16 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, uniforms, tempe
         _ptr(target_logits), _ptr(draft_logits), dtype_flag(target_logits), _ptr(draft_tokens),
         _ptr(uniforms), B, g1 - 1, V, float(temperature), _ptr(accept_len), _ptr(out_tokens),
         _ptr(status), _ptr(workspace), _nbytes(workspace), _stream(stream))
+
+
+def spec_verify_chain_static(target_logits, draft_logits, draft_tokens, uniforms, temperature,
+                             accept_len, out_tokens, status, stream=None) -> int:
+    """spec_verify_chain with the library's static scratch instead of a workspace."""
+    B, g1, V = target_logits.shape
+    return load_library().spec_verify_chain_static(
+        _ptr(target_logits), _ptr(draft_logits), dtype_flag(target_logits), _ptr(draft_tokens),
+        _ptr(uniforms), B, g1 - 1, V, float(temperature), _ptr(accept_len), _ptr(out_tokens),
+        _ptr(status), _stream(stream))
 
 
 def spec_verify_tree(target_logits, parents, node_tokens, accept_len, path_nodes, out_tokens,

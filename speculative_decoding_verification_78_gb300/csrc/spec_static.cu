@@ -1,0 +1,49 @@
+// spec_static.cu -- spec_verify_chain_static: chain verification whose scratch lives in a
+// file-scope device array instead of a caller-provided workspace.
+//
+// Some callers cannot hand the library a workspace: a host process whose device memory is
+// entirely owned by another framework's caching allocator, or a per-step decode path that must
+// not allocate (an allocation can synchronise the device and fragment memory over a long run).
+// For them this entry point uses one statically sized device array, reserved when the library
+// is loaded, and never allocates or frees anything itself.
+#include <atomic>
+
+#include <cuda_runtime.h>
+
+#include "spec_verify.h"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = SPEC_STATIC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+// The scratch itself: the same contents a workspace would hold, none of which needs to start
+// at any particular value.
+static __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
+
+// Its device address, looked up once per device (with that device current) and cached.
+std::atomic<void *> g_scratch_addr[kMaxDevices];
+
+}  // namespace
+
+extern "C" int spec_verify_chain_static(const void *target_logits, const void *draft_logits,
+                                        int dtype, const int32_t *draft_tokens,
+                                        const float *uniforms, int B, int gamma, int V,
+                                        float temperature, int32_t *accept_len,
+                                        int32_t *out_tokens, int32_t *status, void *stream) {
+  // the size check needs no device: a call larger than the array is refused up front
+  if (B >= 0 && gamma >= 0 && gamma <= SPEC_MAX_GAMMA) {
+    const size_t need = spec_workspace_bytes(B, 2 * gamma + 1, V, dtype);
+    if (need > kStaticScratchBytes) return SPEC_ERR_WORKSPACE;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_LAUNCH;
+  void *addr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!addr) {
+    if (cudaGetSymbolAddress(&addr, g_scratch) != cudaSuccess || !addr) return SPEC_ERR_LAUNCH;
+    g_scratch_addr[dev].store(addr, std::memory_order_release);
+  }
+  return spec_verify_chain(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma,
+                           V, temperature, accept_len, out_tokens, status, addr,
+                           kStaticScratchBytes, stream);
+}
