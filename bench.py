@@ -168,11 +168,14 @@ def measured_peak():
 
 
 def kernel_source_hash():
+    """Hash of the sources that define the kernels and their launches (the C ABI's host checks
+    and the static-scratch entry point do not change what a kernel reads or writes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_78_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        if f == "spec_device.cuh" or f == "spec_launch.h" or f.startswith("spec_kernels_"):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 

@@ -166,6 +166,13 @@ void probs_shape(Params &p, int rows, int V, float T) {
 
 // The launch plan of each kind of call (after plan_units).
 FinishPlan chain_finish(const Params &p, bool greedy) {
+  if (!greedy && p.C == 1 && p.R <= kResidentChainMaxRows && p.V <= kWarpTailMaxV) {
+    FinishPlan f{};   // batch-row-resident: one kernel, one CTA of 32*R threads per batch row
+    f.resident = true;
+    f.cluster = 1;
+    f.grid = p.B;
+    return f;
+  }
   return greedy ? cta_plan(p.B, sizeof(int) * (2 * static_cast<size_t>(p.R) + p.gamma))
                 : chain_sample_plan(p);
 }
@@ -174,7 +181,24 @@ FinishPlan tree_finish(const Params &p) {
   return cta_plan(p.B, sizeof(int) * 6 * static_cast<size_t>(p.N));
 }
 
-FinishPlan probs_finish(const Params &p) { return cta_plan(grid_for(p), 0); }
+// Probabilities: row-resident (one kernel; a cluster of S CTAs per row, S the fewest that hold
+// the row's interior in registers) when S <= kMaxCluster, else the stream kernel plus the
+// unit-granular write pass.
+FinishPlan probs_finish(const Params &p, int dtype) {
+  const int epv = 16 / elem_size(dtype);
+  const long long quads = static_cast<long long>(p.V / epv) * epv / 4;
+  const long long cap = static_cast<long long>(kThreads) *
+                        (dtype == SPEC_BF16 ? kResQuads<uint16_t> : kResQuads<float>);
+  const long long S = quads > 0 ? (quads + cap - 1) / cap : 1;
+  if (S <= kMaxCluster) {
+    FinishPlan f{};
+    f.resident = true;
+    f.cluster = static_cast<int>(S);
+    f.grid = p.B * f.cluster;
+    return f;
+  }
+  return cta_plan(grid_for(p), 0);
+}
 
 }  // namespace
 
@@ -283,7 +307,7 @@ int spec_probs(const void *logits, int dtype, int rows, int V, float temperature
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
   const cudaError_t e = launch_probs(greedy ? kProbsGreedy : kProbs, dtype, p, grid_for(p),
-                                     probs_finish(p), static_cast<cudaStream_t>(stream));
+                                     probs_finish(p, dtype), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -313,11 +337,11 @@ int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float t
     probs_shape(p, B, V, temperature);
     const int rc = plan_units(p, dtype);
     if (rc != SPEC_OK) return rc;
-    f = probs_finish(p);
+    f = probs_finish(p, dtype);
   } else {
     return SPEC_ERR_SHAPE;
   }
-  *kernels = 2;
+  *kernels = f.resident ? 1 : 2;
   *grid = f.grid;
   *cluster = f.cluster;
   return SPEC_OK;

@@ -37,6 +37,9 @@ constexpr int kUnitVecs = 32 * kVPL;        // vectors per unit (4 KB)
 constexpr int kSeg = 256;                   // residual segment: 32 lanes x 8 elements
 constexpr int kWarpTailMaxV = 2048;         // rows this short get warp-level chain finishing
 constexpr int kMaxCluster = 8;              // CTAs per batch row in the chain finisher
+template <typename E>
+constexpr int kSegIterOf = (sizeof(E) == 2) ? 4 : 2;   // residual segments per warp and pass
+constexpr int kRegSegs = 2;   // residual segments a warp keeps in registers for the one-pass draw
 static_assert(SPEC_MAX_GAMMA < kThreads, "one draft token per thread");
 static_assert(kMaxCluster <= 32, "one cluster rank per lane");
 
@@ -96,6 +99,19 @@ template <> __device__ __forceinline__ float ld_elem<uint16_t>(const uint16_t *p
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// The same widening, as volatile statements: each use is computed where it stands, so the
+// compiler cannot keep dozens of widened copies alive across a reduction to reuse them later.
+__device__ __forceinline__ float bf_lo_v(uint32_t w) {
+  float f;
+  asm volatile("shl.b32 %0, %1, 16;" : "=f"(f) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float bf_hi_v(uint32_t w) {
+  float f;
+  asm volatile("and.b32 %0, %1, 0xffff0000;" : "=f"(f) : "r"(w));
+  return f;
+}
 
 // element e (0..kPerVec-1) of a 16-byte vector, as fp32
 template <typename E> __device__ __forceinline__ float vec_elem(const uint4 &v, int e);
@@ -537,7 +553,7 @@ __device__ __forceinline__ int segment_pick(const float (&r)[8], float ls, int k
 template <typename E>
 __device__ void segment_sums(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
                              float c2, int V, int lo, int hi, float *out, int out_base) {
-  constexpr int kSegIter = (sizeof(E) == 2) ? 4 : 2;
+  constexpr int kSegIter = kSegIterOf<E>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) & 15u) == 0) &&
                       (!Q || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
@@ -1162,6 +1178,140 @@ __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
   }
 }
 
+// The cluster draw when every CTA's slice has at most kWarps * kRegSegs segments: warp w of
+// CTA `rank` loads segments rank*K + w*kRegSegs .. +kRegSegs - 1 (one round trip) and keeps
+// them in registers. Warp totals -> CTA total -> cluster prefix through distributed shared
+// memory; then the warp whose range holds u*S picks the token from its registers and writes
+// the outputs, with no second pass over the rows and no block barrier after the cluster's.
+template <typename E>
+__device__ __noinline__ void cluster_draw_regs(const Params &p, int b, int n, const E *P, const E *Q, float Mt,
+                                  float iZt, float Md, float iZd, float u, const int *xs, int K,
+                                  float *segsum, TailShared &sh, float &s_total) {
+  namespace cg = cooperative_groups;
+  constexpr int kSI = kRegSegs;
+  cg::cluster_group cl = cg::this_cluster();
+  const int S = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int V = p.V;
+  const float c2 = p.c2;
+  const int nseg = (V + kSeg - 1) / kSeg;
+  const int lo = min(nseg, rank * K), hi = min(nseg, lo + K);
+  const int s0 = lo + warp * kSI;
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) & 15u) == 0) &&
+                      (!Q || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
+  uint4 wp[kSI][2], wq[kSI][2];
+#pragma unroll
+  for (int t = 0; t < kSI; ++t) {
+    const int k0 = (s0 + t < hi) ? (s0 + t) * kSeg + lane * 8 : V;
+    load8_raw<E>(P, k0, V, vec_ok, wp[t]);
+    if (Q) load8_raw<E>(Q, k0, V, vec_ok, wq[t]);
+  }
+  auto rval = [&](int t, int e) -> float {
+    return resid(raw8_elem<E>(wp[t], e), Q ? raw8_elem<E>(wq[t], e) : -INFINITY, Q != nullptr,
+                 Mt, iZt, Md, iZd, c2);
+  };
+  float lsum[kSI], ssum[kSI];
+  float wtot = 0.f;
+#pragma unroll
+  for (int t = 0; t < kSI; ++t) {
+    float ls = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ls = __fadd_rn(ls, rval(t, e));
+    lsum[t] = ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xffffffffu, ls, off));
+    ssum[t] = ls;
+    wtot = __fadd_rn(wtot, ls);
+  }
+  if (lane == 0) sh.warp_tot[warp] = wtot;
+  __syncthreads();
+  // this warp's offset inside the slice and the slice total: sequential over the warps
+  float woff = 0.f, ctot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float v = sh.warp_tot[w];
+    if (w == warp) woff = ctot;
+    ctot = __fadd_rn(ctot, v);
+  }
+  if (threadIdx.x == 0) s_total = ctot;
+  cl.sync();   // every slice total written
+  // every warp: the cluster prefix (lane r holds rank r's inclusive prefix)
+  float pre = (lane < S) ? *cl.map_shared_rank(&s_total, lane) : 0.f;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, pre, off);
+    if (lane >= off) pre = __fadd_rn(pre, y);
+  }
+  cl.sync();   // every CTA has read its peers' totals; shared memory is private again
+  const float Sall = __shfl_sync(0xffffffffu, pre, S - 1);
+  if (Q && Sall == 0.f) {
+    // the residual vanished: draw from p_n alone, on the first CTA of the cluster
+    if (rank != 0) return;
+    const int tok = draw_token_cta<E>(P, nullptr, Mt, iZt, 0.f, 0.f, c2, V, u, segsum, sh);
+    emit_chain(p, b, n, tok, xs, threadIdx.x, kThreads);
+    return;
+  }
+  const float t = __fmul_rn(u, Sall);
+  // owner rank: the first whose inclusive prefix exceeds t, else the last holding mass
+  const unsigned over = __ballot_sync(0xffffffffu, lane < S && pre > t);
+  const float prev = __shfl_up_sync(0xffffffffu, pre, 1);
+  const unsigned mass = __ballot_sync(0xffffffffu, lane < S && pre > (lane ? prev : 0.f));
+  int owner, mode = 0;
+  if (over) {
+    owner = __ffs(over) - 1;
+  } else {
+    mode = 1;
+    owner = mass ? 31 - __clz(mass) : 0;
+  }
+  if (rank != owner) return;
+  const float base = (rank == 0) ? 0.f : __shfl_sync(0xffffffffu, pre, rank - 1);
+  // owner warp inside the CTA: the first whose range ends above t (mode 0), else the last
+  // warp with mass; decided from the warp totals every warp holds
+  int ow = -1, lastw = -1;
+  {
+    float acc = base;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float v = sh.warp_tot[w];
+      const float nx = __fadd_rn(acc, v);
+      if (v > 0.f) lastw = w;
+      if (ow < 0 && mode == 0 && nx > t) ow = w;
+      acc = nx;
+    }
+  }
+  int wmode = mode;
+  if (ow < 0) { ow = max(lastw, 0); wmode = 1; }
+  if (warp != ow) return;
+  // inside the owner warp: the segment, then the element
+  float acc = __fadd_rn(base, woff);
+  int seg = -1, lastseg = -1;
+  float segbase = acc, lastbase = acc;
+#pragma unroll
+  for (int q = 0; q < kSI; ++q) {
+    const float nx = __fadd_rn(acc, ssum[q]);
+    if (s0 + q < hi) {
+      if (ssum[q] > 0.f) { lastseg = q; lastbase = acc; }
+      if (seg < 0 && wmode == 0 && nx > t) { seg = q; segbase = acc; }
+    }
+    acc = nx;
+  }
+  int smode = wmode;
+  if (seg < 0) { seg = max(lastseg, 0); segbase = lastbase; smode = 1; }
+  float r[8];
+  float ls = 0.f;
+#pragma unroll
+  for (int q = 0; q < kSI; ++q)
+    if (q == seg) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[e] = rval(q, e);
+      ls = lsum[q];
+    }
+  int tok = segment_pick(r, ls, (s0 + seg) * kSeg + lane * 8, segbase, t, smode, lane);
+  if (tok < 0) tok = V - 1;   // unreachable when the slice holds mass
+  emit_chain(p, b, n, tok, xs, lane, 32);
+}
+
 // The correction / bonus draw of chain sampling over a thread-block cluster of S CTAs (S = 1:
 // no cluster), after acceptance gave n: CTA `rank` sums r(k) = max(0, p_n(k) - q_n(k)) (or
 // p_gamma(k)) over its slice of 256-element segments into segsum (shared memory); the slice
@@ -1184,6 +1334,10 @@ __device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, c
   const float u = p.uniforms[static_cast<long long>(b) * (gamma + 1) + gamma];
   const int nseg = (p.V + kSeg - 1) / kSeg;
   const int K = (nseg + S - 1) / S;
+  if (K <= kWarps * kRegSegs) {   // the same on every CTA of the cluster
+    cluster_draw_regs<E>(p, b, n, P, Q, Mt, iZt, Md, iZd, u, xs, K, segsum, sh, s_total);
+    return;
+  }
   const int lo = min(nseg, rank * K), hi = min(nseg, lo + K), nl = hi - lo;
   segment_sums<E>(P, Q, Mt, iZt, Md, iZd, p.c2, p.V, lo, hi, segsum, lo);
   __syncthreads();
@@ -1488,6 +1642,272 @@ __global__ void __launch_bounds__(kThreads, 2) finish_probs(Params p) {
       const int kt = g.h + g.nv * kEPV + lane;
       if (lane < g.tl) __stcs(out + kt, val(et, kt));
     }
+  }
+}
+
+// ------------------------------------------------------------------ batch-row-resident chains
+//
+// Chain sampling whose rows are single units (V of at most kUnitVecs 16-byte vectors plus an
+// unaligned head and tail, 2*gamma+1 <= 31 rows): one CTA of 32*R threads per batch row, warp r
+// holding row r in registers. Each warp reduces its row to softmax statistics and picks its
+// draft-token logit out of its registers; warp 0 then runs the acceptance ballot and the warp
+// draw of the correction / bonus token (which re-reads the one or two rows it needs from L2).
+// One kernel, one read of every logit, no partials in global memory.
+constexpr int kResidentChainMaxRows = 31;
+
+template <typename E>
+__global__ void __launch_bounds__(1024, 1) chain_resident(Params p) {
+  __shared__ float sM[kResidentChainMaxRows + 1], sZ[kResidentChainMaxRows + 1];
+  __shared__ float sX[kResidentChainMaxRows + 1];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31, r = threadIdx.x >> 5;
+  const int gamma = p.gamma;
+  int x = -1;
+  if (r != gamma) {
+    const int i = (r < p.Rt) ? r : r - p.Rt;
+    x = __ldg(p.tokens + static_cast<long long>(b) * gamma + i);
+  }
+  const E *row = row_ptr<E>(p, b, r);
+  const RowGeom g = row_geom<E>(row, p.V);
+  uint4 buf[kVPL];
+  float eh, et;
+  load_unit<E>(row, g, 0, lane, buf, eh, et);
+  float m, s;
+  unit_stats<E>(buf, eh, et, p.c2, m, s);
+  float xv = 0.f;
+  if (x >= 0 && x < p.V) span_logit<E>(row, g, 0, kUnitVecs, true, x, lane, buf, &xv);
+  if (lane == 0) { sM[r] = m; sZ[r] = s; sX[r] = xv; }
+  __syncthreads();
+  if (r != 0) return;   // no block barrier follows
+  const int R = p.R;
+  const float m0 = (lane < R) ? sM[lane] : 0.f, z0 = (lane < R) ? sZ[lane] : 1.f;
+  const float lti = (lane < gamma) ? sX[lane] : 0.f;
+  const float ldi = (lane < gamma) ? sX[gamma + 1 + lane] : 0.f;
+  tail_chain_sample_regs<E>(p, b, m0, z0, 0.f, 1.f, lti, ldi);
+}
+
+// ------------------------------------------------------------------ row-resident probabilities
+//
+// When a row fits in the registers of a cluster of at most kMaxCluster CTAs, the probability
+// helper is one kernel: the CTAs of cluster `row` load their share of the row once (groups of
+// four elements, thread t taking groups t, t + 512, ..., so that loads and the 16-byte stores
+// of the results are both contiguous across a warp), reduce it to softmax statistics (or an
+// argmax) through warp shuffles, shared memory and, between CTAs, distributed shared memory,
+// and write the probabilities straight from registers: one read and one write of the row, no
+// partials in global memory, no second pass.
+template <typename E>
+constexpr int kResQuads = (sizeof(E) == 2) ? 16 : 8;   // groups of four per thread (64 KB/CTA)
+
+template <typename E, bool kGreedy>
+__global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
+  namespace cg = cooperative_groups;
+  constexpr int kEPV = Elem<E>::kPerVec;
+  constexpr int kQ = kResQuads<E>;
+  __shared__ float red_a[kWarps];
+  __shared__ int red_i[kWarps];
+  __shared__ float part_a, part_b;
+  __shared__ int part_i;
+  cg::cluster_group cl = cg::this_cluster();
+  const int S = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int row_i = blockIdx.x / S;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int V = p.V;
+  const float c2 = p.c2;
+  const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(row_i) * V;
+  const RowGeom g = row_geom<E>(row, V);
+  const int nq = g.nv * kEPV / 4;                       // interior groups of four
+  const int per = (nq + S - 1) / S;
+  const int qb = rank * per, qe = min(nq, qb + per);
+  const E *rq = row + g.h;
+  uint2 lo[kQ];
+  uint2 hi[sizeof(E) == 4 ? kQ : 1];   // fp32 only: the upper two elements of each group
+#pragma unroll
+  for (int i = 0; i < kQ; ++i) {
+    const int q = qb + tid + kThreads * i;
+    if (q < qe) {
+      if constexpr (sizeof(E) == 2) {
+        lo[i] = ld_quad_raw<uint16_t>(rq + 4 * q);
+      } else {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(rq + 4 * q));
+        lo[i] = make_uint2(v.x, v.y);
+        hi[sizeof(E) == 4 ? i : 0] = make_uint2(v.z, v.w);
+      }
+    } else {
+      lo[i] = make_uint2(Elem<E>::kNegInfWord, Elem<E>::kNegInfWord);
+      if constexpr (sizeof(E) == 4) hi[i] = lo[i];
+    }
+  }
+  // element e of group i, as fp32
+  auto el = [&](int i, int e) -> float {
+    if constexpr (sizeof(E) == 2) {
+      const uint32_t x = (e < 2) ? lo[i].x : lo[i].y;
+      return (e & 1) ? bf_hi_v(x) : bf_lo_v(x);
+    } else {
+      const uint32_t x = e == 0 ? lo[i].x : e == 1 ? lo[i].y : e == 2 ? hi[i].x : hi[i].y;
+      return __uint_as_float(x);
+    }
+  };
+  float eh = -INFINITY, et = -INFINITY;
+  if (rank == 0) {
+    if (tid < g.h) eh = ld_elem<E>(row + tid);
+    if (tid < g.tl) et = ld_elem<E>(row + g.h + g.nv * kEPV + tid);
+  }
+  // this thread's elements, then the warp, the CTA and the cluster (all in fixed orders)
+  float a = -INFINITY, bsum = 0.f;
+  int ai = 0x7fffffff;
+  if constexpr (kGreedy) {
+    // the thread's maximum (NaN-propagating), then the lowest index holding it: head elements
+    // precede the interior groups, which precede the tail
+    a = fmax_nan(eh, et);
+    if constexpr (sizeof(E) == 2) {
+      uint32_t w = bmax2_nan(lo[0].x, lo[0].y);
+#pragma unroll
+      for (int i = 1; i < kQ; ++i) w = bmax2_nan(w, bmax2_nan(lo[i].x, lo[i].y));
+      a = fmax_nan(a, fmax_nan(bf_lo(w), bf_hi(w)));
+    } else {
+#pragma unroll
+      for (int i = 0; i < kQ; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a = fmax_nan(a, el(i, e));
+    }
+    if (a == INFINITY) a = __int_as_float(0x7fc00000);
+    if (a == a && a != -INFINITY) {
+      if (eh == a) {
+        ai = tid;
+      } else {
+#pragma unroll
+        for (int i = kQ - 1; i >= 0; --i)
+#pragma unroll
+          for (int e = 3; e >= 0; --e)
+            if (el(i, e) == a) ai = g.h + 4 * (qb + tid + kThreads * i) + e;
+        if (ai == 0x7fffffff) ai = g.h + g.nv * kEPV + tid;   // the tail element
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, a, off);
+      const int i2 = __shfl_xor_sync(0xffffffffu, ai, off);
+      arg_merge(a, ai, v2, i2);
+    }
+  } else {
+    a = fmax_nan(eh, et);
+    if constexpr (sizeof(E) == 2) {
+      uint32_t w = bmax2_nan(lo[0].x, lo[0].y);
+#pragma unroll
+      for (int i = 1; i < kQ; ++i) w = bmax2_nan(w, bmax2_nan(lo[i].x, lo[i].y));
+      a = fmax_nan(a, fmax_nan(bf_lo(w), bf_hi(w)));
+    } else {
+#pragma unroll
+      for (int i = 0; i < kQ; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a = fmax_nan(a, el(i, e));
+    }
+    if (a != -INFINITY) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < kQ; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          acc[e] = __fadd_rn(acc[e], ex2_shift(el(i, e), a, c2));
+      bsum = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+      bsum = __fadd_rn(bsum, __fadd_rn(ex2_shift(eh, a, c2), ex2_shift(et, a, c2)));
+    }
+    warp_stat_merge(a, bsum, c2);
+  }
+  if (lane == 0) {
+    red_a[warp] = a;
+    if constexpr (kGreedy) red_i[warp] = ai;
+    else red_i[warp] = __float_as_int(bsum);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float v = (lane < kWarps) ? red_a[lane] : -INFINITY;
+    int w = (lane < kWarps) ? red_i[lane] : (kGreedy ? 0x7fffffff : 0);
+    if constexpr (kGreedy) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+        const int i2 = __shfl_xor_sync(0xffffffffu, w, off);
+        arg_merge(v, w, v2, i2);
+      }
+      if (lane == 0) { part_a = v; part_i = w; }
+    } else {
+      float z = __int_as_float(w);
+      warp_stat_merge(v, z, c2);
+      if (lane == 0) { part_a = v; part_b = z; }
+    }
+  }
+  if (S > 1) {
+    cl.sync();   // every CTA's partial written
+    if (warp == 0) {
+      float v = -INFINITY, z = 0.f;
+      int w = 0x7fffffff;
+      if (lane < S) {
+        v = *cl.map_shared_rank(&part_a, lane);
+        if constexpr (kGreedy) w = *cl.map_shared_rank(&part_i, lane);
+        else z = *cl.map_shared_rank(&part_b, lane);
+      }
+      if constexpr (kGreedy) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+          const int i2 = __shfl_xor_sync(0xffffffffu, w, off);
+          arg_merge(v, w, v2, i2);
+        }
+      } else {
+        warp_stat_merge(v, z, c2);
+      }
+      __syncwarp();
+      if (lane == 0) { red_a[0] = v; red_i[0] = kGreedy ? w : __float_as_int(z); }
+    }
+    cl.sync();   // every CTA has read its peers' partials
+  } else {
+    __syncthreads();
+    if (tid == 0) { red_a[0] = part_a; red_i[0] = kGreedy ? part_i : __float_as_int(part_b); }
+  }
+  __syncthreads();
+  const float M = red_a[0];
+  const int gi = red_i[0];
+  const float Z = __int_as_float(red_i[0]);
+  const bool ok = kGreedy ? (arg_ok(M) && M != INFINITY) : stats_ok(M, Z);
+  const float iZ = kGreedy ? 0.f : __frcp_rn(Z);
+  if (!ok && rank == 0 && tid == 0) set_status(p.status, SPEC_ERR_NONFINITE);
+  auto val = [&](float l, int k) -> float {
+    if (!ok) return __int_as_float(0x7fc00000);
+    if constexpr (kGreedy) return (k == gi) ? 1.f : 0.f;
+    else return __fmul_rn(ex2_shift(l, M, c2), iZ);
+  };
+  float *out = p.out_probs + static_cast<long long>(row_i) * V;
+  float *oq = out + g.h;
+  const bool vec_out = ((reinterpret_cast<uintptr_t>(oq) & 15u) == 0);
+#pragma unroll
+  for (int i = 0; i < kQ; ++i) {
+    const int q = qb + tid + kThreads * i;
+    if (q < qe) {
+      const int k = g.h + 4 * q;
+      const float4 y = make_float4(val(el(i, 0), k),
+                                   val(el(i, 1), k + 1),
+                                   val(el(i, 2), k + 2),
+                                   val(el(i, 3), k + 3));
+      if (vec_out) {
+        __stcs(reinterpret_cast<float4 *>(oq + 4 * q), y);
+      } else {
+        __stcs(oq + 4 * q, y.x);
+        __stcs(oq + 4 * q + 1, y.y);
+        __stcs(oq + 4 * q + 2, y.z);
+        __stcs(oq + 4 * q + 3, y.w);
+      }
+    }
+  }
+  if (rank == 0) {
+    if (tid < g.h) __stcs(out + tid, val(eh, tid));
+    const int kt = g.h + g.nv * kEPV + tid;
+    if (tid < g.tl) __stcs(out + kt, val(et, kt));
   }
 }
 

@@ -7,6 +7,9 @@ namespace {
 
 template <typename E, int MODE>
 cudaError_t probs(const Params &p, int grid, const FinishPlan &f, cudaStream_t stream) {
+  if (f.resident)
+    return launch_dependent(probs_resident<E, MODE == kProbsGreedy>, p, f.grid, f.cluster, 0,
+                            stream);
   cudaError_t e = launch_stream<E, MODE>(p, grid, stream);
   if (e != cudaSuccess) return e;
   return launch_dependent(finish_probs<E, MODE == kProbsGreedy>, p, f.grid, 1, 0, stream);

@@ -18,6 +18,7 @@ struct FinishPlan {
   int cluster;     // CTAs per cluster (1 = no cluster)
   size_t smem;     // dynamic shared memory per CTA
   bool warp_tail;  // chain sampling with single-unit rows: one warp per batch row
+  bool resident;   // one kernel holds every row in registers (no stream kernel)
 };
 
 template <typename Kernel>

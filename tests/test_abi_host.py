@@ -164,5 +164,9 @@ def test_launch_shape_host_validation(lib):
     assert lib.spec_launch_shape(sv.SPEC_CALL_PROBS, 4, 2, 1000, sv.SPEC_F32, 1.0,
                                  *ref) == sv.SPEC_ERR_SHAPE
     assert lib.spec_launch_shape(sv.SPEC_CALL_PROBS, 4, 1, 1000, sv.SPEC_BF16, 0.0, *ref) == 0
-    assert k.value == 2
+    assert (k.value, g.value, c.value) == (1, 4, 1)      # rows held in registers, one CTA each
+    assert lib.spec_launch_shape(sv.SPEC_CALL_PROBS, 4, 1, 70001, sv.SPEC_F32, 1.0, *ref) == 0
+    assert (k.value, g.value, c.value) == (1, 20, 5)     # a cluster of 5 CTAs per row
+    assert lib.spec_launch_shape(sv.SPEC_CALL_PROBS, 4, 1, 200000, sv.SPEC_F32, 1.0, *ref) == 0
+    assert k.value == 2                                  # too long: stream kernel + write pass
     assert lib.spec_launch_shape(9, 4, 1, 1000, sv.SPEC_F32, 1.0, *ref) == sv.SPEC_ERR_SHAPE

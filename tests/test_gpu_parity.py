@@ -118,9 +118,19 @@ def test_tree_32k_bf16(orc):
 
 @pytest.mark.parametrize("dtype", [F32, BF16])
 @pytest.mark.parametrize("V,T", [(32000, 1.0), (1001, 0.7), (5, 100.0), (4097, 0.01),
-                                 (3000, 0.0)])
+                                 (3000, 0.0), (70001, 0.9), (70001, 0.0), (200000, 1.0)])
 def test_probs(orc, dtype, V, T):
+    """Rows held by one CTA, by clusters of 2..8 CTAs (V = 70001, and 200000 in bf16), and rows
+    too long for a cluster (200000 in fp32), which take the stream kernel and write pass."""
     import speculative_decoding_verification_78_gb300 as sv
+    k, _, cluster = sv.spec_launch_shape(sv.SPEC_CALL_PROBS, 37, 1, V, dtype, T)
+    epv = 8 if dtype == BF16 else 4
+    per_cta = 512 * (16 if dtype == BF16 else 8) * 4          # elements one CTA holds
+    want = -(-((V // epv) * epv) // per_cta)
+    if want <= 8:
+        assert (k, cluster) == (1, max(want, 1))
+    else:
+        assert k == 2 and V == 200000 and dtype == F32
     rng = np.random.default_rng(V)
     x = (rng.standard_normal((37, V)) * 3).astype(np.float32)
     x[::5, ::7] = -np.inf      # masked entries
@@ -135,16 +145,24 @@ def test_probs(orc, dtype, V, T):
         assert err <= 2e-6     # what the kernel actually reaches (fp32 arithmetic)
 
 
-def test_probs_invalid_rows():
+@pytest.mark.parametrize("V", [300, 40000, 200000])
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_probs_invalid_rows(V, T):
+    """NaN, +inf and all -inf rows (one CTA, a cluster, the two-kernel path; sampling and
+    greedy) are written as NaN and reported; the valid row is untouched."""
     import speculative_decoding_verification_78_gb300 as sv
-    x = np.zeros((4, 300), np.float32)
-    x[0, 7] = np.nan
-    x[1, 0] = np.inf
+    x = np.zeros((4, V), np.float32)
+    x[0, V - 7] = np.nan
+    x[1, V // 2] = np.inf
     x[2, :] = -np.inf
-    pr, st = sv.probs(dev(x), 1.0)
+    pr, st = sv.probs(dev(x), T)
     p = pr.cpu().numpy()
     assert int(st.item()) == sv.SPEC_ERR_NONFINITE
-    assert np.all(np.isnan(p[:3])) and np.allclose(p[3], 1 / 300)
+    assert np.all(np.isnan(p[:3]))
+    if T > 0:
+        assert np.allclose(p[3], 1 / V)
+    else:
+        assert p[3, 0] == 1.0 and np.all(p[3, 1:] == 0.0)
 
 
 # --------------------------------------------------------------------------- edge cases
@@ -236,6 +254,23 @@ def test_long_draft_gamma_40(orc):
     assert gpu[2] == 0
     compare_chain(orc, ci, gpu)
     assert gpu[0].max() > 32
+
+
+@pytest.mark.parametrize("gamma,V,dtype,kernels", [(4, 1000, F32, 1), (15, 2000, BF16, 1),
+                                                   (20, 500, F32, 2), (31, 1024, F32, 2)])
+def test_single_unit_rows(orc, gamma, V, dtype, kernels):
+    """Rows of one unit: up to 31 rows per batch row in one CTA (one kernel); 16 <= gamma <= 31
+    in the stream kernel plus the one-warp finish (two kernels)."""
+    import speculative_decoding_verification_78_gb300 as sv
+    B = 200
+    assert sv.spec_launch_shape(sv.SPEC_CALL_CHAIN, B, 2 * gamma + 1, V, dtype,
+                                1.0)[0] == kernels
+    ci = chain_32k(seed=17 + gamma, B=B, gamma=gamma, V=V, dtype=dtype, peaked=4, boost=3.0)
+    ci.draft = (ci.draft if gamma < 20 else ci.target[:, :gamma].copy())
+    for off in (0, 1):
+        gpu = run_chain(ci, offset_elems=off)
+        assert gpu[2] == 0
+        compare_chain(orc, ci, gpu)
 
 
 def test_largest_vocab(orc):
