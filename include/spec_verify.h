@@ -154,8 +154,10 @@ const char *spec_status_string(int code);
  * nothing and touches no memory (for tests and profiling; the pages have no counterpart).
  *   kind        SPEC_CALL_CHAIN (rows_per_b = 2*gamma+1, any temperature), SPEC_CALL_TREE
  *               (rows_per_b = N) or SPEC_CALL_PROBS (B = rows, rows_per_b = 1)
- *   kernels[0]  kernel launches per call: 2 (a stream kernel over every row, then the
- *               finishing kernel, launched as its programmatic dependent)
+ *   kernels[0]  kernel launches per call: 1 when one kernel holds every row in registers
+ *               (spec_probs with rows of at most 8 x 64 KB of logits), else 2 (a stream kernel
+ *               over every row, then the finishing kernel, launched as its programmatic
+ *               dependent)
  *   grid[0]     CTAs of the launch that finishes the call
  *   cluster[0]  its thread-block cluster size (1 = no cluster)
  * Returns SPEC_OK or SPEC_ERR_NULL / SHAPE / DTYPE / TEMP. The shape depends on the device's

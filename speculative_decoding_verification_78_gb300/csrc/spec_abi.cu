@@ -166,13 +166,6 @@ void probs_shape(Params &p, int rows, int V, float T) {
 
 // The launch plan of each kind of call (after plan_units).
 FinishPlan chain_finish(const Params &p, bool greedy) {
-  if (!greedy && p.C == 1 && p.R <= kResidentChainMaxRows && p.V <= kWarpTailMaxV) {
-    FinishPlan f{};   // batch-row-resident: one kernel, one CTA of 32*R threads per batch row
-    f.resident = true;
-    f.cluster = 1;
-    f.grid = p.B;
-    return f;
-  }
   return greedy ? cta_plan(p.B, sizeof(int) * (2 * static_cast<size_t>(p.R) + p.gamma))
                 : chain_sample_plan(p);
 }

@@ -1645,49 +1645,6 @@ __global__ void __launch_bounds__(kThreads, 2) finish_probs(Params p) {
   }
 }
 
-// ------------------------------------------------------------------ batch-row-resident chains
-//
-// Chain sampling whose rows are single units (V of at most kUnitVecs 16-byte vectors plus an
-// unaligned head and tail, 2*gamma+1 <= 31 rows): one CTA of 32*R threads per batch row, warp r
-// holding row r in registers. Each warp reduces its row to softmax statistics and picks its
-// draft-token logit out of its registers; warp 0 then runs the acceptance ballot and the warp
-// draw of the correction / bonus token (which re-reads the one or two rows it needs from L2).
-// One kernel, one read of every logit, no partials in global memory.
-constexpr int kResidentChainMaxRows = 31;
-
-template <typename E>
-__global__ void __launch_bounds__(1024, 1) chain_resident(Params p) {
-  __shared__ float sM[kResidentChainMaxRows + 1], sZ[kResidentChainMaxRows + 1];
-  __shared__ float sX[kResidentChainMaxRows + 1];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31, r = threadIdx.x >> 5;
-  const int gamma = p.gamma;
-  int x = -1;
-  if (r != gamma) {
-    const int i = (r < p.Rt) ? r : r - p.Rt;
-    x = __ldg(p.tokens + static_cast<long long>(b) * gamma + i);
-  }
-  const E *row = row_ptr<E>(p, b, r);
-  const RowGeom g = row_geom<E>(row, p.V);
-  uint4 buf[kVPL];
-  float eh, et;
-  load_unit<E>(row, g, 0, lane, buf, eh, et);
-  float m, s;
-  unit_stats<E>(buf, eh, et, p.c2, m, s);
-  float xv = 0.f;
-  if (x >= 0 && x < p.V) span_logit<E>(row, g, 0, kUnitVecs, true, x, lane, buf, &xv);
-  if (lane == 0) { sM[r] = m; sZ[r] = s; sX[r] = xv; }
-  __syncthreads();
-  if (r != 0) return;   // no block barrier follows
-  const int R = p.R;
-  const float m0 = (lane < R) ? sM[lane] : 0.f, z0 = (lane < R) ? sZ[lane] : 1.f;
-  const float lti = (lane < gamma) ? sX[lane] : 0.f;
-  const float ldi = (lane < gamma) ? sX[gamma + 1 + lane] : 0.f;
-  tail_chain_sample_regs<E>(p, b, m0, z0, 0.f, 1.f, lti, ldi);
-}
-
 // ------------------------------------------------------------------ row-resident probabilities
 //
 // When a row fits in the registers of a cluster of at most kMaxCluster CTAs, the probability

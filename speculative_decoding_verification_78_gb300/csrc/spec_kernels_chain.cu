@@ -7,18 +7,6 @@ namespace {
 
 template <typename E>
 cudaError_t chain_sample(const Params &p, int grid, const FinishPlan &f, cudaStream_t stream) {
-  if (f.resident) {   // one CTA of 32*R threads per batch row
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(f.grid), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(32 * p.R), 1, 1);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chain_resident<E>, p);
-  }
   cudaError_t e = launch_stream<E, kChainSample>(p, grid, stream);
   if (e != cudaSuccess) return e;
   if (f.warp_tail)

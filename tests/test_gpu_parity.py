@@ -256,11 +256,11 @@ def test_long_draft_gamma_40(orc):
     assert gpu[0].max() > 32
 
 
-@pytest.mark.parametrize("gamma,V,dtype,kernels", [(4, 1000, F32, 1), (15, 2000, BF16, 1),
+@pytest.mark.parametrize("gamma,V,dtype,kernels", [(4, 1000, F32, 2), (15, 2000, BF16, 2),
                                                    (20, 500, F32, 2), (31, 1024, F32, 2)])
 def test_single_unit_rows(orc, gamma, V, dtype, kernels):
-    """Rows of one unit: up to 31 rows per batch row in one CTA (one kernel); 16 <= gamma <= 31
-    in the stream kernel plus the one-warp finish (two kernels)."""
+    """Rows of one unit, up to 63 rows per batch row: the stream kernel plus the one-warp
+    finish, ragged and unaligned."""
     import speculative_decoding_verification_78_gb300 as sv
     B = 200
     assert sv.spec_launch_shape(sv.SPEC_CALL_CHAIN, B, 2 * gamma + 1, V, dtype,

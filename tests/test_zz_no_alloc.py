@@ -37,7 +37,7 @@ def _static_call(ci):
 
 def test_static_scratch_matches_workspace_entry_point():
     import speculative_decoding_verification_78_gb300 as sv
-    cases = [chain_32k(seed=41, B=8, gamma=5, V=32000), chain_tiny(seed=42, B=300)]
+    cases = [chain_32k(seed=41, B=8, gamma=5, V=32000), chain_tiny(seed=42, B=300, gamma=20)]
     for ci in cases:   # both shapes take the two-kernel path, which uses the scratch
         B, g1, V = ci.target.shape
         assert sv.spec_launch_shape(sv.SPEC_CALL_CHAIN, B, 2 * g1 - 1, V, ci.dtype,
