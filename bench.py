@@ -10,11 +10,12 @@ achieved HBM GB/s against the measured copy bandwidth.
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream, max over ranks.
-The launches of a step are captured once per input copy in a CUDA graph, exactly as the C entry
-points enqueue them; a step replays that graph, so the timed region measures the GPU work rather
-than Python's launch rate. Every 8th step instead replays one graph per call with CUDA events
-between them: those give the per-call durations. Inputs rotate over 3 copies, so every buffer is
-reused only after more than 4x the L2 size of other traffic.
+The launches are captured once in CUDA graphs, exactly as the C entry points enqueue them, so
+the timed region measures the GPU work rather than Python's launch rate. The K timed steps run
+as K // 16 blocks: 16 chain calls, then 16 tree calls, then 16 probs calls (one graph each,
+CUDA events between them, which give the per-call durations over the whole timed region), and
+the K % 16 remaining steps as whole-step graphs. Inputs rotate over 6 copies, so a buffer is
+read again only after more than the L2 size (129 MB) of other traffic.
 `e2e` repeats the step through the same C entry points with inputs in pinned host memory:
 host-to-device copies of the step's inputs and device-to-host copies of all its outputs are
 inside the timed region.
@@ -44,8 +45,8 @@ if ROOT not in sys.path:
 METRIC = "verified positions/sec and achieved HBM GB/s (% of GB300 peak) on 1 GPU"
 UNIT = "positions/s"
 L2_BYTES = 129e6
-ROT = 3
-EVENT_EVERY = 8
+ROT = 6
+BLOCK = 16
 KINDS = ("chain", "tree", "probs")
 WORKLOAD = ("verify step: chain B=64 gamma=5 V=32000 bf16 T=1 + tree B=32 N=64 V=32000 bf16 "
             "greedy + probs 384x32000 bf16->fp32 T=1")
@@ -121,7 +122,8 @@ def config_for(world):
     avoided between timed steps."""
     return {"workload": WORKLOAD, "global_batch": world * (64 + 32),
             "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2": f"inputs rotated over {ROT} copies (>4x L2 of traffic between reuses)"}
+            "l2": f"inputs rotated over {ROT} copies (> L2 size of traffic between reuses)",
+            "order": f"timed steps run as blocks of {BLOCK} calls of each kind"}
 
 
 def step_bytes(ci, ti):
@@ -145,10 +147,13 @@ def launch_shapes(ci, ti):
             ("tree", sv.SPEC_CALL_TREE, ti.B, ti.N, ti.V, 0.0, "tree"),
             ("probs", sv.SPEC_CALL_PROBS, ci.B * (ci.gamma + 1), 1, ci.V, 1.0, "probs")):
         k, grid, cluster = sv.spec_launch_shape(code, B, rows, V, sv.SPEC_BF16, T)
-        fin = {"chain-sample": "finish_chain_sample<bf16>", "tree": "finish_cta<bf16, tree>",
-               "probs": "finish_probs<bf16>"}[mode]
-        names = (f"stream_kernel<bf16, {mode}> + {fin} ({grid} CTAs"
-                 + (f", clusters of {cluster})" if cluster > 1 else ")"))
+        shape = f"{grid} CTAs" + (f", clusters of {cluster}" if cluster > 1 else "")
+        if k == 1:
+            names = f"probs_resident<bf16> ({shape})"
+        else:
+            fin = {"chain-sample": "finish_chain_sample<bf16>", "tree": "finish_cta<bf16, tree>",
+                   "probs": "finish_probs<bf16>"}[mode]
+            names = f"stream_kernel<bf16, {mode}> + {fin} ({shape})"
         out[kind] = {"launches": k, "kernels": names}
     return out
 
@@ -322,38 +327,32 @@ class Runner:
             raise RuntimeError(f"{kind} call failed: {rc}")
 
     def capture(self):
-        """CUDA graphs per input copy k: one holding a whole step (the chain, tree and probs
-        calls, six kernel launches exactly as the C entry points enqueue them), and one per
-        call for the steps whose per-call durations are sampled with events in between."""
+        """CUDA graphs, captured once, holding the launches exactly as the C entry points
+        enqueue them: per input copy k, a whole step (chain, tree and probs calls); and per kind
+        of call, BLOCK consecutive calls of that kind over copies 0, 1, ... (mod ROT)."""
         torch = self.torch
-        self.graphs, self.step_graphs = {}, {}
         with torch.cuda.stream(self.stream):
             for k in range(ROT):
                 for kind in KINDS:
                     self.call(kind, k)
         torch.cuda.synchronize()
+        self.step_graphs, self.block_graphs = {}, {}
         for k in range(ROT):
-            for kind in KINDS:
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=self.stream):
-                    self.call(kind, k)
-                self.graphs[kind, k] = g
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=self.stream):
                 for kind in KINDS:
                     self.call(kind, k)
             self.step_graphs[k] = g
+        for kind in KINDS:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for j in range(BLOCK):
+                    self.call(kind, j % ROT)
+            self.block_graphs[kind] = g
         torch.cuda.synchronize()
 
-    def step(self, i, evs=None):
-        k = i % ROT
-        if evs is None:
-            self.step_graphs[k].replay()
-        else:
-            for j, kind in enumerate(KINDS):
-                evs[j].record(self.stream)
-                self.graphs[kind, k].replay()
-            evs[len(KINDS)].record(self.stream)
+    def step(self, i):
+        self.step_graphs[i % ROT].replay()
 
 
 def run_ours(args, rank, world, local):
@@ -362,6 +361,7 @@ def run_ours(args, rank, world, local):
     device = torch.device("cuda", local)
     ci, ti = make_inputs(args.seed_offset + rank)
     r = Runner(ci, ti, device)
+    K = args.steps
     r.capture()
     with torch.cuda.stream(r.stream):
         for i in range(args.warmup):
@@ -369,9 +369,12 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     assert int(r.status.item()) == 0, "device-side error in warm-up"
 
-    K = args.steps
-    nev = (K + EVENT_EVERY - 1) // EVENT_EVERY
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nev)]
+    # K steps of work: K // BLOCK blocks, each the block graph of every kind of call (BLOCK
+    # chain calls, then BLOCK tree calls, then BLOCK probs calls, with CUDA events between
+    # them), then the K % BLOCK remaining steps as whole-step graphs
+    nblk, rem = divmod(K, BLOCK)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KINDS) + 1)]
+           for _ in range(nblk)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -380,8 +383,13 @@ def run_ours(args, rank, world, local):
     host0 = time.perf_counter()
     with torch.cuda.stream(r.stream):
         t0.record(r.stream)
-        for i in range(K):
-            r.step(i, evs[i // EVENT_EVERY] if i % EVENT_EVERY == 0 else None)
+        for b in range(nblk):
+            for j, kind in enumerate(KINDS):
+                evs[b][j].record(r.stream)
+                r.block_graphs[kind].replay()
+            evs[b][len(KINDS)].record(r.stream)
+        for i in range(rem):
+            r.step(i)
         t1.record(r.stream)
     host_issue = time.perf_counter() - host0
     torch.cuda.synchronize()
@@ -391,11 +399,8 @@ def run_ours(args, rank, world, local):
     elapsed = max_over_ranks(elapsed, world, device)
     assert int(r.status.item()) == 0, "device-side error in timed steps"
 
-    per_kernel = {"chain": [], "tree": [], "probs": []}
-    for e in evs:
-        per_kernel["chain"].append(e[0].elapsed_time(e[1]) * 1e-3)
-        per_kernel["tree"].append(e[1].elapsed_time(e[2]) * 1e-3)
-        per_kernel["probs"].append(e[2].elapsed_time(e[3]) * 1e-3)
+    per_kernel = {kind: [e[j].elapsed_time(e[j + 1]) * 1e-3 / BLOCK for e in evs]
+                  for j, kind in enumerate(KINDS)}
     avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
     nbytes = step_bytes(ci, ti)
     peak, peak_kind = measured_peak()

@@ -149,6 +149,18 @@ __device__ __forceinline__ float ex2_shift(float x, float m, float c2) {
 __device__ __forceinline__ uint2 ldcg_u2(const uint2 *p) { return __ldcg(p); }
 __device__ __forceinline__ float ldcg_f(const float *p) { return __ldcg(p); }
 
+// Cluster barrier whose arrival publishes this CTA's earlier shared-memory writes to the other
+// CTAs of the cluster (release / acquire), and one that only orders execution: after it no CTA
+// still needs a peer's shared memory, so a peer may leave or reuse it.
+__device__ __forceinline__ void cluster_sync_publish() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync_exec() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;"
+               ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int code) {
   atomicCAS(reinterpret_cast<int *>(status), 0, code);
 }
@@ -551,7 +563,7 @@ __device__ __forceinline__ int segment_pick(const float (&r)[8], float ls, int k
 // out[seg - out_base]. Each warp takes kSegIter segments per iteration with all their loads
 // in flight together.
 template <typename E>
-__device__ void segment_sums(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
+__device__ __noinline__ void segment_sums(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
                              float c2, int V, int lo, int hi, float *out, int out_base) {
   constexpr int kSegIter = kSegIterOf<E>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -586,7 +598,7 @@ __device__ void segment_sums(const E *P, const E *Q, float Mt, float iZt, float 
 // if rounding leaves no crossing in the slice, the slice's last element with r > 0); mode 1:
 // the last element with r > 0. All threads call it; every thread gets the token.
 template <typename E>
-__device__ int pick_in_slice(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
+__device__ __noinline__ int pick_in_slice(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
                              float c2, int V, const float *segsum, int nl, int lo, float base,
                              float t, int mode, TailShared &sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -662,7 +674,7 @@ __device__ int pick_in_slice(const E *P, const E *Q, float Mt, float iZt, float 
 // CTA-wide inverse-CDF draw over the whole row: the first k whose running sum strictly exceeds
 // u * S. Returns -1 when Q is given and S == 0. segsum: shared memory, ceil(V/kSeg) floats.
 template <typename E>
-__device__ int draw_token_cta(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
+__device__ __noinline__ int draw_token_cta(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
                               float c2, int V, float u, float *segsum, TailShared &sh) {
   const int nseg = (V + kSeg - 1) / kSeg;
   segment_sums<E>(P, Q, Mt, iZt, Md, iZd, c2, V, 0, nseg, segsum, 0);
@@ -1184,7 +1196,7 @@ __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
 // memory; then the warp whose range holds u*S picks the token from its registers and writes
 // the outputs, with no second pass over the rows and no block barrier after the cluster's.
 template <typename E>
-__device__ __noinline__ void cluster_draw_regs(const Params &p, int b, int n, const E *P, const E *Q, float Mt,
+__device__ __forceinline__ void cluster_draw_regs(const Params &p, int b, int n, const E *P, const E *Q, float Mt,
                                   float iZt, float Md, float iZd, float u, const int *xs, int K,
                                   float *segsum, TailShared &sh, float &s_total) {
   namespace cg = cooperative_groups;
@@ -1226,16 +1238,20 @@ __device__ __noinline__ void cluster_draw_regs(const Params &p, int b, int n, co
   }
   if (lane == 0) sh.warp_tot[warp] = wtot;
   __syncthreads();
-  // this warp's offset inside the slice and the slice total: sequential over the warps
-  float woff = 0.f, ctot = 0.f;
+  // every warp: the inclusive scan of the warp totals (lane w holds warps 0..w), so this warp's
+  // offset inside the slice and the slice total come out identical in every warp
+  const float wv = (lane < kWarps) ? sh.warp_tot[lane] : 0.f;
+  float winc = wv;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const float v = sh.warp_tot[w];
-    if (w == warp) woff = ctot;
-    ctot = __fadd_rn(ctot, v);
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, winc, off);
+    if (lane >= off) winc = __fadd_rn(winc, y);
   }
+  const float wexc = __shfl_up_sync(0xffffffffu, winc, 1);
+  const float woff = (warp == 0) ? 0.f : __shfl_sync(0xffffffffu, wexc, warp);
+  const float ctot = __shfl_sync(0xffffffffu, winc, kWarps - 1);
   if (threadIdx.x == 0) s_total = ctot;
-  cl.sync();   // every slice total written
+  cluster_sync_publish();   // every slice total written
   // every warp: the cluster prefix (lane r holds rank r's inclusive prefix)
   float pre = (lane < S) ? *cl.map_shared_rank(&s_total, lane) : 0.f;
 #pragma unroll
@@ -1243,7 +1259,7 @@ __device__ __noinline__ void cluster_draw_regs(const Params &p, int b, int n, co
     const float y = __shfl_up_sync(0xffffffffu, pre, off);
     if (lane >= off) pre = __fadd_rn(pre, y);
   }
-  cl.sync();   // every CTA has read its peers' totals; shared memory is private again
+  cluster_sync_exec();   // every CTA has read its peers' totals
   const float Sall = __shfl_sync(0xffffffffu, pre, S - 1);
   if (Q && Sall == 0.f) {
     // the residual vanished: draw from p_n alone, on the first CTA of the cluster
@@ -1267,21 +1283,16 @@ __device__ __noinline__ void cluster_draw_regs(const Params &p, int b, int n, co
   if (rank != owner) return;
   const float base = (rank == 0) ? 0.f : __shfl_sync(0xffffffffu, pre, rank - 1);
   // owner warp inside the CTA: the first whose range ends above t (mode 0), else the last
-  // warp with mass; decided from the warp totals every warp holds
-  int ow = -1, lastw = -1;
-  {
-    float acc = base;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float v = sh.warp_tot[w];
-      const float nx = __fadd_rn(acc, v);
-      if (v > 0.f) lastw = w;
-      if (ow < 0 && mode == 0 && nx > t) ow = w;
-      acc = nx;
-    }
+  // warp with mass; decided from the scan every warp holds
+  const unsigned wover = __ballot_sync(0xffffffffu, lane < kWarps && __fadd_rn(base, winc) > t);
+  const unsigned wmass = __ballot_sync(0xffffffffu, lane < kWarps && wv > 0.f);
+  int ow, wmode = mode;
+  if (mode == 0 && wover) {
+    ow = __ffs(wover) - 1;
+  } else {
+    wmode = 1;
+    ow = wmass ? 31 - __clz(wmass) : 0;
   }
-  int wmode = mode;
-  if (ow < 0) { ow = max(lastw, 0); wmode = 1; }
   if (warp != ow) return;
   // inside the owner warp: the segment, then the element
   float acc = __fadd_rn(base, woff);
