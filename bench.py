@@ -278,40 +278,43 @@ class Runner:
         self.copies = []
         for _ in range(ROT):
             self.copies.append(dict(ct=d(ci.target), cd=d(ci.draft), tt=d(ti.target)))
-        self.tok, self.uni = d(ci.tokens), d(ci.uniforms)
-        self.par, self.ttok = d(ti.parents), d(ti.tokens)
         B, g, V = ci.B, ci.gamma, ci.V
-        self.acc = torch.empty(B, dtype=torch.int32, device=dev)
-        self.out = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
-        self.tacc = torch.empty(ti.B, dtype=torch.int32, device=dev)
-        self.tpath = torch.empty((ti.B, ti.N), dtype=torch.int32, device=dev)
-        self.tout = torch.empty((ti.B, ti.N), dtype=torch.int32, device=dev)
-        self.probs = [torch.empty(ci.target.shape, dtype=torch.float32, device=dev)
-                      for _ in range(ROT)]
+        # per input copy: the small inputs and all outputs too, so that copies can overlap
+        for c in self.copies:
+            c.update(tok=d(ci.tokens), uni=d(ci.uniforms), par=d(ti.parents),
+                     ttok=d(ti.tokens),
+                     acc=torch.empty(B, dtype=torch.int32, device=dev),
+                     out=torch.empty((B, g + 1), dtype=torch.int32, device=dev),
+                     tacc=torch.empty(ti.B, dtype=torch.int32, device=dev),
+                     tpath=torch.empty((ti.B, ti.N), dtype=torch.int32, device=dev),
+                     tout=torch.empty((ti.B, ti.N), dtype=torch.int32, device=dev),
+                     probs=torch.empty(ci.target.shape, dtype=torch.float32, device=dev))
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.ws_c = sv.new_workspace(B, 2 * g + 1, V, sv.SPEC_BF16, dev)
-        self.ws_t = sv.new_workspace(ti.B, ti.N, ti.V, sv.SPEC_BF16, dev)
         rows = B * (g + 1)
-        self.ws_p = sv.new_workspace(rows, 1, V, sv.SPEC_BF16, dev)
+        # one workspace per copy and call: calls of different steps may overlap in e2e
+        self.ws_c = [sv.new_workspace(B, 2 * g + 1, V, sv.SPEC_BF16, dev) for _ in range(ROT)]
+        self.ws_t = [sv.new_workspace(ti.B, ti.N, ti.V, sv.SPEC_BF16, dev) for _ in range(ROT)]
+        self.ws_p = [sv.new_workspace(rows, 1, V, sv.SPEC_BF16, dev) for _ in range(ROT)]
         self.stream = torch.cuda.Stream(dev)
         vp = ctypes.c_void_p
         sp = vp(self.stream.cuda_stream)
         self.args = []
         for k in range(ROT):
             c = self.copies[k]
-            pk = self.copies[(k + 1) % ROT]["ct"]   # probs reads a copy not touched this step
+            # probs reads the target rows of the chain call just made on the same copy
             chain = (vp(c["ct"].data_ptr()), vp(c["cd"].data_ptr()), sv.SPEC_BF16,
-                     vp(self.tok.data_ptr()), vp(self.uni.data_ptr()), B, g, V,
-                     ctypes.c_float(ci.temperature), vp(self.acc.data_ptr()),
-                     vp(self.out.data_ptr()), vp(self.status.data_ptr()),
-                     vp(self.ws_c.data_ptr()), self.ws_c.numel(), sp)
-            tree = (vp(c["tt"].data_ptr()), sv.SPEC_BF16, vp(self.par.data_ptr()),
-                    vp(self.ttok.data_ptr()), ti.B, ti.N, ti.V, vp(self.tacc.data_ptr()),
-                    vp(self.tpath.data_ptr()), vp(self.tout.data_ptr()),
-                    vp(self.status.data_ptr()), vp(self.ws_t.data_ptr()), self.ws_t.numel(), sp)
-            probs = (vp(pk.data_ptr()), sv.SPEC_BF16, rows, V, ctypes.c_float(1.0),
-                     vp(self.probs[k].data_ptr()), vp(self.status.data_ptr()),
-                     vp(self.ws_p.data_ptr()), self.ws_p.numel(), sp)
+                     vp(c["tok"].data_ptr()), vp(c["uni"].data_ptr()), B, g, V,
+                     ctypes.c_float(ci.temperature), vp(c["acc"].data_ptr()),
+                     vp(c["out"].data_ptr()), vp(self.status.data_ptr()),
+                     vp(self.ws_c[k].data_ptr()), self.ws_c[k].numel(), sp)
+            tree = (vp(c["tt"].data_ptr()), sv.SPEC_BF16, vp(c["par"].data_ptr()),
+                    vp(c["ttok"].data_ptr()), ti.B, ti.N, ti.V, vp(c["tacc"].data_ptr()),
+                    vp(c["tpath"].data_ptr()), vp(c["tout"].data_ptr()),
+                    vp(self.status.data_ptr()), vp(self.ws_t[k].data_ptr()),
+                    self.ws_t[k].numel(), sp)
+            probs = (vp(c["ct"].data_ptr()), sv.SPEC_BF16, rows, V, ctypes.c_float(1.0),
+                     vp(c["probs"].data_ptr()), vp(self.status.data_ptr()),
+                     vp(self.ws_p[k].data_ptr()), self.ws_p[k].numel(), sp)
             self.args.append((chain, tree, probs))
 
     def call(self, kind, k):
@@ -433,7 +436,7 @@ def run_ours(args, rank, world, local):
         "launch_shapes": shapes,
         "clocks": clk,
         "host_issue_us_per_step": host_issue / K * 1e6,
-        "emitted_tokens_per_step": int((r.acc.cpu().numpy() + 1).sum()),
+        "emitted_tokens_per_step": int((r.copies[0]["acc"].cpu().numpy() + 1).sum()),
     }
     out["e2e"] = e2e(r, ci, ti, args.e2e_steps, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -442,63 +445,63 @@ def run_ours(args, rank, world, local):
 
 
 def e2e(r, ci, ti, steps, world, device):
-    """The step through the same C entry points with HOST inputs: H2D copies of the step's
-    inputs from pinned memory and D2H copies of all outputs are timed."""
+    """The step through the same C entry points with HOST inputs: every step copies its inputs
+    from pinned host memory to the device and all its outputs back, inside the timed region.
+    Three streams pipeline consecutive steps: host-to-device copies of step i+1 and
+    device-to-host copies of step i-1 overlap the kernels of step i (each step uses its own
+    device copy of inputs, outputs and workspaces, ROT of them in rotation)."""
     import torch
     pin = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
                      if a.dtype == np.uint16 else torch.from_numpy(a)).pin_memory()
-    h_ct, h_cd, h_tt = pin(ci.target), pin(ci.draft), pin(ti.target)
-    h_tok, h_uni, h_par, h_ttok = pin(ci.tokens), pin(ci.uniforms), pin(ti.parents), \
-        pin(ti.tokens)
-    o_acc = torch.empty_like(r.acc, device="cpu").pin_memory()
-    o_out = torch.empty_like(r.out, device="cpu").pin_memory()
-    o_tacc = torch.empty_like(r.tacc, device="cpu").pin_memory()
-    o_tpath = torch.empty_like(r.tpath, device="cpu").pin_memory()
-    o_tout = torch.empty_like(r.tout, device="cpu").pin_memory()
-    o_pr = torch.empty_like(r.probs[0], device="cpu").pin_memory()
-    bi = sum(t.numel() * t.element_size() for t in (h_ct, h_cd, h_tt, h_tok, h_uni, h_par,
-                                                     h_ttok))
-    bo = sum(t.numel() * t.element_size() for t in (o_acc, o_out, o_tacc, o_tpath, o_tout, o_pr))
+    host_in = dict(ct=pin(ci.target), cd=pin(ci.draft), tt=pin(ti.target), tok=pin(ci.tokens),
+                   uni=pin(ci.uniforms), par=pin(ti.parents), ttok=pin(ti.tokens))
+    c0 = r.copies[0]
+    host_out = {k: torch.empty_like(c0[k], device="cpu").pin_memory()
+                for k in ("acc", "out", "tacc", "tpath", "tout", "probs")}
+    bi = sum(t.numel() * t.element_size() for t in host_in.values())
+    bo = sum(t.numel() * t.element_size() for t in host_out.values())
+    h2d, d2h, ks = torch.cuda.Stream(), torch.cuda.Stream(), r.stream
+    ev_in = [torch.cuda.Event() for _ in range(ROT)]
+    ev_k = [torch.cuda.Event() for _ in range(ROT)]
+    ev_out = [torch.cuda.Event() for _ in range(ROT)]
+    lib = r.lib
 
     def one(i):
         k = i % ROT
         c = r.copies[k]
-        c["ct"].copy_(h_ct, non_blocking=True)
-        c["cd"].copy_(h_cd, non_blocking=True)
-        c["tt"].copy_(h_tt, non_blocking=True)
-        r.tok.copy_(h_tok, non_blocking=True)
-        r.uni.copy_(h_uni, non_blocking=True)
-        r.par.copy_(h_par, non_blocking=True)
-        r.ttok.copy_(h_ttok, non_blocking=True)
-        lib = r.lib
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(ev_k[k])           # the previous user of copy k has read its inputs
+            for name, t in host_in.items():
+                c[name].copy_(t, non_blocking=True)
+            ev_in[k].record(h2d)
+        ks.wait_event(ev_in[k])
+        ks.wait_event(ev_out[k])              # its previous outputs have been copied out
         chain, tree, probs = r.args[k]
-        # probs reads this step's freshly copied target rows
-        probs = (ctypes.c_void_p(c["ct"].data_ptr()),) + probs[1:]
-        rc = lib.spec_verify_chain(*chain) | lib.spec_verify_tree(*tree) | lib.spec_probs(*probs)
+        rc = lib.spec_verify_chain(*chain) | lib.spec_verify_tree(*tree) | \
+            lib.spec_probs(*probs)
         if rc:
             raise RuntimeError(f"verify call failed: {rc}")
-        o_acc.copy_(r.acc, non_blocking=True)
-        o_out.copy_(r.out, non_blocking=True)
-        o_tacc.copy_(r.tacc, non_blocking=True)
-        o_tpath.copy_(r.tpath, non_blocking=True)
-        o_tout.copy_(r.tout, non_blocking=True)
-        o_pr.copy_(r.probs[k], non_blocking=True)
+        ev_k[k].record(ks)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev_k[k])
+            for name, t in host_out.items():
+                t.copy_(c[name], non_blocking=True)
+            ev_out[k].record(d2h)
 
-    # copies and kernels on the one stream the C calls were given
-    with torch.cuda.stream(r.stream):
-        for i in range(5):
-            one(i)
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(r.stream)
-        for i in range(steps):
-            one(i)
-        t1.record(r.stream)
+    for i in range(2 * ROT):
+        one(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(h2d)
+    for i in range(steps):
+        one(i)
+    t1.record(d2h)
     torch.cuda.synchronize()
     el = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world, device)
     pos = sum_over_ranks(positions(ci, ti) * steps, world, device)
     return {"value": pos / el, "unit": UNIT, "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "steps": steps, "ms_per_step": el / steps * 1e3}
+            "d2h_bytes_per_step": bo, "steps": steps, "ms_per_step": el / steps * 1e3,
+            "pipelined": "h2d / kernels / d2h on three streams, consecutive steps overlap"}
 
 
 # ------------------------------------------------------------------ the oracle

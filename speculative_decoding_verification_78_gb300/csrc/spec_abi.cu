@@ -78,8 +78,8 @@ int plan(Params &p, int dtype, void *ws, size_t ws_bytes) {
 }
 
 // Stream kernel grid: two CTAs of 512 threads per SM (all resident at once), never more CTAs
-// than groups of kWarps units. (Trimming the grid so that the last round of loads is full was
-// measured slower: fewer loads in flight.)
+// than groups of kWarps units. (Trimming the grid so that the last round of loads is full, and
+// one CTA per SM streaming through a cp.async ring in shared memory, were both measured slower.)
 int grid_for(const Params &p) {
   const long long cap = 2LL * (sm_count() > 0 ? sm_count() : 1);
   const long long groups = (static_cast<long long>(p.units) + kWarps - 1) / kWarps;

@@ -693,25 +693,51 @@ __device__ __noinline__ int draw_token_cta(const E *P, const E *Q, float Mt, flo
                           t < S ? 0 : 1, sh);
 }
 
-// Warp-wide draw for rows of at most kWarpTailMaxV elements (<= 8 segments).
+// Warp-wide draw for rows of at most kWarpTailMaxV elements (<= 8 segments). The loads of
+// several segments are issued together (four at a time for bf16, two for fp32); for rows of at
+// most four segments the residual values stay in registers, so the crossing element is found
+// without reading the rows again.
 template <typename E>
 __device__ int draw_token_warp(const E *P, const E *Q, float Mt, float iZt, float Md, float iZd,
                                float c2, int V, float u) {
   constexpr int kMaxSeg = kWarpTailMaxV / kSeg;
+  constexpr int kRegSeg = 4;                          // segments kept in registers
+  constexpr int kBatch = (sizeof(E) == 2) ? 4 : 2;    // segments whose loads fly together
   const int lane = threadIdx.x & 31;
   const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) & 15u) == 0) &&
                       (!Q || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
   const int nseg = (V + kSeg - 1) / kSeg;
-  float ss[kMaxSeg];
+  const bool keep = nseg <= kRegSeg;
+  float ss[kMaxSeg], lsv[kRegSeg], rr[kRegSeg][8];
 #pragma unroll
-  for (int s = 0; s < kMaxSeg; ++s) {
-    ss[s] = 0.f;
-    if (s < nseg) {
-      float r[8];
-      float ls = lane_resid<E>(P, Q, s, lane, V, vec_ok, Mt, iZt, Md, iZd, c2, r);
+  for (int s0 = 0; s0 < kMaxSeg; s0 += kBatch) {
+    if (s0 < nseg) {
+      uint4 wp[kBatch][2], wq[kBatch][2];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xffffffffu, ls, off));
-      ss[s] = ls;
+      for (int q = 0; q < kBatch; ++q) {
+        const int k0 = (s0 + q < nseg) ? (s0 + q) * kSeg + lane * 8 : V;
+        load8_raw<E>(P, k0, V, vec_ok, wp[q]);
+        if (Q) load8_raw<E>(Q, k0, V, vec_ok, wq[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int sg = s0 + q;
+        float ls = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float r = resid(raw8_elem<E>(wp[q], e), Q ? raw8_elem<E>(wq[q], e) : -INFINITY,
+                                Q != nullptr, Mt, iZt, Md, iZd, c2);
+          ls = __fadd_rn(ls, r);
+          if (sg < kRegSeg) rr[sg < kRegSeg ? sg : 0][e] = r;
+        }
+        if (sg < kRegSeg) lsv[sg < kRegSeg ? sg : 0] = ls;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xffffffffu, ls, off));
+        ss[sg] = (sg < nseg) ? ls : 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) ss[s0 + q] = 0.f;
     }
   }
   float S = 0.f;
@@ -732,7 +758,21 @@ __device__ int draw_token_warp(const E *P, const E *Q, float Mt, float iZt, floa
   }
   if (seg < 0) { seg = max(lastseg, 0); base = lastbase; mode = 1; }
   float r[8];
-  const float ls = lane_resid<E>(P, Q, seg, lane, V, vec_ok, Mt, iZt, Md, iZd, c2, r);
+  float ls;
+  if (keep) {
+    ls = lsv[0];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = rr[0][e];
+#pragma unroll
+    for (int q = 1; q < kRegSeg; ++q)
+      if (q == seg) {
+        ls = lsv[q];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r[e] = rr[q][e];
+      }
+  } else {
+    ls = lane_resid<E>(P, Q, seg, lane, V, vec_ok, Mt, iZt, Md, iZd, c2, r);
+  }
   const int tok = segment_pick(r, ls, seg * kSeg + lane * 8, base, t, mode, lane);
   return tok < 0 ? V - 1 : tok;
 }
@@ -1101,8 +1141,9 @@ __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared
 
 // Greedy tree verification for trees of at most 64 nodes: all warps combine the argmax
 // partials into shared memory, then warp 0 holds nodes lane and lane + 32 in registers and does
-// the rest with shuffles (no block barriers): accepted flags and depths by pointer jumping, the
-// deepest accepted node by a warp maximum, and the path by walking parents back from it.
+// the rest with warp votes and shuffles (no block barriers): the accepted set level by level
+// as a 64-bit mask, the deepest accepted node by a warp maximum, and the path by walking
+// parents back from it.
 // smem holds g[N] and the row-usable flags okf[N].
 __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1147,26 +1188,26 @@ __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
     if (lane == 0) { set_status(p.status, err); p.accept_len[b] = -1; }
     return;
   }
-  // anc: the node reached so far; pk = (hops << 1) | (every node on the way matched)
-  int anc0 = 0, anc1 = 0, pk0 = 1, pk1 = 1;
-  if (in0 && j0 > 0) { anc0 = par0; pk0 = 2 | (tok0 == g[par0] ? 1 : 0); }
-  if (in1) { anc1 = par1; pk1 = 2 | (tok1 == g[par1] ? 1 : 0); }
-  auto join = [](int a, int c) { return ((((a >> 1) + (c >> 1))) << 1) | (a & c & 1); };
-  for (int span = 1; span < N; span <<= 1) {
-    const int sA = anc0 & 31, sB = anc1 & 31;
-    const int aA0 = __shfl_sync(0xffffffffu, anc0, sA), aA1 = __shfl_sync(0xffffffffu, anc1, sA);
-    const int kA0 = __shfl_sync(0xffffffffu, pk0, sA), kA1 = __shfl_sync(0xffffffffu, pk1, sA);
-    const int aB0 = __shfl_sync(0xffffffffu, anc0, sB), aB1 = __shfl_sync(0xffffffffu, anc1, sB);
-    const int kB0 = __shfl_sync(0xffffffffu, pk0, sB), kB1 = __shfl_sync(0xffffffffu, pk1, sB);
-    const bool hA = anc0 >= 32, hB = anc1 >= 32;
-    pk0 = join(pk0, hA ? kA1 : kA0);
-    pk1 = join(pk1, hB ? kB1 : kB0);
-    anc0 = hA ? aA1 : aA0;
-    anc1 = hB ? aB1 : aB0;
+  // level by level: a node is accepted at step d when its parent was accepted (at step d - 1)
+  // and its token is the parent's argmax, so the step at which it is accepted is its depth
+  // (parents precede children, so a node's parent is always settled first). The accepted set
+  // is one 64-bit mask, extended by two ballots per level.
+  const bool m0 = in0 && j0 > 0 && tok0 == g[par0];
+  const bool m1 = in1 && tok1 == g[par1];
+  unsigned long long accm = 1ull;   // the root
+  int dep0 = (in0 && j0 == 0) ? 0 : -1, dep1 = -1;
+  for (int level = 1; level < N; ++level) {
+    const bool a0 = m0 && dep0 < 0 && ((accm >> par0) & 1ull);
+    const bool a1 = m1 && dep1 < 0 && ((accm >> par1) & 1ull);
+    const unsigned lo = __ballot_sync(0xffffffffu, a0), hi = __ballot_sync(0xffffffffu, a1);
+    if ((lo | hi) == 0u) break;
+    if (a0) dep0 = level;
+    if (a1) dep1 = level;
+    accm |= static_cast<unsigned long long>(lo) | (static_cast<unsigned long long>(hi) << 32);
   }
   int key = -1;
-  if (in0 && (pk0 & 1)) key = ((pk0 >> 1) << 11) | (2047 - j0);
-  if (in1 && (pk1 & 1)) key = max(key, ((pk1 >> 1) << 11) | (2047 - j1));
+  if (dep0 >= 0) key = (dep0 << 11) | (2047 - j0);
+  if (dep1 >= 0) key = max(key, (dep1 << 11) | (2047 - j1));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, off));
   const int best = 2047 - (key & 2047);
@@ -1403,6 +1444,49 @@ __device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, c
 // the stream kernel (so its launch overlaps the stream kernel's last wave), waits for the
 // stream kernel's results and turns them into outputs.
 
+// One unit's result from its registers: the 8-byte partial (softmax statistics or argmax), and
+// for chain sampling the logit at the row's draft token x when this unit holds it.
+template <typename E, int MODE>
+__device__ __forceinline__ void unit_work(const Params &p, int unit, const UnitId &u,
+                                          const E *row, const RowGeom &g,
+                                          const uint4 (&buf)[kVPL], float eh, float et, int x,
+                                          int lane) {
+  constexpr bool kStats = (MODE == kChainSample || MODE == kProbs);
+  uint2 part;
+  if constexpr (kStats) {
+    float m, s;
+    unit_stats<E>(buf, eh, et, p.c2, m, s);
+    part = make_uint2(__float_as_uint(m), __float_as_uint(s));
+  } else {
+    float v;
+    int i;
+    unit_argmax<E>(buf, eh, et, g, u.chunk * kUnitVecs, lane, v, i);
+    part = make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
+  }
+  if (lane == 0) p.ws_part[unit] = part;
+  if constexpr (MODE == kChainSample) {
+    if (x >= 0 && x < p.V) {
+      const int vb = u.chunk * kUnitVecs;
+      float val = 0.f;
+      if (span_logit<E>(row, g, vb, vb + kUnitVecs, u.chunk == 0, x, lane, buf, &val) &&
+          lane == 0)
+        p.ws_xlogit[static_cast<long long>(u.b) * p.R + u.r] = val;
+    }
+  }
+}
+
+// The draft token of a chain-sampling row (-1 for the bonus row and other modes).
+template <int MODE>
+__device__ __forceinline__ int unit_token(const Params &p, const UnitId &u) {
+  if constexpr (MODE == kChainSample) {
+    if (u.r != p.gamma) {
+      const int i = (u.r < p.Rt) ? u.r : u.r - p.Rt;
+      return __ldg(p.tokens + static_cast<long long>(u.b) * p.gamma + i);
+    }
+  }
+  return -1;
+}
+
 // The stream kernel: warp w of the grid reduces units w, w + W, w + 2W, ... (W warps in all),
 // each to one 8-byte partial. For chain sampling it also records the logit at each row's draft
 // token, taken from the registers of the lane that loaded it (or, for a head/tail element,
@@ -1410,7 +1494,6 @@ __device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, c
 // only after this grid has completed.
 template <typename E, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) stream_kernel(Params p) {
-  constexpr bool kStats = (MODE == kChainSample || MODE == kProbs);
   // The finishing kernel may be scheduled as soon as every CTA of this grid is running; this
   // grid itself reads nothing before the kernel ahead of it on the stream has completed.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1420,39 +1503,13 @@ __global__ void __launch_bounds__(kThreads, 2) stream_kernel(Params p) {
   for (int unit = blockIdx.x * kWarps + (threadIdx.x >> 5); unit < p.units; unit += W) {
     const UnitId u = unit_id(p, unit);
     // the draft token of this row, fetched before the unit's data so both loads overlap
-    int x = -1;
-    if constexpr (MODE == kChainSample) {
-      if (u.r != p.gamma) {
-        const int i = (u.r < p.Rt) ? u.r : u.r - p.Rt;
-        x = __ldg(p.tokens + static_cast<long long>(u.b) * p.gamma + i);
-      }
-    }
+    const int x = unit_token<MODE>(p, u);
     const E *row = row_ptr<E>(p, u.b, u.r);
     const RowGeom g = row_geom<E>(row, p.V);
     uint4 buf[kVPL];
     float eh, et;
     load_unit<E>(row, g, u.chunk, lane, buf, eh, et);
-    uint2 part;
-    if constexpr (kStats) {
-      float m, s;
-      unit_stats<E>(buf, eh, et, p.c2, m, s);
-      part = make_uint2(__float_as_uint(m), __float_as_uint(s));
-    } else {
-      float v;
-      int i;
-      unit_argmax<E>(buf, eh, et, g, u.chunk * kUnitVecs, lane, v, i);
-      part = make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
-    }
-    if (lane == 0) p.ws_part[unit] = part;
-    if constexpr (MODE == kChainSample) {
-      if (x >= 0 && x < p.V) {
-        const int vb = u.chunk * kUnitVecs;
-        float val = 0.f;
-        if (span_logit<E>(row, g, vb, vb + kUnitVecs, u.chunk == 0, x, lane, buf, &val) &&
-            lane == 0)
-          p.ws_xlogit[static_cast<long long>(u.b) * p.R + u.r] = val;
-      }
-    }
+    unit_work<E, MODE>(p, unit, u, row, g, buf, eh, et, x, lane);
   }
 }
 
@@ -1499,9 +1556,10 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
 
 // Finishing kernel for chain sampling when every row is a single unit (gamma <= 31, V <=
 // kWarpTailMaxV): one warp per batch row; lane i holds rows i and i + 32 and the draft-token
-// logits of position i.
+// logits of position i. One CTA per SM at most is plenty (B / 16 CTAs), so each thread may use
+// up to 128 registers and the draw keeps the residual of the rows in registers.
 template <typename E>
-__global__ void __launch_bounds__(kThreads, 2) finish_chain_sample_warp(Params p) {
+__global__ void __launch_bounds__(kThreads, 1) finish_chain_sample_warp(Params p) {
   wait_stream_kernel();
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
