@@ -404,6 +404,8 @@ def run_ours(args, rank, world, local):
 
     per_kernel = {kind: [e[j].elapsed_time(e[j + 1]) * 1e-3 / BLOCK for e in evs]
                   for j, kind in enumerate(KINDS)}
+    if args.steps < BLOCK:
+        raise SystemExit(f"--steps must be at least {BLOCK} (one block of each call)")
     avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
     nbytes = step_bytes(ci, ti)
     peak, peak_kind = measured_peak()
