@@ -55,8 +55,12 @@ def _load():
             lib.oracle_verify_chain.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, dbl, vp,
                                                 vp, vp]
             lib.oracle_verify_tree.argtypes = [vp, i32, vp, vp, i64, i64, i64, vp, vp, vp]
+            lib.oracle_sample.argtypes = [vp, i32, i64, i64, dbl, vp, vp, vp]
+            lib.oracle_topk.argtypes = [vp, i32, i64, i64, i64, vp]
+            lib.oracle_tree_mask.argtypes = [vp, i64, i64, vp]
             for f in (lib.oracle_probs, lib.oracle_argmax, lib.oracle_verify_chain,
-                      lib.oracle_verify_tree):
+                      lib.oracle_verify_tree, lib.oracle_sample, lib.oracle_topk,
+                      lib.oracle_tree_mask):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -125,3 +129,36 @@ def verify_tree(target, dtype, parents, tokens):
     rc = _load().oracle_verify_tree(_ptr(tg), dtype, _ptr(par), _ptr(tok), B, N, V, _ptr(acc),
                                     _ptr(path), _ptr(out))
     return acc, path, out, rc
+
+
+def sample(logits, dtype, uniforms, temperature):
+    """[rows, V] logits -> (tokens [rows] int32, margin [rows] float64, rc)."""
+    lg = _logits(logits, dtype)
+    V = lg.shape[-1]
+    rows = lg.size // V
+    uni = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(rows)
+    out = np.empty(rows, dtype=np.int32)
+    mg = np.empty(rows, dtype=np.float64)
+    rc = _load().oracle_sample(_ptr(lg), dtype, rows, V, float(temperature), _ptr(uni),
+                               _ptr(out), _ptr(mg))
+    return out, mg, rc
+
+
+def topk(logits, dtype, k):
+    """[rows, V] logits -> (indices [rows, k] int32, rc)."""
+    lg = _logits(logits, dtype)
+    V = lg.shape[-1]
+    rows = lg.size // V
+    out = np.empty((rows, k), dtype=np.int32)
+    rc = _load().oracle_topk(_ptr(lg), dtype, rows, V, int(k), _ptr(out))
+    return out, rc
+
+
+def tree_mask(parents):
+    """[B, N] parents -> (words [B, N, ceil(N/32)] uint32, rc)."""
+    par = np.ascontiguousarray(parents, dtype=np.int32)
+    B, N = par.shape
+    W = (N + 31) // 32
+    out = np.empty((B, N, W), dtype=np.uint32)
+    rc = _load().oracle_tree_mask(_ptr(par), B, N, _ptr(out))
+    return out, rc

@@ -357,3 +357,110 @@ int oracle_verify_tree(const void *target, int dtype, const int32_t *parents,
   free(g); free(acc); free(depth); free(path);
   return rc;
 }
+
+/* ------------------------------------------------------------------ public: drafter side */
+
+/*
+ * Drafter-side sampling, the step before verification: the draft model proposes x_i by
+ * sampling its own distribution q_i ("Fast Inference from Transformers via Speculative
+ * Decoding", pith.science review, "The pith": the small model proposes tokens that the large
+ * model then checks).
+ *   out_tokens[r] = the inverse-CDF draw from softmax(logits[r] / T) with uniform u[r]: the first
+ *   k whose running sum of p exceeds u (sums in index order); T == 0: the lowest-index argmax;
+ *   -1 for an invalid row. margin[r] (may be NULL): the CDF margin of the draw (+inf at T == 0).
+ */
+int oracle_sample(const void *logits, int dtype, long rows, long V, double T,
+                  const float *uniforms, int32_t *out_tokens, double *margin) {
+  if (rows < 0 || V < 1 || !(T >= 0.0) || isinf(T)) return ORC_ERR_ARG;
+  double *p = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!p) return ORC_ERR_MEM;
+  int rc = ORC_OK;
+  for (long r = 0; r < rows; ++r) {
+    size_t off = (size_t)r * (size_t)V;
+    if (margin) margin[r] = INFINITY;
+    if (!row_valid(logits, dtype, off, V)) {
+      out_tokens[r] = -1;
+      if (rc == ORC_OK) rc = ORC_ERR_ROW;
+      continue;
+    }
+    if (T == 0.0) {
+      out_tokens[r] = (int32_t)argmax_row(logits, dtype, off, V);
+      continue;
+    }
+    softmax_row(logits, dtype, off, V, T, p);
+    double mg = 0.0;
+    out_tokens[r] = (int32_t)inverse_cdf(p, V, (double)uniforms[r], 1.0, &mg);
+    if (margin) margin[r] = mg;
+  }
+  free(p);
+  return rc;
+}
+
+/*
+ * Top-n candidates per row, for building a draft tree: Falcon expands each node of its decoding
+ * tree with the drafter's most likely tokens at that node ("Falcon: Faster and Parallel
+ * Inference of Large Language Models through Enhanced Semi-Autoregressive Drafting and
+ * Custom-Designed Decoding Tree", pith.science review, "What carries the argument": deeper
+ * branches for higher-probability tokens).
+ *   out_idx[r, 0..k) = the indices of the k largest logits of row r, largest first, equal values
+ *   in increasing index order (so out_idx[r, 0] is the lowest-index argmax); a logit's rank does
+ *   not depend on the temperature. -1 everywhere for an invalid row. 1 <= k <= V.
+ */
+int oracle_topk(const void *logits, int dtype, long rows, long V, long k, int32_t *out_idx) {
+  if (rows < 0 || V < 1 || k < 1 || k > V) return ORC_ERR_ARG;
+  char *taken = (char *)malloc((size_t)V);
+  if (!taken) return ORC_ERR_MEM;
+  int rc = ORC_OK;
+  for (long r = 0; r < rows; ++r) {
+    size_t off = (size_t)r * (size_t)V;
+    int32_t *o = out_idx + (size_t)r * (size_t)k;
+    if (!row_valid(logits, dtype, off, V)) {
+      for (long j = 0; j < k; ++j) o[j] = -1;
+      if (rc == ORC_OK) rc = ORC_ERR_ROW;
+      continue;
+    }
+    memset(taken, 0, (size_t)V);
+    for (long j = 0; j < k; ++j) {   /* repeated selection of the best remaining element */
+      long best = -1;
+      double bv = 0.0;
+      for (long q = 0; q < V; ++q) {
+        if (taken[q]) continue;
+        double v = logit_at(logits, dtype, off + (size_t)q);
+        if (best < 0 || v > bv) { best = q; bv = v; }
+      }
+      taken[best] = 1;
+      o[j] = (int32_t)best;
+    }
+  }
+  free(taken);
+  return rc;
+}
+
+/*
+ * Tree-attention mask: in Falcon's decoding tree every node attends to itself and its
+ * ancestors only (Falcon review, Figure 3, "SAR decoding tree attention").
+ *   words[b, i, w] (W = ceil(N / 32) words per node) has bit j % 32 of word j / 32 set iff node j
+ *   is node i or an ancestor of node i. parents as for oracle_verify_tree; an invalid tree gets
+ *   an all-zero mask and ORC_ERR_PARENT.
+ */
+int oracle_tree_mask(const int32_t *parents, long B, long N, uint32_t *words) {
+  if (B < 0 || N < 1) return ORC_ERR_ARG;
+  long W = (N + 31) / 32;
+  int rc = ORC_OK;
+  for (long b = 0; b < B; ++b) {
+    const int32_t *par = parents + (size_t)b * (size_t)N;
+    uint32_t *m = words + (size_t)b * (size_t)N * (size_t)W;
+    for (long q = 0; q < N * W; ++q) m[q] = 0u;
+    int bad = par[0] != -1;
+    for (long i = 1; i < N && !bad; ++i)
+      if (par[i] < 0 || par[i] >= i) bad = 1;
+    if (bad) {
+      if (rc == ORC_OK) rc = ORC_ERR_PARENT;
+      continue;
+    }
+    for (long i = 0; i < N; ++i)   /* walk from the node up to the root */
+      for (long j = i; j >= 0; j = (j > 0) ? par[j] : -1)
+        m[(size_t)i * (size_t)W + (size_t)(j / 32)] |= 1u << (j % 32);
+  }
+  return rc;
+}
