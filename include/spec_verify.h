@@ -146,6 +146,49 @@ int spec_probs(const void *logits, int dtype, int rows, int V, float temperature
                float *out_probs, int32_t *status, void *workspace, size_t workspace_bytes,
                void *stream);
 
+/*
+ * Drafter-side sampling, the step before verification: each row's token drawn from
+ * softmax(logits[r, :] / T) by inverse CDF with uniform u = uniforms[r] (the first k whose running
+ * sum strictly exceeds u * S), exactly as spec_verify_chain draws its bonus token; T == 0 gives
+ * the lowest-index argmax (uniforms not read, may be NULL). An invalid row gets token -1 and sets
+ * *status (SPEC_ERR_NONFINITE).
+ *   logits     [rows, V]   dtype
+ *   uniforms   [rows]      fp32 in (0, 1)
+ *   out_tokens [rows]      int32 out
+ *   workspace  at least spec_workspace_bytes(rows, 1, V, dtype) bytes (scratch)
+ * Limits: 1 <= V <= SPEC_MAX_V, rows >= 0, temperature as for spec_verify_chain.
+ */
+int spec_sample(const void *logits, int dtype, int rows, int V, float temperature,
+                const float *uniforms, int32_t *out_tokens, int32_t *status, void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * Top-n candidates per row, for expanding a draft tree with the drafter's most likely tokens at
+ * each node (Falcon, pith.science review, "What carries the argument"): out_idx[r, 0..k) = the
+ * indices of the k largest logits of row r, largest first, equal values by increasing index.
+ * An invalid row (NaN, +inf, or no finite value) gets -1 everywhere and sets *status
+ * (SPEC_ERR_NONFINITE). No workspace.
+ *   logits  [rows, V]  dtype
+ *   out_idx [rows, k]  int32 out
+ * Limits: 1 <= k <= min(V, SPEC_MAX_TOPK), 1 <= V <= SPEC_MAX_V, rows >= 0.
+ */
+#define SPEC_MAX_TOPK 16
+int spec_topk(const void *logits, int dtype, int rows, int V, int k, int32_t *out_idx,
+              int32_t *status, void *stream);
+
+/*
+ * Tree-attention mask of B candidate trees (Falcon review, Figure 3, "SAR decoding tree
+ * attention": every node attends to itself and its ancestors): with W = ceil(N / 32), bit j % 32
+ * of mask_words[b, i, j / 32] is set iff node j is node i or an ancestor of node i. Parents as
+ * for spec_verify_tree; an invalid tree gets an all-zero mask and sets *status
+ * (SPEC_ERR_PARENT). No workspace.
+ *   parents    [B, N]     int32
+ *   mask_words [B, N, W]  uint32 out
+ * Limits: 1 <= N <= SPEC_MAX_NODES, B >= 0.
+ */
+int spec_tree_mask(const int32_t *parents, int B, int N, uint32_t *mask_words, int32_t *status,
+                   void *stream);
+
 /* Static text for any SPEC_* code ("unknown status" otherwise). */
 const char *spec_status_string(int code);
 

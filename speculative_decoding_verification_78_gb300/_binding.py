@@ -26,7 +26,8 @@ SPEC_MAX_V, SPEC_MAX_GAMMA, SPEC_MAX_NODES = 1 << 20, 255, 1024
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_workspace_bytes", "spec_workspace_init", "spec_verify_chain",
            "spec_verify_tree", "spec_probs", "spec_status_string", "spec_launch_shape",
-           "spec_verify_chain_static")
+           "spec_verify_chain_static", "spec_sample", "spec_topk", "spec_tree_mask")
+SPEC_MAX_TOPK = 16
 SPEC_STATIC_SCRATCH_BYTES = 4 << 20
 SPEC_CALL_CHAIN, SPEC_CALL_TREE, SPEC_CALL_PROBS = 0, 1, 2
 
@@ -70,6 +71,12 @@ def load_library():
         lib.spec_verify_chain_static.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, f32, vp, vp,
                                                  vp, vp]
         lib.spec_verify_chain_static.restype = i32
+        lib.spec_sample.argtypes = [vp, i32, i32, i32, f32, vp, vp, vp, vp, sz, vp]
+        lib.spec_sample.restype = i32
+        lib.spec_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
+        lib.spec_topk.restype = i32
+        lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
+        lib.spec_tree_mask.restype = i32
         _lib = lib
         return lib
 
@@ -171,6 +178,30 @@ def spec_launch_shape(kind: int, B: int, rows_per_b: int, V: int, dtype: int,
     return k.value, g.value, c.value
 
 
+def spec_sample(logits, temperature, uniforms, out_tokens, status, workspace, stream=None) -> int:
+    """logits [rows, V] -> out_tokens [rows] int32 (uniforms [rows] fp32)."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V if V else 0
+    return load_library().spec_sample(
+        _ptr(logits), dtype_flag(logits), rows, V, float(temperature), _ptr(uniforms),
+        _ptr(out_tokens), _ptr(status), _ptr(workspace), _nbytes(workspace), _stream(stream))
+
+
+def spec_topk(logits, k, out_idx, status, stream=None) -> int:
+    """logits [rows, V] -> out_idx [rows, k] int32."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V if V else 0
+    return load_library().spec_topk(_ptr(logits), dtype_flag(logits), rows, V, int(k),
+                                    _ptr(out_idx), _ptr(status), _stream(stream))
+
+
+def spec_tree_mask(parents, mask_words, status, stream=None) -> int:
+    """parents [B, N] int32 -> mask_words [B, N, ceil(N/32)] (int32 tensor holding the bits)."""
+    B, N = parents.shape
+    return load_library().spec_tree_mask(_ptr(parents), B, N, _ptr(mask_words), _ptr(status),
+                                         _stream(stream))
+
+
 def spec_status_string(code: int) -> str:
     try:
         return load_library().spec_status_string(int(code)).decode()
@@ -235,4 +266,39 @@ def probs(logits, temperature, workspace=None, stream=None):
     out = torch.empty(logits.shape, dtype=torch.float32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     check(spec_probs(logits, temperature, out, st, workspace, stream), "spec_probs")
+    return out, st
+
+
+def sample(logits, temperature, uniforms=None, workspace=None, stream=None):
+    """Allocates the output and runs spec_sample. Returns (tokens [rows] int32, status)."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    dev = logits.device
+    if workspace is None:
+        workspace = new_workspace(rows, 1, V, dtype_flag(logits), dev)
+    out = torch.empty(rows, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    check(spec_sample(logits, temperature, uniforms, out, st, workspace, stream), "spec_sample")
+    return out, st
+
+
+def topk(logits, k, stream=None):
+    """Allocates the output and runs spec_topk. Returns (indices [rows, k] int32, status)."""
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    dev = logits.device
+    out = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    check(spec_topk(logits, k, out, st, stream), "spec_topk")
+    return out, st
+
+
+def tree_mask(parents, stream=None):
+    """Allocates the output and runs spec_tree_mask. Returns (mask words [B, N, W] int32 holding
+    the uint32 bit patterns, status)."""
+    B, N = parents.shape
+    W = (N + 31) // 32
+    out = torch.empty((B, N, W), dtype=torch.int32, device=parents.device)
+    st = torch.zeros(1, dtype=torch.int32, device=parents.device)
+    check(spec_tree_mask(parents, out, st, stream), "spec_tree_mask")
     return out, st

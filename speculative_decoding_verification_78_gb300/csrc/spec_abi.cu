@@ -304,6 +304,71 @@ int spec_probs(const void *logits, int dtype, int rows, int V, float temperature
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
+int spec_sample(const void *logits, int dtype, int rows, int V, float temperature,
+                const float *uniforms, int32_t *out_tokens, int32_t *status, void *workspace,
+                size_t workspace_bytes, void *stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (rows < 0 || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_SHAPE;
+  if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
+  const bool greedy = temperature == 0.f;
+  if (!logits || !out_tokens || !status || !workspace || (!greedy && !uniforms))
+    return SPEC_ERR_NULL;
+  if (!aligned(logits, elem_size(dtype)) || (uniforms && !aligned(uniforms, 4)) ||
+      !aligned(out_tokens, 4) || !aligned(status, 4) || !aligned(workspace, 16))
+    return SPEC_ERR_ALIGN;
+  if (rows == 0) return SPEC_OK;
+  // a chain step with no drafts: the bonus draw from each row (argmax at T == 0)
+  Params p = blank();
+  chain_shape(p, rows, 0, V, temperature);
+  p.tgt = logits;
+  p.uniforms = greedy ? nullptr : uniforms;
+  p.accept_len = nullptr;
+  p.out_tokens = out_tokens;
+  p.status = status;
+  const int rc = plan(p, dtype, workspace, workspace_bytes);
+  if (rc != SPEC_OK) return rc;
+  const FinishPlan f = chain_finish(p, greedy);
+  const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
+                                     f, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+int spec_topk(const void *logits, int dtype, int rows, int V, int k, int32_t *out_idx,
+              int32_t *status, void *stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (rows < 0 || V < 1 || V > SPEC_MAX_V || k < 1 || k > SPEC_MAX_TOPK || k > V)
+    return SPEC_ERR_SHAPE;
+  if (!logits || !out_idx || !status) return SPEC_ERR_NULL;
+  if (!aligned(logits, elem_size(dtype)) || !aligned(out_idx, 4) || !aligned(status, 4))
+    return SPEC_ERR_ALIGN;
+  if (rows == 0) return SPEC_OK;
+  Params p = blank();
+  probs_shape(p, rows, V, 1.f);
+  p.tgt = logits;
+  p.out_tokens = out_idx;
+  p.status = status;
+  p.topk = k;
+  const cudaError_t e = launch_topk(dtype, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+int spec_tree_mask(const int32_t *parents, int B, int N, uint32_t *mask_words, int32_t *status,
+                   void *stream) {
+  if (B < 0 || N < 1 || N > SPEC_MAX_NODES) return SPEC_ERR_SHAPE;
+  if (!parents || !mask_words || !status) return SPEC_ERR_NULL;
+  if (!aligned(parents, 4) || !aligned(mask_words, 4) || !aligned(status, 4))
+    return SPEC_ERR_ALIGN;
+  if (B == 0) return SPEC_OK;
+  Params p = blank();
+  p.parents = parents;
+  p.mask_words = mask_words;
+  p.status = status;
+  p.B = B;
+  p.N = N;
+  const cudaError_t e = launch_tree_mask(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
 int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float temperature,
                       int *kernels, int *grid, int *cluster) {
   if (!kernels || !grid || !cluster) return SPEC_ERR_NULL;

@@ -62,6 +62,8 @@ struct Params {
   int upb;                   // units per batch row, R*C
   int B, gamma, N, V;
   int Rt, Rd, R, C;          // rows per batch row: target, draft, total; units per row
+  int topk;                  // top-n: candidates per row (1..SPEC_MAX_TOPK)
+  uint32_t *mask_words;      // tree mask output: [B, N, ceil(N / 32)] words
   float c2;                  // log2(e) / T
 };
 
@@ -782,7 +784,7 @@ __device__ int draw_token_warp(const E *P, const E *Q, float Mt, float iZt, floa
 __device__ __forceinline__ void fail_chain_row(const Params &p, int b, int tid, int nthreads) {
   const int g1 = p.gamma + 1;
   for (int j = tid; j < g1; j += nthreads) p.out_tokens[static_cast<long long>(b) * g1 + j] = -1;
-  if (tid == 0) p.accept_len[b] = -1;
+  if (tid == 0 && p.accept_len) p.accept_len[b] = -1;   // no accept_len when only sampling
 }
 
 // the acceptance test u <= p_i(x_i)/q_i(x_i), with
@@ -956,7 +958,7 @@ __device__ __forceinline__ void emit_chain(const Params &p, int b, int n, int to
   const int g1 = p.gamma + 1;
   int32_t *o = p.out_tokens + static_cast<long long>(b) * g1;
   for (int j = tid; j < g1; j += nthreads) o[j] = (j < n) ? x[j] : (j == n ? tok : -1);
-  if (tid == 0) p.accept_len[b] = n;
+  if (tid == 0 && p.accept_len) p.accept_len[b] = n;
 }
 
 // Chain sampling, one warp, for steps whose rows are single units (gamma <= 31, V <=
@@ -1711,6 +1713,168 @@ __global__ void __launch_bounds__(kThreads, 2) finish_probs(Params p) {
       const int kt = g.h + g.nv * kEPV + lane;
       if (lane < g.tl) __stcs(out + kt, val(et, kt));
     }
+  }
+}
+
+// ------------------------------------------------------------------ top-n candidates
+//
+// The k largest logits of each row (value descending, equal values by increasing index), for
+// expanding a draft tree. One CTA per row: every thread streams its share of the row (16-byte
+// vectors tid, tid + 512, ..., plus the unaligned head and tail on the first threads) keeping a
+// sorted list of its kK best (value, index) pairs in registers; the lists go to shared memory
+// and k rounds of a block-wide maximum over the lists' heads pick the row's k best in order.
+// Every element of the row's top k is within its thread's top kK >= k, so this is exact.
+
+// (v, i) ranks before (w, j)
+__device__ __forceinline__ bool ranks_before(float v, int i, float w, int j) {
+  return v > w || (v == w && i < j);
+}
+
+template <int kK>
+__device__ __forceinline__ void topk_insert(float (&lv)[kK], int (&li)[kK], float v, int i) {
+  if (!ranks_before(v, i, lv[kK - 1], li[kK - 1])) return;
+  lv[kK - 1] = v;
+  li[kK - 1] = i;
+#pragma unroll
+  for (int j = kK - 1; j > 0; --j) {   // one bubble pass: the rest of the list is sorted
+    if (ranks_before(lv[j], li[j], lv[j - 1], li[j - 1])) {
+      const float tv = lv[j];
+      lv[j] = lv[j - 1];
+      lv[j - 1] = tv;
+      const int ti = li[j];
+      li[j] = li[j - 1];
+      li[j - 1] = ti;
+    }
+  }
+}
+
+template <typename E, int kK>
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(Params p) {
+  constexpr int kEPV = Elem<E>::kPerVec;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float *cv = reinterpret_cast<float *>(smem_raw);        // [kThreads * kK] candidate values
+  int *ci = reinterpret_cast<int *>(cv + kThreads * kK);  // [kThreads * kK] candidate indices
+  __shared__ float rv[kWarps];
+  __shared__ int ri[kWarps];
+  __shared__ int bad_any;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row_i = blockIdx.x;
+  const int V = p.V, k = p.topk;
+  const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(row_i) * V;
+  const RowGeom g = row_geom<E>(row, V);
+  if (tid == 0) bad_any = 0;
+  float lv[kK];
+  int li[kK];
+#pragma unroll
+  for (int j = 0; j < kK; ++j) { lv[j] = -INFINITY; li[j] = 0x7fffffff; }
+  bool bad = false;   // NaN or +inf seen
+  auto take = [&](float v, int i) {
+    if (v != v || v == INFINITY) bad = true;
+    else topk_insert<kK>(lv, li, v, i);
+  };
+  if (tid < g.h) take(ld_elem<E>(row + tid), tid);
+  if (tid < g.tl) take(ld_elem<E>(row + g.h + g.nv * kEPV + tid), g.h + g.nv * kEPV + tid);
+  for (int v0 = tid; v0 < g.nv; v0 += kThreads * kVPL) {
+    uint4 buf[kVPL];
+#pragma unroll
+    for (int j = 0; j < kVPL; ++j) {
+      const int v = v0 + j * kThreads;
+      buf[j] = (v < g.nv) ? ld_stream(g.vecs + v)
+                          : make_uint4(Elem<E>::kNegInfWord, Elem<E>::kNegInfWord,
+                                       Elem<E>::kNegInfWord, Elem<E>::kNegInfWord);
+    }
+#pragma unroll
+    for (int j = 0; j < kVPL; ++j) {
+      const int v = v0 + j * kThreads;
+      if (v < g.nv) {
+#pragma unroll
+        for (int e = 0; e < kEPV; ++e) take(vec_elem<E>(buf[j], e), g.h + v * kEPV + e);
+      }
+    }
+  }
+  if (bad) atomicOr(&bad_any, 1);
+#pragma unroll
+  for (int j = 0; j < kK; ++j) {
+    cv[tid * kK + j] = lv[j];
+    ci[tid * kK + j] = li[j];
+  }
+  __syncthreads();
+  int32_t *out = p.out_tokens + static_cast<long long>(row_i) * k;
+  // a row with NaN / +inf, or with no element above -inf, is invalid
+  const bool invalid = bad_any != 0;
+  int head = 0;   // this thread's next candidate
+  for (int r = 0; r < k; ++r) {
+    float v = (head < kK) ? cv[tid * kK + head] : -INFINITY;
+    int i = (head < kK) ? ci[tid * kK + head] : 0x7fffffff;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+      const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
+      if (ranks_before(v2, i2, v, i)) { v = v2; i = i2; }
+    }
+    if (lane == 0) { rv[warp] = v; ri[warp] = i; }
+    __syncthreads();
+    float bv = rv[0];
+    int bi = ri[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w)
+      if (ranks_before(rv[w], ri[w], bv, bi)) { bv = rv[w]; bi = ri[w]; }
+    if (head < kK && ci[tid * kK + head] == bi) ++head;   // indices are unique
+    const bool row_bad = invalid || (r == 0 && bv == -INFINITY);
+    if (tid == 0) {
+      if (row_bad) {
+        for (int j = 0; j < k; ++j) out[j] = -1;
+        set_status(p.status, SPEC_ERR_NONFINITE);
+      } else {
+        out[r] = bi;
+      }
+    }
+    __syncthreads();
+    if (row_bad) return;   // the same on every thread
+  }
+}
+
+// ------------------------------------------------------------------ tree-attention mask
+//
+// Bit j of word j / 32 of row i is set iff node j is node i or one of its ancestors: the mask
+// with which every node of a decoding tree attends to its own root path. One CTA per tree; the
+// parents go to shared memory and are checked; thread t builds the rows of nodes t, t + 512, ...
+// in its own shared-memory row by walking parent pointers, then writes them out.
+constexpr int kMaskMaxWords = (SPEC_MAX_NODES + 31) / 32;
+
+// (A template only so that the header can define it in every translation unit.)
+template <int kUnused = 0>
+__global__ void __launch_bounds__(kThreads, 1) tree_mask_kernel(Params p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  int *par = reinterpret_cast<int *>(smem_raw);                          // [N]
+  uint32_t *rows = reinterpret_cast<uint32_t *>(par + SPEC_MAX_NODES);   // [kThreads][W]
+  __shared__ int bad;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int N = p.N, W = (N + 31) / 32;
+  const long long base = static_cast<long long>(b) * N;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  for (int i = tid; i < N; i += kThreads) {
+    const int q = p.parents[base + i];
+    par[i] = q;
+    if (i == 0 ? (q != -1) : (q < 0 || q >= i)) atomicOr(&bad, 1);
+  }
+  __syncthreads();
+  uint32_t *out = p.mask_words + base * W;
+  if (bad) {
+    for (long long q = tid; q < static_cast<long long>(N) * W; q += kThreads) out[q] = 0u;
+    if (tid == 0) set_status(p.status, SPEC_ERR_PARENT);
+    return;
+  }
+  uint32_t *mine = rows + tid * W;
+  for (int i = tid; i < N; i += kThreads) {
+    for (int w = 0; w < W; ++w) mine[w] = 0u;
+    for (int j = i; j >= 0; j = par[j]) mine[j >> 5] |= 1u << (j & 31);   // par[0] = -1 ends it
+    for (int w = 0; w < W; ++w) out[static_cast<long long>(i) * W + w] = mine[w];
   }
 }
 
