@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-helpers", action="store_true")
     ap.add_argument("--seed-offset", type=int, default=0)
     return ap.parse_args()
 
@@ -443,7 +444,85 @@ def run_ours(args, rank, world, local):
     out["e2e"] = e2e(r, ci, ti, args.e2e_steps, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(ci, ti, budget_s=10.0)
+    if not args.no_helpers:
+        out["helpers"] = helpers(ci, ti, device, peak, with_oracle=(rank == 0 and world == 1
+                                                                      and not args.no_cpu_baseline))
     return out
+
+
+def helpers(ci, ti, device, peak, with_oracle):
+    """The drafter-side helpers on the same data, outside the step: spec_sample of the chain's
+    320 draft rows, spec_topk (k = 4) of the same rows, spec_tree_mask of the 32 trees. Each is
+    timed as one CUDA graph of 32 back-to-back calls over 6 rotated input copies (CUDA events
+    around it); the oracle's time per call comes from a bounded sample of rows."""
+    import torch
+    import speculative_decoding_verification_78_gb300 as sv
+    from speculative_decoding_verification_78_gb300 import _binding as B_
+    V = ci.V
+    drafts = torch.from_numpy(ci.draft.reshape(-1, V).view(np.int16)).to(device) \
+        .view(torch.bfloat16)
+    rows = drafts.shape[0]
+    copies = [drafts.clone() for _ in range(ROT)]
+    rng = np.random.default_rng(7)
+    from workloads import make_uniforms
+    u_h = make_uniforms(rng, (rows,))
+    u = torch.from_numpy(u_h).to(device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    tok = torch.empty(rows, dtype=torch.int32, device=device)
+    idx = torch.empty((rows, 4), dtype=torch.int32, device=device)
+    par = torch.from_numpy(ti.parents).to(device)
+    mask = torch.empty((ti.B, ti.N, (ti.N + 31) // 32), dtype=torch.int32, device=device)
+    ws = sv.new_workspace(rows, 1, V, sv.SPEC_BF16, device)
+    stream = torch.cuda.Stream(device)
+    calls = {
+        "sample": (lambda k: B_.spec_sample(copies[k % ROT], ci.temperature, u, tok, st, ws,
+                                            stream), rows * V * 2 + rows * 8),
+        "topk": (lambda k: B_.spec_topk(copies[k % ROT], 4, idx, st, stream),
+                 rows * V * 2 + rows * 16),
+        "tree_mask": (lambda k: B_.spec_tree_mask(par, mask, st, stream),
+                      ti.B * ti.N * 4 + ti.B * ti.N * ((ti.N + 31) // 32) * 4),
+    }
+    res = {}
+    for name, (fn, nbytes) in calls.items():
+        with torch.cuda.stream(stream):
+            for k in range(ROT):
+                if fn(k):
+                    raise RuntimeError(f"{name} call failed")
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(32):
+                fn(k)
+        ts = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3 / 32)
+        t = float(np.median(ts))
+        res[name] = {"us_per_call": t * 1e6, "algorithmic_bytes": nbytes,
+                     "GBps": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / peak}
+    assert int(st.item()) == 0, "device-side error in the helpers"
+    res["shapes"] = {"sample": f"{rows} x {V} bf16, T = {ci.temperature}",
+                     "topk": f"{rows} x {V} bf16, k = 4", "tree_mask": f"{ti.B} x {ti.N}"}
+    if with_oracle:
+        import oracle
+        from workloads import BF16
+        dh = ci.draft.reshape(-1, V)
+        t0 = time.perf_counter()
+        oracle.sample(dh[:32], BF16, u_h[:32], ci.temperature)
+        res["sample"]["oracle_us_per_call"] = (time.perf_counter() - t0) / 32 * rows * 1e6
+        t0 = time.perf_counter()
+        oracle.topk(dh[:8], BF16, 4)
+        res["topk"]["oracle_us_per_call"] = (time.perf_counter() - t0) / 8 * rows * 1e6
+        t0 = time.perf_counter()
+        oracle.tree_mask(ti.parents)
+        res["tree_mask"]["oracle_us_per_call"] = (time.perf_counter() - t0) * 1e6
+        res["oracle_sample"] = "32 / 8 / 32 rows or trees timed on one host core, scaled"
+    return res
 
 
 def e2e(r, ci, ti, steps, world, device):

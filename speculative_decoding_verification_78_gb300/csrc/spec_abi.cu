@@ -111,7 +111,9 @@ FinishPlan chain_sample_plan(const Params &p) {
   f.warp_tail = false;
   f.cluster = S;
   f.grid = p.B * S;
-  f.smem = sizeof(float) * (2 * static_cast<size_t>(p.R) + nseg);
+  // rowM, rowZ (2R floats: 8-byte aligned end), the bonus row's unit partials, the segment sums
+  f.smem = sizeof(float) * 2 * static_cast<size_t>(p.R) +
+           sizeof(uint2) * static_cast<size_t>(p.C) + sizeof(float) * nseg;
   return f;
 }
 

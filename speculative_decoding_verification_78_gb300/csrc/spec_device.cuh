@@ -806,8 +806,11 @@ __device__ __forceinline__ bool arg_ok(float v) { return v == v && v != -INFINIT
 // Combines the unit partials of rows r = warp, warp + kWarps, ... of batch row b into per-row
 // statistics. The loads for four rows per warp (two partials per lane each) are issued before
 // any is combined, so this costs one round trip when C <= 64.
+//
+// keep (may be NULL): the unit partials of row keep_row are also copied there (C entries).
 __device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float *rowM,
-                                                   float *rowZ) {
+                                                   float *rowZ, uint2 *keep = nullptr,
+                                                   int keep_row = -1) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint2 *base = p.ws_part + static_cast<long long>(b) * p.R * p.C;
   for (int r0 = warp; r0 < p.R; r0 += 4 * kWarps) {
@@ -826,6 +829,11 @@ __device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float
     for (int q = 0; q < 4; ++q) {
       const int r = r0 + q * kWarps;
       if (r < p.R) {
+        const bool kp = keep && r == keep_row;
+        if (kp) {
+          if (lane < p.C) keep[lane] = v[q][0];
+          if (lane + 32 < p.C) keep[lane + 32] = v[q][1];
+        }
         float m = -INFINITY, s = 0.f;
         stat_merge(m, s, __uint_as_float(v[q][0].x), __uint_as_float(v[q][0].y), p.c2);
         stat_merge(m, s, __uint_as_float(v[q][1].x), __uint_as_float(v[q][1].y), p.c2);
@@ -837,8 +845,10 @@ __device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float
           for (int t = 0; t < 4; ++t)
             w[t] = (c0 + 32 * t < p.C) ? ldcg_u2(pr + c0 + 32 * t) : make_uint2(0xff800000u, 0u);
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
+          for (int t = 0; t < 4; ++t) {
+            if (kp && c0 + 32 * t < p.C) keep[c0 + 32 * t] = w[t];
             stat_merge(m, s, __uint_as_float(w[t].x), __uint_as_float(w[t].y), p.c2);
+          }
         }
         warp_stat_merge(m, s, p.c2);
         if (lane == 0) { rowM[r] = m; rowZ[r] = s; }
@@ -900,7 +910,7 @@ __device__ __forceinline__ void combine_rows_arg(const Params &p, int b, int *g,
 // draft with one warp ballot per 32 positions. Returns 0 with *n = the number of accepted
 // drafts (on every thread), or a device error code (a non-finite row, a token outside [0, V)).
 __device__ inline int chain_accept(const Params &p, int b, float *rowM, float *rowZ, int *xs,
-                                   TailShared &sh, int *n_out) {
+                                   TailShared &sh, int *n_out, uint2 *keep_bonus = nullptr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = p.R, gamma = p.gamma;
   const float c2 = p.c2;
@@ -919,7 +929,7 @@ __device__ inline int chain_accept(const Params &p, int b, float *rowM, float *r
   // gamma <= SPEC_MAX_GAMMA < kThreads: one draft per thread, kept in a register until the
   // partial loads below have been issued (a shared store would wait for it)
   const int xv = (static_cast<int>(threadIdx.x) < gamma) ? x[threadIdx.x] : 0;
-  combine_rows_stats(p, b, rowM, rowZ);
+  combine_rows_stats(p, b, rowM, rowZ, keep_bonus, gamma);
   if (static_cast<int>(threadIdx.x) < gamma) xs[threadIdx.x] = xv;
   __syncthreads();
   if (warp == 0) {
@@ -1233,6 +1243,118 @@ __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
   }
 }
 
+// The bonus draw (from p_gamma alone) of a row with no unaligned head or tail, from the stream
+// kernel's unit partials: unit u holds p-mass w_u = s_u * 2^((m_u - M) * c2) / Z, so the unit
+// where the running sum crosses t = u * sum(w) is found without reading the row; warp 0 then
+// reads that one unit (4 KB) and finds the element with warp scans, in index order. Writes the
+// outputs.
+template <typename E>
+__device__ void bonus_draw_units(const Params &p, int b, int n, float M, float Z,
+                                 const uint2 *part, const int *xs) {
+  constexpr int kEPV = Elem<E>::kPerVec;
+  const int lane = threadIdx.x & 31;
+  const int C = p.C;
+  const float c2 = p.c2, iZ = __frcp_rn(Z);
+  const float u = p.uniforms[static_cast<long long>(b) * (p.gamma + 1) + p.gamma];
+  // lane l sums the masses of units [l*q, (l+1)*q) in order; a warp scan gives every prefix
+  const int q = (C + 31) / 32;
+  const int u0 = min(C, lane * q), u1 = min(C, u0 + q);
+  auto mass = [&](int uc) -> float {
+    const uint2 w = part[uc];
+    return __fmul_rn(__fmul_rn(__uint_as_float(w.y), ex2_shift(__uint_as_float(w.x), M, c2)), iZ);
+  };
+  float ls = 0.f;
+  for (int uc = u0; uc < u1; ++uc) ls = __fadd_rn(ls, mass(uc));
+  float inc = ls;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc = __fadd_rn(inc, y);
+  }
+  const float S = __shfl_sync(0xffffffffu, inc, 31);
+  const float t = __fmul_rn(u, S);
+  const float exc = __shfl_up_sync(0xffffffffu, inc, 1);
+  // the crossing unit: the owner lane scans its block; no crossing (rounding): last unit with mass
+  const unsigned over = __ballot_sync(0xffffffffu, inc > t);
+  int uc_sel = -1, mode = 0;
+  float base = 0.f;
+  if (over) {
+    const int ol = __ffs(over) - 1;
+    if (lane == ol) {
+      float acc = (lane == 0) ? 0.f : exc;
+      for (int uc = u0; uc < u1; ++uc) {
+        const float nx = __fadd_rn(acc, mass(uc));
+        if (nx > t) { uc_sel = uc; base = acc; break; }
+        acc = nx;
+      }
+      if (uc_sel < 0) { uc_sel = u1 - 1; base = acc; }
+    }
+    uc_sel = __shfl_sync(0xffffffffu, uc_sel, ol);
+    base = __shfl_sync(0xffffffffu, base, ol);
+  } else {
+    mode = 1;
+    int last = -1;
+    for (int uc = u0; uc < u1; ++uc)
+      if (mass(uc) > 0.f) last = uc;
+    const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
+    uc_sel = __shfl_sync(0xffffffffu, last, has ? 31 - __clz(has) : 0);
+    uc_sel = max(uc_sel, 0);
+  }
+  // the element inside unit uc_sel: vectors j*32 + lane, elements in order
+  const E *row = row_ptr<E>(p, b, n);
+  const RowGeom g = row_geom<E>(row, p.V);
+  uint4 buf[kVPL];
+  float eh, et;
+  load_span<E>(row, g, uc_sel * kUnitVecs, g.nv, false, lane, buf, eh, et);
+  int tok = -1, lastpos = -1;
+#pragma unroll
+  for (int j = 0; j < kVPL; ++j) {
+    float pe[kEPV];
+    float vs = 0.f;
+#pragma unroll
+    for (int e = 0; e < kEPV; ++e) {
+      pe[e] = __fmul_rn(ex2_shift(vec_elem<E>(buf[j], e), M, c2), iZ);
+      vs = __fadd_rn(vs, pe[e]);
+    }
+    const int k0 = (uc_sel * kUnitVecs + j * 32 + lane) * kEPV;
+#pragma unroll
+    for (int e = 0; e < kEPV; ++e)
+      if (pe[e] > 0.f) lastpos = k0 + e;
+    float vi = vs;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, vi, off);
+      if (lane >= off) vi = __fadd_rn(vi, y);
+    }
+    if (mode == 0 && tok < 0) {
+      const float ve = __shfl_up_sync(0xffffffffu, vi, 1);
+      const float lex = (lane == 0) ? base : __fadd_rn(base, ve);
+      const unsigned cr = __ballot_sync(0xffffffffu, __fadd_rn(base, vi) > t);
+      if (cr) {
+        const int cl = __ffs(cr) - 1;
+        int tk = -1;
+        if (lane == cl) {
+          float acc = lex;
+          for (int e = 0; e < kEPV; ++e) {
+            const float nx = __fadd_rn(acc, pe[e]);
+            if (nx > t) { tk = k0 + e; break; }
+            acc = nx;
+          }
+          if (tk < 0) tk = (lastpos >= k0) ? lastpos : k0 + kEPV - 1;
+        }
+        tok = __shfl_sync(0xffffffffu, tk, cl);
+      }
+      base = __fadd_rn(base, __shfl_sync(0xffffffffu, vi, 31));
+    }
+  }
+  if (tok < 0) {   // rounding left no crossing inside the unit: its last element with mass
+    const unsigned has = __ballot_sync(0xffffffffu, lastpos >= 0);
+    tok = has ? __shfl_sync(0xffffffffu, lastpos, 31 - __clz(has)) : 0;
+    tok = max(tok, 0);
+  }
+  emit_chain(p, b, n, tok, xs, lane, 32);
+}
+
 // The cluster draw when every CTA's slice has at most kWarps * kRegSegs segments: warp w of
 // CTA `rank` loads segments rank*K + w*kRegSegs .. +kRegSegs - 1 (one round trip) and keeps
 // them in registers. Warp totals -> CTA total -> cluster prefix through distributed shared
@@ -1534,7 +1656,9 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   float *rowM = reinterpret_cast<float *>(smem_raw);
   float *rowZ = rowM + p.R;
-  float *segsum = rowZ + p.R;
+  // [C] the bonus row's unit partials, at byte offset 8R: 8-byte aligned for every R
+  uint2 *bonus_part = reinterpret_cast<uint2 *>(rowZ + p.R);
+  float *segsum = reinterpret_cast<float *>(bonus_part + p.C);
   __shared__ TailShared sh;
   __shared__ int xs[SPEC_MAX_GAMMA];
   __shared__ float s_total;
@@ -1545,13 +1669,23 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   const int b = blockIdx.x / S;
   wait_stream_kernel();
   int n = 0;
-  const int err = chain_accept(p, b, rowM, rowZ, xs, sh, &n);
+  const int err = chain_accept(p, b, rowM, rowZ, xs, sh, &n, bonus_part);
   if (err) {   // the same on every CTA of the cluster: all of them leave here
     if (rank == 0) {
       if (threadIdx.x == 0) set_status(p.status, err);
       fail_chain_row(p, b, threadIdx.x, kThreads);
     }
     return;
+  }
+  if (n == p.gamma) {
+    // the bonus draw, from the unit partials when the row has no unaligned head or tail (the
+    // same decision on every CTA of the cluster; no CTA has touched a peer's shared memory)
+    const RowGeom g = row_geom<E>(row_ptr<E>(p, b, n), p.V);
+    if (g.h == 0 && g.tl == 0) {
+      if (rank == 0 && threadIdx.x < 32)
+        bonus_draw_units<E>(p, b, n, rowM[n], rowZ[n], bonus_part, xs);
+      return;
+    }
   }
   cluster_draw<E>(p, b, n, rowM, rowZ, xs, segsum, sh, s_total, s_pre);
 }
