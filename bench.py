@@ -473,11 +473,12 @@ def helpers(ci, ti, device, peak, with_oracle):
     par = torch.from_numpy(ti.parents).to(device)
     mask = torch.empty((ti.B, ti.N, (ti.N + 31) // 32), dtype=torch.int32, device=device)
     ws = sv.new_workspace(rows, 1, V, sv.SPEC_BF16, device)
+    ws4 = sv.new_workspace(rows, 4, V, sv.SPEC_BF16, device)
     stream = torch.cuda.Stream(device)
     calls = {
         "sample": (lambda k: B_.spec_sample(copies[k % ROT], ci.temperature, u, tok, st, ws,
                                             stream), rows * V * 2 + rows * 8),
-        "topk": (lambda k: B_.spec_topk(copies[k % ROT], 4, idx, st, stream),
+        "topk": (lambda k: B_.spec_topk(copies[k % ROT], 4, idx, st, ws4, stream),
                  rows * V * 2 + rows * 16),
         "tree_mask": (lambda k: B_.spec_tree_mask(par, mask, st, stream),
                       ti.B * ti.N * 4 + ti.B * ti.N * ((ti.N + 31) // 32) * 4),

@@ -72,7 +72,8 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 /*
  * Bytes of workspace needed by a call over B batch rows of `rows_per_b` logits rows of V
  * elements: rows_per_b = 2*gamma+1 for spec_verify_chain (any temperature), N for
- * spec_verify_tree, 1 for spec_probs (with B = rows). Returns 0 for invalid arguments.
+ * spec_verify_tree, 1 for spec_probs and spec_sample (with B = rows), k for spec_topk (with
+ * B = rows). Returns 0 for invalid arguments.
  */
 size_t spec_workspace_bytes(int B, int rows_per_b, int V, int dtype);
 
@@ -167,14 +168,15 @@ int spec_sample(const void *logits, int dtype, int rows, int V, float temperatur
  * each node (Falcon, pith.science review, "What carries the argument"): out_idx[r, 0..k) = the
  * indices of the k largest logits of row r, largest first, equal values by increasing index.
  * An invalid row (NaN, +inf, or no finite value) gets -1 everywhere and sets *status
- * (SPEC_ERR_NONFINITE). No workspace.
- *   logits  [rows, V]  dtype
- *   out_idx [rows, k]  int32 out
+ * (SPEC_ERR_NONFINITE).
+ *   logits    [rows, V]  dtype
+ *   out_idx   [rows, k]  int32 out
+ *   workspace at least spec_workspace_bytes(rows, k, V, dtype) bytes (scratch)
  * Limits: 1 <= k <= min(V, SPEC_MAX_TOPK), 1 <= V <= SPEC_MAX_V, rows >= 0.
  */
 #define SPEC_MAX_TOPK 16
 int spec_topk(const void *logits, int dtype, int rows, int V, int k, int32_t *out_idx,
-              int32_t *status, void *stream);
+              int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Tree-attention mask of B candidate trees (Falcon review, Figure 3, "SAR decoding tree

@@ -73,7 +73,7 @@ def load_library():
         lib.spec_verify_chain_static.restype = i32
         lib.spec_sample.argtypes = [vp, i32, i32, i32, f32, vp, vp, vp, vp, sz, vp]
         lib.spec_sample.restype = i32
-        lib.spec_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
+        lib.spec_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, sz, vp]
         lib.spec_topk.restype = i32
         lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
         lib.spec_tree_mask.restype = i32
@@ -187,12 +187,13 @@ def spec_sample(logits, temperature, uniforms, out_tokens, status, workspace, st
         _ptr(out_tokens), _ptr(status), _ptr(workspace), _nbytes(workspace), _stream(stream))
 
 
-def spec_topk(logits, k, out_idx, status, stream=None) -> int:
+def spec_topk(logits, k, out_idx, status, workspace, stream=None) -> int:
     """logits [rows, V] -> out_idx [rows, k] int32."""
     V = logits.shape[-1]
     rows = logits.numel() // V if V else 0
     return load_library().spec_topk(_ptr(logits), dtype_flag(logits), rows, V, int(k),
-                                    _ptr(out_idx), _ptr(status), _stream(stream))
+                                    _ptr(out_idx), _ptr(status), _ptr(workspace),
+                                    _nbytes(workspace), _stream(stream))
 
 
 def spec_tree_mask(parents, mask_words, status, stream=None) -> int:
@@ -282,14 +283,16 @@ def sample(logits, temperature, uniforms=None, workspace=None, stream=None):
     return out, st
 
 
-def topk(logits, k, stream=None):
+def topk(logits, k, workspace=None, stream=None):
     """Allocates the output and runs spec_topk. Returns (indices [rows, k] int32, status)."""
     V = logits.shape[-1]
     rows = logits.numel() // V
     dev = logits.device
+    if workspace is None:
+        workspace = new_workspace(rows, k, V, dtype_flag(logits), dev)
     out = torch.empty((rows, k), dtype=torch.int32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    check(spec_topk(logits, k, out, st, stream), "spec_topk")
+    check(spec_topk(logits, k, out, st, workspace, stream), "spec_topk")
     return out, st
 
 

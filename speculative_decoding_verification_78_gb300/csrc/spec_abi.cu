@@ -336,12 +336,13 @@ int spec_sample(const void *logits, int dtype, int rows, int V, float temperatur
 }
 
 int spec_topk(const void *logits, int dtype, int rows, int V, int k, int32_t *out_idx,
-              int32_t *status, void *stream) {
+              int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
   if (rows < 0 || V < 1 || V > SPEC_MAX_V || k < 1 || k > SPEC_MAX_TOPK || k > V)
     return SPEC_ERR_SHAPE;
-  if (!logits || !out_idx || !status) return SPEC_ERR_NULL;
-  if (!aligned(logits, elem_size(dtype)) || !aligned(out_idx, 4) || !aligned(status, 4))
+  if (!logits || !out_idx || !status || !workspace) return SPEC_ERR_NULL;
+  if (!aligned(logits, elem_size(dtype)) || !aligned(out_idx, 4) || !aligned(status, 4) ||
+      !aligned(workspace, 16))
     return SPEC_ERR_ALIGN;
   if (rows == 0) return SPEC_OK;
   Params p = blank();
@@ -350,7 +351,17 @@ int spec_topk(const void *logits, int dtype, int rows, int V, int k, int32_t *ou
   p.out_tokens = out_idx;
   p.status = status;
   p.topk = k;
-  const cudaError_t e = launch_topk(dtype, p, static_cast<cudaStream_t>(stream));
+  const int rc = plan_units(p, dtype);
+  if (rc != SPEC_OK) return rc;
+  // k candidates (8 bytes each) per unit: the unit partials region of a call with k rows per row
+  if (workspace_bytes < layout(rows, k, p.C).total) return SPEC_ERR_WORKSPACE;
+  p.ws_part = static_cast<uint2 *>(workspace);
+  // one CTA of 512 threads per SM (up to 128 registers per thread for the lists)
+  const long long cap = sm_count() > 0 ? sm_count() : 1;
+  const long long groups = (static_cast<long long>(p.units) + kWarps - 1) / kWarps;
+  const int grid = static_cast<int>(groups < cap ? groups : cap);
+  const cudaError_t e = launch_topk(dtype, p, grid < 1 ? 1 : grid,
+                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 

@@ -1853,11 +1853,12 @@ __global__ void __launch_bounds__(kThreads, 2) finish_probs(Params p) {
 // ------------------------------------------------------------------ top-n candidates
 //
 // The k largest logits of each row (value descending, equal values by increasing index), for
-// expanding a draft tree. One CTA per row: every thread streams its share of the row (16-byte
-// vectors tid, tid + 512, ..., plus the unaligned head and tail on the first threads) keeping a
-// sorted list of its kK best (value, index) pairs in registers; the lists go to shared memory
-// and k rounds of a block-wide maximum over the lists' heads pick the row's k best in order.
-// Every element of the row's top k is within its thread's top kK >= k, so this is exact.
+// expanding a draft tree. Two kernels, as for verification: the stream pass reduces every unit
+// (4 KB of one row, one warp) to that unit's own top k -- each lane keeps a sorted list of its
+// kK >= k best (value, index) pairs in registers, then k rounds of a warp maximum over the
+// lists' heads -- and writes the k candidates to the workspace; the finishing kernel (one warp
+// per row, a programmatic dependent) merges the row's C*k candidates the same way. Exact: every
+// element of the row's top k is in its own unit's top k. A NaN or +inf poisons the row.
 
 // (v, i) ranks before (w, j)
 __device__ __forceinline__ bool ranks_before(float v, int i, float w, int j) {
@@ -1882,92 +1883,184 @@ __device__ __forceinline__ void topk_insert(float (&lv)[kK], int (&li)[kK], floa
   }
 }
 
-template <typename E, int kK>
-__global__ void __launch_bounds__(kThreads, 1) topk_kernel(Params p) {
-  constexpr int kEPV = Elem<E>::kPerVec;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  float *cv = reinterpret_cast<float *>(smem_raw);        // [kThreads * kK] candidate values
-  int *ci = reinterpret_cast<int *>(cv + kThreads * kK);  // [kThreads * kK] candidate indices
-  __shared__ float rv[kWarps];
-  __shared__ int ri[kWarps];
-  __shared__ int bad_any;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row_i = blockIdx.x;
-  const int V = p.V, k = p.topk;
-  const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(row_i) * V;
-  const RowGeom g = row_geom<E>(row, V);
-  if (tid == 0) bad_any = 0;
-  float lv[kK];
-  int li[kK];
-#pragma unroll
-  for (int j = 0; j < kK; ++j) { lv[j] = -INFINITY; li[j] = 0x7fffffff; }
-  bool bad = false;   // NaN or +inf seen
-  auto take = [&](float v, int i) {
-    if (v != v || v == INFINITY) bad = true;
-    else topk_insert<kK>(lv, li, v, i);
-  };
-  if (tid < g.h) take(ld_elem<E>(row + tid), tid);
-  if (tid < g.tl) take(ld_elem<E>(row + g.h + g.nv * kEPV + tid), g.h + g.nv * kEPV + tid);
-  for (int v0 = tid; v0 < g.nv; v0 += kThreads * kVPL) {
-    uint4 buf[kVPL];
-#pragma unroll
-    for (int j = 0; j < kVPL; ++j) {
-      const int v = v0 + j * kThreads;
-      buf[j] = (v < g.nv) ? ld_stream(g.vecs + v)
-                          : make_uint4(Elem<E>::kNegInfWord, Elem<E>::kNegInfWord,
-                                       Elem<E>::kNegInfWord, Elem<E>::kNegInfWord);
-    }
-#pragma unroll
-    for (int j = 0; j < kVPL; ++j) {
-      const int v = v0 + j * kThreads;
-      if (v < g.nv) {
-#pragma unroll
-        for (int e = 0; e < kEPV; ++e) take(vec_elem<E>(buf[j], e), g.h + v * kEPV + e);
-      }
-    }
-  }
-  if (bad) atomicOr(&bad_any, 1);
-#pragma unroll
-  for (int j = 0; j < kK; ++j) {
-    cv[tid * kK + j] = lv[j];
-    ci[tid * kK + j] = li[j];
-  }
-  __syncthreads();
-  int32_t *out = p.out_tokens + static_cast<long long>(row_i) * k;
-  // a row with NaN / +inf, or with no element above -inf, is invalid
-  const bool invalid = bad_any != 0;
-  int head = 0;   // this thread's next candidate
+// k rounds of a warp maximum over the lanes' sorted lists: round r's winner goes to
+// (out_v[r], out_i[r]) on lane 0. Lists are consumed.
+template <int kK>
+__device__ __forceinline__ void warp_take_topk(float (&lv)[kK], int (&li)[kK], int k, int lane,
+                                               uint2 *out) {
   for (int r = 0; r < k; ++r) {
-    float v = (head < kK) ? cv[tid * kK + head] : -INFINITY;
-    int i = (head < kK) ? ci[tid * kK + head] : 0x7fffffff;
+    float v = lv[0];
+    int i = li[0];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
       const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
       if (ranks_before(v2, i2, v, i)) { v = v2; i = i2; }
     }
-    if (lane == 0) { rv[warp] = v; ri[warp] = i; }
-    __syncthreads();
-    float bv = rv[0];
-    int bi = ri[0];
+    if (li[0] == i) {   // indices are unique: exactly the winning lane pops its head
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w)
-      if (ranks_before(rv[w], ri[w], bv, bi)) { bv = rv[w]; bi = ri[w]; }
-    if (head < kK && ci[tid * kK + head] == bi) ++head;   // indices are unique
-    const bool row_bad = invalid || (r == 0 && bv == -INFINITY);
-    if (tid == 0) {
-      if (row_bad) {
-        for (int j = 0; j < k; ++j) out[j] = -1;
-        set_status(p.status, SPEC_ERR_NONFINITE);
-      } else {
-        out[r] = bi;
+      for (int j = 0; j < kK - 1; ++j) { lv[j] = lv[j + 1]; li[j] = li[j + 1]; }
+      lv[kK - 1] = -INFINITY;
+      li[kK - 1] = 0x7fffffff;
+    }
+    if (lane == 0) out[r] = make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
+  }
+}
+
+// Per unit: if T is the k-th largest of the 32 lanes' maxima, every element of the unit's top k
+// is >= T (the k largest lane maxima are k distinct elements, all >= T). The elements >= T --
+// usually about k of them -- go to a per-warp candidate buffer in shared memory, ranked there.
+// When more than kTopkCand qualify (heavy ties), the unit falls back to sorted per-lane lists.
+constexpr int kTopkCand = 64;
+
+template <typename E, int kK>
+__global__ void __launch_bounds__(kThreads, 1) topk_stream_kernel(Params p) {
+  constexpr int kEPV = Elem<E>::kPerVec;
+  __shared__ uint2 cbuf[kWarps][kTopkCand];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int W = gridDim.x * kWarps;
+  const int k = p.topk;
+  uint2 *cand = cbuf[warp];
+  for (int unit = blockIdx.x * kWarps + warp; unit < p.units; unit += W) {
+    const UnitId u = unit_id(p, unit);
+    const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(u.b) * p.V;
+    const RowGeom g = row_geom<E>(row, p.V);
+    uint4 buf[kVPL];
+    float eh, et;
+    load_unit<E>(row, g, u.chunk, lane, buf, eh, et);
+    const bool has_h = u.chunk == 0 && lane < g.h, has_t = u.chunk == 0 && lane < g.tl;
+    const int v0 = u.chunk * kUnitVecs + lane;
+    // this lane's maximum (NaN-propagating); +inf and NaN poison the row
+    float lm = fmax_nan(has_h ? eh : -INFINITY, has_t ? et : -INFINITY);
+#pragma unroll
+    for (int j = 0; j < kVPL; ++j)
+      if (v0 + j * 32 < g.nv) lm = fmax_nan(lm, vec_max<E>(buf[j]));
+    const bool any_elem = has_h || has_t || v0 < g.nv;
+    const bool bad = (lm != lm) || lm == INFINITY;
+    uint2 *out = p.ws_part + static_cast<long long>(unit) * k;
+    if (__any_sync(0xffffffffu, bad)) {   // poison the unit: its first candidate NaN
+      if (lane == 0) out[0] = make_uint2(0x7fc00000u, 0u);
+      continue;
+    }
+    // T: the k-th largest lane maximum (k rounds of a warp maximum; -inf if fewer lanes)
+    float T = -INFINITY;
+    {
+      bool taken = !any_elem;
+      for (int r = 0; r < k; ++r) {
+        float v = taken ? -INFINITY : lm;
+        int who = taken ? 32 : lane;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+          const int w2 = __shfl_xor_sync(0xffffffffu, who, off);
+          if (ranks_before(v2, w2, v, who)) { v = v2; who = w2; }
+        }
+        if (who == lane) taken = true;
+        T = v;
       }
     }
-    __syncthreads();
-    if (row_bad) return;   // the same on every thread
+    // count, then gather, this lane's elements >= T
+    int cnt = 0;
+    if (has_h && eh >= T) ++cnt;
+    if (has_t && et >= T) ++cnt;
+#pragma unroll
+    for (int j = 0; j < kVPL; ++j)
+      if (v0 + j * 32 < g.nv)
+#pragma unroll
+        for (int e = 0; e < kEPV; ++e) cnt += (vec_elem<E>(buf[j], e) >= T) ? 1 : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total <= kTopkCand && T != -INFINITY) {
+      int pos = incl - cnt;
+      auto put = [&](float v, int i) {
+        cand[pos++] = make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
+      };
+      if (has_h && eh >= T) put(eh, lane);
+#pragma unroll
+      for (int j = 0; j < kVPL; ++j)
+        if (v0 + j * 32 < g.nv)
+#pragma unroll
+          for (int e = 0; e < kEPV; ++e) {
+            const float v = vec_elem<E>(buf[j], e);
+            if (v >= T) put(v, g.h + (v0 + j * 32) * kEPV + e);
+          }
+      if (has_t && et >= T) put(et, g.h + g.nv * kEPV + lane);
+      __syncwarp();
+      // two candidates per lane, ranked; k rounds of a warp maximum
+      float lv[2];
+      int li[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int c = lane + 32 * q;
+        const uint2 w = (c < total) ? cand[c] : make_uint2(0xff800000u, 0x7fffffffu);
+        lv[q] = __uint_as_float(w.x);
+        li[q] = (c < total) ? static_cast<int>(w.y) : 0x7fffffff;
+      }
+      if (ranks_before(lv[1], li[1], lv[0], li[0])) {
+        const float tv = lv[0]; lv[0] = lv[1]; lv[1] = tv;
+        const int ti = li[0]; li[0] = li[1]; li[1] = ti;
+      }
+      __syncwarp();   // the buffer is reused by this warp's next unit
+      warp_take_topk<2>(lv, li, k, lane, out);
+      continue;
+    }
+    // fallback: sorted per-lane lists of kK (value, index) pairs
+    float lv[kK];
+    int li[kK];
+#pragma unroll
+    for (int j = 0; j < kK; ++j) { lv[j] = -INFINITY; li[j] = 0x7fffffff; }
+    if (has_h) topk_insert<kK>(lv, li, eh, lane);
+    if (has_t) topk_insert<kK>(lv, li, et, g.h + g.nv * kEPV + lane);
+#pragma unroll
+    for (int j = 0; j < kVPL; ++j) {
+      const int v = v0 + j * 32;
+      if (v < g.nv) {
+#pragma unroll
+        for (int e = 0; e < kEPV; ++e) topk_insert<kK>(lv, li, vec_elem<E>(buf[j], e), g.h + v * kEPV + e);
+      }
+    }
+    warp_take_topk<kK>(lv, li, k, lane, out);
   }
+}
+
+// One warp per row: the row's C*k unit candidates, merged.
+template <int kK>
+__global__ void __launch_bounds__(kThreads, 1) topk_finish(Params p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int row_i = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (row_i >= p.B) return;
+  const int k = p.topk, n = p.C * k;
+  const uint2 *cand = p.ws_part + static_cast<long long>(row_i) * n;
+  float lv[kK];
+  int li[kK];
+#pragma unroll
+  for (int j = 0; j < kK; ++j) { lv[j] = -INFINITY; li[j] = 0x7fffffff; }
+  bool bad = false;
+  for (int c = lane; c < n; c += 32) {
+    const uint2 w = ldcg_u2(cand + c);
+    const float v = __uint_as_float(w.x);
+    if (v != v) bad = true;
+    else topk_insert<kK>(lv, li, v, static_cast<int>(w.y));
+  }
+  __shared__ uint2 sel[kWarps][SPEC_MAX_TOPK];
+  uint2 *mine = sel[threadIdx.x >> 5];
+  const bool row_bad = __any_sync(0xffffffffu, bad);
+  warp_take_topk<kK>(lv, li, k, lane, mine);
+  __syncwarp();
+  int32_t *out = p.out_tokens + static_cast<long long>(row_i) * k;
+  // no element above -inf: no finite value in the row
+  const bool invalid = row_bad || __uint_as_float(mine[0].x) == -INFINITY;
+  if (invalid && lane == 0) set_status(p.status, SPEC_ERR_NONFINITE);
+  for (int r = lane; r < k; r += 32) out[r] = invalid ? -1 : static_cast<int>(mine[r].y);
 }
 
 // ------------------------------------------------------------------ tree-attention mask

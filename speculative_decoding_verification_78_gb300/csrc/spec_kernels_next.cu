@@ -1,5 +1,6 @@
 // spec_kernels_next.cu -- kernel instances for the drafter-side helpers: top-n candidates per
-// row and the tree-attention mask. (Sampling reuses the chain kernels with gamma = 0.)
+// row (stream pass + merge) and the tree-attention mask. (Sampling reuses the chain kernels with
+// gamma = 0.)
 #include <atomic>
 
 #include "spec_launch.h"
@@ -19,27 +20,25 @@ cudaError_t allow_smem(Kernel kernel, size_t bytes, std::atomic<bool> &done) {
 }
 
 template <typename E, int kK>
-cudaError_t topk_k(const Params &p, cudaStream_t stream) {
-  static std::atomic<bool> done{false};
-  const size_t smem = static_cast<size_t>(kThreads) * kK * 8;
-  const cudaError_t e = allow_smem(topk_kernel<E, kK>, smem, done);
+cudaError_t topk_k(const Params &p, int grid, cudaStream_t stream) {
+  const cudaError_t e = launch_dependent(topk_stream_kernel<E, kK>, p, grid, 1, 0, stream);
   if (e != cudaSuccess) return e;
-  return launch_dependent(topk_kernel<E, kK>, p, p.B, 1, smem, stream);
+  return launch_dependent(topk_finish<kK>, p, (p.B + kWarps - 1) / kWarps, 1, 0, stream);
 }
 
 template <typename E>
-cudaError_t topk_e(const Params &p, cudaStream_t stream) {
-  if (p.topk <= 1) return topk_k<E, 1>(p, stream);
-  if (p.topk <= 2) return topk_k<E, 2>(p, stream);
-  if (p.topk <= 4) return topk_k<E, 4>(p, stream);
-  if (p.topk <= 8) return topk_k<E, 8>(p, stream);
-  return topk_k<E, 16>(p, stream);
+cudaError_t topk_e(const Params &p, int grid, cudaStream_t stream) {
+  if (p.topk <= 1) return topk_k<E, 1>(p, grid, stream);
+  if (p.topk <= 2) return topk_k<E, 2>(p, grid, stream);
+  if (p.topk <= 4) return topk_k<E, 4>(p, grid, stream);
+  if (p.topk <= 8) return topk_k<E, 8>(p, grid, stream);
+  return topk_k<E, 16>(p, grid, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_topk(int dtype, const Params &p, cudaStream_t stream) {
-  return dtype == SPEC_BF16 ? topk_e<uint16_t>(p, stream) : topk_e<float>(p, stream);
+cudaError_t launch_topk(int dtype, const Params &p, int grid, cudaStream_t stream) {
+  return dtype == SPEC_BF16 ? topk_e<uint16_t>(p, grid, stream) : topk_e<float>(p, grid, stream);
 }
 
 cudaError_t launch_tree_mask(const Params &p, cudaStream_t stream) {

@@ -62,7 +62,7 @@ cudaError_t launch_tree(int dtype, const Params &p, int grid, const FinishPlan &
                         cudaStream_t stream);
 cudaError_t launch_probs(int mode, int dtype, const Params &p, int grid, const FinishPlan &f,
                          cudaStream_t stream);
-cudaError_t launch_topk(int dtype, const Params &p, cudaStream_t stream);
+cudaError_t launch_topk(int dtype, const Params &p, int grid, cudaStream_t stream);
 cudaError_t launch_tree_mask(const Params &p, cudaStream_t stream);
 
 }  // namespace specv
