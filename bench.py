@@ -179,7 +179,7 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_78_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f == "spec_device.cuh" or f == "spec_launch.h" or f.startswith("spec_kernels_"):
+        if f.endswith(".cuh") or f == "spec_launch.h" or f.startswith("spec_kernels_"):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
