@@ -303,15 +303,12 @@ __device__ __forceinline__ void unit_stats(const uint4 (&buf)[kVPL], float eh, f
 // ------------------------------------------------------------------ greedy argmax
 
 // (v, i) <- the larger value, the smaller index on equal values. NaN marks a bad row.
+// Selects instead of branches: it sits in shuffle-reduction chains on the critical path.
 __device__ __forceinline__ void arg_merge(float &v, int &i, float v2, int i2) {
-  if (v2 != v2 || v != v) {
-    v = __int_as_float(0x7fc00000);
-    return;
-  }
-  if (v2 > v || (v2 == v && i2 < i)) {
-    v = v2;
-    i = i2;
-  }
+  const bool nan = (v2 != v2) | (v != v);
+  const bool take = (v2 > v) | ((v2 == v) & (i2 < i));
+  i = take ? i2 : i;
+  v = nan ? __int_as_float(0x7fc00000) : (take ? v2 : v);
 }
 
 // NaN-propagating maximum of one vector.

@@ -31,56 +31,70 @@ __device__ __forceinline__ bool stats_ok(float m, float z) {
 // argmax of a row is usable when it is finite (no NaN/+inf seen, some element above -inf)
 __device__ __forceinline__ bool arg_ok(float v) { return v == v && v != -INFINITY; }
 
-// Combines the unit partials of rows r = warp, warp + kWarps, ... of batch row b into per-row
-// statistics. The loads for four rows per warp (two partials per lane each) are issued before
-// any is combined, so this costs one round trip when C <= 64.
+// Lanes that combine one row's unit partials: the smallest power of two L with 2L >= C (at most
+// 32), so that each lane merges at most two partials (when C <= 64) before log2(L) shuffle
+// rounds inside its group of L lanes; a warp combines 32 / L rows at once. Short dependent
+// chains matter here: this runs after the stream pass, on the critical path of every call.
+__device__ __forceinline__ int combine_lanes(int C) {
+  int L = 1;
+  while (L < 32 && 2 * L < C) L <<= 1;
+  return L;
+}
+
+// Combines the unit partials of every row of batch row b into per-row statistics (rowM, rowZ
+// in shared memory). Each warp takes 32 / L rows per pass and two passes per round trip: all
+// of a round's loads are issued before any is merged. Partials beyond the first 2L of a row
+// (C > 64) are merged four per lane per round trip, in a fixed order.
 //
 // keep (may be NULL): the unit partials of row keep_row are also copied there (C entries).
 __device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float *rowM,
                                                    float *rowZ, uint2 *keep = nullptr,
                                                    int keep_row = -1) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint2 *base = p.ws_part + static_cast<long long>(b) * p.R * p.C;
-  for (int r0 = warp; r0 < p.R; r0 += 4 * kWarps) {
-    uint2 v[4][2];
+  const int R = p.R, C = p.C;
+  const int L = combine_lanes(C);
+  const int sub = lane & (L - 1), rpw = 32 / L, pass = kWarps * rpw;
+  const uint2 *base = p.ws_part + static_cast<long long>(b) * R * C;
+  const uint2 none = make_uint2(0xff800000u, 0u);
+  for (int r0 = warp * rpw; r0 < R; r0 += 2 * pass) {
+    uint2 v[2][2];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = r0 + q * kWarps;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int c = lane + 32 * t;
-        v[q][t] = (r < p.R && c < p.C) ? ldcg_u2(base + static_cast<long long>(r) * p.C + c)
-                                       : make_uint2(0xff800000u, 0u);
-      }
+    for (int q = 0; q < 2; ++q) {
+      const int r = r0 + q * pass + lane / L;
+      const uint2 *pr = base + static_cast<long long>(r) * C;
+      v[q][0] = (r < R && sub < C) ? ldcg_u2(pr + sub) : none;
+      v[q][1] = (r < R && sub + L < C) ? ldcg_u2(pr + sub + L) : none;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = r0 + q * kWarps;
-      if (r < p.R) {
-        const bool kp = keep && r == keep_row;
-        if (kp) {
-          if (lane < p.C) keep[lane] = v[q][0];
-          if (lane + 32 < p.C) keep[lane + 32] = v[q][1];
-        }
-        float m = -INFINITY, s = 0.f;
-        stat_merge(m, s, __uint_as_float(v[q][0].x), __uint_as_float(v[q][0].y), p.c2);
-        stat_merge(m, s, __uint_as_float(v[q][1].x), __uint_as_float(v[q][1].y), p.c2);
-        // partials beyond the first 64: four loads in flight per lane, merged in index order
-        const uint2 *pr = base + static_cast<long long>(r) * p.C;
-        for (int c0 = lane + 64; c0 < p.C; c0 += 128) {
-          uint2 w[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            w[t] = (c0 + 32 * t < p.C) ? ldcg_u2(pr + c0 + 32 * t) : make_uint2(0xff800000u, 0u);
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if (kp && c0 + 32 * t < p.C) keep[c0 + 32 * t] = w[t];
-            stat_merge(m, s, __uint_as_float(w[t].x), __uint_as_float(w[t].y), p.c2);
-          }
-        }
-        warp_stat_merge(m, s, p.c2);
-        if (lane == 0) { rowM[r] = m; rowZ[r] = s; }
+    for (int q = 0; q < 2; ++q) {
+      if (r0 + q * pass >= R) break;   // warp-uniform
+      const int r = r0 + q * pass + lane / L;
+      const bool kp = keep && r == keep_row;
+      if (kp) {
+        if (sub < C) keep[sub] = v[q][0];
+        if (sub + L < C) keep[sub + L] = v[q][1];
       }
+      float m = -INFINITY, s = 0.f;
+      stat_merge(m, s, __uint_as_float(v[q][0].x), __uint_as_float(v[q][0].y), p.c2);
+      stat_merge(m, s, __uint_as_float(v[q][1].x), __uint_as_float(v[q][1].y), p.c2);
+      const uint2 *pr = base + static_cast<long long>(r) * C;
+      for (int c0 = sub + 2 * L; c0 < C + sub; c0 += 4 * L) {   // C > 64 only (then L = 32)
+        uint2 w[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          w[t] = (r < R && c0 + t * L < C) ? ldcg_u2(pr + c0 + t * L) : none;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (kp && c0 + t * L < C) keep[c0 + t * L] = w[t];
+          stat_merge(m, s, __uint_as_float(w[t].x), __uint_as_float(w[t].y), p.c2);
+        }
+      }
+      for (int off = L >> 1; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+        stat_merge(m, s, m2, s2, p.c2);
+      }
+      if (r < R && sub == 0) { rowM[r] = m; rowZ[r] = s; }
     }
   }
 }
@@ -89,46 +103,44 @@ __device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float
 // usable (finite maximum, no NaN / +inf seen).
 __device__ __forceinline__ void combine_rows_arg(const Params &p, int b, int *g, int *ok) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint2 *base = p.ws_part + static_cast<long long>(b) * p.R * p.C;
-  for (int r0 = warp; r0 < p.R; r0 += 4 * kWarps) {
-    uint2 v[4][2];
+  const int R = p.R, C = p.C;
+  const int L = combine_lanes(C);
+  const int sub = lane & (L - 1), rpw = 32 / L, pass = kWarps * rpw;
+  const uint2 *base = p.ws_part + static_cast<long long>(b) * R * C;
+  const uint2 none = make_uint2(0xff800000u, 0x7fffffffu);
+  for (int r0 = warp * rpw; r0 < R; r0 += 2 * pass) {
+    uint2 v[2][2];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = r0 + q * kWarps;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int c = lane + 32 * t;
-        v[q][t] = (r < p.R && c < p.C) ? ldcg_u2(base + static_cast<long long>(r) * p.C + c)
-                                       : make_uint2(0xff800000u, 0x7fffffffu);
-      }
+    for (int q = 0; q < 2; ++q) {
+      const int r = r0 + q * pass + lane / L;
+      const uint2 *pr = base + static_cast<long long>(r) * C;
+      v[q][0] = (r < R && sub < C) ? ldcg_u2(pr + sub) : none;
+      v[q][1] = (r < R && sub + L < C) ? ldcg_u2(pr + sub + L) : none;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = r0 + q * kWarps;
-      if (r < p.R) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        arg_merge(bv, bi, __uint_as_float(v[q][0].x), static_cast<int>(v[q][0].y));
-        arg_merge(bv, bi, __uint_as_float(v[q][1].x), static_cast<int>(v[q][1].y));
-        const uint2 *pr = base + static_cast<long long>(r) * p.C;
-        for (int c0 = lane + 64; c0 < p.C; c0 += 128) {
-          uint2 w[4];
+    for (int q = 0; q < 2; ++q) {
+      if (r0 + q * pass >= R) break;   // warp-uniform
+      const int r = r0 + q * pass + lane / L;
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      arg_merge(bv, bi, __uint_as_float(v[q][0].x), static_cast<int>(v[q][0].y));
+      arg_merge(bv, bi, __uint_as_float(v[q][1].x), static_cast<int>(v[q][1].y));
+      const uint2 *pr = base + static_cast<long long>(r) * C;
+      for (int c0 = sub + 2 * L; c0 < C + sub; c0 += 4 * L) {   // C > 64 only (then L = 32)
+        uint2 w[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            w[t] = (c0 + 32 * t < p.C) ? ldcg_u2(pr + c0 + 32 * t)
-                                       : make_uint2(0xff800000u, 0x7fffffffu);
+        for (int t = 0; t < 4; ++t)
+          w[t] = (r < R && c0 + t * L < C) ? ldcg_u2(pr + c0 + t * L) : none;
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            arg_merge(bv, bi, __uint_as_float(w[t].x), static_cast<int>(w[t].y));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
-          const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
-          arg_merge(bv, bi, v2, i2);
-        }
-        if (lane == 0) { g[r] = bi; ok[r] = arg_ok(bv) ? 1 : 0; }
+        for (int t = 0; t < 4; ++t)
+          arg_merge(bv, bi, __uint_as_float(w[t].x), static_cast<int>(w[t].y));
       }
+      for (int off = L >> 1; off > 0; off >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int i2 = __shfl_xor_sync(0xffffffffu, bi, off);
+        arg_merge(bv, bi, v2, i2);
+      }
+      if (r < R && sub == 0) { g[r] = bi; ok[r] = arg_ok(bv) ? 1 : 0; }
     }
   }
 }
@@ -381,15 +393,19 @@ __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared
 
 // Greedy tree verification for trees of at most 64 nodes: all warps combine the argmax
 // partials into shared memory, then warp 0 holds nodes lane and lane + 32 in registers and does
-// the rest with warp votes and shuffles (no block barriers): the accepted set level by level
-// as a 64-bit mask, the deepest accepted node by a warp maximum, and the path by walking
-// parents back from it.
-// smem holds g[N] and the row-usable flags okf[N].
+// the rest without block barriers. Acceptance and depth come from pointer jumping: each node
+// keeps (ancestor, edges to it, all of those edges matched) and composes it with its ancestor's
+// triple, so a tree of depth D takes ceil(log2(D + 1)) rounds of shuffles. The deepest accepted
+// node is one warp maximum; the path is walked back through parents staged in shared memory,
+// one lane per depth.
+// smem holds g[N], the row-usable flags okf[N], then parents and tokens [N] each.
 __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int N = p.N;
   int *g = reinterpret_cast<int *>(smem);
   int *okf = g + N;
+  int *par_s = okf + N;
+  int *tok_s = par_s + N;
   const long long bN = static_cast<long long>(b) * N;
   int par0 = -1, par1 = -1, tok0 = 0, tok1 = 0;
   if (warp == 0) {   // issued before the partial loads, used after them
@@ -407,63 +423,68 @@ __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
   if (warp != 0) return;   // no block barrier follows
   const int j0 = lane, j1 = lane + 32;
   const bool in0 = j0 < N, in1 = j1 < N;
-  auto code = [&](int j, bool in, int par, int tok, int what) -> bool {
-    if (!in) return false;
-    if (what == 0) return okf[j] == 0;
-    if (what == 1) return j == 0 ? (par != -1) : (par < 0 || par >= j);
-    return j > 0 && (tok < 0 || tok >= p.V);
+  // the first failing check of a node: 1 its row is not usable, 2 a bad parent, 3 a bad token;
+  // the tree's error is the smallest over its nodes
+  auto check = [&](int j, bool in, int par, int tok) -> int {
+    if (!in) return 4;
+    if (okf[j] == 0) return 1;
+    if (j == 0 ? (par != -1) : (par < 0 || par >= j)) return 2;
+    if (j > 0 && (tok < 0 || tok >= p.V)) return 3;
+    return 4;
   };
-  int err = 0;
-  const int codes[3] = {SPEC_ERR_NONFINITE, SPEC_ERR_PARENT, SPEC_ERR_TOKEN};
-#pragma unroll
-  for (int w = 0; w < 3; ++w) {
-    const bool bad = code(j0, in0, par0, tok0, w) || code(j1, in1, par1, tok1, w);
-    if (!err && __any_sync(0xffffffffu, bad)) err = codes[w];
-  }
+  const int first = __reduce_min_sync(0xffffffffu, min(check(j0, in0, par0, tok0),
+                                                       check(j1, in1, par1, tok1)));
   int32_t *pn = p.path_nodes + bN;
   int32_t *ot = p.out_tokens + bN;
-  if (err) {
+  if (first < 4) {
     if (in0) { pn[j0] = -1; ot[j0] = -1; }
     if (in1) { pn[j1] = -1; ot[j1] = -1; }
-    if (lane == 0) { set_status(p.status, err); p.accept_len[b] = -1; }
+    if (lane == 0) {
+      set_status(p.status, first == 1 ? SPEC_ERR_NONFINITE
+                                      : (first == 2 ? SPEC_ERR_PARENT : SPEC_ERR_TOKEN));
+      p.accept_len[b] = -1;
+    }
     return;
   }
-  // level by level: a node is accepted at step d when its parent was accepted (at step d - 1)
-  // and its token is the parent's argmax, so the step at which it is accepted is its depth
-  // (parents precede children, so a node's parent is always settled first). The accepted set
-  // is one 64-bit mask, extended by two ballots per level.
-  const bool m0 = in0 && j0 > 0 && tok0 == g[par0];
-  const bool m1 = in1 && tok1 == g[par1];
-  unsigned long long accm = 1ull;   // the root
-  int dep0 = (in0 && j0 == 0) ? 0 : -1, dep1 = -1;
-  for (int level = 1; level < N; ++level) {
-    const bool a0 = m0 && dep0 < 0 && ((accm >> par0) & 1ull);
-    const bool a1 = m1 && dep1 < 0 && ((accm >> par1) & 1ull);
-    const unsigned lo = __ballot_sync(0xffffffffu, a0), hi = __ballot_sync(0xffffffffu, a1);
-    if ((lo | hi) == 0u) break;
-    if (a0) dep0 = level;
-    if (a1) dep1 = level;
-    accm |= static_cast<unsigned long long>(lo) | (static_cast<unsigned long long>(hi) << 32);
+  if (in0) { par_s[j0] = par0; tok_s[j0] = tok0; }
+  if (in1) { par_s[j1] = par1; tok_s[j1] = tok1; }
+  // node state: bits 0..6 ancestor + 1 (0: past the root), 7..13 edges to it, 14 all matched
+  auto pack = [](int anc, int dep, bool ok) -> int {
+    return (anc + 1) | (dep << 7) | (ok ? (1 << 14) : 0);
+  };
+  int s0 = pack(-1, 0, in0);   // the root (j0 == 0) is accepted at depth 0
+  if (in0 && j0 > 0) s0 = pack(par0, 1, tok0 == g[par0]);
+  int s1 = in1 ? pack(par1, 1, tok1 == g[par1]) : pack(-1, 0, false);
+  for (;;) {
+    const int a0 = (s0 & 127) - 1, a1 = (s1 & 127) - 1;
+    if (!__any_sync(0xffffffffu, a0 >= 0 || a1 >= 0)) break;
+    // every lane reads the old states of both ancestors before any state changes
+    const int x0 = __shfl_sync(0xffffffffu, s0, a0 & 31), y0 = __shfl_sync(0xffffffffu, s1, a0 & 31);
+    const int x1 = __shfl_sync(0xffffffffu, s0, a1 & 31), y1 = __shfl_sync(0xffffffffu, s1, a1 & 31);
+    const int t0 = (a0 >= 32) ? y0 : x0, t1 = (a1 >= 32) ? y1 : x1;
+    // compose: the ancestor's ancestor, the summed edge counts, both chains matched
+    // (depths add without carry: a tree of at most 64 nodes is at most 63 deep)
+    constexpr int kDep = 127 << 7;
+    if (a0 >= 0) s0 = (t0 & 127) | ((s0 & kDep) + (t0 & kDep)) | (s0 & t0 & (1 << 14));
+    if (a1 >= 0) s1 = (t1 & 127) | ((s1 & kDep) + (t1 & kDep)) | (s1 & t1 & (1 << 14));
   }
-  int key = -1;
-  if (dep0 >= 0) key = (dep0 << 11) | (2047 - j0);
-  if (dep1 >= 0) key = max(key, (dep1 << 11) | (2047 - j1));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, off));
-  const int best = 2047 - (key & 2047);
-  const int D = key >> 11;
+  // deepest accepted node, smallest index on equal depth (the root is always accepted)
+  auto key = [](int s, int j) -> unsigned {
+    return (s & (1 << 14)) ? ((static_cast<unsigned>((s >> 7) & 127) << 11) | (2047u - j)) + 1u
+                           : 0u;
+  };
+  const unsigned kmax = __reduce_max_sync(0xffffffffu, max(key(s0, j0), in1 ? key(s1, j1) : 0u));
+  const int best = 2047 - static_cast<int>((kmax - 1u) & 2047u);
+  const int D = static_cast<int>((kmax - 1u) >> 11);
   if (in0 && j0 > D) { pn[j0] = -1; ot[j0] = -1; }
   if (in1 && j1 > D) { pn[j1] = -1; ot[j1] = -1; }
-  int v = best;
-  for (int d = D; d >= 0; --d) {   // warp-uniform walk from the deepest node to the root
-    const int src = v & 31;
-    const int t0 = __shfl_sync(0xffffffffu, tok0, src), t1 = __shfl_sync(0xffffffffu, tok1, src);
-    const int q0 = __shfl_sync(0xffffffffu, par0, src), q1 = __shfl_sync(0xffffffffu, par1, src);
-    if (lane == 0) {
-      pn[d] = v;
-      if (d > 0) ot[d - 1] = (v >= 32) ? t1 : t0;
-    }
-    v = (v >= 32) ? q1 : q0;
+  __syncwarp();   // parents and tokens staged
+  // lane d writes the path node at depth d (and d + 32): D - d steps up from the deepest node
+  for (int d = lane; d <= D; d += 32) {
+    int v = best;
+    for (int k = d; k < D; ++k) v = par_s[v];
+    pn[d] = v;
+    if (d > 0) ot[d - 1] = tok_s[v];
   }
   if (lane == 0) {
     ot[D] = g[best];
