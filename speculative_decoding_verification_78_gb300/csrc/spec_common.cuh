@@ -129,6 +129,42 @@ __device__ __forceinline__ float ex2_shift(float x, float m, float c2) {
   return ex2(__fmul_rn(__fsub_rn(x, m), c2));
 }
 
+// ------------------------------------------------------------------ paired fp32 arithmetic
+//
+// Blackwell's f32x2 instructions apply one operation to two fp32 values held in a register
+// pair. Each half is rounded to nearest exactly like the scalar instruction, so paired code
+// gives the same bits as the scalar code it replaces, with half the arithmetic instructions.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void up2(f32x2 v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// ex2_shift of two values: 2^((x - m) * c2) for both halves of x (m2, c22: m and c2 twice)
+__device__ __forceinline__ f32x2 ex2_shift2(f32x2 x, f32x2 m2, f32x2 c22) {
+  float t0, t1;
+  up2(mul2(sub2(x, m2), c22), t0, t1);
+  return pk2(ex2(t0), ex2(t1));
+}
+
 __device__ __forceinline__ uint2 ldcg_u2(const uint2 *p) { return __ldcg(p); }
 __device__ __forceinline__ float ldcg_f(const float *p) { return __ldcg(p); }
 
@@ -285,12 +321,19 @@ __device__ __forceinline__ void unit_stats(const uint4 (&buf)[kVPL], float eh, f
   const float m = unit_lane_max<E>(buf, eh, et);
   float s = 0.f;
   if (m != -INFINITY) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // four running sums (element e goes to sum e mod 4), two per paired instruction
+    f32x2 a01 = pk2(0.f, 0.f), a23 = pk2(0.f, 0.f);
+    const f32x2 m2 = pk2(m, m), c22 = pk2(c2, c2);
 #pragma unroll
     for (int j = 0; j < kVPL; ++j)
 #pragma unroll
-      for (int e = 0; e < kEPV; ++e)
-        acc[e & 3] = __fadd_rn(acc[e & 3], ex2_shift(vec_elem<E>(buf[j], e), m, c2));
+      for (int e = 0; e < kEPV; e += 4) {
+        a01 = add2(a01, ex2_shift2(pk2(vec_elem<E>(buf[j], e), vec_elem<E>(buf[j], e + 1)), m2, c22));
+        a23 = add2(a23, ex2_shift2(pk2(vec_elem<E>(buf[j], e + 2), vec_elem<E>(buf[j], e + 3)), m2, c22));
+      }
+    float acc[4];
+    up2(a01, acc[0], acc[1]);
+    up2(a23, acc[2], acc[3]);
     s = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
     s = __fadd_rn(s, __fadd_rn(ex2_shift(eh, m, c2), ex2_shift(et, m, c2)));
   }

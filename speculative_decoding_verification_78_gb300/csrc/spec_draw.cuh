@@ -51,6 +51,36 @@ __device__ __forceinline__ float raw8_elem(const uint4 (&w)[2], int e) {
   else return vec_elem<float>(e < 4 ? w[0] : w[1], e & 3);
 }
 
+// The row constants of a draw, each twice, for the paired form of resid.
+struct ResidK {
+  f32x2 Mt, iZt, Md, iZd, c2;
+};
+__device__ __forceinline__ ResidK resid_k(float Mt, float iZt, float Md, float iZd, float c2) {
+  return ResidK{pk2(Mt, Mt), pk2(iZt, iZt), pk2(Md, Md), pk2(iZd, iZd), pk2(c2, c2)};
+}
+
+// resid of the 8 elements of one lane's slot (wq unused without Q), two elements per paired
+// instruction: the same operations and roundings as resid, hence the same values.
+template <typename E>
+__device__ __forceinline__ void resid8(const uint4 (&wp)[2], const uint4 (&wq)[2], bool hasq,
+                                       const ResidK &k, float (&r)[8]) {
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const f32x2 p =
+        mul2(ex2_shift2(pk2(raw8_elem<E>(wp, e), raw8_elem<E>(wp, e + 1)), k.Mt, k.c2), k.iZt);
+    if (!hasq) {
+      up2(p, r[e], r[e + 1]);
+      continue;
+    }
+    const f32x2 q =
+        mul2(ex2_shift2(pk2(raw8_elem<E>(wq, e), raw8_elem<E>(wq, e + 1)), k.Md, k.c2), k.iZd);
+    float d0, d1;
+    up2(sub2(p, q), d0, d1);
+    r[e] = fmaxf(d0, 0.f);
+    r[e + 1] = fmaxf(d1, 0.f);
+  }
+}
+
 // Segment sum over this lane's 8 elements of segment `seg` (sequential), and the 8 values.
 template <typename E>
 __device__ __forceinline__ float lane_resid(const E *P, const E *Q, int seg, int lane, int V,
@@ -60,13 +90,10 @@ __device__ __forceinline__ float lane_resid(const E *P, const E *Q, int seg, int
   uint4 wp[2], wq[2];
   load8_raw<E>(P, k0, V, vec_ok, wp);
   if (Q) load8_raw<E>(Q, k0, V, vec_ok, wq);
+  resid8<E>(wp, wq, Q != nullptr, resid_k(Mt, iZt, Md, iZd, c2), r);
   float ls = 0.f;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    r[e] = resid(raw8_elem<E>(wp, e), Q ? raw8_elem<E>(wq, e) : -INFINITY, Q != nullptr, Mt,
-                 iZt, Md, iZd, c2);
-    ls = __fadd_rn(ls, r[e]);
-  }
+  for (int e = 0; e < 8; ++e) ls = __fadd_rn(ls, r[e]);
   return ls;
 }
 
@@ -132,13 +159,14 @@ __device__ __noinline__ void segment_sums(const E *P, const E *Q, float Mt, floa
       load8_raw<E>(P, k0, V, vec_ok, wp[t]);
       if (Q) load8_raw<E>(Q, k0, V, vec_ok, wq[t]);
     }
+    const ResidK rk = resid_k(Mt, iZt, Md, iZd, c2);
 #pragma unroll
     for (int t = 0; t < kSegIter; ++t) {
+      float r[8];
+      resid8<E>(wp[t], wq[t], Q != nullptr, rk, r);
       float ls = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        ls = __fadd_rn(ls, resid(raw8_elem<E>(wp[t], e), Q ? raw8_elem<E>(wq[t], e) : -INFINITY,
-                                 Q != nullptr, Mt, iZt, Md, iZd, c2));
+      for (int e = 0; e < 8; ++e) ls = __fadd_rn(ls, r[e]);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xffffffffu, ls, off));
       if (lane == 0 && s0 + t < hi) out[s0 + t - out_base] = ls;
@@ -263,6 +291,7 @@ __device__ int draw_token_warp(const E *P, const E *Q, float Mt, float iZt, floa
                       (!Q || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);
   const int nseg = (V + kSeg - 1) / kSeg;
   const bool keep = nseg <= kRegSeg;
+  const ResidK rk = resid_k(Mt, iZt, Md, iZd, c2);
   float ss[kMaxSeg], lsv[kRegSeg], rr[kRegSeg][8];
 #pragma unroll
   for (int s0 = 0; s0 < kMaxSeg; s0 += kBatch) {
@@ -277,13 +306,13 @@ __device__ int draw_token_warp(const E *P, const E *Q, float Mt, float iZt, floa
 #pragma unroll
       for (int q = 0; q < kBatch; ++q) {
         const int sg = s0 + q;
+        float r8[8];
+        resid8<E>(wp[q], wq[q], Q != nullptr, rk, r8);
         float ls = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float r = resid(raw8_elem<E>(wp[q], e), Q ? raw8_elem<E>(wq[q], e) : -INFINITY,
-                                Q != nullptr, Mt, iZt, Md, iZd, c2);
-          ls = __fadd_rn(ls, r);
-          if (sg < kRegSeg) rr[sg < kRegSeg ? sg : 0][e] = r;
+          ls = __fadd_rn(ls, r8[e]);
+          if (sg < kRegSeg) rr[sg < kRegSeg ? sg : 0][e] = r8[e];
         }
         if (sg < kRegSeg) lsv[sg < kRegSeg ? sg : 0] = ls;
 #pragma unroll

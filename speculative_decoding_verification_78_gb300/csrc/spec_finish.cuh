@@ -633,17 +633,16 @@ __device__ __forceinline__ void cluster_draw_regs(const Params &p, int b, int n,
     load8_raw<E>(P, k0, V, vec_ok, wp[t]);
     if (Q) load8_raw<E>(Q, k0, V, vec_ok, wq[t]);
   }
-  auto rval = [&](int t, int e) -> float {
-    return resid(raw8_elem<E>(wp[t], e), Q ? raw8_elem<E>(wq[t], e) : -INFINITY, Q != nullptr,
-                 Mt, iZt, Md, iZd, c2);
-  };
+  const ResidK rk = resid_k(Mt, iZt, Md, iZd, c2);
   float lsum[kSI], ssum[kSI];
   float wtot = 0.f;
 #pragma unroll
   for (int t = 0; t < kSI; ++t) {
+    float r8[8];
+    resid8<E>(wp[t], wq[t], Q != nullptr, rk, r8);
     float ls = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ls = __fadd_rn(ls, rval(t, e));
+    for (int e = 0; e < 8; ++e) ls = __fadd_rn(ls, r8[e]);
     lsum[t] = ls;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xffffffffu, ls, off));
@@ -728,8 +727,7 @@ __device__ __forceinline__ void cluster_draw_regs(const Params &p, int b, int n,
 #pragma unroll
   for (int q = 0; q < kSI; ++q)
     if (q == seg) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) r[e] = rval(q, e);
+      resid8<E>(wp[q], wq[q], Q != nullptr, rk, r);
       ls = lsum[q];
     }
   int tok = segment_pick(r, ls, (s0 + seg) * kSeg + lane * 8, segbase, t, smode, lane);

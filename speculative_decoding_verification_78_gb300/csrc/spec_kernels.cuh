@@ -415,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
         for (int e = 0; e < 4; ++e) a = fmax_nan(a, el(i, e));
     }
     if (a != -INFINITY) {
+      // (scalar: the paired form of this pass measured slower here, unlike the write pass)
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < kQ; ++i)
@@ -492,15 +493,23 @@ __global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
   float *out = p.out_probs + static_cast<long long>(row_i) * V;
   float *oq = out + g.h;
   const bool vec_out = ((reinterpret_cast<uintptr_t>(oq) & 15u) == 0);
+  const f32x2 M2 = pk2(M, M), c22 = pk2(c2, c2), iZ2 = pk2(iZ, iZ);
+  // the four probabilities of group i: val() of each element, two per paired instruction
+  auto val4 = [&](int i, int k) -> float4 {
+    if (kGreedy || !ok)
+      return make_float4(val(el(i, 0), k), val(el(i, 1), k + 1), val(el(i, 2), k + 2),
+                         val(el(i, 3), k + 3));
+    float4 y;
+    up2(mul2(ex2_shift2(pk2(el(i, 0), el(i, 1)), M2, c22), iZ2), y.x, y.y);
+    up2(mul2(ex2_shift2(pk2(el(i, 2), el(i, 3)), M2, c22), iZ2), y.z, y.w);
+    return y;
+  };
 #pragma unroll
   for (int i = 0; i < kQ; ++i) {
     const int q = qb + tid + kThreads * i;
     if (q < qe) {
       const int k = g.h + 4 * q;
-      const float4 y = make_float4(val(el(i, 0), k),
-                                   val(el(i, 1), k + 1),
-                                   val(el(i, 2), k + 2),
-                                   val(el(i, 3), k + 3));
+      const float4 y = val4(i, k);
       if (vec_out) {
         __stcs(reinterpret_cast<float4 *>(oq + 4 * q), y);
       } else {
