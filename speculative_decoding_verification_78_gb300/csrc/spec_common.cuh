@@ -168,15 +168,12 @@ __device__ __forceinline__ f32x2 ex2_shift2(f32x2 x, f32x2 m2, f32x2 c22) {
 __device__ __forceinline__ uint2 ldcg_u2(const uint2 *p) { return __ldcg(p); }
 __device__ __forceinline__ float ldcg_f(const float *p) { return __ldcg(p); }
 
-// Cluster barrier whose arrival publishes this CTA's earlier shared-memory writes to the other
-// CTAs of the cluster (release / acquire), and one that only orders execution: after it no CTA
-// still needs a peer's shared memory, so a peer may leave or reuse it.
+// Cluster barrier whose arrival publishes this CTA's earlier writes, including its stores into
+// peers' shared memory, to every CTA of the cluster (release / acquire). The exchanges push:
+// each CTA stores its value into a slot of every peer before the barrier, so after it every
+// value is local and no CTA reads a peer's shared memory (a peer may then leave at once).
 __device__ __forceinline__ void cluster_sync_publish() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync_exec() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;"
                ::: "memory");
 }
 

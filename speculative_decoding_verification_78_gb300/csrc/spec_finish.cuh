@@ -606,13 +606,14 @@ __device__ void bonus_draw_units(const Params &p, int b, int n, float M, float Z
 
 // The cluster draw when every CTA's slice has at most kWarps * kRegSegs segments: warp w of
 // CTA `rank` loads segments rank*K + w*kRegSegs .. +kRegSegs - 1 (one round trip) and keeps
-// them in registers. Warp totals -> CTA total -> cluster prefix through distributed shared
-// memory; then the warp whose range holds u*S picks the token from its registers and writes
-// the outputs, with no second pass over the rows and no block barrier after the cluster's.
+// them in registers. Warp totals -> CTA total, pushed into every peer's shared memory before
+// one cluster barrier -> cluster prefix; then the warp whose range holds u*S picks the token
+// from its registers and writes the outputs, with no second pass over the rows and no block
+// barrier after the cluster's.
 template <typename E>
 __device__ __forceinline__ void cluster_draw_regs(const Params &p, int b, int n, const E *P, const E *Q, float Mt,
                                   float iZt, float Md, float iZd, float u, const int *xs, int K,
-                                  float *segsum, TailShared &sh, float &s_total) {
+                                  float *segsum, TailShared &sh, float *s_tot) {
   namespace cg = cooperative_groups;
   constexpr int kSI = kRegSegs;
   cg::cluster_group cl = cg::this_cluster();
@@ -663,16 +664,17 @@ __device__ __forceinline__ void cluster_draw_regs(const Params &p, int b, int n,
   const float wexc = __shfl_up_sync(0xffffffffu, winc, 1);
   const float woff = (warp == 0) ? 0.f : __shfl_sync(0xffffffffu, wexc, warp);
   const float ctot = __shfl_sync(0xffffffffu, winc, kWarps - 1);
-  if (threadIdx.x == 0) s_total = ctot;
-  cluster_sync_publish();   // every slice total written
+  // push this CTA's slice total into slot `rank` of every CTA of the cluster, then one barrier:
+  // afterwards every total is local, and no CTA touches a peer's shared memory again
+  if (warp == 0 && lane < S) *cl.map_shared_rank(&s_tot[rank], lane) = ctot;
+  cluster_sync_publish();
   // every warp: the cluster prefix (lane r holds rank r's inclusive prefix)
-  float pre = (lane < S) ? *cl.map_shared_rank(&s_total, lane) : 0.f;
+  float pre = (lane < S) ? s_tot[lane] : 0.f;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const float y = __shfl_up_sync(0xffffffffu, pre, off);
     if (lane >= off) pre = __fadd_rn(pre, y);
   }
-  cluster_sync_exec();   // every CTA has read its peers' totals
   const float Sall = __shfl_sync(0xffffffffu, pre, S - 1);
   if (Q && Sall == 0.f) {
     // the residual vanished: draw from p_n alone, on the first CTA of the cluster
@@ -737,13 +739,13 @@ __device__ __forceinline__ void cluster_draw_regs(const Params &p, int b, int n,
 
 // The correction / bonus draw of chain sampling over a thread-block cluster of S CTAs (S = 1:
 // no cluster), after acceptance gave n: CTA `rank` sums r(k) = max(0, p_n(k) - q_n(k)) (or
-// p_gamma(k)) over its slice of 256-element segments into segsum (shared memory); the slice
-// totals are exchanged through distributed shared memory between two cluster barriers; the CTA
+// p_gamma(k)) over its slice of 256-element segments into segsum (shared memory); each CTA
+// pushes its slice total into every peer's shared memory before one cluster barrier; the CTA
 // whose slice holds u * S picks the token and writes the outputs. Every CTA of the cluster calls
 // it; CTAs other than the writer return from it early.
 template <typename E>
 __device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, const float *rowZ,
-                             const int *xs, float *segsum, TailShared &sh, float &s_total,
+                             const int *xs, float *segsum, TailShared &sh, float *s_tot,
                              float *s_pre) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
@@ -758,7 +760,7 @@ __device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, c
   const int nseg = (p.V + kSeg - 1) / kSeg;
   const int K = (nseg + S - 1) / S;
   if (K <= kWarps * kRegSegs) {   // the same on every CTA of the cluster
-    cluster_draw_regs<E>(p, b, n, P, Q, Mt, iZt, Md, iZd, u, xs, K, segsum, sh, s_total);
+    cluster_draw_regs<E>(p, b, n, P, Q, Mt, iZt, Md, iZd, u, xs, K, segsum, sh, s_tot);
     return;
   }
   const int lo = min(nseg, rank * K), hi = min(nseg, lo + K), nl = hi - lo;
@@ -769,12 +771,12 @@ __device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, c
     for (int j = threadIdx.x; j < nl; j += 32) tot = __fadd_rn(tot, segsum[j]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) tot = __fadd_rn(tot, __shfl_xor_sync(0xffffffffu, tot, off));
-    if (threadIdx.x == 0) s_total = tot;
+    if (threadIdx.x < S) *cl.map_shared_rank(&s_tot[rank], threadIdx.x) = tot;
   }
-  cl.sync();   // every slice total written
-  if (threadIdx.x < 32) {   // lane r reads rank r's total; inclusive scan in rank order
+  cluster_sync_publish();   // every slice total pushed to every CTA
+  if (threadIdx.x < 32) {   // lane r holds rank r's total; inclusive scan in rank order
     const int r = threadIdx.x;
-    float v = (r < S) ? *cl.map_shared_rank(&s_total, r) : 0.f;
+    float v = (r < S) ? s_tot[r] : 0.f;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float y = __shfl_up_sync(0xffffffffu, v, off);
@@ -783,7 +785,7 @@ __device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, c
     if (r < S) s_pre[r + 1] = v;
     if (r == 0) s_pre[0] = 0.f;
   }
-  cl.sync();   // every CTA has read its peers' totals; shared memory is private again
+  __syncthreads();   // local only: no CTA reads a peer's shared memory after the barrier
   const float Sall = s_pre[S];
   int tok = -1;
   if (Q && Sall == 0.f) {

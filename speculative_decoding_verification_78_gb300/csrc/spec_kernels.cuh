@@ -93,8 +93,8 @@ __device__ __forceinline__ void wait_stream_kernel() {
 // cluster size, blockIdx.x = b * S + rank). Every CTA of the cluster combines the row's
 // partials and decides acceptance (cheap, redundant); CTA `rank` then sums the residual (or
 // bonus) weights over its slice of the vocabulary into shared memory. The slice totals are
-// exchanged through distributed shared memory after a cluster barrier; the CTA whose slice
-// holds the crossing draws the token from its own segment sums and writes the outputs.
+// pushed into every CTA's shared memory before one cluster barrier; the CTA whose slice holds
+// the crossing draws the token from its own segment sums and writes the outputs.
 template <typename E>
 __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   namespace cg = cooperative_groups;
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   float *segsum = reinterpret_cast<float *>(bonus_part + p.C);
   __shared__ TailShared sh;
   __shared__ int xs[SPEC_MAX_GAMMA];
-  __shared__ float s_total;
+  __shared__ float s_tot[kMaxCluster];   // slice totals pushed by every CTA of the cluster
   __shared__ float s_pre[kMaxCluster + 1];
   cg::cluster_group cl = cg::this_cluster();
   const int S = static_cast<int>(cl.num_blocks());
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
       return;
     }
   }
-  cluster_draw<E>(p, b, n, rowM, rowZ, xs, segsum, sh, s_total, s_pre);
+  cluster_draw<E>(p, b, n, rowM, rowZ, xs, segsum, sh, s_tot, s_pre);
 }
 
 // Finishing kernel for chain sampling when every row is a single unit (gamma <= 31, V <=
@@ -314,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
   constexpr int kQ = kResQuads<E>;
   __shared__ float red_a[kWarps];
   __shared__ int red_i[kWarps];
-  __shared__ float part_a, part_b;
-  __shared__ int part_i;
+  __shared__ float in_a[kMaxCluster];   // the CTA partials of the cluster, pushed by each CTA
+  __shared__ int in_b[kMaxCluster];
   cg::cluster_group cl = cg::this_cluster();
   const int S = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
@@ -443,23 +443,29 @@ __global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
         const int i2 = __shfl_xor_sync(0xffffffffu, w, off);
         arg_merge(v, w, v2, i2);
       }
-      if (lane == 0) { part_a = v; part_i = w; }
+      if (S == 1 && lane == 0) { red_a[0] = v; red_i[0] = w; }
+      // push this CTA's partial (the same on every lane after the butterfly) into slot
+      // `rank` of every CTA of the cluster
+      if (S > 1 && lane < S) {
+        *cl.map_shared_rank(&in_a[rank], lane) = v;
+        *cl.map_shared_rank(&in_b[rank], lane) = w;
+      }
     } else {
       float z = __int_as_float(w);
       warp_stat_merge(v, z, c2);
-      if (lane == 0) { part_a = v; part_b = z; }
+      if (S == 1 && lane == 0) { red_a[0] = v; red_i[0] = __float_as_int(z); }
+      if (S > 1 && lane < S) {
+        *cl.map_shared_rank(&in_a[rank], lane) = v;
+        *cl.map_shared_rank(&in_b[rank], lane) = __float_as_int(z);
+      }
     }
   }
   if (S > 1) {
-    cl.sync();   // every CTA's partial written
+    // one barrier: afterwards every partial is local and no CTA touches a peer's memory again
+    cluster_sync_publish();
     if (warp == 0) {
-      float v = -INFINITY, z = 0.f;
-      int w = 0x7fffffff;
-      if (lane < S) {
-        v = *cl.map_shared_rank(&part_a, lane);
-        if constexpr (kGreedy) w = *cl.map_shared_rank(&part_i, lane);
-        else z = *cl.map_shared_rank(&part_b, lane);
-      }
+      float v = (lane < S) ? in_a[lane] : -INFINITY;
+      int w = (lane < S) ? in_b[lane] : (kGreedy ? 0x7fffffff : 0);
       if constexpr (kGreedy) {
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -467,16 +473,13 @@ __global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
           const int i2 = __shfl_xor_sync(0xffffffffu, w, off);
           arg_merge(v, w, v2, i2);
         }
+        if (lane == 0) { red_a[0] = v; red_i[0] = w; }
       } else {
+        float z = __int_as_float(w);
         warp_stat_merge(v, z, c2);
+        if (lane == 0) { red_a[0] = v; red_i[0] = __float_as_int(z); }
       }
-      __syncwarp();
-      if (lane == 0) { red_a[0] = v; red_i[0] = kGreedy ? w : __float_as_int(z); }
     }
-    cl.sync();   // every CTA has read its peers' partials
-  } else {
-    __syncthreads();
-    if (tid == 0) { red_a[0] = part_a; red_i[0] = kGreedy ? part_i : __float_as_int(part_b); }
   }
   __syncthreads();
   const float M = red_a[0];
