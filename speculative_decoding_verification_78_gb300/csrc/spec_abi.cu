@@ -96,7 +96,7 @@ FinishPlan chain_sample_plan(const Params &p) {
   if (p.C == 1 && p.V <= kWarpTailMaxV && p.gamma <= 31) {
     f.warp_tail = true;
     f.cluster = 1;
-    f.grid = (p.B + kWarps - 1) / kWarps;
+    f.grid = (p.B + kTailWarpsPerCta - 1) / kTailWarpsPerCta;
     f.smem = 0;
     return f;
   }

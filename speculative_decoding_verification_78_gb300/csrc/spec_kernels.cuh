@@ -137,13 +137,14 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
 
 // Finishing kernel for chain sampling when every row is a single unit (gamma <= 31, V <=
 // kWarpTailMaxV): one warp per batch row; lane i holds rows i and i + 32 and the draft-token
-// logits of position i. One CTA per SM at most is plenty (B / 16 CTAs), so each thread may use
-// up to 128 registers and the draw keeps the residual of the rows in registers.
+// logits of position i. Launched with small CTAs (any number of warps each) so that the batch
+// rows spread over every SM; each thread may use up to 128 registers, and the draw keeps the
+// residual of the rows in registers.
 template <typename E>
 __global__ void __launch_bounds__(kThreads, 1) finish_chain_sample_warp(Params p) {
   wait_stream_kernel();
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int b = blockIdx.x * static_cast<int>(blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= p.B) return;
   const int R = p.R, gamma = p.gamma;
   const uint2 *part = p.ws_part + static_cast<long long>(b) * R;   // C == 1

@@ -10,7 +10,8 @@ cudaError_t chain_sample(const Params &p, int grid, const FinishPlan &f, cudaStr
   cudaError_t e = launch_stream<E, kChainSample>(p, grid, stream);
   if (e != cudaSuccess) return e;
   if (f.warp_tail)
-    return launch_dependent(finish_chain_sample_warp<E>, p, f.grid, 1, 0, stream);
+    return launch_dependent(finish_chain_sample_warp<E>, p, f.grid, 1, 0, stream,
+                            32 * kTailWarpsPerCta);
   return launch_dependent(finish_chain_sample<E>, p, f.grid, f.cluster, f.smem, stream);
 }
 

@@ -13,6 +13,10 @@
 namespace specv {
 
 // Launch shape of the finishing kernel chosen on the host.
+// Warps per CTA of the one-warp-per-batch-row chain finisher: small CTAs spread the batch rows
+// over every SM, so fewer warps share each scheduler.
+constexpr int kTailWarpsPerCta = 4;
+
 struct FinishPlan {
   int grid;        // CTAs
   int cluster;     // CTAs per cluster (1 = no cluster)
@@ -23,10 +27,10 @@ struct FinishPlan {
 
 template <typename Kernel>
 inline cudaError_t launch_dependent(Kernel kernel, const Params &p, int grid, int cluster,
-                                    size_t smem, cudaStream_t stream) {
+                                    size_t smem, cudaStream_t stream, int threads = kThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
