@@ -91,13 +91,24 @@ int grid_for(const Params &p) {
 // Otherwise one cluster of S CTAs per batch row: S is the largest power of two (at most 8) for
 // which all B*S CTAs are resident at once (two per SM) and every CTA gets at least 8 residual
 // segments.
-FinishPlan chain_sample_plan(const Params &p) {
+FinishPlan chain_sample_plan(const Params &p, int dtype) {
   FinishPlan f{};
   if (p.C == 1 && p.V <= kWarpTailMaxV && p.gamma <= 31) {
     f.warp_tail = true;
     f.cluster = 1;
     f.grid = (p.B + kTailWarpsPerCta - 1) / kTailWarpsPerCta;
     f.smem = 0;
+    return f;
+  }
+  // Sampling (no drafts) with every row on a 16-byte boundary: the draw needs only the row's
+  // unit partials and one unit, which one warp does (its C partials staged in shared memory).
+  const bool rows_aligned = (reinterpret_cast<uintptr_t>(p.tgt) & 15u) == 0 &&
+                            (static_cast<long long>(p.V) * elem_size(dtype)) % 16 == 0;
+  if (p.gamma == 0 && rows_aligned) {
+    f.sample_warp = true;
+    f.cluster = 1;
+    f.grid = (p.B + kTailWarpsPerCta - 1) / kTailWarpsPerCta;
+    f.smem = sizeof(uint2) * static_cast<size_t>(kTailWarpsPerCta) * static_cast<size_t>(p.C);
     return f;
   }
   const int nseg = (p.V + kSeg - 1) / kSeg;
@@ -167,9 +178,9 @@ void probs_shape(Params &p, int rows, int V, float T) {
 }
 
 // The launch plan of each kind of call (after plan_units).
-FinishPlan chain_finish(const Params &p, bool greedy) {
+FinishPlan chain_finish(const Params &p, bool greedy, int dtype) {
   return greedy ? cta_plan(p.B, sizeof(int) * (2 * static_cast<size_t>(p.R) + p.gamma))
-                : chain_sample_plan(p);
+                : chain_sample_plan(p, dtype);
 }
 
 FinishPlan tree_finish(const Params &p) {
@@ -245,7 +256,7 @@ int spec_verify_chain(const void *target_logits, const void *draft_logits, int d
   p.status = status;
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const FinishPlan f = chain_finish(p, greedy);
+  const FinishPlan f = chain_finish(p, greedy, dtype);
   const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
                                      f, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
@@ -329,7 +340,7 @@ int spec_sample(const void *logits, int dtype, int rows, int V, float temperatur
   p.status = status;
   const int rc = plan(p, dtype, workspace, workspace_bytes);
   if (rc != SPEC_OK) return rc;
-  const FinishPlan f = chain_finish(p, greedy);
+  const FinishPlan f = chain_finish(p, greedy, dtype);
   const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
                                      f, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
@@ -395,7 +406,7 @@ int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float t
     chain_shape(p, B, (rows_per_b - 1) / 2, V, temperature);
     const int rc = plan_units(p, dtype);
     if (rc != SPEC_OK) return rc;
-    f = chain_finish(p, temperature == 0.f);
+    f = chain_finish(p, temperature == 0.f, dtype);
   } else if (kind == SPEC_CALL_TREE) {
     if (rows_per_b > SPEC_MAX_NODES) return SPEC_ERR_SHAPE;
     tree_shape(p, B, rows_per_b, V);

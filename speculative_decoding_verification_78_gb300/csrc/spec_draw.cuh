@@ -277,7 +277,7 @@ __device__ __noinline__ int draw_token_cta(const E *P, const E *Q, float Mt, flo
 }
 
 // Warp-wide draw for rows of at most kWarpTailMaxV elements (<= 8 segments). The loads of
-// several segments are issued together (four at a time for bf16, two for fp32); for rows of at
+// several segments are issued together (four at a time); for rows of at
 // most four segments the residual values stay in registers, so the crossing element is found
 // without reading the rows again.
 template <typename E>
@@ -285,7 +285,7 @@ __device__ int draw_token_warp(const E *P, const E *Q, float Mt, float iZt, floa
                                float c2, int V, float u) {
   constexpr int kMaxSeg = kWarpTailMaxV / kSeg;
   constexpr int kRegSeg = 4;                          // segments kept in registers
-  constexpr int kBatch = (sizeof(E) == 2) ? 4 : 2;    // segments whose loads fly together
+  constexpr int kBatch = 4;                           // segments whose loads fly together
   const int lane = threadIdx.x & 31;
   const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) & 15u) == 0) &&
                       (!Q || (reinterpret_cast<uintptr_t>(Q) & 15u) == 0);

@@ -135,6 +135,47 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   cluster_draw<E>(p, b, n, rowM, rowZ, xs, segsum, sh, s_tot, s_pre);
 }
 
+// Finishing kernel for sampling (gamma = 0, so every row's draw is the bonus draw from p_0) when
+// every row starts and ends on a 16-byte boundary: one warp per row, in CTAs of any number of
+// warps. The warp combines the row's C unit partials (staging them in shared memory), then
+// bonus_draw_units finds the unit where the running mass crosses u * S from those partials and
+// the element inside it from one 4 KB read of the row: no pass over the row.
+template <typename E>
+__global__ void __launch_bounds__(kThreads, 1) finish_sample_warp(Params p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  wait_stream_kernel();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int b = blockIdx.x * static_cast<int>(blockDim.x >> 5) + w;
+  if (b >= p.B) return;
+  const int C = p.C;
+  uint2 *part = reinterpret_cast<uint2 *>(smem_raw) + static_cast<long long>(w) * C;
+  const uint2 *src = p.ws_part + static_cast<long long>(b) * C;   // one row per batch row
+  const uint2 none = make_uint2(0xff800000u, 0u);
+  float m = -INFINITY, s = 0.f;
+  for (int c0 = 0; c0 < C; c0 += 128) {   // four loads in flight per lane, merged in order
+    uint2 v[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int c = c0 + lane + 32 * t;
+      v[t] = (c < C) ? ldcg_u2(src + c) : none;
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int c = c0 + lane + 32 * t;
+      if (c < C) part[c] = v[t];
+      stat_merge(m, s, __uint_as_float(v[t].x), __uint_as_float(v[t].y), p.c2);
+    }
+  }
+  warp_stat_merge(m, s, p.c2);
+  if (!stats_ok(m, s)) {
+    if (lane == 0) set_status(p.status, SPEC_ERR_NONFINITE);
+    fail_chain_row(p, b, lane, 32);
+    return;
+  }
+  __syncwarp();   // the partials staged by every lane
+  bonus_draw_units<E>(p, b, 0, m, s, part, nullptr);
+}
+
 // Finishing kernel for chain sampling when every row is a single unit (gamma <= 31, V <=
 // kWarpTailMaxV): one warp per batch row; lane i holds rows i and i + 32 and the draft-token
 // logits of position i. Launched with small CTAs (any number of warps each) so that the batch

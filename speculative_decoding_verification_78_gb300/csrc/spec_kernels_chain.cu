@@ -12,6 +12,9 @@ cudaError_t chain_sample(const Params &p, int grid, const FinishPlan &f, cudaStr
   if (f.warp_tail)
     return launch_dependent(finish_chain_sample_warp<E>, p, f.grid, 1, 0, stream,
                             32 * kTailWarpsPerCta);
+  if (f.sample_warp)
+    return launch_dependent(finish_sample_warp<E>, p, f.grid, 1, f.smem, stream,
+                            32 * kTailWarpsPerCta);
   return launch_dependent(finish_chain_sample<E>, p, f.grid, f.cluster, f.smem, stream);
 }
 

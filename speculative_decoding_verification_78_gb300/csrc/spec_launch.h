@@ -22,6 +22,7 @@ struct FinishPlan {
   int cluster;     // CTAs per cluster (1 = no cluster)
   size_t smem;     // dynamic shared memory per CTA
   bool warp_tail;  // chain sampling with single-unit rows: one warp per batch row
+  bool sample_warp;  // sampling (gamma = 0) with 16-byte aligned rows: one warp per row
   bool resident;   // one kernel holds every row in registers (no stream kernel)
 };
 

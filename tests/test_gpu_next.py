@@ -63,6 +63,28 @@ def test_sample_invalid_rows(orc):
 
 
 @pytest.mark.parametrize("dtype", [F32, BF16])
+def test_sample_invalid_rows_multi_unit(orc, dtype):
+    """Rows of several units on 16-byte boundaries (the one-warp-per-row sampling finisher):
+    a NaN, an all -inf and a +inf row are flagged, the other rows still sampled."""
+    import speculative_decoding_verification_78_gb300 as sv
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((6, 40000)) * 3).astype(np.float32)
+    x[1, 17] = np.nan
+    x[3, :] = -np.inf
+    x[4, 39999] = np.inf
+    lg = f32_to_bf16(x) if dtype == BF16 else x
+    u = make_uniforms(rng, (6,))
+    want, mg, _ = orc.sample(lg, dtype, u, 1.0)
+    tok, st = sv.sample(dev(lg), 1.0, dev(u))
+    tok = tok.cpu().numpy()
+    assert int(st.item()) == sv.SPEC_ERR_NONFINITE
+    assert list(tok[[1, 3, 4]]) == [-1, -1, -1]
+    good = np.array([0, 2, 5])
+    close = mg[good] < MARGIN
+    np.testing.assert_array_equal(tok[good][~close], want[good][~close])
+
+
+@pytest.mark.parametrize("dtype", [F32, BF16])
 @pytest.mark.parametrize("V,k", [(16, 16), (1001, 3), (32000, 8), (152064, 16), (5, 1),
                                  (40000, 5)])
 def test_topk(orc, dtype, V, k):
