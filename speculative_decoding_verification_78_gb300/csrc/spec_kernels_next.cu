@@ -19,11 +19,13 @@ cudaError_t allow_smem(Kernel kernel, size_t bytes, std::atomic<bool> &done) {
   return e;
 }
 
+// the merge runs in CTAs of a few warps, so that the rows spread over every SM
 template <typename E, int kK>
 cudaError_t topk_k(const Params &p, int grid, cudaStream_t stream) {
   const cudaError_t e = launch_dependent(topk_stream_kernel<E, kK>, p, grid, 1, 0, stream);
   if (e != cudaSuccess) return e;
-  return launch_dependent(topk_finish<kK>, p, (p.B + kWarps - 1) / kWarps, 1, 0, stream);
+  return launch_dependent(topk_finish<kK>, p, (p.B + kTailWarpsPerCta - 1) / kTailWarpsPerCta, 1,
+                          0, stream, 32 * kTailWarpsPerCta);
 }
 
 template <typename E>
