@@ -145,6 +145,34 @@ def test_probs(orc, dtype, V, T):
         assert err <= 2e-6     # what the kernel actually reaches (fp32 arithmetic)
 
 
+@pytest.mark.parametrize("dtype,V,rows", [(BF16, 32000, 700), (F32, 70001, 130), (F32, 3000, 1000)])
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_probs_more_rows_than_resident(orc, dtype, V, rows, T):
+    """More rows (or clusters) than the GPU holds at once at two CTAs per SM, so the launch runs
+    in several waves. Rows 0 and 600 / 30 / 900 are invalid (NaN, all -inf): a flagged row in
+    the first and in a later wave; unaligned rows (offset 1) exercise the head and tail
+    elements."""
+    import speculative_decoding_verification_78_gb300 as sv
+    _, grid, cluster = sv.spec_launch_shape(sv.SPEC_CALL_PROBS, rows, 1, V, dtype, T)
+    assert grid == rows * cluster
+    rng = np.random.default_rng(V + rows)
+    x = (rng.standard_normal((rows, V)) * 3).astype(np.float32)
+    x[::3, ::11] = -np.inf
+    bad = (0, rows - 100)
+    x[bad[0], 5] = np.nan
+    x[bad[1], :] = -np.inf
+    lg = f32_to_bf16(x) if dtype == BF16 else x
+    po, _ = orc.probs(lg, dtype, T)
+    good = np.setdiff1d(np.arange(rows), bad)
+    for off in (0, 1):
+        pr, st = sv.probs(dev(lg, off), T)
+        pr = pr.cpu().numpy()
+        assert int(st.item()) == sv.SPEC_ERR_NONFINITE
+        assert np.all(np.isnan(pr[list(bad)]))
+        err = np.abs(pr[good].astype(np.float64) - po[good]).max()
+        assert err <= 2e-6, err
+
+
 @pytest.mark.parametrize("V", [300, 40000, 200000])
 @pytest.mark.parametrize("T", [1.0, 0.0])
 def test_probs_invalid_rows(V, T):
