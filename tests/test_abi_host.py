@@ -170,3 +170,9 @@ def test_launch_shape_host_validation(lib):
     assert lib.spec_launch_shape(sv.SPEC_CALL_PROBS, 4, 1, 200000, sv.SPEC_F32, 1.0, *ref) == 0
     assert k.value == 2                                  # too long: stream kernel + write pass
     assert lib.spec_launch_shape(9, 4, 1, 1000, sv.SPEC_F32, 1.0, *ref) == sv.SPEC_ERR_SHAPE
+    # sampling (a chain without drafts) over multi-unit rows: one warp per row, four per CTA
+    assert lib.spec_launch_shape(sv.SPEC_CALL_CHAIN, 37, 1, 32000, sv.SPEC_BF16, 1.0, *ref) == 0
+    assert (k.value, g.value, c.value) == (2, 10, 1)
+    # single-unit rows: the one-warp chain finisher, four warps per CTA
+    assert lib.spec_launch_shape(sv.SPEC_CALL_CHAIN, 37, 9, 1000, sv.SPEC_F32, 1.0, *ref) == 0
+    assert (k.value, g.value, c.value) == (2, 10, 1)
