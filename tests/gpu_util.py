@@ -78,13 +78,13 @@ def compare_chain(orc, ci, gpu, rows=None):
 
 
 def report(name, **kw):
-    """Appends one line per comparison to gpurun_out/parity_report.jsonl when that folder
-    exists (the counts of near-boundary draws are part of the result)."""
+    """Appends one JSON line per comparison to the file named by SPEC_PARITY_REPORT, when that
+    variable is set (the counts of near-boundary draws are part of the result)."""
     import json
     import os
-    d = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
-    if os.path.isdir(d):
-        with open(os.path.join(d, "parity_report.jsonl"), "a") as f:
+    path = os.environ.get("SPEC_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
             f.write(json.dumps(dict(name=name, **kw)) + "\n")
 
 
