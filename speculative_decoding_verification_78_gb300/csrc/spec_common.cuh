@@ -113,6 +113,18 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Order-preserving map of fp32 values to unsigned integers (negative bit patterns reversed, the
+// sign bit set on the others): a < b as floats iff key(a) < key(b), -0 just below +0, and every
+// NaN, whatever its sign bit, the largest key (above +inf). key_float undoes it (NaN comes back
+// as 0x7fffffff).
+__device__ __forceinline__ unsigned float_key(float f) {
+  const unsigned b = __float_as_uint(f);
+  const unsigned k = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (f != f) ? 0xffffffffu : k;
+}
+__device__ __forceinline__ float key_float(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float y;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
@@ -377,9 +389,9 @@ __device__ __forceinline__ void unit_argmax(const uint4 (&buf)[kVPL], float eh, 
   float lm = fmax_nan(eh, et);
 #pragma unroll
   for (int j = 0; j < kVPL; ++j) lm = fmax_nan(lm, vm[j]);
-  float wm = lm;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) wm = fmax_nan(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+  // the warp maximum as one redux.sync over an order-preserving integer image of the floats, in
+  // which NaN ranks above +inf, so that it still poisons the unit
+  float wm = key_float(__reduce_max_sync(0xffffffffu, float_key(lm)));
   int idx = 0x7fffffff;
   if (wm != wm || wm == INFINITY) {
     wm = __int_as_float(0x7fc00000);
@@ -407,8 +419,7 @@ __device__ __forceinline__ void unit_argmax(const uint4 (&buf)[kVPL], float eh, 
         }
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, off));
+    idx = __reduce_min_sync(0xffffffffu, idx);
   }
   v_out = wm;
   i_out = idx;

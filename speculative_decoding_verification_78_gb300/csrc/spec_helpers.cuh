@@ -40,19 +40,17 @@ __device__ __forceinline__ void topk_insert(float (&lv)[kK], int (&li)[kK], floa
 }
 
 // k rounds of a warp maximum over the lanes' sorted lists: round r's winner goes to
-// (out_v[r], out_i[r]) on lane 0. Lists are consumed.
+// (out_v[r], out_i[r]) on lane 0. Lists are consumed. Each round is two redux.sync: the largest
+// value (through its order-preserving integer image, -0 folded into +0 so that equal values tie;
+// the lists hold no NaN), then the smallest index among the lanes holding it.
 template <int kK>
 __device__ __forceinline__ void warp_take_topk(float (&lv)[kK], int (&li)[kK], int k, int lane,
                                                uint2 *out) {
   for (int r = 0; r < k; ++r) {
-    float v = lv[0];
-    int i = li[0];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
-      const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
-      if (ranks_before(v2, i2, v, i)) { v = v2; i = i2; }
-    }
+    const unsigned key = float_key(__fadd_rn(lv[0], 0.f));
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
+    const int i = __reduce_min_sync(0xffffffffu, key == kmax ? li[0] : 0x7fffffff);
+    const float v = key_float(kmax);
     if (li[0] == i) {   // indices are unique: exactly the winning lane pops its head
 #pragma unroll
       for (int j = 0; j < kK - 1; ++j) { lv[j] = lv[j + 1]; li[j] = li[j + 1]; }
@@ -81,13 +79,35 @@ __global__ void __launch_bounds__(kThreads, 1) topk_stream_kernel(Params p) {
   const int W = gridDim.x * kWarps;
   const int k = p.topk;
   uint2 *cand = cbuf[warp];
+  // Short lists (k <= 4) leave room for a second unit's registers: the next unit's loads are
+  // issued before this unit is ranked, so two units per warp are in flight.
+  constexpr bool kAhead = kK <= 4;
+  auto fetch = [&](int un, uint4 (&b)[kVPL], float &h, float &t) {
+    const UnitId uu = unit_id(p, un);
+    const E *rr = static_cast<const E *>(p.tgt) + static_cast<long long>(uu.b) * p.V;
+    load_unit<E>(rr, row_geom<E>(rr, p.V), uu.chunk, lane, b, h, t);
+  };
+  uint4 nbuf[kAhead ? kVPL : 1];
+  float neh = -INFINITY, net = -INFINITY;
+  if constexpr (kAhead) {
+    const int first = blockIdx.x * kWarps + warp;
+    if (first < p.units) fetch(first, nbuf, neh, net);
+  }
   for (int unit = blockIdx.x * kWarps + warp; unit < p.units; unit += W) {
     const UnitId u = unit_id(p, unit);
     const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(u.b) * p.V;
     const RowGeom g = row_geom<E>(row, p.V);
     uint4 buf[kVPL];
     float eh, et;
-    load_unit<E>(row, g, u.chunk, lane, buf, eh, et);
+    if constexpr (kAhead) {
+#pragma unroll
+      for (int j = 0; j < kVPL; ++j) buf[j] = nbuf[j];
+      eh = neh;
+      et = net;
+      if (unit + W < p.units) fetch(unit + W, nbuf, neh, net);
+    } else {
+      load_unit<E>(row, g, u.chunk, lane, buf, eh, et);
+    }
     const bool has_h = u.chunk == 0 && lane < g.h, has_t = u.chunk == 0 && lane < g.tl;
     const int v0 = u.chunk * kUnitVecs + lane;
     // this lane's maximum (NaN-propagating); +inf and NaN poison the row
@@ -102,21 +122,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_stream_kernel(Params p) {
       if (lane == 0) out[0] = make_uint2(0x7fc00000u, 0u);
       continue;
     }
-    // T: the k-th largest lane maximum (k rounds of a warp maximum; -inf if fewer lanes)
+    // T: the k-th largest lane maximum (-inf if fewer lanes hold elements). Each round one
+    // redux.sync over the order-preserving integer images (0 for lanes already taken, below
+    // every real value) and a ballot that retires the lowest lane holding the maximum.
     float T = -INFINITY;
     {
       bool taken = !any_elem;
       for (int r = 0; r < k; ++r) {
-        float v = taken ? -INFINITY : lm;
-        int who = taken ? 32 : lane;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
-          const int w2 = __shfl_xor_sync(0xffffffffu, who, off);
-          if (ranks_before(v2, w2, v, who)) { v = v2; who = w2; }
-        }
-        if (who == lane) taken = true;
-        T = v;
+        const unsigned key = taken ? 0u : float_key(__fadd_rn(lm, 0.f));   // -0 -> +0
+        const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
+        const unsigned holders = __ballot_sync(0xffffffffu, !taken && key == kmax);
+        if (holders && lane == __ffs(holders) - 1) taken = true;
+        T = holders ? key_float(kmax) : -INFINITY;
       }
     }
     // count, then gather, this lane's elements >= T

@@ -104,6 +104,23 @@ def test_topk(orc, dtype, V, k):
         np.testing.assert_array_equal(idx.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("dtype", [F32, BF16])
+def test_topk_signed_zero_ties(orc, dtype):
+    """-0.0 and +0.0 are equal values: the lower index ranks first, whatever the signs."""
+    import speculative_decoding_verification_78_gb300 as sv
+    rng = np.random.default_rng(7)
+    x = -np.abs(rng.standard_normal((8, 5000))).astype(np.float32) - 1.0
+    for r in range(8):
+        cols = rng.choice(5000, size=6, replace=False)
+        x[r, cols] = np.where(rng.random(6) < 0.5, -0.0, 0.0).astype(np.float32)
+    lg = f32_to_bf16(x) if dtype == BF16 else x
+    want, rc = orc.topk(lg, dtype, 4)
+    assert rc == 0
+    idx, st = sv.topk(dev(lg), 4)
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(idx.cpu().numpy(), want)
+
+
 def test_topk_invalid_rows(orc):
     import speculative_decoding_verification_78_gb300 as sv
     x = np.zeros((5, 300), np.float32)
