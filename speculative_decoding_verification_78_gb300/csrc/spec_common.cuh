@@ -314,13 +314,16 @@ __device__ __forceinline__ void stat_merge(float &m, float &s, float m2, float s
   s = __fadd_rn(a, b);
 }
 
+// The warp's combined pair on every lane: the maximum M in one redux.sync (NaN, then +inf,
+// rank highest, so they still poison), then each lane's sum rescaled to M once and the scaled
+// sums added by a butterfly (identical on every lane: each step adds the same two values).
 __device__ __forceinline__ void warp_stat_merge(float &m, float &s, float c2) {
+  const float M = key_float(__reduce_max_sync(0xffffffffu, float_key(m)));
+  float t = (M == -INFINITY) ? 0.f : __fmul_rn(s, ex2_shift(m, M, c2));
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-    stat_merge(m, s, m2, s2, c2);
-  }
+  for (int off = 16; off > 0; off >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, off));
+  m = M;
+  s = t;
 }
 
 template <typename E>
