@@ -89,12 +89,13 @@ __device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float
           stat_merge(m, s, __uint_as_float(w[t].x), __uint_as_float(w[t].y), p.c2);
         }
       }
-      for (int off = L >> 1; off > 0; off >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-        stat_merge(m, s, m2, s2, p.c2);
-      }
-      if (r < R && sub == 0) { rowM[r] = m; rowZ[r] = s; }
+      // the group's pair: its maximum (NaN-propagating), then each lane's sum rescaled to it
+      // once and the scaled sums added, both by butterflies inside the group of L lanes
+      float M = m;
+      for (int off = L >> 1; off > 0; off >>= 1) M = fmax_nan(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float t = (M == -INFINITY) ? 0.f : __fmul_rn(s, ex2_shift(m, M, p.c2));
+      for (int off = L >> 1; off > 0; off >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, off));
+      if (r < R && sub == 0) { rowM[r] = M; rowZ[r] = t; }
     }
   }
 }
