@@ -208,6 +208,35 @@ FinishPlan probs_finish(const Params &p, int dtype) {
 
 }  // namespace
 
+namespace specv {
+
+// The host checks of a chain call, in the order the header documents: dtype, shape,
+// temperature, null pointers, alignment. The workspace is checked only when asked (the
+// static-scratch entry point has none); nothing here needs a device.
+int chain_args_check(const void *target_logits, const void *draft_logits, int dtype,
+                     const int32_t *draft_tokens, const float *uniforms, int B, int gamma, int V,
+                     float temperature, const int32_t *accept_len, const int32_t *out_tokens,
+                     const int32_t *status, const void *workspace, bool need_workspace) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (B < 0 || gamma < 0 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V)
+    return SPEC_ERR_SHAPE;
+  if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
+  const bool greedy = temperature == 0.f;
+  if (!target_logits || !accept_len || !out_tokens || !status || (need_workspace && !workspace))
+    return SPEC_ERR_NULL;
+  if (gamma > 0 && !draft_tokens) return SPEC_ERR_NULL;
+  if (!greedy && (!uniforms || (gamma > 0 && !draft_logits))) return SPEC_ERR_NULL;
+  const int es = elem_size(dtype);
+  if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)) ||
+      (draft_tokens && !aligned(draft_tokens, 4)) || (uniforms && !aligned(uniforms, 4)) ||
+      !aligned(accept_len, 4) || !aligned(out_tokens, 4) || !aligned(status, 4) ||
+      (need_workspace && !aligned(workspace, 16)))
+    return SPEC_ERR_ALIGN;
+  return SPEC_OK;
+}
+
+}  // namespace specv
+
 extern "C" {
 
 size_t spec_workspace_bytes(int B, int rows_per_b, int V, int dtype) {
@@ -229,20 +258,11 @@ int spec_verify_chain(const void *target_logits, const void *draft_logits, int d
                       const int32_t *draft_tokens, const float *uniforms, int B, int gamma, int V,
                       float temperature, int32_t *accept_len, int32_t *out_tokens,
                       int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
-  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
-  if (B < 0 || gamma < 0 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V)
-    return SPEC_ERR_SHAPE;
-  if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
+  const int chk = specv::chain_args_check(target_logits, draft_logits, dtype, draft_tokens,
+                                          uniforms, B, gamma, V, temperature, accept_len,
+                                          out_tokens, status, workspace, true);
+  if (chk != SPEC_OK) return chk;
   const bool greedy = temperature == 0.f;
-  if (!target_logits || !accept_len || !out_tokens || !status || !workspace) return SPEC_ERR_NULL;
-  if (gamma > 0 && !draft_tokens) return SPEC_ERR_NULL;
-  if (!greedy && (!uniforms || (gamma > 0 && !draft_logits))) return SPEC_ERR_NULL;
-  const int es = elem_size(dtype);
-  if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)) ||
-      (draft_tokens && !aligned(draft_tokens, 4)) || (uniforms && !aligned(uniforms, 4)) ||
-      !aligned(accept_len, 4) || !aligned(out_tokens, 4) || !aligned(status, 4) ||
-      !aligned(workspace, 16))
-    return SPEC_ERR_ALIGN;
   if (B == 0) return SPEC_OK;
 
   Params p = blank();

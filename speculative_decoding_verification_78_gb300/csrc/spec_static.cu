@@ -12,6 +12,13 @@
 
 #include "spec_verify.h"
 
+namespace specv {
+int chain_args_check(const void *target_logits, const void *draft_logits, int dtype,
+                     const int32_t *draft_tokens, const float *uniforms, int B, int gamma, int V,
+                     float temperature, const int32_t *accept_len, const int32_t *out_tokens,
+                     const int32_t *status, const void *workspace, bool need_workspace);
+}  // namespace specv
+
 namespace {
 
 constexpr size_t kStaticScratchBytes = SPEC_STATIC_SCRATCH_BYTES;
@@ -31,11 +38,15 @@ extern "C" int spec_verify_chain_static(const void *target_logits, const void *d
                                         const float *uniforms, int B, int gamma, int V,
                                         float temperature, int32_t *accept_len,
                                         int32_t *out_tokens, int32_t *status, void *stream) {
-  // the size check needs no device: a call larger than the array is refused up front
-  if (B >= 0 && gamma >= 0 && gamma <= SPEC_MAX_GAMMA) {
-    const size_t need = spec_workspace_bytes(B, 2 * gamma + 1, V, dtype);
-    if (need > kStaticScratchBytes) return SPEC_ERR_WORKSPACE;
-  }
+  // the argument and size checks need no device: bad arguments, and a call larger than the
+  // array, are refused up front
+  const int chk = specv::chain_args_check(target_logits, draft_logits, dtype, draft_tokens,
+                                          uniforms, B, gamma, V, temperature, accept_len,
+                                          out_tokens, status, nullptr, false);
+  if (chk != SPEC_OK) return chk;
+  if (B == 0) return SPEC_OK;
+  if (spec_workspace_bytes(B, 2 * gamma + 1, V, dtype) > kStaticScratchBytes)
+    return SPEC_ERR_WORKSPACE;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_LAUNCH;
   void *addr = g_scratch_addr[dev].load(std::memory_order_acquire);

@@ -137,6 +137,76 @@ def test_tree_and_probs_host_validation(lib):
     assert pr(rows=0) == sv.SPEC_OK
 
 
+def test_helpers_host_validation(lib):
+    """spec_sample, spec_topk, spec_tree_mask and spec_verify_chain_static reject bad arguments
+    on the host, before anything is enqueued (the fake device addresses are never touched)."""
+    import speculative_decoding_verification_78_gb300 as sv
+    vp = ctypes.c_void_p
+
+    def sample(**kw):
+        a = dict(t=FAKE, dtype=1, rows=5, V=1000, T=1.0, uni=FAKE, out=FAKE, st=FAKE, ws=FAKE,
+                 wsb=1 << 30)
+        a.update(kw)
+        return lib.spec_sample(vp(a["t"]), a["dtype"], a["rows"], a["V"], a["T"], vp(a["uni"]),
+                               vp(a["out"]), vp(a["st"]), vp(a["ws"]), a["wsb"], None)
+
+    assert sample(dtype=2) == sv.SPEC_ERR_DTYPE
+    assert sample(V=0) == sv.SPEC_ERR_SHAPE
+    assert sample(rows=-1) == sv.SPEC_ERR_SHAPE
+    assert sample(T=float("nan")) == sv.SPEC_ERR_TEMP
+    assert sample(uni=0) == sv.SPEC_ERR_NULL
+    assert sample(ws=0) == sv.SPEC_ERR_NULL
+    assert sample(t=FAKE + 1) == sv.SPEC_ERR_ALIGN
+    assert sample(uni=FAKE + 2) == sv.SPEC_ERR_ALIGN
+    assert sample(wsb=8) == sv.SPEC_ERR_WORKSPACE
+    assert sample(rows=0) == sv.SPEC_OK
+    # greedy sampling needs no uniforms
+    assert sample(T=0.0, uni=0, wsb=8) == sv.SPEC_ERR_WORKSPACE
+
+    def topk(**kw):
+        a = dict(t=FAKE, dtype=0, rows=5, V=1000, k=4, out=FAKE, st=FAKE, ws=FAKE, wsb=1 << 30)
+        a.update(kw)
+        return lib.spec_topk(vp(a["t"]), a["dtype"], a["rows"], a["V"], a["k"], vp(a["out"]),
+                             vp(a["st"]), vp(a["ws"]), a["wsb"], None)
+
+    assert topk(dtype=5) == sv.SPEC_ERR_DTYPE
+    assert topk(k=0) == sv.SPEC_ERR_SHAPE
+    assert topk(k=sv.SPEC_MAX_TOPK + 1) == sv.SPEC_ERR_SHAPE
+    assert topk(V=3, k=4) == sv.SPEC_ERR_SHAPE           # k > V
+    assert topk(out=0) == sv.SPEC_ERR_NULL
+    assert topk(t=FAKE + 2) == sv.SPEC_ERR_ALIGN          # fp32 rows need 4-byte alignment
+    assert topk(wsb=64) == sv.SPEC_ERR_WORKSPACE
+    assert topk(rows=0) == sv.SPEC_OK
+
+    def mask(**kw):
+        a = dict(par=FAKE, B=3, N=64, out=FAKE, st=FAKE)
+        a.update(kw)
+        return lib.spec_tree_mask(vp(a["par"]), a["B"], a["N"], vp(a["out"]), vp(a["st"]), None)
+
+    assert mask(N=0) == sv.SPEC_ERR_SHAPE
+    assert mask(N=sv.SPEC_MAX_NODES + 1) == sv.SPEC_ERR_SHAPE
+    assert mask(B=-1) == sv.SPEC_ERR_SHAPE
+    assert mask(out=0) == sv.SPEC_ERR_NULL
+    assert mask(par=FAKE + 2) == sv.SPEC_ERR_ALIGN
+    assert mask(B=0) == sv.SPEC_OK
+
+    def static(**kw):
+        a = dict(t=FAKE, d=FAKE, dtype=1, tok=FAKE, uni=FAKE, B=4, g=3, V=1000, T=1.0, acc=FAKE,
+                 out=FAKE, st=FAKE)
+        a.update(kw)
+        return lib.spec_verify_chain_static(vp(a["t"]), vp(a["d"]), a["dtype"], vp(a["tok"]),
+                                            vp(a["uni"]), a["B"], a["g"], a["V"], a["T"],
+                                            vp(a["acc"]), vp(a["out"]), vp(a["st"]), None)
+
+    assert static(dtype=9) == sv.SPEC_ERR_DTYPE
+    assert static(g=-1) == sv.SPEC_ERR_SHAPE
+    assert static(T=-2.0) == sv.SPEC_ERR_TEMP
+    assert static(acc=0) == sv.SPEC_ERR_NULL
+    # more scratch than the library's static array holds
+    assert static(B=4096, g=8, V=128256) == sv.SPEC_ERR_WORKSPACE
+    assert static(B=0) == sv.SPEC_OK
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import speculative_decoding_verification_78_gb300._binding as bnd
     monkeypatch.setattr(bnd, "_lib", None)
