@@ -54,11 +54,14 @@ def _load():
             lib.oracle_argmax.argtypes = [vp, i32, i64, i64, vp]
             lib.oracle_verify_chain.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, dbl, vp,
                                                 vp, vp]
+            lib.oracle_verify_chain_detail.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, dbl,
+                                                       dbl, vp, vp, vp, vp, vp, vp]
             lib.oracle_verify_tree.argtypes = [vp, i32, vp, vp, i64, i64, i64, vp, vp, vp]
             lib.oracle_sample.argtypes = [vp, i32, i64, i64, dbl, vp, vp, vp]
             lib.oracle_topk.argtypes = [vp, i32, i64, i64, i64, vp]
             lib.oracle_tree_mask.argtypes = [vp, i64, i64, vp]
             for f in (lib.oracle_probs, lib.oracle_argmax, lib.oracle_verify_chain,
+                      lib.oracle_verify_chain_detail,
                       lib.oracle_verify_tree, lib.oracle_sample, lib.oracle_topk,
                       lib.oracle_tree_mask):
                 f.restype = ctypes.c_int
@@ -115,6 +118,31 @@ def verify_chain(target, draft, dtype, tokens, uniforms, temperature):
     rc = _load().oracle_verify_chain(_ptr(tg), dptr, dtype, _ptr(tok), _ptr(uni), B, gamma, V,
                                      float(temperature), _ptr(acc), _ptr(out), _ptr(mg))
     return acc, out, mg, rc
+
+
+def verify_chain_detail(target, draft, dtype, tokens, uniforms, temperature, band=1e-5):
+    """Every position of every batch row, as if the step had reached it (see
+    oracle_verify_chain_detail). Returns a dict of numpy arrays: accept [B, gamma] (0/1),
+    dmargin [B, gamma], tok / cmargin / lo / hi [B, gamma+1], and rc."""
+    tg = _logits(target, dtype)
+    B, g1, V = tg.shape
+    gamma = g1 - 1
+    dr = None if draft is None else _logits(draft, dtype)
+    if dr is not None:
+        assert dr.shape == (B, gamma, V)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, gamma)
+    uni = (None if uniforms is None else
+           np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, gamma + 1))
+    out = dict(accept=np.empty((B, gamma), np.int32), dmargin=np.empty((B, gamma), np.float64),
+               tok=np.empty((B, g1), np.int32), cmargin=np.empty((B, g1), np.float64),
+               lo=np.empty((B, g1), np.int32), hi=np.empty((B, g1), np.int32))
+    dptr = _ptr(dr) if dr is not None and dr.size else None
+    rc = _load().oracle_verify_chain_detail(
+        _ptr(tg), dptr, dtype, _ptr(tok), _ptr(uni), B, gamma, V, float(temperature),
+        float(band), _ptr(out["accept"]), _ptr(out["dmargin"]), _ptr(out["tok"]),
+        _ptr(out["cmargin"]), _ptr(out["lo"]), _ptr(out["hi"]))
+    out["rc"] = rc
+    return out
 
 
 def verify_tree(target, dtype, parents, tokens):

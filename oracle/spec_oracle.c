@@ -286,6 +286,140 @@ int oracle_verify_chain(const void *target, const void *draft, int dtype, const 
   return rc;
 }
 
+/*
+ * The band of one inverse-CDF draw: with c_k the inclusive running sums of r (index order,
+ * c_{-1} = 0), S = c_{V-1} and t = u * S, the tokens k whose CDF cell [c_{k-1}, c_k] comes
+ * within band * scale of t: c_k >= t - band * scale and c_{k-1} <= t + band * scale. The cells
+ * are consecutive, so this is the index interval [*lo, *hi]; it holds the drawn token. A token
+ * outside it needs a cumulative-sum error above band * scale to be drawn.
+ */
+static void cdf_band(const double *r, long V, double u, double scale, double band, long *lo,
+                     long *hi) {
+  double S = 0.0;
+  for (long k = 0; k < V; ++k) S += r[k];
+  const double t = u * S, w = band * scale;
+  *lo = V - 1;
+  *hi = 0;
+  int seen = 0;
+  double c = 0.0;
+  for (long k = 0; k < V; ++k) {
+    double prev = c;
+    c += r[k];
+    if (c >= t - w && prev <= t + w) {
+      if (!seen) *lo = k;
+      *hi = k;
+      seen = 1;
+    }
+  }
+}
+
+/*
+ * Per-position detail of batched chain verify, for tests that compare an implementation working
+ * in fp32 with this one. oracle_verify_chain follows one path, the one the uniforms select;
+ * here every batch row is evaluated at every position, as if the step had reached it, so that
+ * a run whose path left the oracle's at a near-boundary decision can still be checked decision
+ * by decision and draw by draw:
+ *   accept[b, i]   i < gamma: 1 if u_i <= p_i(x_i) / q_i(x_i) (T == 0: x_i == argmax of target
+ *                  row i), else 0
+ *   dmargin[b, i]  |u_i - ratio_i| / ratio_i, as in oracle_verify_chain (+inf when the ratio is
+ *                  +inf or 0, and at T == 0)
+ *   tok[b, j]      j <= gamma: the token the step emits if it stops at position j -- for j <
+ *                  gamma the correction drawn with u_gamma from norm(max(0, p_j - q_j)) (p_j if
+ *                  that sums to 0), for j == gamma the bonus drawn from p_gamma (T == 0: the
+ *                  argmax of target row j)
+ *   cmargin[b, j]  the CDF margin of that draw (relative to P, as in oracle_verify_chain; +inf
+ *                  at T == 0)
+ *   lo[b, j], hi[b, j]  the draw's band (cdf_band) for the given band width (T == 0: the token)
+ * The path oracle_verify_chain takes is n = the first i with accept[b, i] == 0 (or gamma);
+ * its outputs are tok[b, n] after x_0..x_{n-1}. An invalid batch row gets accept = 0, margins
+ * +inf and tok = lo = hi = -1. Returns 0 or the first error code met.
+ */
+int oracle_verify_chain_detail(const void *target, const void *draft, int dtype,
+                               const int32_t *tokens, const float *uniforms, long B, long gamma,
+                               long V, double T, double band, int32_t *accept, double *dmargin,
+                               int32_t *tok, double *cmargin, int32_t *lo, int32_t *hi) {
+  if (B < 0 || gamma < 0 || V < 1 || !(T >= 0.0) || isinf(T) || !(band >= 0.0))
+    return ORC_ERR_ARG;
+  double *p = (double *)malloc(sizeof(double) * (size_t)V);
+  double *q = (double *)malloc(sizeof(double) * (size_t)V);
+  double *r = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!p || !q || !r) { free(p); free(q); free(r); return ORC_ERR_MEM; }
+  int rc = ORC_OK;
+  for (long b = 0; b < B; ++b) {
+    const size_t trow0 = (size_t)b * (size_t)(gamma + 1);
+    const size_t drow0 = (size_t)b * (size_t)gamma;
+    const int32_t *x = tokens + (size_t)b * (size_t)gamma;
+    const float *u = uniforms ? uniforms + (size_t)b * (size_t)(gamma + 1) : NULL;
+    int32_t *acc_b = accept + drow0;
+    double *dm_b = dmargin + drow0;
+    int32_t *tok_b = tok + trow0, *lo_b = lo + trow0, *hi_b = hi + trow0;
+    double *cm_b = cmargin + trow0;
+    for (long i = 0; i < gamma; ++i) { acc_b[i] = 0; dm_b[i] = INFINITY; }
+    for (long j = 0; j <= gamma; ++j) {
+      tok_b[j] = lo_b[j] = hi_b[j] = -1;
+      cm_b[j] = INFINITY;
+    }
+
+    int err = ORC_OK;   /* the same validation as oracle_verify_chain */
+    for (long i = 0; i <= gamma && !err; ++i)
+      if (!row_valid(target, dtype, (trow0 + (size_t)i) * (size_t)V, V)) err = ORC_ERR_ROW;
+    if (T > 0.0)
+      for (long i = 0; i < gamma && !err; ++i)
+        if (!row_valid(draft, dtype, (drow0 + (size_t)i) * (size_t)V, V)) err = ORC_ERR_ROW;
+    for (long i = 0; i < gamma && !err; ++i)
+      if (x[i] < 0 || x[i] >= V) err = ORC_ERR_TOKEN;
+    if (err) {
+      if (rc == ORC_OK) rc = err;
+      continue;
+    }
+
+    for (long j = 0; j <= gamma; ++j) {
+      const size_t toff = (trow0 + (size_t)j) * (size_t)V;
+      if (T == 0.0) {
+        long g = argmax_row(target, dtype, toff, V);
+        if (j < gamma) acc_b[j] = (x[j] == g);
+        tok_b[j] = lo_b[j] = hi_b[j] = (int32_t)g;
+        continue;
+      }
+      softmax_row(target, dtype, toff, V, T, p);
+      double scale = 1.0;
+      if (j < gamma) {
+        softmax_row(draft, dtype, (drow0 + (size_t)j) * (size_t)V, V, T, q);
+        double px = p[x[j]], qx = q[x[j]];
+        double ratio = (qx > 0.0) ? px / qx : (px > 0.0 ? INFINITY : 0.0);
+        double uj = (double)u[j];
+        acc_b[j] = !(uj > ratio);
+        if (isfinite(ratio))
+          dm_b[j] = fabs(uj - ratio) / (ratio > 1e-300 ? ratio : 1e-300);
+        /* the correction this position would draw: residual max(0, p - q) */
+        double S = 0.0;
+        scale = 0.0;
+        for (long k = 0; k < V; ++k) {
+          double d = p[k] - q[k];
+          r[k] = d > 0.0 ? d : 0.0;
+          S += r[k];
+          if (r[k] > 0.0) scale += p[k];
+        }
+        if (S == 0.0) {
+          for (long k = 0; k < V; ++k) r[k] = p[k];
+          scale = 1.0;
+        }
+      } else {
+        for (long k = 0; k < V; ++k) r[k] = p[k];
+      }
+      double cm;
+      long lk, hk;
+      tok_b[j] = (int32_t)inverse_cdf(r, V, (double)u[gamma], scale, &cm);
+      cm_b[j] = cm;
+      cdf_band(r, V, (double)u[gamma], scale, band, &lk, &hk);
+      lo_b[j] = (int32_t)lk;
+      hi_b[j] = (int32_t)hk;
+    }
+  }
+  free(p); free(q); free(r);
+  return rc;
+}
+
 /* ------------------------------------------------------------------ public: tree verify */
 
 /*

@@ -51,3 +51,40 @@ def tree_cases():
             path_nodes=np.asarray(c["path_nodes"], dtype=np.int32),
             out_tokens=np.asarray(c["out_tokens"], dtype=np.int32)))
     return out
+
+
+def _rational(v):
+    """'a/b' -> a/b as a float ('1/ln2' -> 1/ln 2); numbers pass through."""
+    import math
+    from fractions import Fraction
+    if isinstance(v, str):
+        if v == "1/ln2":
+            return 1.0 / math.log(2.0)
+        if v == "inf":
+            return math.inf
+        return float(Fraction(v))
+    return float(v)
+
+
+def margin_cases():
+    """The boundary-margin fixtures: inputs as for chain_cases, plus the per-position
+    expectations of the oracle's detail (accept, dmargin, tok, cmargin, lo, hi)."""
+    with open(os.path.join(GOLDEN, "margin_cases.json")) as f:
+        data = json.load(f)
+    out = []
+    for c in data["cases"]:
+        V, g = c["V"], c["gamma"]
+        tgt = _f32(c["target"])
+        B = tgt.shape[0]
+        rat = lambda x: np.asarray([[_rational(v) for v in row] for row in x], np.float64)
+        out.append(dict(
+            name=c["name"], T=_rational(c["T"]), V=V, gamma=g, band=float(data["band"]),
+            target=tgt.reshape(B, g + 1, V), draft=_f32(c["draft"], (B, g, V)),
+            tokens=np.asarray(c["tokens"], dtype=np.int32).reshape(B, g),
+            uniforms=rat(c["uniforms"]).astype(np.float32),
+            accept=np.asarray(c["accept"], dtype=np.int32), dmargin=rat(c["dmargin"]),
+            tok=np.asarray(c["tok"], dtype=np.int32), cmargin=rat(c["cmargin"]),
+            lo=np.asarray(c["lo"], dtype=np.int32), hi=np.asarray(c["hi"], dtype=np.int32),
+            accept_len=np.asarray(c["accept_len"], dtype=np.int32),
+            out_tokens=np.asarray(c["out_tokens"], dtype=np.int32).reshape(B, g + 1)))
+    return out

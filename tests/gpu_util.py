@@ -48,33 +48,110 @@ def run_tree(ti, offset_elems=0):
 
 
 def compare_chain(orc, ci, gpu, rows=None):
-    """Exact match on every batch row whose oracle margin is >= MARGIN. Rows below it
-    (near-boundary draws) are counted and reported; their GPU outputs must still be a valid
-    step: n in [0, gamma], the accepted prefix equal to the drafts, one token in [0, V), then
-    -1. Returns (flagged, flagged_and_different, oracle accept_len)."""
+    """Checks a GPU chain result against the oracle draw by draw.
+
+    The oracle's detail evaluates every position of every batch row (decision, and the draw the
+    step would make if it stopped there). With n the GPU's accept length:
+      - every decision the GPU took (accept x_i for i < n, reject x_n when n < gamma) must be the
+        oracle's, unless that decision's margin is below MARGIN (then either is correct);
+      - the accepted prefix equals the drafts, entries after position n are -1;
+      - the emitted token equals the oracle's draw at position n, unless that draw's margin is
+        below MARGIN: then it must lie in the draw's band (the tokens whose CDF cell comes within
+        MARGIN * P of u * S) and have p_n > 0 (for a correction also p_n >= (1 - MARGIN) q_n,
+        i.e. a residual that fp32 rounding can make positive).
+    So accept_len is compared exactly unless the deciding draw is itself near a boundary.
+    Invalid rows must match exactly (-1 everywhere). Returns (flagged draws on the oracle's
+    path, of those the ones where the GPU differs, oracle accept_len)."""
     acc, out, _ = gpu
     tgt, drf, tok, uni = ci.target, ci.draft, ci.tokens, ci.uniforms
     if rows is not None:
         tgt, drf, tok, uni = tgt[rows], drf[rows], tok[rows], uni[rows]
         acc, out = acc[rows], out[rows]
-    oa, oo, om, rc = orc.verify_chain(tgt, drf if drf.size else None, ci.dtype, tok, uni,
-                                      ci.temperature)
-    ok = om >= MARGIN
-    diff = (acc != oa) | np.any(out != oo, axis=1)
-    bad = np.nonzero(ok & diff)[0]
-    assert bad.size == 0, (f"{ci.name}: {bad.size} rows differ, e.g. row {bad[:5]}: "
-                           f"gpu {acc[bad[:3]]} {out[bad[:3]]} oracle {oa[bad[:3]]} "
-                           f"{oo[bad[:3]]} margins {om[bad[:3]]}")
-    g = ci.gamma
-    for b in np.nonzero(~ok)[0]:
-        n = int(acc[b])
-        assert 0 <= n <= g
-        assert np.array_equal(out[b, :n], tok[b, :n])
-        assert 0 <= out[b, n] < ci.V and np.all(out[b, n + 1:] == -1)
-    flagged = int((~ok).sum())
-    fdiff = int((~ok & diff).sum())
-    report(ci.name, rows=len(ok), flagged=flagged, flagged_and_different=fdiff)
-    return flagged, fdiff, oa
+    g, T = ci.gamma, ci.temperature
+    dr = drf if drf.size and T > 0 else None
+    oa, oo, _, _ = orc.verify_chain(tgt, dr, ci.dtype, tok, uni, T)
+    d = orc.verify_chain_detail(tgt, dr, ci.dtype, tok, uni, T, band=MARGIN)
+    n_dec = n_draw = f_dec = f_draw = f_diff = 0
+    bad = []
+    for b in range(len(acc)):
+        n, no = int(acc[b]), int(oa[b])
+        if no < 0 or d["tok"][b, 0] < 0:          # invalid row: exact
+            if n != -1 or np.any(out[b] != -1):
+                bad.append((b, "invalid row not reported"))
+            continue
+        # the oracle's path: its decisions and its draw, flagged when near a boundary
+        path_dec = range(min(no + 1, g))
+        n_dec += len(path_dec)
+        n_draw += 1
+        fl_dec = [i for i in path_dec if d["dmargin"][b, i] < MARGIN]
+        fl_draw = d["cmargin"][b, no] < MARGIN
+        f_dec += len(fl_dec)
+        f_draw += int(fl_draw)
+        if not 0 <= n <= g:
+            bad.append((b, f"accept_len {n}"))
+            continue
+        ok = True
+        for i in range(min(n + 1, g)):        # the decisions the GPU took
+            gpu_accepts = i < n
+            if gpu_accepts != bool(d["accept"][b, i]) and d["dmargin"][b, i] >= MARGIN:
+                bad.append((b, f"decision {i}: gpu n={n}, oracle n={no}, "
+                               f"margin {d['dmargin'][b, i]:.3g}"))
+                ok = False
+                break
+        if not ok:
+            continue
+        if not np.array_equal(out[b, :n], tok[b, :n]) or np.any(out[b, n + 1:] != -1):
+            bad.append((b, "prefix or padding"))
+            continue
+        t = int(out[b, n])
+        if d["cmargin"][b, n] >= MARGIN:
+            if t != d["tok"][b, n]:
+                bad.append((b, f"token {t} != {d['tok'][b, n]} at n={n}, "
+                               f"margin {d['cmargin'][b, n]:.3g}"))
+        elif not (d["lo"][b, n] <= t <= d["hi"][b, n] and _drawable(orc, ci, tgt, dr, b, n, t)):
+            bad.append((b, f"token {t} outside band [{d['lo'][b, n]}, {d['hi'][b, n]}] at n={n}"))
+        # a row that passed and still differs from the oracle's path has a flagged draw on it
+        f_diff += int(n != no or t != int(oo[b, n]))
+    assert not bad, f"{ci.name}: {len(bad)} rows fail, e.g. {bad[:4]}"
+    report(ci.name, rows=len(acc), decisions=n_dec, draws=n_draw, flagged_decisions=f_dec,
+           flagged_draws=f_draw, flagged_and_different=f_diff, outside_band=0)
+    return f_dec + f_draw, f_diff, oa
+
+
+def _drawable(orc, ci, tgt, dr, b, n, t):
+    """The emitted token has p_n(t) > 0 and, for a correction (n < gamma), a residual that
+    rounding can make positive: p_n(t) >= (1 - MARGIN) q_n(t)."""
+    T = ci.temperature
+    p, _ = orc.probs(tgt[b, n:n + 1], ci.dtype, T)
+    if p[0, t] <= 0:
+        return False
+    if n < ci.gamma and dr is not None:
+        q, _ = orc.probs(dr[b, n:n + 1], ci.dtype, T)
+        return p[0, t] >= (1 - MARGIN) * q[0, t]
+    return True
+
+
+def compare_sample(orc, lg, dtype, u, T, tok):
+    """spec_sample against the oracle, draw by draw (a sample is a chain step with no drafts:
+    its one draw is the bonus draw): the token must equal the oracle's unless the draw's margin
+    is below MARGIN, and then lie in the draw's band with p > 0. Returns the flagged count."""
+    want, mg, rc = orc.sample(lg, dtype, u, T)
+    rows, V = lg.shape
+    d = orc.verify_chain_detail(lg.reshape(rows, 1, V), None, dtype,
+                                np.zeros((rows, 0), np.int32), u.reshape(rows, 1), T,
+                                band=MARGIN)
+    np.testing.assert_array_equal(d["tok"][:, 0], want)
+    p, _ = orc.probs(lg, dtype, T)
+    flagged = 0
+    for r in range(rows):
+        if want[r] < 0 or mg[r] >= MARGIN:
+            assert tok[r] == want[r], (r, tok[r], want[r], mg[r])
+        else:
+            flagged += 1
+            assert d["lo"][r, 0] <= tok[r] <= d["hi"][r, 0] and p[r, tok[r]] > 0, \
+                (r, tok[r], d["lo"][r, 0], d["hi"][r, 0])
+    report("sample", rows=rows, draws=rows, flagged_draws=flagged, outside_band=0)
+    return flagged
 
 
 def report(name, **kw):

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import dev
+from gpu_util import compare_sample, dev
 from workloads import BF16, F32, f32_to_bf16, make_uniforms, tree_shape
 
 pytestmark = pytest.mark.gpu
@@ -33,20 +33,17 @@ def test_sample(orc, dtype, V, T):
     x[:, 1::9] = -np.inf
     lg = f32_to_bf16(x) if dtype == BF16 else x
     u = make_uniforms(rng, (rows,))
-    want, mg, rc = orc.sample(lg, dtype, u, T)
+    _, _, rc = orc.sample(lg, dtype, u, T)
     assert rc == 0
-    p, _ = orc.probs(lg, dtype, T)
     for off in (0, 1):
         tok, st = sv.sample(dev(lg, off), T, dev(u))
         torch.cuda.synchronize()
         tok = tok.cpu().numpy()
         assert int(st.item()) == 0
-        # draws within MARGIN of a CDF boundary (common for long, flat rows) only have to be
-        # tokens of positive probability; the others must match exactly
-        close = mg < MARGIN
-        np.testing.assert_array_equal(tok[~close], want[~close])
-        assert (~close).sum() >= rows // 2
-        assert all(p[r, tok[r]] > 0 for r in range(rows))
+        # a draw within MARGIN of a CDF boundary (common for long, flat rows) must land in the
+        # oracle's band for it; every other draw must match exactly
+        flagged = compare_sample(orc, lg, dtype, u, T, tok)
+        assert flagged <= rows // 2
 
 
 def test_sample_invalid_rows(orc):
@@ -74,14 +71,11 @@ def test_sample_invalid_rows_multi_unit(orc, dtype):
     x[4, 39999] = np.inf
     lg = f32_to_bf16(x) if dtype == BF16 else x
     u = make_uniforms(rng, (6,))
-    want, mg, _ = orc.sample(lg, dtype, u, 1.0)
     tok, st = sv.sample(dev(lg), 1.0, dev(u))
     tok = tok.cpu().numpy()
     assert int(st.item()) == sv.SPEC_ERR_NONFINITE
     assert list(tok[[1, 3, 4]]) == [-1, -1, -1]
-    good = np.array([0, 2, 5])
-    close = mg[good] < MARGIN
-    np.testing.assert_array_equal(tok[good][~close], want[good][~close])
+    compare_sample(orc, lg, dtype, u, 1.0, tok)
 
 
 @pytest.mark.parametrize("dtype", [F32, BF16])

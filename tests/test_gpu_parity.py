@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from golden_io import chain_cases, tree_cases
+from golden_io import chain_cases, margin_cases, tree_cases
 from gpu_util import compare_chain, dev, run_chain, run_tree
 from workloads import (BF16, F32, ChainInputs, TreeInputs, bf16_to_f32, chain_128k, chain_32k,
                        chain_tiny, f32_to_bf16, make_uniforms, sweep_152k, tree_32k, tree_shape)
@@ -40,6 +40,20 @@ def test_golden_chain(case):
     assert st == 0
     np.testing.assert_array_equal(acc, case["accept_len"])
     np.testing.assert_array_equal(out, case["out_tokens"])
+
+
+@pytest.mark.parametrize("case", margin_cases(), ids=lambda c: c["name"])
+def test_golden_margin_cases(orc, case):
+    """The hand-derived boundary cases (dyadic probabilities: the kernels' fp32 arithmetic is
+    exact on them): the emitted tokens must be the hand-derived ones, and the per-draw
+    comparison with the oracle must pass."""
+    ci = ChainInputs(case["name"], case["target"], case["draft"], F32, case["tokens"],
+                     case["uniforms"], float(np.float32(case["T"])))
+    gpu = run_chain(ci)
+    assert gpu[2] == 0
+    np.testing.assert_array_equal(gpu[0], case["accept_len"])
+    np.testing.assert_array_equal(gpu[1], case["out_tokens"])
+    compare_chain(orc, ci, gpu)
 
 
 @pytest.mark.parametrize("case", tree_cases(), ids=lambda c: c["name"])
@@ -93,9 +107,11 @@ def test_sweep_152k_fp32(orc, B, gamma):
     compare_chain(orc, ci, gpu, rows=rows)
 
 
-def test_sweep_152k_fp32_largest(orc):
-    """B=1024, gamma=7, V=152064 fp32: 9.3 GB of logits in one call; 16 rows checked."""
-    ci = sweep_152k(B=1024, gamma=7)
+@pytest.mark.parametrize("gamma", [3, 7])
+def test_sweep_152k_fp32_largest(orc, gamma):
+    """B=1024, V=152064 fp32: 4.4 GB (gamma 3) and 9.3 GB (gamma 7) of logits in one call;
+    16 rows checked draw by draw."""
+    ci = sweep_152k(B=1024, gamma=gamma)
     gpu = run_chain(ci)
     assert gpu[2] == 0
     compare_chain(orc, ci, gpu, rows=np.arange(0, 1024, 64))
@@ -111,6 +127,25 @@ def test_tree_32k_bf16(orc):
     np.testing.assert_array_equal(path, rp)
     np.testing.assert_array_equal(out, ro)
     assert acc.max() >= 2
+
+
+def test_tree_32k_bf16_ties_at_the_maximum(orc):
+    """Full-size tree call (32 trees x 64 nodes x 32000 bf16) whose every node holds its maximum
+    at five ids: the lowest, the next element of the same 16-byte vector, one 600 ids on (same
+    4 KB unit, another lane), one 2100 on (the next unit) and one 9000 on (four units later).
+    Argmaxes, paths and bonus tokens bit-exact against the oracle (lowest index wins)."""
+    ti = tree_32k(seed=40, tie_offsets=(1, 600, 2100, 9000))
+    acc, path, out, st = run_tree(ti)
+    ra, rp, ro, rc = orc.verify_tree(ti.target, BF16, ti.parents, ti.tokens)
+    assert st == 0 and rc == 0
+    np.testing.assert_array_equal(acc, ra)
+    np.testing.assert_array_equal(path, rp)
+    np.testing.assert_array_equal(out, ro)
+    assert acc.max() >= 2
+    # the bonus token is the lowest of the tied ids at the deepest accepted node
+    des = ti.meta["designated"]
+    best = path[np.arange(ti.B), acc]
+    np.testing.assert_array_equal(out[np.arange(ti.B), acc], des[np.arange(ti.B), best])
 
 
 # --------------------------------------------------------------------------- probabilities

@@ -502,7 +502,8 @@ def test_chain_invalid_rows_and_tokens(orc):
 
 def test_margins_flag_near_boundary_draws(orc):
     """The decision margin is |u - ratio| / ratio and the CDF margin is the distance of
-    u * S to the nearest CDF step, relative to S."""
+    u * S to the nearest CDF step, relative to P (for this bonus draw P = S = 1; residual draws
+    with P != S are pinned by tests/golden/margin_cases.json)."""
     V = 4
     tgt = np.zeros((1, 2, V), np.float32)                     # p_0 = 1/4 each
     drf = np.array([[[0, 0, -np.inf, -np.inf]]], np.float32)  # q_0 = (1/2, 1/2, 0, 0)
@@ -515,3 +516,52 @@ def test_margins_flag_near_boundary_draws(orc):
         # t = 0.6 at its nearest step (relative to S = 1)
         assert mg[0] == pytest.approx(min(abs(np.float32(u0) - 0.5) / 0.5, 0.15 - 0.05),
                                       rel=1e-6)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_detail_band_holds_every_draw_within_band(orc, seed):
+    """Brute force over the uniform: the band [lo, hi] the detail reports for a draw holds every
+    token the oracle draws when t = u * S moves by at most band * P, and its ends are drawn
+    when they carry mass. Residual draws (x_0 has p = 0, so position 0 always rejects) and
+    bonus draws; a wide band (0.2) so that it spans several tokens."""
+    rng = np.random.default_rng(seed)
+    V, band = 12, 0.2
+    t = (rng.standard_normal((1, 2, V)) * 1.5).astype(np.float32)
+    d = t[:, :1] + (rng.standard_normal((1, 1, V)) * 1.0).astype(np.float32)
+    t[0, 1, 5] = -np.inf                          # a masked token in the bonus row
+    x = np.array([[3]], np.int32)
+    t[0, 0, 3] = -np.inf                          # p_0(x_0) = 0: ratio 0, always rejected
+    p, _ = orc.probs(t[0], F32, 1.0)
+    q, _ = orc.probs(d[0], F32, 1.0)
+    r0 = np.maximum(p[0] - q[0], 0.0)
+    spans = []
+    for j, (S, P) in enumerate([(r0.sum(), p[0][r0 > 0].sum()), (1.0, 1.0)]):
+        u = np.float32(0.2 + 0.6 * rng.random())
+        det = orc.verify_chain_detail(t, d, F32, x, np.array([[0.5, u]], np.float32), 1.0,
+                                      band=band)
+        lo, hi = int(det["lo"][0, j]), int(det["hi"][0, j])
+        grid = np.linspace(float(u) - band * P / S, float(u) + band * P / S, 4001)
+        grid = grid[(grid > 0) & (grid < 1)].astype(np.float32)
+        uu = np.stack([np.full(len(grid), 0.5, np.float32), grid], axis=1)
+        T_ = np.repeat(t, len(grid), axis=0)
+        D_ = np.repeat(d, len(grid), axis=0)
+        X_ = np.repeat(x, len(grid), axis=0)
+        if j == 0:
+            acc, out, _, _ = orc.verify_chain(T_, D_, F32, X_, uu, 1.0)
+            assert np.all(acc == 0)
+            drawn = out[:, 0]
+        else:   # the bonus draw from p_1, reached through a draft that is always accepted
+            T2 = T_.copy()
+            T2[:, 0, :] = 0.0
+            D2 = np.zeros_like(D_)
+            acc, out, _, _ = orc.verify_chain(T2, D2, F32, X_, uu, 1.0)
+            assert np.all(acc == 1)
+            drawn = out[:, 1]
+            det = orc.verify_chain_detail(T2[:1], D2[:1], F32, x, np.array([[0.5, u]], np.float32),
+                                          1.0, band=band)
+            lo, hi = int(det["lo"][0, 1]), int(det["hi"][0, 1])
+        assert drawn.min() >= lo and drawn.max() <= hi, (j, lo, hi, np.unique(drawn))
+        w = r0 if j == 0 else p[1]
+        assert (w[lo] == 0 or lo in drawn) and (w[hi] == 0 or hi in drawn), (j, lo, hi)
+        spans.append(hi > lo)
+    assert any(spans)           # the wide band spans more than one token at least once

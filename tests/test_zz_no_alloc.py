@@ -1,8 +1,8 @@
 """spec_verify_chain_static -- chain verification whose scratch is a static device array inside
-the library -- against spec_verify_chain with a caller-owned workspace: identical outputs on two
-calls in a row (different shapes and inputs sharing the one static array), and a call that needs
-more scratch than the array holds refused before anything is enqueued. Collected last, and
-independent of what ran before it."""
+the library -- against spec_verify_chain with a caller-owned workspace and against the CPU oracle: identical
+outputs on calls in a row (different shapes, sampling and greedy, sharing the one static array),
+and a call that needs more scratch than the array holds refused before anything is enqueued.
+Collected last, and independent of what ran before it."""
 
 import ctypes
 
@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import dev
+from gpu_util import compare_chain, dev
 from workloads import chain_32k, chain_tiny
 
 pytestmark = pytest.mark.gpu
@@ -35,10 +35,14 @@ def _static_call(ci):
     return rc, (tg, dr, tok, uni), acc, out, st
 
 
-def test_static_scratch_matches_workspace_entry_point():
+def test_static_scratch_matches_workspace_entry_point(orc):
+    """Sampling (T = 1) and greedy (T = 0) calls, each shape against both the workspace entry
+    point (identical outputs) and the oracle (the per-draw comparison of the parity tests)."""
     import speculative_decoding_verification_78_gb300 as sv
-    cases = [chain_32k(seed=41, B=8, gamma=5, V=32000), chain_tiny(seed=42, B=300, gamma=20)]
-    for ci in cases:   # both shapes take the two-kernel path, which uses the scratch
+    greedy = chain_32k(seed=43, B=16, gamma=4, V=9000, temperature=0.0)
+    cases = [chain_32k(seed=41, B=8, gamma=5, V=32000), chain_tiny(seed=42, B=300, gamma=20),
+             greedy]
+    for ci in cases:   # every shape takes the two-kernel path, which uses the scratch
         B, g1, V = ci.target.shape
         assert sv.spec_launch_shape(sv.SPEC_CALL_CHAIN, B, 2 * g1 - 1, V, ci.dtype,
                                     ci.temperature)[0] == 2
@@ -55,6 +59,7 @@ def test_static_scratch_matches_workspace_entry_point():
         np.testing.assert_array_equal(acc_s.cpu().numpy(), acc.cpu().numpy())
         np.testing.assert_array_equal(out_s.cpu().numpy(), out.cpu().numpy())
         assert (acc.cpu().numpy() >= 0).all()
+        compare_chain(orc, ci, (acc_s.cpu().numpy(), out_s.cpu().numpy(), 0))
 
 
 def test_static_scratch_refuses_oversized_calls():

@@ -312,14 +312,19 @@ def tree_shape(rng: np.random.Generator, n_nodes: int = 64,
 
 
 def tree_32k(seed: int = 4, B: int = 32, N: int = 64, V: int = 32000, dtype: int = BF16,
-             p_follow: float = 0.7, peaked: int = 50) -> TreeInputs:
+             p_follow: float = 0.7, peaked: int = 50, tie_offsets=()) -> TreeInputs:
     """Greedy tree verify workload.
 
     Node logits: N(0,3^2) clipped to +-12 plus +8 on 50 distinct ids, and one designated id
     (the first of the 50) set to 24, strictly above every other logit of that node. The
     designated id is therefore the node's greedy (argmax) token by construction, so this
     module never has to compute an argmax. A node's token is its parent's designated id with
-    probability p_follow, otherwise a uniform id in [0, V)."""
+    probability p_follow, otherwise a uniform id in [0, V).
+
+    tie_offsets (positive, increasing): the ids designated + offset get the same value 24, so
+    the node's maximum is held by several ids (bf16 ties, e.g. in the same 16-byte vector, the
+    same 4 KB unit and later units). The designated id is drawn below V - max(tie_offsets) and is
+    the lowest of the tied ids by construction, i.e. still the node's lowest-index argmax."""
     r_shape, r_t, r_p, r_tok = _rngs(seed, 4)
     target_f = np.empty((B, N, V), dtype=np.float32)
     designated = np.empty((B, N), dtype=np.int64)
@@ -332,8 +337,14 @@ def tree_32k(seed: int = 4, B: int = 32, N: int = 64, V: int = 32000, dtype: int
         for j in range(N):
             ids = r_p.choice(V, size=npk, replace=False)
             t[j, ids] += np.float32(8.0)
-            t[j, ids[0]] = np.float32(24.0)
-            designated[b, j] = ids[0]
+            if tie_offsets:
+                d = int(r_p.integers(0, V - int(tie_offsets[-1])))
+                for off in (0,) + tuple(tie_offsets):
+                    t[j, d + int(off)] = np.float32(24.0)
+                designated[b, j] = d
+            else:
+                t[j, ids[0]] = np.float32(24.0)
+                designated[b, j] = ids[0]
         target_f[b] = t
         follow = r_tok.random(N) < p_follow
         rand_tok = r_tok.integers(0, V, size=N)
