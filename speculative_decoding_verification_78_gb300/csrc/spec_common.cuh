@@ -189,6 +189,19 @@ __device__ __forceinline__ void cluster_sync_publish() {
                ::: "memory");
 }
 
+// A CTA may touch a peer's shared memory only once that peer is known to be running. Every
+// thread of a clustered kernel arrives here at entry (relaxed: nothing is published), and
+// waits (cluster_started_wait) before its first store into a peer; by then the other CTAs have
+// long arrived, so the wait costs almost nothing. The arrival and the wait are one barrier
+// phase: the publish barrier that follows is the next one. A CTA that leaves without storing
+// into peers (every CTA of its cluster takes the same path) never waits.
+__device__ __forceinline__ void cluster_started_arrive() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_started_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(int32_t *status, int code) {
   atomicCAS(reinterpret_cast<int *>(status), 0, code);
 }

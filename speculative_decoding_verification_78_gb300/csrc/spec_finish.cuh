@@ -665,8 +665,10 @@ __device__ __forceinline__ void cluster_draw_regs(const Params &p, int b, int n,
   const float wexc = __shfl_up_sync(0xffffffffu, winc, 1);
   const float woff = (warp == 0) ? 0.f : __shfl_sync(0xffffffffu, wexc, warp);
   const float ctot = __shfl_sync(0xffffffffu, winc, kWarps - 1);
-  // push this CTA's slice total into slot `rank` of every CTA of the cluster, then one barrier:
-  // afterwards every total is local, and no CTA touches a peer's shared memory again
+  // push this CTA's slice total into slot `rank` of every CTA of the cluster (every peer has
+  // started: the entry arrival's phase completes here), then one barrier: afterwards every
+  // total is local, and no CTA touches a peer's shared memory again
+  cluster_started_wait();
   if (warp == 0 && lane < S) *cl.map_shared_rank(&s_tot[rank], lane) = ctot;
   cluster_sync_publish();
   // every warp: the cluster prefix (lane r holds rank r's inclusive prefix)
@@ -767,6 +769,7 @@ __device__ void cluster_draw(const Params &p, int b, int n, const float *rowM, c
   const int lo = min(nseg, rank * K), hi = min(nseg, lo + K), nl = hi - lo;
   segment_sums<E>(P, Q, Mt, iZt, Md, iZd, p.c2, p.V, lo, hi, segsum, lo);
   __syncthreads();
+  cluster_started_wait();   // every peer is running before any store into its shared memory
   if (threadIdx.x < 32) {   // slice total: strided lane sums, then a fixed xor tree
     float tot = 0.f;
     for (int j = threadIdx.x; j < nl; j += 32) tot = __fadd_rn(tot, segsum[j]);

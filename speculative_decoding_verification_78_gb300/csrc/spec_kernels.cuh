@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   const int S = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
   const int b = blockIdx.x / S;
+  cluster_started_arrive();   // the draw's exchange waits for it before touching peers
   wait_stream_kernel();
   int n = 0;
   const int err = chain_accept(p, b, rowM, rowZ, xs, sh, &n, bonus_part);
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
   const int rank = static_cast<int>(cl.block_rank());
   const int row_i = blockIdx.x / S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (S > 1) cluster_started_arrive();   // waited for before the first store into a peer
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int V = p.V;
@@ -475,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
     else red_i[warp] = __float_as_int(bsum);
   }
   __syncthreads();
+  if (S > 1) cluster_started_wait();   // every peer is running before warp 0 stores into it
   if (warp == 0) {
     float v = (lane < kWarps) ? red_a[lane] : -INFINITY;
     int w = (lane < kWarps) ? red_i[lane] : (kGreedy ? 0x7fffffff : 0);
