@@ -226,8 +226,10 @@ int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float t
  *   - A call whose spec_workspace_bytes(B, 2*gamma+1, V, dtype) exceeds the array returns
  *     SPEC_ERR_WORKSPACE before anything is enqueued.
  *   - The array's device address is looked up (cudaGetSymbolAddress) on the first call made on
- *     each device, with that device current, and cached; make that first call before any
- *     stream capture begins.
+ *     each device, with that device current, and cached (for device ordinals below 64; a
+ *     device with a higher ordinal repeats the lookup on every call); make that first call
+ *     before any stream capture begins. SPEC_ERR_LAUNCH here means that the lookup failed
+ *     (no usable device).
  *   - Every call on a device shares the one array: two calls that may run at the same time (on
  *     different streams, or from different host threads without ordering) race on it and give
  *     undefined results. Calls ordered on one stream are fine.

@@ -115,6 +115,45 @@ def _nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
 
 
+def _expect(t, name, numel, dtypes):
+    """Raises ValueError / TypeError unless tensor t (when given) holds `numel` elements of one
+    of `dtypes`: the library reads and writes exactly that many elements behind each pointer."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t)}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {' or '.join(map(str, dtypes))}")
+    if t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements ({tuple(t.shape)}), expected {numel}")
+
+
+def _chain_shape_check(target_logits, draft_logits, draft_tokens, uniforms, temperature,
+                       accept_len, out_tokens, status):
+    """(B, gamma, V) of a chain call, after checking every operand against them: the draft
+    logits [B, gamma, V] of the target's dtype, int32 tokens [B, gamma], fp32 uniforms
+    [B, gamma+1], int32 outputs [B] and [B, gamma+1] and status [1]. NULL (None) operands are
+    left to the library's own checks."""
+    if not isinstance(target_logits, torch.Tensor) or target_logits.dim() != 3:
+        raise ValueError("target_logits must be a [B, gamma+1, V] tensor")
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    if gamma < 0:
+        raise ValueError("target_logits must have gamma+1 >= 1 positions")
+    dtype_flag(target_logits)
+    if draft_logits is not None:
+        if draft_logits.dtype != target_logits.dtype:
+            raise TypeError(f"draft_logits dtype {draft_logits.dtype} differs from "
+                            f"target_logits dtype {target_logits.dtype}")
+        _expect(draft_logits, "draft_logits", B * gamma * V, (target_logits.dtype,))
+    _expect(draft_tokens, "draft_tokens", B * gamma, (torch.int32,))
+    _expect(uniforms, "uniforms", B * (gamma + 1), (torch.float32,))
+    _expect(accept_len, "accept_len", B, (torch.int32,))
+    _expect(out_tokens, "out_tokens", B * (gamma + 1), (torch.int32,))
+    _expect(status, "status", 1, (torch.int32,))
+    return B, gamma, V
+
+
 # ------------------------------------------------------------------ the C entry points
 
 def spec_workspace_bytes(B: int, rows_per_b: int, V: int, dtype: int) -> int:
@@ -129,21 +168,25 @@ def spec_verify_chain(target_logits, draft_logits, draft_tokens, uniforms, tempe
                       accept_len, out_tokens, status, workspace, stream=None) -> int:
     """target_logits [B, gamma+1, V], draft_logits [B, gamma, V] (fp32 or bf16), draft_tokens
     [B, gamma] int32, uniforms [B, gamma+1] fp32; outputs accept_len [B], out_tokens
-    [B, gamma+1] int32; status [1] int32; workspace uint8 (scratch, no initialisation)."""
-    B, g1, V = target_logits.shape
+    [B, gamma+1] int32; status [1] int32; workspace uint8 (scratch, no initialisation).
+    Raises ValueError / TypeError when an operand's size or dtype does not match (B, gamma, V)."""
+    B, gamma, V = _chain_shape_check(target_logits, draft_logits, draft_tokens, uniforms,
+                                     temperature, accept_len, out_tokens, status)
     return load_library().spec_verify_chain(
         _ptr(target_logits), _ptr(draft_logits), dtype_flag(target_logits), _ptr(draft_tokens),
-        _ptr(uniforms), B, g1 - 1, V, float(temperature), _ptr(accept_len), _ptr(out_tokens),
+        _ptr(uniforms), B, gamma, V, float(temperature), _ptr(accept_len), _ptr(out_tokens),
         _ptr(status), _ptr(workspace), _nbytes(workspace), _stream(stream))
 
 
 def spec_verify_chain_static(target_logits, draft_logits, draft_tokens, uniforms, temperature,
                              accept_len, out_tokens, status, stream=None) -> int:
-    """spec_verify_chain with the library's static scratch instead of a workspace."""
-    B, g1, V = target_logits.shape
+    """spec_verify_chain with the library's static scratch instead of a workspace (same
+    operand checks)."""
+    B, gamma, V = _chain_shape_check(target_logits, draft_logits, draft_tokens, uniforms,
+                                     temperature, accept_len, out_tokens, status)
     return load_library().spec_verify_chain_static(
         _ptr(target_logits), _ptr(draft_logits), dtype_flag(target_logits), _ptr(draft_tokens),
-        _ptr(uniforms), B, g1 - 1, V, float(temperature), _ptr(accept_len), _ptr(out_tokens),
+        _ptr(uniforms), B, gamma, V, float(temperature), _ptr(accept_len), _ptr(out_tokens),
         _ptr(status), _stream(stream))
 
 

@@ -48,11 +48,13 @@ extern "C" int spec_verify_chain_static(const void *target_logits, const void *d
   if (spec_workspace_bytes(B, 2 * gamma + 1, V, dtype) > kStaticScratchBytes)
     return SPEC_ERR_WORKSPACE;
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_LAUNCH;
-  void *addr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return SPEC_ERR_LAUNCH;
+  // devices beyond the cache table look the address up on every call (same result, slower)
+  const bool cached = dev < kMaxDevices;
+  void *addr = cached ? g_scratch_addr[dev].load(std::memory_order_acquire) : nullptr;
   if (!addr) {
     if (cudaGetSymbolAddress(&addr, g_scratch) != cudaSuccess || !addr) return SPEC_ERR_LAUNCH;
-    g_scratch_addr[dev].store(addr, std::memory_order_release);
+    if (cached) g_scratch_addr[dev].store(addr, std::memory_order_release);
   }
   return spec_verify_chain(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma,
                            V, temperature, accept_len, out_tokens, status, addr,

@@ -246,3 +246,46 @@ def test_launch_shape_host_validation(lib):
     # single-unit rows: the one-warp chain finisher, four warps per CTA
     assert lib.spec_launch_shape(sv.SPEC_CALL_CHAIN, 37, 9, 1000, sv.SPEC_F32, 1.0, *ref) == 0
     assert (k.value, g.value, c.value) == (2, 10, 1)
+
+
+def test_binding_checks_chain_operands(lib):
+    """The binding refuses operands whose size or dtype does not match (B, gamma, V) before any
+    pointer reaches the library: a short draft tensor would be read past its end, int64 tokens
+    or fp64 uniforms would be read as other values. CPU tensors suffice: nothing is launched."""
+    import torch
+    import speculative_decoding_verification_78_gb300 as sv
+    B, g, V = 3, 2, 10
+    tgt = torch.zeros((B, g + 1, V), dtype=torch.float32)
+    ok = dict(draft_logits=torch.zeros((B, g, V), dtype=torch.float32),
+              draft_tokens=torch.zeros((B, g), dtype=torch.int32),
+              uniforms=torch.full((B, g + 1), 0.5, dtype=torch.float32),
+              accept_len=torch.zeros(B, dtype=torch.int32),
+              out_tokens=torch.zeros((B, g + 1), dtype=torch.int32),
+              status=torch.zeros(1, dtype=torch.int32))
+    bad = [("draft_logits", torch.zeros((B, g - 1, V), dtype=torch.float32), ValueError),
+           ("draft_logits", torch.zeros((B, g, V), dtype=torch.bfloat16), TypeError),
+           ("draft_tokens", torch.zeros((B, g), dtype=torch.int64), TypeError),
+           ("draft_tokens", torch.zeros((B, g + 1), dtype=torch.int32), ValueError),
+           ("uniforms", torch.zeros((B, g + 1), dtype=torch.float64), TypeError),
+           ("uniforms", torch.zeros((B, g), dtype=torch.float32), ValueError),
+           ("accept_len", torch.zeros(B + 1, dtype=torch.int32), ValueError),
+           ("out_tokens", torch.zeros((B, g + 1), dtype=torch.int64), TypeError),
+           ("status", torch.zeros(2, dtype=torch.int32), ValueError)]
+    for name, t, exc in bad:
+        args = dict(ok, **{name: t})
+        with pytest.raises(exc):
+            sv.spec_verify_chain(tgt, args["draft_logits"], args["draft_tokens"],
+                                 args["uniforms"], 1.0, args["accept_len"], args["out_tokens"],
+                                 args["status"], torch.zeros(16, dtype=torch.uint8))
+        with pytest.raises(exc):
+            sv.spec_verify_chain_static(tgt, args["draft_logits"], args["draft_tokens"],
+                                        args["uniforms"], 1.0, args["accept_len"],
+                                        args["out_tokens"], args["status"])
+    with pytest.raises(ValueError):
+        sv.spec_verify_chain(torch.zeros((B, V), dtype=torch.float32), None, None, None, 0.0,
+                             ok["accept_len"], ok["out_tokens"], ok["status"], None)
+    # well-formed operands get past the checks (then refused as host tensors by _ptr)
+    with pytest.raises(ValueError, match="device tensor"):
+        sv.spec_verify_chain(tgt, ok["draft_logits"], ok["draft_tokens"], ok["uniforms"], 1.0,
+                             ok["accept_len"], ok["out_tokens"], ok["status"],
+                             torch.zeros(16, dtype=torch.uint8))
