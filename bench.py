@@ -1,27 +1,31 @@
-"""Benchmark of the verify step on GB300.
+"""Benchmark of the speculative-decoding verify step on GB300.
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-  chain verify  B=64, gamma=5, V=32000, bf16, T=1   (softmax statistics, acceptance ballot,
-                                                     correction/bonus draw, emit)
-  tree verify   B=32 trees of 64 nodes, V=32000, bf16, greedy (argmax, path, bonus)
-  probs         the chain's 384 target rows -> fp32 probabilities, T=1
-Metric: verified positions per second (chain positions B*(gamma+1) plus tree nodes B*N), and
-achieved HBM GB/s against the measured copy bandwidth.
+Headline (the JSON line's `value`): the largest single-GPU configuration of the workload list,
+chain verification of B=256 steps of gamma=8 drafts over V=128256 bf16 logits at T=0.7 (target
+N(0, 3^2) plus a Zipf(1.1) log-prior over token ids, draft noise sigma=1). One step = one
+spec_verify_chain call over that batch: softmax statistics of all 256 x 17 rows, the
+acceptance ballot, the correction / bonus draw and the emitted tokens (two kernels: the stream
+kernel over every logit, then the finishing kernel). Metric: verified positions per second,
+B * (gamma + 1) per step, and achieved HBM GB/s against the measured copy bandwidth.
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream, max over ranks.
-The launches are captured once in CUDA graphs, exactly as the C entry points enqueue them, so
-the timed region measures the GPU work rather than Python's launch rate. The K timed steps run
-as K // 16 blocks: 16 chain calls, then 16 tree calls, then 16 probs calls (one graph each,
-CUDA events between them, which give the per-call durations over the whole timed region), and
-the K % 16 remaining steps as whole-step graphs. Inputs rotate over 6 copies, so a buffer is
-read again only after more than the L2 size (129 MB) of other traffic.
-`e2e` repeats the step through the same C entry points with inputs in pinned host memory:
-host-to-device copies of the step's inputs and device-to-host copies of all its outputs are
-inside the timed region.
+Each call reads 1.116 GB of logits, more than the L2 size (129 MB), so no input is served from
+L2 between steps (two input copies alternate all the same).
 
---impl reference times the CPU oracle (test infrastructure, single-threaded C, fp64) on a
-bounded row sample of the same workload each step.
+`rows`: every configuration of the workload list (and the probability and drafter-side
+helpers), each timed independently of --steps: one CUDA graph of at least 10 back-to-back calls
+over enough rotated input copies that a buffer is read again only after more than three L2
+sizes of other traffic, replayed until at least 50 calls are timed; CUDA events around each
+replay; the median per-call time over the replays.
+
+`e2e`: the headline step through the same C entry point with inputs in pinned host memory;
+host-to-device copies of the step's inputs and device-to-host copies of its outputs are inside
+the timed region (three streams pipeline consecutive steps).
+
+`cpu_baseline` / --impl reference: the CPU oracle (test infrastructure: single-threaded C,
+fp64) timed on a bounded sample of the headline's batch rows; the same sample's GPU outputs are
+checked against the oracle (the parity tests' per-draw rule) and the result reported.
 """
 
 from __future__ import annotations
@@ -30,7 +34,9 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -45,24 +51,25 @@ if ROOT not in sys.path:
 METRIC = "verified positions/sec and achieved HBM GB/s (% of GB300 peak) on 1 GPU"
 UNIT = "positions/s"
 L2_BYTES = 129e6
-ROT = 6
-BLOCK = 16
-KINDS = ("chain", "tree", "probs")
-WORKLOAD = ("verify step: chain B=64 gamma=5 V=32000 bf16 T=1 + tree B=32 N=64 V=32000 bf16 "
-            "greedy + probs 384x32000 bf16->fp32 T=1")
+MARGIN = 1e-5
+WORKLOAD = ("chain verify B=256 gamma=8 V=128256 bf16 T=0.7 (target N(0,3^2) - 1.1 ln(k+1), "
+            "draft noise sigma=1): workload configuration 3")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--rows", default="all",
+                    help="'all', 'none', or a comma list of row names (see ROW_NAMES)")
+    ap.add_argument("--min-calls", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-helpers", action="store_true")
     ap.add_argument("--seed-offset", type=int, default=0)
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -109,58 +116,32 @@ def sum_over_ranks(x, world, device="cpu"):
     return float(t.item())
 
 
-# ------------------------------------------------------------------ workload
+# ------------------------------------------------------------------ the headline workload
 
-def make_inputs(seed_offset=0):
-    from workloads import chain_32k, tree_32k
-    ci = chain_32k(seed=2 + 100 * seed_offset)
-    ti = tree_32k(seed=4 + 100 * seed_offset)
-    return ci, ti
+def headline_inputs(seed_offset=0):
+    from workloads import chain_128k
+    return chain_128k(sigma=1.0) if seed_offset == 0 else chain_128k(seed=3 + 100 * seed_offset,
+                                                                    sigma=1.0)
 
 
 def config_for(world):
     """The JSON line's config: the workload, its batch over all replicas, and how L2 reuse is
     avoided between timed steps."""
-    return {"workload": WORKLOAD, "global_batch": world * (64 + 32),
+    return {"workload": WORKLOAD, "global_batch": world * 256,
             "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2": f"inputs rotated over {ROT} copies (> L2 size of traffic between reuses)",
-            "order": f"timed steps run as blocks of {BLOCK} calls of each kind"}
+            "l2": "each step reads 1.116 GB of logits (> L2 size); two input copies alternate"}
 
 
-def step_bytes(ci, ti):
-    """Algorithmic bytes of one step per kernel: every logit read once, small int/fp32 arrays
-    read or written once, the probabilities written once."""
-    B, g, V = ci.B, ci.gamma, ci.V
-    chain = (ci.target.nbytes + ci.draft.nbytes + ci.tokens.nbytes + ci.uniforms.nbytes
-             + 4 * B + 4 * B * (g + 1))
-    tree = ti.target.nbytes + ti.parents.nbytes + ti.tokens.nbytes + 4 * ti.B * (2 * ti.N + 1)
-    probs = ci.target.nbytes + 4 * ci.target.size
-    return {"chain": chain, "tree": tree, "probs": probs}
+def chain_bytes(B, gamma, V, esz, greedy=False):
+    """Algorithmic bytes of a chain call: every logit read once (target rows, and the draft rows
+    unless greedy), drafts and uniforms read once, accept_len and out_tokens written once."""
+    rows = (gamma + 1) + (0 if greedy else gamma)
+    return B * rows * V * esz + 4 * B * gamma + (0 if greedy else 4 * B * (gamma + 1)) + \
+        4 * B + 4 * B * (gamma + 1)
 
 
-def launch_shapes(ci, ti):
-    """Per call of the step: the kernels it launches (from the library's own launch plan)."""
-    import speculative_decoding_verification_78_gb300 as sv
-    out = {}
-    for kind, code, B, rows, V, T, mode in (
-            ("chain", sv.SPEC_CALL_CHAIN, ci.B, 2 * ci.gamma + 1, ci.V, ci.temperature,
-             "chain-sample"),
-            ("tree", sv.SPEC_CALL_TREE, ti.B, ti.N, ti.V, 0.0, "tree"),
-            ("probs", sv.SPEC_CALL_PROBS, ci.B * (ci.gamma + 1), 1, ci.V, 1.0, "probs")):
-        k, grid, cluster = sv.spec_launch_shape(code, B, rows, V, sv.SPEC_BF16, T)
-        shape = f"{grid} CTAs" + (f", clusters of {cluster}" if cluster > 1 else "")
-        if k == 1:
-            names = f"probs_resident<bf16> ({shape})"
-        else:
-            fin = {"chain-sample": "finish_chain_sample<bf16>", "tree": "finish_cta<bf16, tree>",
-                   "probs": "finish_probs<bf16>"}[mode]
-            names = f"stream_kernel<bf16, {mode}> + {fin} ({shape})"
-        out[kind] = {"launches": k, "kernels": names}
-    return out
-
-
-def positions(ci, ti):
-    return ci.B * (ci.gamma + 1) + ti.B * ti.N
+def tree_bytes(B, N, V, esz):
+    return B * N * V * esz + 8 * B * N + 4 * B * (2 * N + 1)
 
 
 def measured_peak():
@@ -185,18 +166,31 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
-    """dram read+write bytes per launch of `kernel` from the committed ncu summary, if it was
-    taken on the current kernel source."""
+def ncu_traffic(key):
+    """dram read+write bytes per call of `key` from the committed ncu summary, if it was taken
+    on the current kernel sources."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         if d.get("kernel_source_hash") != kernel_source_hash():
             return None
-        return d["per_launch_bytes"].get(kernel)
+        return d["per_call_bytes"].get(key)
     except Exception:
         return None
+
+
+def host_info():
+    model = platform.processor() or platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    return {"cpu_model": model, "nproc": os.cpu_count(), "machine": platform.machine()}
 
 
 # ------------------------------------------------------------------ clocks
@@ -213,12 +207,13 @@ class ClockSampler:
 
     def start(self):
         import tempfile
-        self.path = tempfile.mktemp(suffix=".csv")
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -227,14 +222,14 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -244,6 +239,7 @@ class ClockSampler:
                 try:
                     sm.append(float(parts[1]))
                     smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
                 except ValueError:
                     continue
                 for n, v in zip(names, parts[5:9]):
@@ -252,315 +248,384 @@ class ClockSampler:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ calls
+
+class ChainCall:
+    """Pre-marshalled spec_verify_chain calls over `ncopies` device copies of one chain input
+    (target, draft, tokens, uniforms), each copy with its own outputs and workspace."""
+
+    def __init__(self, lib, sv, inputs, dtype, T, stream, ncopies, device):
+        import torch
+        tgt, drf, tok, uni = inputs
+        B, g1, V = tgt.shape
+        self.B, self.gamma, self.V, self.T, self.dtype = B, g1 - 1, V, T, dtype
+        self.lib, self.stream = lib, stream
+        greedy = T == 0
+        vp = ctypes.c_void_p
+        sp = vp(stream.cuda_stream)
+        self.copies, self.args = [], []
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        for k in range(ncopies):
+            c = dict(tgt=tgt if k == 0 else tgt.clone(),
+                     drf=drf if (k == 0 or greedy) else drf.clone(), tok=tok, uni=uni,
+                     acc=torch.empty(B, dtype=torch.int32, device=device),
+                     out=torch.empty((B, g1), dtype=torch.int32, device=device),
+                     ws=sv.new_workspace(B, 2 * (g1 - 1) + 1, V, dtype, device))
+            self.copies.append(c)
+            self.args.append((vp(c["tgt"].data_ptr()),
+                              None if greedy or not c["drf"].numel() else vp(c["drf"].data_ptr()),
+                              dtype, vp(tok.data_ptr()) if tok.numel() else None,
+                              vp(uni.data_ptr()), B, g1 - 1, V, ctypes.c_float(T),
+                              vp(c["acc"].data_ptr()), vp(c["out"].data_ptr()),
+                              vp(self.status.data_ptr()), vp(c["ws"].data_ptr()),
+                              c["ws"].numel(), sp))
+        # the copies were made on the current stream; the calls run on `stream`
+        torch.cuda.synchronize()
+
+    def __call__(self, k):
+        rc = self.lib.spec_verify_chain(*self.args[k % len(self.args)])
+        if rc:
+            raise RuntimeError(f"spec_verify_chain failed: {rc}")
+
+
+def copies_for(nbytes):
+    """Input copies to rotate over so that a buffer is read again only after more than three
+    L2 sizes of other traffic."""
+    return max(1, min(128, math.ceil(3 * L2_BYTES / max(1, nbytes)) + 1))
+
+
+def time_calls(call, ncopies, stream, min_calls=50):
+    """Median per-call time (seconds) of `call(k)` over copies k = 0, 1, ...: a CUDA graph of
+    L = max(10, ncopies) consecutive calls, replayed until at least min_calls calls were timed,
+    CUDA events around each replay on the launching stream. Returns (median, min, max, calls)."""
+    import torch
+    L = max(10, ncopies)
+    with torch.cuda.stream(stream):
+        for k in range(ncopies):
+            call(k)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for j in range(L):
+            call(j % ncopies)
+    reps = max(5, math.ceil(min_calls / L))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        g.replay()                                   # warm
+        for e0, e1 in evs:
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    per = [e0.elapsed_time(e1) * 1e-3 / L for e0, e1 in evs]
+    del g
+    return statistics.median(per), min(per), max(per), reps * L
+
+
+# ------------------------------------------------------------------ the per-configuration rows
+
+ROW_NAMES = ("cfg1_chain_tiny", "cfg2_chain_32k", "cfg3_sigma0.25", "cfg3_sigma1", "cfg3_sigma4",
+             "cfg4_tree_32k", "cfg5_B1_g3", "cfg5_B1_g7", "cfg5_B16_g3", "cfg5_B16_g7",
+             "cfg5_B128_g3", "cfg5_B128_g7", "cfg5_B1024_g3", "cfg5_B1024_g7", "probs_32k")
+
+
+def _dev(a, device):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def row_inputs(name, device):
+    """(description, chain inputs as device tensors (target, draft, tokens, uniforms), dtype,
+    temperature) of a chain row; tree and probs rows are handled by their own callers. The
+    large configurations are drawn on the device (workloads.device), the others on the host
+    (workloads.synthetic, the generators the parity tests use)."""
+    from workloads import BF16, F32, chain_32k, chain_tiny, sweep_152k
+    from workloads.device import device_chain
+    if name == "cfg1_chain_tiny":
+        ci = chain_tiny()
+        return ("1000 x 4 x 1000 fp32, T=1 (1000 independent steps, one call)",
+                tuple(_dev(a, device) for a in (ci.target, ci.draft, ci.tokens, ci.uniforms)),
+                F32, 1.0)
+    if name == "cfg2_chain_32k":
+        ci = chain_32k()
+        return ("64 x 5 x 32000 bf16, T=1",
+                tuple(_dev(a, device) for a in (ci.target, ci.draft, ci.tokens, ci.uniforms)),
+                BF16, 1.0)
+    if name.startswith("cfg3_sigma"):
+        sigma = float(name[len("cfg3_sigma"):])
+        return (f"256 x 8 x 128256 bf16, T=0.7, sigma={sigma} (drawn on the device)",
+                device_chain(256, 8, 128256, BF16, 0.7, 3.0, sigma, zipf_s=1.1,
+                             seed=300 + int(100 * sigma), device=device), BF16, 0.7)
+    if name.startswith("cfg5_"):
+        B, g = (int(x[1:]) for x in name[len("cfg5_"):].split("_"))
+        if B <= 16:
+            ci = sweep_152k(B=B, gamma=g)
+            return (f"{B} x {g} x 152064 fp32, T=1",
+                    tuple(_dev(a, device) for a in (ci.target, ci.draft, ci.tokens,
+                                                    ci.uniforms)), F32, 1.0)
+        return (f"{B} x {g} x 152064 fp32, T=1 (drawn on the device)",
+                device_chain(B, g, 152064, F32, 1.0, 2.0, 0.5, seed=500 + 10 * B + g,
+                             device=device), F32, 1.0)
+    raise KeyError(name)
+
+
+def measure_rows(names, lib, sv, device, stream, peak, min_calls):
+    import torch
+    from workloads import BF16, chain_32k, tree_32k
+    rows = {}
+    for name in names:
+        torch.cuda.nvtx.range_push(f"row {name}")
+        if name == "cfg4_tree_32k":
+            ti = tree_32k()
+            nbytes = tree_bytes(ti.B, ti.N, ti.V, 2)
+            nc = copies_for(ti.target.nbytes)
+            tt = [_dev(ti.target, device) for _ in range(nc)]
+            par, tok = _dev(ti.parents, device), _dev(ti.tokens, device)
+            acc = torch.empty(ti.B, dtype=torch.int32, device=device)
+            path = torch.empty((ti.B, ti.N), dtype=torch.int32, device=device)
+            out = torch.empty((ti.B, ti.N), dtype=torch.int32, device=device)
+            st = torch.zeros(1, dtype=torch.int32, device=device)
+            ws = sv.new_workspace(ti.B, ti.N, ti.V, BF16, device)
+            vp = ctypes.c_void_p
+            args = [(vp(t.data_ptr()), BF16, vp(par.data_ptr()), vp(tok.data_ptr()), ti.B, ti.N,
+                     ti.V, vp(acc.data_ptr()), vp(path.data_ptr()), vp(out.data_ptr()),
+                     vp(st.data_ptr()), vp(ws.data_ptr()), ws.numel(),
+                     vp(stream.cuda_stream)) for t in tt]
+            call = lambda k: lib.spec_verify_tree(*args[k % nc])
+            desc, pos = "32 trees x 64 nodes x 32000 bf16, greedy", ti.B * ti.N
+            torch.cuda.synchronize()
+        elif name == "probs_32k":
+            ci = chain_32k()
+            x = ci.target.reshape(-1, ci.V)
+            nbytes = x.nbytes + 4 * x.size
+            nc = copies_for(nbytes)
+            xs = [_dev(x, device) for _ in range(nc)]
+            outs = [torch.empty(x.shape, dtype=torch.float32, device=device) for _ in range(nc)]
+            st = torch.zeros(1, dtype=torch.int32, device=device)
+            ws = sv.new_workspace(x.shape[0], 1, ci.V, BF16, device)
+            vp = ctypes.c_void_p
+            args = [(vp(xs[k].data_ptr()), BF16, x.shape[0], ci.V, ctypes.c_float(1.0),
+                     vp(outs[k].data_ptr()), vp(st.data_ptr()), vp(ws.data_ptr()), ws.numel(),
+                     vp(stream.cuda_stream)) for k in range(nc)]
+            call = lambda k: lib.spec_probs(*args[k % nc])
+            desc, pos = "384 x 32000 bf16 -> fp32 probabilities, T=1", 0
+            torch.cuda.synchronize()
+        else:
+            desc, inputs, dtype, T = row_inputs(name, device)
+            B, g1, V = inputs[0].shape
+            esz = 2 if dtype == BF16 else 4
+            nbytes = chain_bytes(B, g1 - 1, V, esz, greedy=(T == 0))
+            nc = copies_for(nbytes)
+            call = ChainCall(lib, sv, inputs, dtype, T, stream, nc, device)
+            st = call.status
+            pos = B * g1
+        med, lo, hi, n = time_calls(call, nc, stream, min_calls)
+        torch.cuda.synchronize()
+        if int(st.item()) != 0:
+            raise RuntimeError(f"{name}: device-side error {int(st.item())}")
+        gbs = nbytes / med / 1e9
+        rows[name] = {"shape": desc, "calls_timed": n, "input_copies": nc,
+                      "us_median": med * 1e6, "us_min": lo * 1e6, "us_max": hi * 1e6,
+                      "algorithmic_bytes": nbytes, "GBps": gbs, "frac_of_peak": gbs / peak}
+        if pos:
+            rows[name]["verified_positions_per_call"] = pos
+            rows[name]["positions_per_s"] = pos / med
+        torch.cuda.nvtx.range_pop()
+        del call
+        torch.cuda.empty_cache()
+    return rows
+
+
+def helpers(device, peak, stream, min_calls):
+    """The drafter-side helpers on configuration 2's data: spec_sample of its 320 draft rows,
+    spec_topk (k = 4) of the same rows, spec_tree_mask of configuration 4's 32 trees."""
+    import torch
+    import speculative_decoding_verification_78_gb300 as sv
+    from speculative_decoding_verification_78_gb300 import _binding as B_
+    from workloads import chain_32k, make_uniforms, tree_32k
+    ci, ti = chain_32k(), tree_32k()
+    V = ci.V
+    drafts = _dev(ci.draft.reshape(-1, V), device)
+    rows = drafts.shape[0]
+    nc = copies_for(drafts.numel() * 2)
+    copies = [drafts.clone() for _ in range(nc)]
+    u = torch.from_numpy(make_uniforms(np.random.default_rng(7), (rows,))).to(device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    tok = torch.empty(rows, dtype=torch.int32, device=device)
+    idx = torch.empty((rows, 4), dtype=torch.int32, device=device)
+    par = _dev(ti.parents, device)
+    mask = torch.empty((ti.B, ti.N, (ti.N + 31) // 32), dtype=torch.int32, device=device)
+    ws = sv.new_workspace(rows, 1, V, sv.SPEC_BF16, device)
+    ws4 = sv.new_workspace(rows, 4, V, sv.SPEC_BF16, device)
+    torch.cuda.synchronize()   # inputs made on the current stream, calls on `stream`
+    calls = {
+        "sample": (lambda k: B_.spec_sample(copies[k % nc], ci.temperature, u, tok, st, ws,
+                                            stream), rows * V * 2 + rows * 8, nc),
+        "topk": (lambda k: B_.spec_topk(copies[k % nc], 4, idx, st, ws4, stream),
+                 rows * V * 2 + rows * 16, nc),
+        "tree_mask": (lambda k: B_.spec_tree_mask(par, mask, st, stream),
+                      ti.B * ti.N * 4 + ti.B * ti.N * ((ti.N + 31) // 32) * 4, 1),
+    }
+    res = {}
+    for name, (fn, nbytes, ncop) in calls.items():
+        med, lo, hi, n = time_calls(fn, ncop, stream, min_calls)
+        res[name] = {"us_median": med * 1e6, "calls_timed": n, "algorithmic_bytes": nbytes,
+                     "GBps": nbytes / med / 1e9, "frac_of_peak": nbytes / med / 1e9 / peak}
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "device-side error in the helpers"
+    res["shapes"] = {"sample": f"{rows} x {V} bf16, T = {ci.temperature}",
+                     "topk": f"{rows} x {V} bf16, k = 4", "tree_mask": f"{ti.B} x {ti.N}"}
+    return res
 
 
 # ------------------------------------------------------------------ our arm
 
-class Runner:
-    """Pre-marshalled C calls of one step on device buffers (copy `k` of each input)."""
-
-    def __init__(self, ci, ti, device):
-        import torch
-        import speculative_decoding_verification_78_gb300 as sv
-        from speculative_decoding_verification_78_gb300._binding import load_library
-        self.torch, self.sv = torch, sv
-        self.lib = load_library()
-        self.ci, self.ti = ci, ti
-        dev = device
-
-        def d(a):
-            a = np.ascontiguousarray(a)
-            if a.dtype == np.uint16:
-                return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
-            return torch.from_numpy(a).to(dev)
-
-        self.d = d
-        self.copies = []
-        for _ in range(ROT):
-            self.copies.append(dict(ct=d(ci.target), cd=d(ci.draft), tt=d(ti.target)))
-        B, g, V = ci.B, ci.gamma, ci.V
-        # per input copy: the small inputs and all outputs too, so that copies can overlap
-        for c in self.copies:
-            c.update(tok=d(ci.tokens), uni=d(ci.uniforms), par=d(ti.parents),
-                     ttok=d(ti.tokens),
-                     acc=torch.empty(B, dtype=torch.int32, device=dev),
-                     out=torch.empty((B, g + 1), dtype=torch.int32, device=dev),
-                     tacc=torch.empty(ti.B, dtype=torch.int32, device=dev),
-                     tpath=torch.empty((ti.B, ti.N), dtype=torch.int32, device=dev),
-                     tout=torch.empty((ti.B, ti.N), dtype=torch.int32, device=dev),
-                     probs=torch.empty(ci.target.shape, dtype=torch.float32, device=dev))
-        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        rows = B * (g + 1)
-        # one workspace per copy and call: calls of different steps may overlap in e2e
-        self.ws_c = [sv.new_workspace(B, 2 * g + 1, V, sv.SPEC_BF16, dev) for _ in range(ROT)]
-        self.ws_t = [sv.new_workspace(ti.B, ti.N, ti.V, sv.SPEC_BF16, dev) for _ in range(ROT)]
-        self.ws_p = [sv.new_workspace(rows, 1, V, sv.SPEC_BF16, dev) for _ in range(ROT)]
-        self.stream = torch.cuda.Stream(dev)
-        vp = ctypes.c_void_p
-        sp = vp(self.stream.cuda_stream)
-        self.args = []
-        for k in range(ROT):
-            c = self.copies[k]
-            # probs reads the target rows of the chain call just made on the same copy
-            chain = (vp(c["ct"].data_ptr()), vp(c["cd"].data_ptr()), sv.SPEC_BF16,
-                     vp(c["tok"].data_ptr()), vp(c["uni"].data_ptr()), B, g, V,
-                     ctypes.c_float(ci.temperature), vp(c["acc"].data_ptr()),
-                     vp(c["out"].data_ptr()), vp(self.status.data_ptr()),
-                     vp(self.ws_c[k].data_ptr()), self.ws_c[k].numel(), sp)
-            tree = (vp(c["tt"].data_ptr()), sv.SPEC_BF16, vp(c["par"].data_ptr()),
-                    vp(c["ttok"].data_ptr()), ti.B, ti.N, ti.V, vp(c["tacc"].data_ptr()),
-                    vp(c["tpath"].data_ptr()), vp(c["tout"].data_ptr()),
-                    vp(self.status.data_ptr()), vp(self.ws_t[k].data_ptr()),
-                    self.ws_t[k].numel(), sp)
-            probs = (vp(c["ct"].data_ptr()), sv.SPEC_BF16, rows, V, ctypes.c_float(1.0),
-                     vp(c["probs"].data_ptr()), vp(self.status.data_ptr()),
-                     vp(self.ws_p[k].data_ptr()), self.ws_p[k].numel(), sp)
-            self.args.append((chain, tree, probs))
-
-    def call(self, kind, k):
-        chain, tree, probs = self.args[k]
-        lib = self.lib
-        if kind == "chain":
-            rc = lib.spec_verify_chain(*chain)
-        elif kind == "tree":
-            rc = lib.spec_verify_tree(*tree)
-        else:
-            rc = lib.spec_probs(*probs)
-        if rc:
-            raise RuntimeError(f"{kind} call failed: {rc}")
-
-    def capture(self):
-        """CUDA graphs, captured once, holding the launches exactly as the C entry points
-        enqueue them: per input copy k, a whole step (chain, tree and probs calls); and per kind
-        of call, BLOCK consecutive calls of that kind over copies 0, 1, ... (mod ROT)."""
-        torch = self.torch
-        with torch.cuda.stream(self.stream):
-            for k in range(ROT):
-                for kind in KINDS:
-                    self.call(kind, k)
-        torch.cuda.synchronize()
-        self.step_graphs, self.block_graphs = {}, {}
-        for k in range(ROT):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=self.stream):
-                for kind in KINDS:
-                    self.call(kind, k)
-            self.step_graphs[k] = g
-        for kind in KINDS:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=self.stream):
-                for j in range(BLOCK):
-                    self.call(kind, j % ROT)
-            self.block_graphs[kind] = g
-        torch.cuda.synchronize()
-
-    def step(self, i):
-        self.step_graphs[i % ROT].replay()
+def accept_stats(acc, gamma):
+    acc = acc[acc >= 0].astype(np.float64)
+    decisions = np.minimum(acc + 1, gamma).sum()
+    return {"mean_accept_len": float(acc.mean()),
+            "acceptance_rate": float(acc.sum() / decisions) if decisions else None,
+            "emitted_tokens_per_step": int((acc + 1).sum())}
 
 
 def run_ours(args, rank, world, local):
     import torch
+    import speculative_decoding_verification_78_gb300 as sv
+    from speculative_decoding_verification_78_gb300._binding import load_library
+    from workloads import BF16
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    ci, ti = make_inputs(args.seed_offset + rank)
-    r = Runner(ci, ti, device)
-    K = args.steps
-    r.capture()
-    with torch.cuda.stream(r.stream):
-        for i in range(args.warmup):
-            r.step(i)
-    torch.cuda.synchronize()
-    assert int(r.status.item()) == 0, "device-side error in warm-up"
+    lib = load_library()
+    ci = headline_inputs(args.seed_offset + rank)
+    stream = torch.cuda.Stream(device)
+    inputs = tuple(_dev(a, device) for a in (ci.target, ci.draft, ci.tokens, ci.uniforms))
+    head = ChainCall(lib, sv, inputs, BF16, ci.temperature, stream, 2, device)
+    K, W = args.steps, args.warmup
+    if K < 1 or W < 0:
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
+    peak, peak_kind = measured_peak()
 
-    # K steps of work: K // BLOCK blocks, each the block graph of every kind of call (BLOCK
-    # chain calls, then BLOCK tree calls, then BLOCK probs calls, with CUDA events between
-    # them), then the K % BLOCK remaining steps as whole-step graphs
-    nblk, rem = divmod(K, BLOCK)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KINDS) + 1)]
-           for _ in range(nblk)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            head(i)
+    torch.cuda.synchronize()
+    assert int(head.status.item()) == 0, "device-side error in warm-up"
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    host0 = time.perf_counter()
-    with torch.cuda.stream(r.stream):
-        t0.record(r.stream)
-        for b in range(nblk):
-            for j, kind in enumerate(KINDS):
-                evs[b][j].record(r.stream)
-                r.block_graphs[kind].replay()
-            evs[b][len(KINDS)].record(r.stream)
-        for i in range(rem):
-            r.step(i)
-        t1.record(r.stream)
-    host_issue = time.perf_counter() - host0
+    torch.cuda.nvtx.range_push("timed steps")
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(K):
+            head(i)
+        t1.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
-    clk = clocks.stop()
     elapsed = t0.elapsed_time(t1) * 1e-3
     elapsed = max_over_ranks(elapsed, world, device)
-    assert int(r.status.item()) == 0, "device-side error in timed steps"
+    assert int(head.status.item()) == 0, "device-side error in timed steps"
 
-    per_kernel = {kind: [e[j].elapsed_time(e[j + 1]) * 1e-3 / BLOCK for e in evs]
-                  for j, kind in enumerate(KINDS)}
-    if args.steps < BLOCK:
-        raise SystemExit(f"--steps must be at least {BLOCK} (one block of each call)")
-    avg = {k: float(np.mean(v)) for k, v in per_kernel.items()}
-    nbytes = step_bytes(ci, ti)
-    peak, peak_kind = measured_peak()
-    rows = {}
-    for k in ("chain", "tree", "probs"):
-        gbs = nbytes[k] / avg[k] / 1e9
-        rows[k] = {"us_per_launch": avg[k] * 1e6, "algorithmic_bytes": nbytes[k],
-                   "GBps": gbs, "frac_of_peak": gbs / peak}
-    rows["chain"]["verified_positions"] = ci.B * (ci.gamma + 1)
-    rows["tree"]["verified_positions"] = ti.B * ti.N
-    dom = max(("chain", "tree", "probs"), key=lambda k: avg[k])
-    shapes = launch_shapes(ci, ti)
-    kname = shapes[dom]["kernels"]
-    pos_total = sum_over_ranks(positions(ci, ti) * K, world, device)
-    value = pos_total / elapsed
-    step_total_bytes = sum(nbytes.values())
+    B, g = ci.B, ci.gamma
+    per_call = elapsed / K
+    nbytes = chain_bytes(B, g, ci.V, 2)
+    achieved = nbytes / per_call / 1e9
+    pos_total = sum_over_ranks(B * (g + 1) * K, world, device)
+    acc0 = head.copies[0]["acc"].cpu().numpy()
+    out0 = head.copies[0]["out"].cpu().numpy()
+    k_, grid, cluster = sv.spec_launch_shape(sv.SPEC_CALL_CHAIN, B, 2 * g + 1, ci.V, BF16,
+                                             ci.temperature)
+    kname = (f"stream_kernel<bf16, chain-sample> + finish_chain_sample<bf16> ({grid} CTAs, "
+             f"clusters of {cluster})")
     out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": elapsed / K * 1e3, "higher_is_better": True,
+        "metric": METRIC, "value": pos_total / elapsed, "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": elapsed / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_for(world), positions_per_step=positions(ci, ti) * world),
-        "achieved_GBps": step_total_bytes * world * K / elapsed / 1e9 / world,
-        "roofline": {"bound": "hbm", "kernel": kname, "achieved": rows[dom]["GBps"],
-                     "peak": peak, "unit": "GB/s", "frac": rows[dom]["GBps"] / peak,
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "traffic": ncu_traffic(dom), "algorithmic_bytes": nbytes[dom]},
-        "rows": rows,
-        "gpu_launches": sum(v["launches"] for v in shapes.values()) * K,
-        "launch_shapes": shapes,
-        "clocks": clk,
-        "host_issue_us_per_step": host_issue / K * 1e6,
-        "emitted_tokens_per_step": int((r.copies[0]["acc"].cpu().numpy() + 1).sum()),
+        "config": dict(config_for(world), positions_per_step=B * (g + 1) * world),
+        "achieved_GBps": achieved,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)"
+                                     if peak_kind == "measured" else "fallback 6.8 TB/s"),
+                     "traffic": ncu_traffic("cfg3_sigma1"), "algorithmic_bytes": nbytes,
+                     "duration": "average call over the K timed steps (CUDA events)"},
+        "gpu_launches": k_ * K,
+        "launches_per_step": k_,
+        "step_stats": accept_stats(acc0, g),
     }
-    out["e2e"] = e2e(r, ci, ti, args.e2e_steps, world, device)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(ci, ti, budget_s=10.0)
+    names = ([] if args.rows == "none" else list(ROW_NAMES) if args.rows == "all"
+             else [n for n in args.rows.split(",") if n])
+    if names:
+        out["rows"] = measure_rows(names, lib, sv, device, stream, peak, args.min_calls)
     if not args.no_helpers:
-        out["helpers"] = helpers(ci, ti, device, peak, with_oracle=(rank == 0 and world == 1
-                                                                      and not args.no_cpu_baseline))
+        out["helpers"] = helpers(device, peak, stream, args.min_calls)
+    out["clocks"] = clocks.stop()
+    out["clocks"]["window"] = "warm-up, timed steps and the rows (sampled every 50 ms)"
+    if args.e2e_steps > 0:
+        out["e2e"] = e2e(lib, ci, head, args.e2e_steps, world, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(ci, acc0, out0, budget_s=10.0)
     return out
 
 
-def helpers(ci, ti, device, peak, with_oracle):
-    """The drafter-side helpers on the same data, outside the step: spec_sample of the chain's
-    320 draft rows, spec_topk (k = 4) of the same rows, spec_tree_mask of the 32 trees. Each is
-    timed as one CUDA graph of 32 back-to-back calls over 6 rotated input copies (CUDA events
-    around it); the oracle's time per call comes from a bounded sample of rows."""
+def e2e(lib, ci, head, steps, world, device):
+    """The headline step through the same C entry point with HOST inputs: every step copies its
+    inputs from pinned host memory to the device and its outputs back, inside the timed region.
+    Three streams pipeline consecutive steps: the host-to-device copies of step i+1 and the
+    device-to-host copies of step i-1 overlap the kernels of step i (two device copies of
+    inputs, outputs and workspace in rotation)."""
     import torch
-    import speculative_decoding_verification_78_gb300 as sv
-    from speculative_decoding_verification_78_gb300 import _binding as B_
-    V = ci.V
-    drafts = torch.from_numpy(ci.draft.reshape(-1, V).view(np.int16)).to(device) \
-        .view(torch.bfloat16)
-    rows = drafts.shape[0]
-    copies = [drafts.clone() for _ in range(ROT)]
-    rng = np.random.default_rng(7)
-    from workloads import make_uniforms
-    u_h = make_uniforms(rng, (rows,))
-    u = torch.from_numpy(u_h).to(device)
-    st = torch.zeros(1, dtype=torch.int32, device=device)
-    tok = torch.empty(rows, dtype=torch.int32, device=device)
-    idx = torch.empty((rows, 4), dtype=torch.int32, device=device)
-    par = torch.from_numpy(ti.parents).to(device)
-    mask = torch.empty((ti.B, ti.N, (ti.N + 31) // 32), dtype=torch.int32, device=device)
-    ws = sv.new_workspace(rows, 1, V, sv.SPEC_BF16, device)
-    ws4 = sv.new_workspace(rows, 4, V, sv.SPEC_BF16, device)
-    stream = torch.cuda.Stream(device)
-    calls = {
-        "sample": (lambda k: B_.spec_sample(copies[k % ROT], ci.temperature, u, tok, st, ws,
-                                            stream), rows * V * 2 + rows * 8),
-        "topk": (lambda k: B_.spec_topk(copies[k % ROT], 4, idx, st, ws4, stream),
-                 rows * V * 2 + rows * 16),
-        "tree_mask": (lambda k: B_.spec_tree_mask(par, mask, st, stream),
-                      ti.B * ti.N * 4 + ti.B * ti.N * ((ti.N + 31) // 32) * 4),
-    }
-    res = {}
-    for name, (fn, nbytes) in calls.items():
-        with torch.cuda.stream(stream):
-            for k in range(ROT):
-                if fn(k):
-                    raise RuntimeError(f"{name} call failed")
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(32):
-                fn(k)
-        ts = []
-        for _ in range(10):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                g.replay()
-                e1.record(stream)
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1) * 1e-3 / 32)
-        t = float(np.median(ts))
-        res[name] = {"us_per_call": t * 1e6, "algorithmic_bytes": nbytes,
-                     "GBps": nbytes / t / 1e9, "frac_of_peak": nbytes / t / 1e9 / peak}
-    assert int(st.item()) == 0, "device-side error in the helpers"
-    res["shapes"] = {"sample": f"{rows} x {V} bf16, T = {ci.temperature}",
-                     "topk": f"{rows} x {V} bf16, k = 4", "tree_mask": f"{ti.B} x {ti.N}"}
-    if with_oracle:
-        import oracle
-        from workloads import BF16
-        dh = ci.draft.reshape(-1, V)
-        t0 = time.perf_counter()
-        oracle.sample(dh[:32], BF16, u_h[:32], ci.temperature)
-        res["sample"]["oracle_us_per_call"] = (time.perf_counter() - t0) / 32 * rows * 1e6
-        t0 = time.perf_counter()
-        oracle.topk(dh[:8], BF16, 4)
-        res["topk"]["oracle_us_per_call"] = (time.perf_counter() - t0) / 8 * rows * 1e6
-        t0 = time.perf_counter()
-        oracle.tree_mask(ti.parents)
-        res["tree_mask"]["oracle_us_per_call"] = (time.perf_counter() - t0) * 1e6
-        res["oracle_sample"] = "32 / 8 / 32 rows or trees timed on one host core, scaled"
-    return res
 
+    def pin(a):
+        a = np.ascontiguousarray(a)
+        t = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
+             else torch.from_numpy(a))
+        return t.pin_memory()
 
-def e2e(r, ci, ti, steps, world, device):
-    """The step through the same C entry points with HOST inputs: every step copies its inputs
-    from pinned host memory to the device and all its outputs back, inside the timed region.
-    Three streams pipeline consecutive steps: host-to-device copies of step i+1 and
-    device-to-host copies of step i-1 overlap the kernels of step i (each step uses its own
-    device copy of inputs, outputs and workspaces, ROT of them in rotation)."""
-    import torch
-    pin = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
-                     if a.dtype == np.uint16 else torch.from_numpy(a)).pin_memory()
-    host_in = dict(ct=pin(ci.target), cd=pin(ci.draft), tt=pin(ti.target), tok=pin(ci.tokens),
-                   uni=pin(ci.uniforms), par=pin(ti.parents), ttok=pin(ti.tokens))
-    c0 = r.copies[0]
-    host_out = {k: torch.empty_like(c0[k], device="cpu").pin_memory()
-                for k in ("acc", "out", "tacc", "tpath", "tout", "probs")}
-    bi = sum(t.numel() * t.element_size() for t in host_in.values())
+    host_in = dict(tgt=pin(ci.target), drf=pin(ci.draft))
+    small = dict(tok=pin(ci.tokens), uni=pin(ci.uniforms))
+    c0 = head.copies[0]
+    host_out = {k: torch.empty_like(c0[k], device="cpu").pin_memory() for k in ("acc", "out")}
+    bi = sum(t.numel() * t.element_size() for t in list(host_in.values()) + list(small.values()))
     bo = sum(t.numel() * t.element_size() for t in host_out.values())
-    h2d, d2h, ks = torch.cuda.Stream(), torch.cuda.Stream(), r.stream
-    ev_in = [torch.cuda.Event() for _ in range(ROT)]
-    ev_k = [torch.cuda.Event() for _ in range(ROT)]
-    ev_out = [torch.cuda.Event() for _ in range(ROT)]
-    lib = r.lib
+    n = len(head.copies)
+    # per copy: its own small inputs too (the headline's copies share tokens and uniforms)
+    dsmall = [dict(tok=torch.empty_like(c0["tok"]), uni=torch.empty_like(c0["uni"]))
+              for _ in range(n)]
+    vp = ctypes.c_void_p
+    args = []
+    for k, c in enumerate(head.copies):
+        a = list(head.args[k])
+        a[3] = vp(dsmall[k]["tok"].data_ptr())
+        a[4] = vp(dsmall[k]["uni"].data_ptr())
+        args.append(tuple(a))
+    h2d, d2h, ks = torch.cuda.Stream(), torch.cuda.Stream(), head.stream
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_k = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
 
     def one(i):
-        k = i % ROT
-        c = r.copies[k]
+        k = i % n
+        c = head.copies[k]
         with torch.cuda.stream(h2d):
             h2d.wait_event(ev_k[k])           # the previous user of copy k has read its inputs
-            for name, t in host_in.items():
-                c[name].copy_(t, non_blocking=True)
+            c["tgt"].copy_(host_in["tgt"], non_blocking=True)
+            c["drf"].copy_(host_in["drf"], non_blocking=True)
+            dsmall[k]["tok"].copy_(small["tok"], non_blocking=True)
+            dsmall[k]["uni"].copy_(small["uni"], non_blocking=True)
             ev_in[k].record(h2d)
         ks.wait_event(ev_in[k])
         ks.wait_event(ev_out[k])              # its previous outputs have been copied out
-        chain, tree, probs = r.args[k]
-        rc = lib.spec_verify_chain(*chain) | lib.spec_verify_tree(*tree) | \
-            lib.spec_probs(*probs)
+        rc = lib.spec_verify_chain(*args[k])
         if rc:
             raise RuntimeError(f"verify call failed: {rc}")
         ev_k[k].record(ks)
@@ -570,7 +635,7 @@ def e2e(r, ci, ti, steps, world, device):
                 t.copy_(c[name], non_blocking=True)
             ev_out[k].record(d2h)
 
-    for i in range(2 * ROT):
+    for i in range(2 * n):
         one(i)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -580,7 +645,7 @@ def e2e(r, ci, ti, steps, world, device):
     t1.record(d2h)
     torch.cuda.synchronize()
     el = max_over_ranks(t0.elapsed_time(t1) * 1e-3, world, device)
-    pos = sum_over_ranks(positions(ci, ti) * steps, world, device)
+    pos = sum_over_ranks(ci.B * (ci.gamma + 1) * steps, world, device)
     return {"value": pos / el, "unit": UNIT, "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "steps": steps, "ms_per_step": el / steps * 1e3,
             "pipelined": "h2d / kernels / d2h on three streams, consecutive steps overlap"}
@@ -588,72 +653,105 @@ def e2e(r, ci, ti, steps, world, device):
 
 # ------------------------------------------------------------------ the oracle
 
-def oracle_step(ci, ti, crow, trow, prow):
-    """One bounded sample of the step on the CPU oracle: chain rows crow, tree rows trow, probs
-    rows prow (numpy index arrays). Returns the positions verified."""
+def oracle_rows(ci, rows):
+    """The CPU oracle (single-threaded C, fp64) on batch rows `rows` of the headline input.
+    Returns the positions verified."""
     import oracle
     from workloads import BF16
-    oracle.verify_chain(ci.target[crow], ci.draft[crow], BF16, ci.tokens[crow],
-                        ci.uniforms[crow], ci.temperature)
-    oracle.verify_tree(ti.target[trow], BF16, ti.parents[trow], ti.tokens[trow])
-    flat = ci.target.reshape(-1, ci.V)
-    oracle.probs(flat[prow], BF16, 1.0)
-    return len(crow) * (ci.gamma + 1) + len(trow) * ti.N
+    oracle.verify_chain(ci.target[rows], ci.draft[rows], BF16, ci.tokens[rows],
+                        ci.uniforms[rows], ci.temperature)
+    return len(rows) * (ci.gamma + 1)
 
 
-def cpu_baseline(ci, ti, budget_s=10.0):
-    """The oracle as it stands, single-threaded, on whole steps of the same workload, repeated
-    until about budget_s seconds of CPU work."""
-    crow, trow = np.arange(ci.B), np.arange(ti.B)
-    prow = np.arange(ci.B * (ci.gamma + 1))
-    pos, n = 0, 0
+def parity_sample(ci, rows, acc, out):
+    """The GPU outputs of batch rows `rows` against the oracle, draw by draw: decisions and
+    tokens must be the oracle's, except draws within MARGIN of a boundary, whose outcome must
+    lie in the oracle's band. Returns counts."""
+    import oracle
+    from workloads import BF16
+    d = oracle.verify_chain_detail(ci.target[rows], ci.draft[rows], BF16, ci.tokens[rows],
+                                   ci.uniforms[rows], ci.temperature, band=MARGIN)
+    g = ci.gamma
+    exact = flagged = bad = 0
+    for j, b in enumerate(rows):
+        acc_o = g
+        for i in range(g):
+            if not d["accept"][j, i]:
+                acc_o = i
+                break
+        n = int(acc[b])
+        fl = any(d["dmargin"][j, i] < MARGIN for i in range(min(acc_o + 1, g))) or \
+            d["cmargin"][j, acc_o] < MARGIN
+        flagged += int(fl)
+        same = n == acc_o and int(out[b, n]) == int(d["tok"][j, n]) and \
+            np.array_equal(out[b, :n], ci.tokens[b, :n])
+        exact += int(same)
+        if not same:
+            ok = 0 <= n <= g and all(
+                (i < n) == bool(d["accept"][j, i]) or d["dmargin"][j, i] < MARGIN
+                for i in range(min(n + 1, g)))
+            t = int(out[b, n]) if 0 <= n <= g else -1
+            ok = ok and (d["tok"][j, n] == t or (d["cmargin"][j, n] < MARGIN and
+                                                 d["lo"][j, n] <= t <= d["hi"][j, n]))
+            bad += int(not ok)
+    return {"rows": len(rows), "equal_to_oracle": exact, "rows_with_flagged_draws": flagged,
+            "outside_rule": bad}
+
+
+def cpu_baseline(ci, acc, out, budget_s=10.0):
+    """The oracle as it stands, single-threaded, on rows of the headline batch (8 at a time,
+    cycling through the batch) until about budget_s seconds of CPU work; then the GPU outputs of
+    the rows it covered are checked against the oracle."""
+    rows_done, pos, n = [], 0, 0
     t0 = time.perf_counter()
     while True:
-        pos += oracle_step(ci, ti, crow, trow, prow)
+        rows = (np.arange(8) + 8 * n) % ci.B
+        pos += oracle_rows(ci, rows)
+        rows_done.extend(rows.tolist())
         n += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
-    return {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} full steps of the same workload (chain 64 rows, tree 32 rows, probs "
-                      f"384 rows) in {el:.1f} s on one host core, fp64 C oracle"}
+    chk = sorted(set(rows_done))[:64]
+    res = {"value": pos / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"{len(rows_done)} batch rows ({n} calls of 8 rows) of the headline batch "
+                     f"in {el:.1f} s on one host core, fp64 C oracle",
+           "host": host_info()}
+    res["parity_sample"] = parity_sample(ci, np.asarray(chk), acc, out)
+    return res
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    ci, ti = make_inputs(args.seed_offset)
-    # size each step's row sample so that warm-up + timed steps take about 2 minutes
-    full = time.perf_counter()
-    oracle_step(ci, ti, np.arange(4), np.arange(2), np.arange(24))
-    t_small = time.perf_counter() - full          # 1/16 of a full step
-    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
-    frac = min(1.0, per_step_budget / (16 * t_small))
-    nc = max(1, int(round(ci.B * frac)))
-    nt = max(1, int(round(ti.B * frac)))
-    npb = max(1, int(round(ci.B * (ci.gamma + 1) * frac)))
+    ci = headline_inputs(args.seed_offset)
+    t = time.perf_counter()
+    oracle_rows(ci, np.arange(2))
+    per_row = (time.perf_counter() - t) / 2
+    # size each step's row sample so that warm-up + timed steps take about two minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    nr = int(max(1, min(ci.B, round(budget / per_row))))
 
     def rows(i):
-        return ((np.arange(nc) + i * nc) % ci.B, (np.arange(nt) + i * nt) % ti.B,
-                (np.arange(npb) + i * npb) % (ci.B * (ci.gamma + 1)))
+        return (np.arange(nr) + i * nr) % ci.B
 
     for i in range(args.warmup):
-        oracle_step(ci, ti, *rows(i))
+        oracle_rows(ci, rows(i))
     pos = 0
     t0 = time.perf_counter()
     for i in range(args.steps):
-        pos += oracle_step(ci, ti, *rows(i + args.warmup))
+        pos += oracle_rows(ci, rows(i + args.warmup))
     el = time.perf_counter() - t0
     value = pos / el
-    sample = (f"each step: {nc}/{ci.B} chain rows, {nt}/{ti.B} tree rows, {npb}/"
-              f"{ci.B * (ci.gamma + 1)} probs rows of the same workload, one host core")
+    sample = (f"each step: {nr} of the {ci.B} batch rows of the headline batch, one host core, "
+              f"fp64 C oracle")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": dict(config_for(1), positions_per_step=positions(ci, ti)),
+            "config": dict(config_for(1), positions_per_step=nr * (ci.gamma + 1)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "host": host_info()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

@@ -62,3 +62,22 @@ def test_bench_config_names_replicas(world):
     cfg = bench.config_for(world)
     assert cfg["parallelism"] == ("single" if world == 1 else f"replicas{world}")
     assert "workload" in cfg and "model" not in cfg
+
+
+def test_bench_sizes_and_rotation():
+    """Algorithmic bytes of the headline (configuration 3) and the copy rotation that keeps a
+    re-read buffer out of L2."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.chain_bytes(256, 8, 128256, 2) == (256 * 17 * 128256 * 2 + 4 * 256 * 8
+                                                    + 4 * 256 * 9 + 4 * 256 + 4 * 256 * 9)
+    assert abs(bench.chain_bytes(256, 8, 128256, 2) / 1e9 - 1.116) < 0.001
+    for nbytes in (4.26e6, 36e6, 45.06e6, 131e6, 1.116e9):
+        n = bench.copies_for(nbytes)
+        assert (n - 1) * nbytes > 3 * bench.L2_BYTES or n == 1 or n == 128
+        assert n == 1 or (n - 2) * nbytes <= 3 * bench.L2_BYTES
+    assert set(bench.ROW_NAMES) >= {"cfg1_chain_tiny", "cfg2_chain_32k", "cfg3_sigma0.25",
+                                    "cfg3_sigma1", "cfg3_sigma4", "cfg4_tree_32k",
+                                    "cfg5_B1024_g3", "cfg5_B1024_g7"}
+    a = bench.parse([])
+    assert a.steps >= 1 and a.warmup >= 3 and a.rows == "all"
