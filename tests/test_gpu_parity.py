@@ -447,3 +447,53 @@ def test_deterministic_and_workspace_reuse(orc):
         assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
         assert again[2] == 0
     compare_chain(orc, ci, first)
+
+
+# --------------------------------------------------------------------------- more chain shapes
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype,T", [
+    (1, 5, 32000, BF16, 0.7),      # one batch row
+    (3, 15, 4096, BF16, 1.3),      # 31 rows per batch row
+    (16, 2, 32000, F32, 1.0),
+    (40, 1, 8, BF16, 1.0),         # one 16-byte vector per row
+    (7, 3, 6000, F32, 0.05),       # near-greedy temperature
+])
+def test_chain_shapes_masked_and_all_accepting(orc, B, gamma, V, dtype, T):
+    """Chain shapes with masked (-inf) entries in every row and every fourth step accepting all
+    its drafts (draft == target), at an aligned and an unaligned base, against the oracle draw
+    by draw."""
+    ci = chain_32k(seed=50 + gamma, B=B, gamma=gamma, V=V, dtype=dtype, temperature=T,
+                   peaked=min(50, V // 4))
+    if V > 16:
+        t = bf16_to_f32(ci.target) if dtype == BF16 else ci.target
+        t[:, :, 3::11] = -np.inf                 # masked tokens in every row
+        ci.target = f32_to_bf16(t) if dtype == BF16 else t
+        ci.tokens[:, :] = np.where(ci.tokens % 11 == 3, (ci.tokens + 1) % V, ci.tokens)
+    ci.draft[::4] = ci.target[::4, :gamma]       # every fourth step accepts all its drafts
+    for off in (0, 1):
+        gpu = run_chain(ci, offset_elems=off)
+        assert gpu[2] == 0
+        compare_chain(orc, ci, gpu)
+        assert gpu[0][::4].min() == gamma
+
+
+def test_chain_invalid_rows_and_repeats(orc):
+    """Invalid batch rows (NaN in the bonus row, +inf in a draft row, a target row with no
+    finite value, a token out of range) report -1 and a status; the other rows are unaffected,
+    and repeated calls are bit-identical."""
+    import speculative_decoding_verification_78_gb300 as sv
+    ci = chain_32k(seed=61, B=12, gamma=5, V=4096, dtype=F32)
+    ci.target[1, 5, 100] = np.nan
+    ci.draft[2, 0, 4000] = np.inf
+    ci.target[3, 1, :] = -np.inf
+    ci.tokens[4, 3] = 4096
+    first = run_chain(ci)
+    assert first[2] in (sv.SPEC_ERR_NONFINITE, sv.SPEC_ERR_TOKEN)
+    assert list(first[0][1:5]) == [-1, -1, -1, -1] and np.all(first[1][1:5] == -1)
+    good = np.array([0] + list(range(5, 12)))
+    compare_chain(orc, ci, first, rows=good)
+    for _ in range(2):
+        again = run_chain(ci)
+        np.testing.assert_array_equal(again[0], first[0])
+        np.testing.assert_array_equal(again[1], first[1])

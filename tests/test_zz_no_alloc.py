@@ -40,7 +40,7 @@ def test_static_scratch_matches_workspace_entry_point(orc):
     point (identical outputs) and the oracle (the per-draw comparison of the parity tests)."""
     import speculative_decoding_verification_78_gb300 as sv
     greedy = chain_32k(seed=43, B=16, gamma=4, V=9000, temperature=0.0)
-    cases = [chain_32k(seed=41, B=8, gamma=5, V=32000), chain_tiny(seed=42, B=300, gamma=20),
+    cases = [chain_32k(seed=41, B=8, gamma=5, V=100000), chain_tiny(seed=42, B=300, gamma=20),
              greedy]
     for ci in cases:   # every shape takes the two-kernel path, which uses the scratch
         B, g1, V = ci.target.shape
