@@ -134,10 +134,17 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Temperature softmax of `rows` logits rows into fp32 probabilities:
+ * Temperature softmax of `rows` logits rows into fp32 probabilities: the target and draft
+ * distributions p and q that the verification step compares ("Fast Inference from Transformers
+ * via Speculative Decoding", pith.science review, "The pith" and "What carries the argument":
+ * the step works on the target's own output distribution; at temperature 0 the distribution is
+ * the greedy one-hot, as in Falcon's Figure 4):
  *   out_probs[r, k] = exp((l[r,k] - max_k l[r,k]) / T) / sum_j exp((l[r,j] - max l[r]) / T)
  * T == 0 gives the one-hot vector at the lowest-index argmax. An invalid row is written as NaN
- * and reported through *status (SPEC_ERR_NONFINITE).
+ * and reported through *status (SPEC_ERR_NONFINITE). Besides the logits, T and the output, the
+ * call takes a status word (so that invalid rows are reported as in the verify calls) and a
+ * workspace (rows too long to be held on chip take the stream kernel, whose unit partials live
+ * there).
  *
  *   logits    [rows, V]   dtype
  *   out_probs [rows, V]   fp32 out (4-byte aligned)
