@@ -57,12 +57,15 @@ def _load():
             lib.oracle_verify_chain_detail.argtypes = [vp, vp, i32, vp, vp, i64, i64, i64, dbl,
                                                        dbl, vp, vp, vp, vp, vp, vp]
             lib.oracle_verify_tree.argtypes = [vp, i32, vp, vp, i64, i64, i64, vp, vp, vp]
+            lib.oracle_verify_tree_sample.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i64,
+                                                      dbl, vp, vp, vp, vp]
             lib.oracle_sample.argtypes = [vp, i32, i64, i64, dbl, vp, vp, vp]
             lib.oracle_topk.argtypes = [vp, i32, i64, i64, i64, vp]
             lib.oracle_tree_mask.argtypes = [vp, i64, i64, vp]
             for f in (lib.oracle_probs, lib.oracle_argmax, lib.oracle_verify_chain,
                       lib.oracle_verify_chain_detail,
-                      lib.oracle_verify_tree, lib.oracle_sample, lib.oracle_topk,
+                      lib.oracle_verify_tree, lib.oracle_verify_tree_sample,
+                      lib.oracle_sample, lib.oracle_topk,
                       lib.oracle_tree_mask):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -157,6 +160,28 @@ def verify_tree(target, dtype, parents, tokens):
     rc = _load().oracle_verify_tree(_ptr(tg), dtype, _ptr(par), _ptr(tok), B, N, V, _ptr(acc),
                                     _ptr(path), _ptr(out))
     return acc, path, out, rc
+
+
+def verify_tree_sample(target, draft, dtype, parents, tokens, uniforms, temperature):
+    """Stochastic tree verify (see oracle_verify_tree_sample). uniforms [B, N]: u[b,0] the final
+    draw, u[b,i] node i's acceptance test. Returns (accept_len [B], path_nodes [B, N],
+    out_tokens [B, N], margin [B], rc)."""
+    tg = _logits(target, dtype)
+    B, N, V = tg.shape
+    dr = _logits(draft, dtype) if draft is not None else tg
+    assert dr.shape == (B, N, V)
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+    uni = (np.zeros((B, N), np.float32) if uniforms is None else
+           np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, N))
+    acc = np.empty(B, dtype=np.int32)
+    path = np.empty((B, N), dtype=np.int32)
+    out = np.empty((B, N), dtype=np.int32)
+    mg = np.empty(B, dtype=np.float64)
+    rc = _load().oracle_verify_tree_sample(_ptr(tg), _ptr(dr), dtype, _ptr(par), _ptr(tok),
+                                           _ptr(uni), B, N, V, float(temperature), _ptr(acc),
+                                           _ptr(path), _ptr(out), _ptr(mg))
+    return acc, path, out, mg, rc
 
 
 def sample(logits, dtype, uniforms, temperature):

@@ -492,6 +492,132 @@ int oracle_verify_tree(const void *target, int dtype, const int32_t *parents,
   return rc;
 }
 
+/*
+ * Batched stochastic (T > 0) tree verify: the tree's walk by sequential per-sibling rejection
+ * sampling. The pages verify Falcon's tree only greedily (Falcon review, Figure 4, "greedy
+ * (temperature=0)"); for sampling this build takes the rejection rule of chain verification
+ * ("Fast Inference from Transformers via Speculative Decoding", pith.science review, "The pith",
+ * "Desk Editor's Note": accept while u <= p/q, correct a rejection from norm(max(0, p - q)))
+ * and applies it to the siblings of a node one after another, the residual of each rejection
+ * becoming the target of the next sibling's test. When every child of a node was drafted
+ * independently from the drafter's distribution q at that node, each emitted token is an exact
+ * sample of the target given the tokens before it.
+ *   target   [B, N, V]  target logits at every node (p_i: the next token after node i's path)
+ *   draft    [B, N, V]  draft logits at every node (q_i: the distribution node i's children
+ *                       were drafted from)
+ *   parents  [B, N]     parents[b,0] = -1, 0 <= parents[b,i] < i
+ *   tokens   [B, N]     node tokens (node 0's is unused)
+ *   uniforms [B, N]     u[b,0]: the final draw; u[b,i], i >= 1: node i's acceptance test
+ * Per batch row, from cur = the root:
+ *   r = p_cur, q = q_cur;
+ *   for each child c of cur, in increasing index: x = tokens[c],
+ *     ratio = r(x) / q(x) (q(x) = 0: +inf if r(x) > 0, else 0);
+ *     u[c] <= ratio: accept c (emit x, cur = c, start again at c);
+ *     else r = norm(max(0, r - q)) (unchanged if that sums to 0);
+ *   no child accepted (or none): draw the last token from r with u[b,0] (inverse CDF, first k
+ *   whose running sum strictly exceeds u * sum(r)).
+ * T == 0 is greedy tree verification (oracle_verify_tree; draft logits and uniforms unused).
+ * Outputs as oracle_verify_tree: accept_len = accepted tokens (the final node's depth),
+ * path_nodes = root .. final node, out_tokens = accepted tokens then the drawn token, then -1.
+ * margin[B] (may be NULL): the minimum over the walk's decisions and its draw, each relative to
+ * the rounding amplification A of the residual it used: A = product over its updates of P/S
+ * (P = the previous r's mass on the new support, S = the mass of max(0, r - q)); a decision
+ * |u - ratio| / (ratio A), the draw min(c_k - t, t - c_{k-1}) / A (A = 1 with no update, as for
+ * the chain's bonus draw; one update gives the chain's P/S).
+ */
+int oracle_verify_tree_sample(const void *target, const void *draft, int dtype,
+                              const int32_t *parents, const int32_t *tokens, const float *uniforms,
+                              long B, long N, long V, double T, int32_t *accept_len,
+                              int32_t *path_nodes, int32_t *out_tokens, double *margin) {
+  if (B < 0 || N < 1 || V < 1 || !(T >= 0.0) || isinf(T)) return ORC_ERR_ARG;
+  if (T == 0.0) {
+    for (long b = 0; b < B && margin; ++b) margin[b] = INFINITY;
+    return oracle_verify_tree(target, dtype, parents, tokens, B, N, V, accept_len, path_nodes,
+                              out_tokens);
+  }
+  double *r = (double *)malloc(sizeof(double) * (size_t)V);
+  double *q = (double *)malloc(sizeof(double) * (size_t)V);
+  double *w = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!r || !q || !w) { free(r); free(q); free(w); return ORC_ERR_MEM; }
+  int rc = ORC_OK;
+  for (long b = 0; b < B; ++b) {
+    const int32_t *par = parents + (size_t)b * (size_t)N;
+    const int32_t *tok = tokens + (size_t)b * (size_t)N;
+    const float *u = uniforms + (size_t)b * (size_t)N;
+    int32_t *pn = path_nodes + (size_t)b * (size_t)N;
+    int32_t *ot = out_tokens + (size_t)b * (size_t)N;
+    for (long j = 0; j < N; ++j) { pn[j] = -1; ot[j] = -1; }
+    if (margin) margin[b] = INFINITY;
+
+    int err = ORC_OK;   /* the same validation as greedy tree verify, plus the draft rows */
+    if (par[0] != -1) err = ORC_ERR_PARENT;
+    for (long i = 1; i < N && !err; ++i)
+      if (par[i] < 0 || par[i] >= i) err = ORC_ERR_PARENT;
+    for (long i = 1; i < N && !err; ++i)
+      if (tok[i] < 0 || tok[i] >= V) err = ORC_ERR_TOKEN;
+    for (long j = 0; j < N && !err; ++j) {
+      const size_t off = ((size_t)b * (size_t)N + (size_t)j) * (size_t)V;
+      if (!row_valid(target, dtype, off, V) || !row_valid(draft, dtype, off, V))
+        err = ORC_ERR_ROW;
+    }
+    if (err) {
+      accept_len[b] = -1;
+      if (rc == ORC_OK) rc = err;
+      continue;
+    }
+
+    double mg = INFINITY;
+    long cur = 0, depth = 0;
+    pn[0] = 0;
+    for (;;) {
+      const size_t off = ((size_t)b * (size_t)N + (size_t)cur) * (size_t)V;
+      softmax_row(target, dtype, off, V, T, r);
+      softmax_row(draft, dtype, off, V, T, q);
+      double A = 1.0;
+      long next = -1;
+      for (long c = cur + 1; c < N && next < 0; ++c) {
+        if (par[c] != cur) continue;
+        const long x = tok[c];
+        double ratio = (q[x] > 0.0) ? r[x] / q[x] : (r[x] > 0.0 ? INFINITY : 0.0);
+        double uc = (double)u[c];
+        if (isfinite(ratio)) {
+          double m = fabs(uc - ratio) / fmax(ratio * A, 1e-300);
+          if (m < mg) mg = m;
+        }
+        if (uc <= ratio) { next = c; break; }
+        /* rejected: the residual becomes the target of the next sibling's test */
+        double S = 0.0, P = 0.0;
+        for (long k = 0; k < V; ++k) {
+          double d = r[k] - q[k];
+          w[k] = d > 0.0 ? d : 0.0;
+          S += w[k];
+          if (w[k] > 0.0) P += r[k];
+        }
+        if (S > 0.0) {
+          for (long k = 0; k < V; ++k) r[k] = w[k] / S;
+          A *= P / S;
+        }
+      }
+      if (next >= 0) {
+        ++depth;
+        pn[depth] = (int32_t)next;
+        ot[depth - 1] = tok[next];
+        cur = next;
+        continue;
+      }
+      double cm;
+      const long t = inverse_cdf(r, V, (double)u[0], A, &cm);
+      if (cm < mg) mg = cm;
+      ot[depth] = (int32_t)t;
+      break;
+    }
+    accept_len[b] = (int32_t)depth;
+    if (margin) margin[b] = mg;
+  }
+  free(r); free(q); free(w);
+  return rc;
+}
+
 /* ------------------------------------------------------------------ public: drafter side */
 
 /*

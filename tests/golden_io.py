@@ -88,3 +88,24 @@ def margin_cases():
             accept_len=np.asarray(c["accept_len"], dtype=np.int32),
             out_tokens=np.asarray(c["out_tokens"], dtype=np.int32).reshape(B, g + 1)))
     return out
+
+
+def tree_sample_cases():
+    """The stochastic tree-verification fixtures (one tree per case, B = 1)."""
+    with open(os.path.join(GOLDEN, "tree_sample_cases.json")) as f:
+        data = json.load(f)
+    out = []
+    for c in data["cases"]:
+        V = c["V"]
+        N = len(c["parents"])
+        out.append(dict(
+            name=c["name"], T=_rational(c["T"]), V=V,
+            target=_f32(c["target"], (1, N, V)), draft=_f32(c["draft"], (1, N, V)),
+            parents=np.asarray(c["parents"], dtype=np.int32).reshape(1, N),
+            tokens=np.asarray(c["tokens"], dtype=np.int32).reshape(1, N),
+            uniforms=np.asarray(c["uniforms"], dtype=np.float32).reshape(1, N),
+            accept_len=np.asarray([c["accept_len"]], dtype=np.int32),
+            path_nodes=np.asarray(c["path_nodes"], dtype=np.int32).reshape(1, N),
+            out_tokens=np.asarray(c["out_tokens"], dtype=np.int32).reshape(1, N),
+            margin=_rational(c["margin"])))
+    return out
