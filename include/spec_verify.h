@@ -72,8 +72,8 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 /*
  * Bytes of workspace needed by a call over B batch rows of `rows_per_b` logits rows of V
  * elements: rows_per_b = 2*gamma+1 for spec_verify_chain (any temperature), N for
- * spec_verify_tree, 1 for spec_probs and spec_sample (with B = rows), k for spec_topk (with
- * B = rows). Returns 0 for invalid arguments.
+ * spec_verify_tree, 2*N for spec_verify_tree_sample at T > 0, 1 for spec_probs and spec_sample
+ * (with B = rows), k for spec_topk (with B = rows). Returns 0 for invalid arguments.
  */
 size_t spec_workspace_bytes(int B, int rows_per_b, int V, int dtype);
 
@@ -132,6 +132,47 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
                      const int32_t *node_tokens, int B, int N, int V, int32_t *accept_len,
                      int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Stochastic (T > 0) tree verification, batched over B candidate trees of N nodes: the walk of
+ * each tree by sequential per-sibling rejection sampling. The pages verify Falcon's tree only
+ * greedily ("Falcon: ...", pith.science review, Figure 4, "greedy (temperature=0)"); for sampling
+ * this library applies chain verification's rule ("Fast Inference from Transformers via
+ * Speculative Decoding", pith.science review, "The pith", "Desk Editor's Note": accept while
+ * u <= p/q, correct a rejection from norm(max(0, p - q))) to the siblings of a node in turn:
+ *
+ *   p_j = softmax(target_logits[b, j, :] / T), q_j = softmax(draft_logits[b, j, :] / T)
+ *   (q_j: the distribution node j's children were drafted from). From the root: r = p_cur; for
+ *   each child c of the current node, in increasing index, with x = node_tokens[b, c]:
+ *   accepted if uniforms[b, c] <= r(x) / q_cur(x) (q(x) = 0: +inf if r(x) > 0, else 0), and the
+ *   walk moves to c; else r = norm(max(0, r - q_cur)) (unchanged if that sums to 0). When every
+ *   child is rejected, or the node has none, the last token is drawn from r with
+ *   u = uniforms[b, 0] (inverse CDF: the first k whose running sum strictly exceeds u * S).
+ *   When every node's children were drafted independently from q at that node, each emitted
+ *   token is an exact sample of the target given the tokens before it.
+ *
+ *   target_logits, draft_logits [B, N, V]  dtype
+ *   parents, node_tokens       [B, N]      int32, as for spec_verify_tree
+ *   uniforms                   [B, N]      fp32 in (0, 1): [b, 0] the final draw, [b, i] node
+ *                                          i's acceptance test (i >= 1)
+ *   accept_len, path_nodes, out_tokens     as for spec_verify_tree: the accepted nodes' depth,
+ *                                          root .. last accepted node, their tokens then the
+ *                                          drawn token, then -1
+ *   workspace  at least spec_workspace_bytes(B, 2 * N, V, dtype) bytes (scratch)
+ * T == 0 is spec_verify_tree (greedy; draft_logits and uniforms are not read, may be NULL; a
+ * workspace of spec_workspace_bytes(B, N, V, dtype) suffices). A node with many rejected
+ * children costs one pass over its two rows per rejection. Invalid trees (a bad parent, a
+ * token outside [0, V), a non-finite target or draft row) report accept_len = -1, all -1, and
+ * *status.
+ * Limits: 1 <= N <= SPEC_MAX_NODES, 1 <= V <= SPEC_MAX_V, B >= 0, temperature as for
+ * spec_verify_chain.
+ */
+int spec_verify_tree_sample(const void *target_logits, const void *draft_logits, int dtype,
+                            const int32_t *parents, const int32_t *node_tokens,
+                            const float *uniforms, int B, int N, int V, float temperature,
+                            int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens,
+                            int32_t *status, void *workspace, size_t workspace_bytes,
+                            void *stream);
 
 /*
  * Temperature softmax of `rows` logits rows into fp32 probabilities: the target and draft

@@ -59,12 +59,16 @@ def _load():
             lib.oracle_verify_tree.argtypes = [vp, i32, vp, vp, i64, i64, i64, vp, vp, vp]
             lib.oracle_verify_tree_sample.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i64,
                                                       dbl, vp, vp, vp, vp]
+            lib.oracle_verify_tree_sample_detail.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64,
+                                                             i64, dbl, dbl, vp, vp, vp, vp, vp,
+                                                             vp, vp]
             lib.oracle_sample.argtypes = [vp, i32, i64, i64, dbl, vp, vp, vp]
             lib.oracle_topk.argtypes = [vp, i32, i64, i64, i64, vp]
             lib.oracle_tree_mask.argtypes = [vp, i64, i64, vp]
             for f in (lib.oracle_probs, lib.oracle_argmax, lib.oracle_verify_chain,
                       lib.oracle_verify_chain_detail,
                       lib.oracle_verify_tree, lib.oracle_verify_tree_sample,
+                      lib.oracle_verify_tree_sample_detail,
                       lib.oracle_sample, lib.oracle_topk,
                       lib.oracle_tree_mask):
                 f.restype = ctypes.c_int
@@ -182,6 +186,27 @@ def verify_tree_sample(target, draft, dtype, parents, tokens, uniforms, temperat
                                            _ptr(uni), B, N, V, float(temperature), _ptr(acc),
                                            _ptr(path), _ptr(out), _ptr(mg))
     return acc, path, out, mg, rc
+
+
+def verify_tree_sample_detail(target, draft, dtype, parents, tokens, uniforms, temperature,
+                              band=1e-5):
+    """The walk with its margins apart: a dict of accept_len, path_nodes, out_tokens, dmargin
+    (smallest decision margin), cmargin (the final draw's), lo / hi (the draw's band), rc."""
+    tg = _logits(target, dtype)
+    B, N, V = tg.shape
+    dr = _logits(draft, dtype) if draft is not None else tg
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, N)
+    uni = (np.zeros((B, N), np.float32) if uniforms is None else
+           np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, N))
+    o = dict(accept_len=np.empty(B, np.int32), path_nodes=np.empty((B, N), np.int32),
+             out_tokens=np.empty((B, N), np.int32), dmargin=np.empty(B, np.float64),
+             cmargin=np.empty(B, np.float64), lo=np.empty(B, np.int32), hi=np.empty(B, np.int32))
+    o["rc"] = _load().oracle_verify_tree_sample_detail(
+        _ptr(tg), _ptr(dr), dtype, _ptr(par), _ptr(tok), _ptr(uni), B, N, V, float(temperature),
+        float(band), _ptr(o["accept_len"]), _ptr(o["path_nodes"]), _ptr(o["out_tokens"]),
+        _ptr(o["dmargin"]), _ptr(o["cmargin"]), _ptr(o["lo"]), _ptr(o["hi"]))
+    return o
 
 
 def sample(logits, dtype, uniforms, temperature):

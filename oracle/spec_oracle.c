@@ -525,15 +525,31 @@ int oracle_verify_tree(const void *target, int dtype, const int32_t *parents,
  * |u - ratio| / (ratio A), the draw min(c_k - t, t - c_{k-1}) / A (A = 1 with no update, as for
  * the chain's bonus draw; one update gives the chain's P/S).
  */
-int oracle_verify_tree_sample(const void *target, const void *draft, int dtype,
-                              const int32_t *parents, const int32_t *tokens, const float *uniforms,
-                              long B, long N, long V, double T, int32_t *accept_len,
-                              int32_t *path_nodes, int32_t *out_tokens, double *margin) {
-  if (B < 0 || N < 1 || V < 1 || !(T >= 0.0) || isinf(T)) return ORC_ERR_ARG;
+/*
+ * The walk of oracle_verify_tree_sample with its two kinds of margin apart (each may be NULL):
+ * dmargin[b] the smallest over the walk's decisions, cmargin[b] the final draw's, and the
+ * draw's band [lo[b], hi[b]] (cdf_band, width band * A in the normalised residual). T == 0:
+ * margins +inf, the band the drawn token.
+ */
+int oracle_verify_tree_sample_detail(const void *target, const void *draft, int dtype,
+                                     const int32_t *parents, const int32_t *tokens,
+                                     const float *uniforms, long B, long N, long V, double T,
+                                     double band, int32_t *accept_len, int32_t *path_nodes,
+                                     int32_t *out_tokens, double *dmargin, double *cmargin,
+                                     int32_t *lo, int32_t *hi) {
+  if (B < 0 || N < 1 || V < 1 || !(T >= 0.0) || isinf(T) || !(band >= 0.0)) return ORC_ERR_ARG;
   if (T == 0.0) {
-    for (long b = 0; b < B && margin; ++b) margin[b] = INFINITY;
-    return oracle_verify_tree(target, dtype, parents, tokens, B, N, V, accept_len, path_nodes,
-                              out_tokens);
+    int rc0 = oracle_verify_tree(target, dtype, parents, tokens, B, N, V, accept_len, path_nodes,
+                                 out_tokens);
+    for (long b = 0; b < B; ++b) {
+      const int32_t a = accept_len[b];
+      const int32_t t = a >= 0 ? out_tokens[(size_t)b * (size_t)N + (size_t)a] : -1;
+      if (dmargin) dmargin[b] = INFINITY;
+      if (cmargin) cmargin[b] = INFINITY;
+      if (lo) lo[b] = t;
+      if (hi) hi[b] = t;
+    }
+    return rc0;
   }
   double *r = (double *)malloc(sizeof(double) * (size_t)V);
   double *q = (double *)malloc(sizeof(double) * (size_t)V);
@@ -547,7 +563,10 @@ int oracle_verify_tree_sample(const void *target, const void *draft, int dtype,
     int32_t *pn = path_nodes + (size_t)b * (size_t)N;
     int32_t *ot = out_tokens + (size_t)b * (size_t)N;
     for (long j = 0; j < N; ++j) { pn[j] = -1; ot[j] = -1; }
-    if (margin) margin[b] = INFINITY;
+    if (dmargin) dmargin[b] = INFINITY;
+    if (cmargin) cmargin[b] = INFINITY;
+    if (lo) lo[b] = -1;
+    if (hi) hi[b] = -1;
 
     int err = ORC_OK;   /* the same validation as greedy tree verify, plus the draft rows */
     if (par[0] != -1) err = ORC_ERR_PARENT;
@@ -607,14 +626,33 @@ int oracle_verify_tree_sample(const void *target, const void *draft, int dtype,
       }
       double cm;
       const long t = inverse_cdf(r, V, (double)u[0], A, &cm);
-      if (cm < mg) mg = cm;
+      long lk, hk;
+      cdf_band(r, V, (double)u[0], A, band, &lk, &hk);
+      if (cmargin) cmargin[b] = cm;
+      if (lo) lo[b] = (int32_t)lk;
+      if (hi) hi[b] = (int32_t)hk;
       ot[depth] = (int32_t)t;
       break;
     }
     accept_len[b] = (int32_t)depth;
-    if (margin) margin[b] = mg;
+    if (dmargin) dmargin[b] = mg;
   }
   free(r); free(q); free(w);
+  return rc;
+}
+
+int oracle_verify_tree_sample(const void *target, const void *draft, int dtype,
+                              const int32_t *parents, const int32_t *tokens, const float *uniforms,
+                              long B, long N, long V, double T, int32_t *accept_len,
+                              int32_t *path_nodes, int32_t *out_tokens, double *margin) {
+  double *cm = margin ? (double *)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1)) : NULL;
+  if (margin && !cm) return ORC_ERR_MEM;
+  int rc = oracle_verify_tree_sample_detail(target, draft, dtype, parents, tokens, uniforms, B, N,
+                                            V, T, 0.0, accept_len, path_nodes, out_tokens, margin,
+                                            cm, NULL, NULL);
+  for (long b = 0; b < B && margin; ++b)
+    if (cm[b] < margin[b]) margin[b] = cm[b];
+  free(cm);
   return rc;
 }
 

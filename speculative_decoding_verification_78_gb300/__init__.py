@@ -12,5 +12,6 @@ from ._binding import (  # noqa: F401
     SPEC_MAX_GAMMA, SPEC_MAX_NODES, SPEC_MAX_V, SPEC_OK, SPEC_STATIC_SCRATCH_BYTES, SpecError,
     SPEC_MAX_TOPK, check, dtype_flag, load_library, new_workspace, probs, sample,
     spec_launch_shape, spec_probs, spec_sample, spec_status_string, spec_topk, spec_tree_mask,
-    spec_verify_chain, spec_verify_chain_static, spec_verify_tree, spec_workspace_bytes,
-    spec_workspace_init, topk, tree_mask, verify_chain, verify_tree)
+    spec_verify_chain, spec_verify_chain_static, spec_verify_tree, spec_verify_tree_sample,
+    spec_workspace_bytes,
+    spec_workspace_init, topk, tree_mask, verify_chain, verify_tree, verify_tree_sample)

@@ -25,8 +25,9 @@ SPEC_MAX_V, SPEC_MAX_GAMMA, SPEC_MAX_NODES = 1 << 20, 255, 1024
 
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_workspace_bytes", "spec_workspace_init", "spec_verify_chain",
-           "spec_verify_tree", "spec_probs", "spec_status_string", "spec_launch_shape",
-           "spec_verify_chain_static", "spec_sample", "spec_topk", "spec_tree_mask")
+           "spec_verify_tree", "spec_verify_tree_sample", "spec_probs", "spec_status_string",
+           "spec_launch_shape", "spec_verify_chain_static", "spec_sample", "spec_topk",
+           "spec_tree_mask")
 SPEC_MAX_TOPK = 16
 SPEC_STATIC_SCRATCH_BYTES = 4 << 20
 SPEC_CALL_CHAIN, SPEC_CALL_TREE, SPEC_CALL_PROBS = 0, 1, 2
@@ -62,6 +63,9 @@ def load_library():
         lib.spec_verify_tree.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, sz,
                                          vp]
         lib.spec_verify_tree.restype = i32
+        lib.spec_verify_tree_sample.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32,
+                                                vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_tree_sample.restype = i32
         lib.spec_probs.argtypes = [vp, i32, i32, i32, f32, vp, vp, vp, sz, vp]
         lib.spec_probs.restype = i32
         lib.spec_status_string.argtypes = [i32]
@@ -201,6 +205,25 @@ def spec_verify_tree(target_logits, parents, node_tokens, accept_len, path_nodes
         _nbytes(workspace), _stream(stream))
 
 
+def spec_verify_tree_sample(target_logits, draft_logits, parents, node_tokens, uniforms,
+                            temperature, accept_len, path_nodes, out_tokens, status, workspace,
+                            stream=None) -> int:
+    """target_logits, draft_logits [B, N, V]; parents, node_tokens [B, N] int32; uniforms [B, N]
+    fp32 ([b, 0] the final draw, [b, i] node i's test); outputs as spec_verify_tree."""
+    B, N, V = target_logits.shape
+    if draft_logits is not None and (draft_logits.dtype != target_logits.dtype or
+                                     tuple(draft_logits.shape) != (B, N, V)):
+        raise ValueError("draft_logits must match target_logits in dtype and shape")
+    _expect(uniforms, "uniforms", B * N, (torch.float32,))
+    _expect(parents, "parents", B * N, (torch.int32,))
+    _expect(node_tokens, "node_tokens", B * N, (torch.int32,))
+    return load_library().spec_verify_tree_sample(
+        _ptr(target_logits), _ptr(draft_logits), dtype_flag(target_logits), _ptr(parents),
+        _ptr(node_tokens), _ptr(uniforms), B, N, V, float(temperature), _ptr(accept_len),
+        _ptr(path_nodes), _ptr(out_tokens), _ptr(status), _ptr(workspace), _nbytes(workspace),
+        _stream(stream))
+
+
 def spec_probs(logits, temperature, out_probs, status, workspace, stream=None) -> int:
     """logits [..., V] -> out_probs [..., V] fp32."""
     V = logits.shape[-1]
@@ -297,6 +320,24 @@ def verify_tree(target_logits, parents, node_tokens, workspace=None, stream=None
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     check(spec_verify_tree(target_logits, parents, node_tokens, acc, path, out, st, workspace,
                            stream), "spec_verify_tree")
+    return acc, path, out, st
+
+
+def verify_tree_sample(target_logits, draft_logits, parents, node_tokens, uniforms, temperature,
+                       workspace=None, stream=None):
+    """Allocates the outputs and runs spec_verify_tree_sample. Returns (accept_len, path_nodes,
+    out_tokens, status) device tensors."""
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    if workspace is None:
+        workspace = new_workspace(B, 2 * N, V, dtype_flag(target_logits), dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    out = torch.empty((B, N), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    check(spec_verify_tree_sample(target_logits, draft_logits, parents, node_tokens, uniforms,
+                                  temperature, acc, path, out, st, workspace, stream),
+          "spec_verify_tree_sample")
     return acc, path, out, st
 
 

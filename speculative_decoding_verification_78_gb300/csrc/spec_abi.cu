@@ -313,6 +313,56 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
+int spec_verify_tree_sample(const void *target_logits, const void *draft_logits, int dtype,
+                            const int32_t *parents, const int32_t *node_tokens,
+                            const float *uniforms, int B, int N, int V, float temperature,
+                            int32_t *accept_len, int32_t *path_nodes, int32_t *out_tokens,
+                            int32_t *status, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_DTYPE;
+  if (B < 0 || N < 1 || N > SPEC_MAX_NODES || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_SHAPE;
+  if (!temp_ok(temperature)) return SPEC_ERR_TEMP;
+  if (temperature == 0.f)   // greedy: the argmax walk, draft logits and uniforms not read
+    return spec_verify_tree(target_logits, dtype, parents, node_tokens, B, N, V, accept_len,
+                            path_nodes, out_tokens, status, workspace, workspace_bytes, stream);
+  if (!target_logits || !draft_logits || !parents || !node_tokens || !uniforms || !accept_len ||
+      !path_nodes || !out_tokens || !status || !workspace)
+    return SPEC_ERR_NULL;
+  const int es = elem_size(dtype);
+  if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(parents, 4) ||
+      !aligned(node_tokens, 4) || !aligned(uniforms, 4) || !aligned(accept_len, 4) ||
+      !aligned(path_nodes, 4) || !aligned(out_tokens, 4) || !aligned(status, 4) ||
+      !aligned(workspace, 16))
+    return SPEC_ERR_ALIGN;
+  if (B == 0) return SPEC_OK;
+  Params p = blank();
+  p.B = B;
+  p.N = N;
+  p.V = V;
+  p.Rt = N;   // rows 0 .. N-1: target; N .. 2N-1: draft
+  p.Rd = N;
+  p.R = 2 * N;
+  p.c2 = c2_of(temperature);
+  p.tgt = target_logits;
+  p.drf = draft_logits;
+  p.parents = parents;
+  p.tokens = node_tokens;
+  p.uniforms = uniforms;
+  p.accept_len = accept_len;
+  p.path_nodes = path_nodes;
+  p.out_tokens = out_tokens;
+  p.status = status;
+  const int rc = plan(p, dtype, workspace, workspace_bytes);
+  if (rc != SPEC_OK) return rc;
+  // rowM, rowZ [2N] floats; parents, tokens, children [N] ints; segment sums
+  const size_t smem = sizeof(float) * 4 * static_cast<size_t>(N) +
+                      sizeof(int) * 3 * static_cast<size_t>(N) +
+                      sizeof(float) * static_cast<size_t>((V + kSeg - 1) / kSeg);
+  const cudaError_t e = launch_tree_sample(dtype, p, grid_for(p), smem,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
 int spec_probs(const void *logits, int dtype, int rows, int V, float temperature,
                float *out_probs, int32_t *status, void *workspace, size_t workspace_bytes,
                void *stream) {

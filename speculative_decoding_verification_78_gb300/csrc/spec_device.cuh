@@ -14,7 +14,8 @@
 //                 of a thread-block cluster (a bonus draw from the unit partials alone when it
 //                 can); rows of a single unit finish in one warp per batch row;
 //   chain, T = 0  argmax comparison of every draft token, then the greedy correction token;
-//   tree          accepted set and depths of all nodes, deepest node, path and bonus token.
+//   tree          accepted set and depths of all nodes, deepest node, path and bonus token;
+//   tree, T > 0   the walk from the root by per-sibling rejection sampling (one CTA per tree).
 //
 // The probability helper holds each row in the registers of a cluster of CTAs (one kernel, one
 // read and one write); top-n candidates follow the stream / finish pattern; the tree mask is
@@ -29,6 +30,7 @@
 //   spec_finish.cuh   combining partials, acceptance, emitting, greedy chains, trees, cluster
 //                     draws
 //   spec_kernels.cuh  the verification and probability kernels
+//   spec_tree_sample.cuh  stochastic tree verification: the walk by per-sibling rejection
 //   spec_helpers.cuh  top-n candidates and the tree-attention mask
 #pragma once
 
@@ -36,4 +38,5 @@
 #include "spec_draw.cuh"
 #include "spec_finish.cuh"
 #include "spec_kernels.cuh"
+#include "spec_tree_sample.cuh"
 #include "spec_helpers.cuh"

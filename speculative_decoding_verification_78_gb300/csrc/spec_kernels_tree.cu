@@ -1,9 +1,35 @@
-// spec_kernels_tree.cu -- kernel instances for greedy tree verification.
+// spec_kernels_tree.cu -- kernel instances for tree verification: greedy, and stochastic (the
+// walk by per-sibling rejection sampling).
+#include <atomic>
+
 #include "spec_launch.h"
 
 namespace specv {
 
 namespace {
+
+// The walk's finishing kernel needs more than the default 48 KB of dynamic shared memory for the
+// largest trees and vocabularies: its limit is raised to the device's opt-in maximum once per
+// device.
+template <typename E>
+cudaError_t tree_sample(const Params &p, int grid, size_t smem, cudaStream_t stream) {
+  static std::atomic<int> raised[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !raised[dev].load(std::memory_order_acquire)) {
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(finish_tree_sample<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(sizeof(TsShared)));
+    if (e != cudaSuccess) return e;
+    if (dev < 64) raised[dev].store(1, std::memory_order_release);
+  }
+  e = launch_stream<E, kProbs>(p, grid, stream);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(finish_tree_sample<E>, p, p.B, 1, smem, stream);
+}
 
 template <typename E>
 cudaError_t tree(const Params &p, int grid, const FinishPlan &f, cudaStream_t stream) {
@@ -17,6 +43,12 @@ cudaError_t tree(const Params &p, int grid, const FinishPlan &f, cudaStream_t st
 cudaError_t launch_tree(int dtype, const Params &p, int grid, const FinishPlan &f,
                         cudaStream_t stream) {
   return dtype == SPEC_BF16 ? tree<uint16_t>(p, grid, f, stream) : tree<float>(p, grid, f, stream);
+}
+
+cudaError_t launch_tree_sample(int dtype, const Params &p, int grid, size_t smem,
+                               cudaStream_t stream) {
+  return dtype == SPEC_BF16 ? tree_sample<uint16_t>(p, grid, smem, stream)
+                            : tree_sample<float>(p, grid, smem, stream);
 }
 
 }  // namespace specv

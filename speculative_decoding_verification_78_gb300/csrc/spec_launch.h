@@ -65,6 +65,10 @@ cudaError_t launch_chain(int mode, int dtype, const Params &p, int grid, const F
                          cudaStream_t stream);
 cudaError_t launch_tree(int dtype, const Params &p, int grid, const FinishPlan &f,
                         cudaStream_t stream);
+// Stochastic tree verification: the stream kernel over every target and draft row, then one
+// finishing CTA per tree with `smem` bytes of dynamic shared memory.
+cudaError_t launch_tree_sample(int dtype, const Params &p, int grid, size_t smem,
+                               cudaStream_t stream);
 cudaError_t launch_probs(int mode, int dtype, const Params &p, int grid, const FinishPlan &f,
                          cudaStream_t stream);
 cudaError_t launch_topk(int dtype, const Params &p, int grid, cudaStream_t stream);

@@ -170,3 +170,64 @@ def to_np_logits(t: torch.Tensor, dtype: int) -> np.ndarray:
     if dtype == BF16:
         return t.view(torch.int16).numpy().view(np.uint16)
     return t.numpy()
+
+
+def run_tree_sample(ti, draft, uniforms, T, offset_elems=0):
+    import speculative_decoding_verification_78_gb300 as sv
+    acc, path, out, st = sv.verify_tree_sample(dev(ti.target, offset_elems),
+                                               dev(draft, offset_elems), dev(ti.parents),
+                                               dev(ti.tokens), dev(uniforms), T)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), path.cpu().numpy(), out.cpu().numpy(), int(st.item())
+
+
+def compare_tree_sample(orc, ti, draft, uniforms, T, gpu, name="tree_sample"):
+    """Stochastic tree verification against the oracle. A tree whose walk has no decision within
+    MARGIN of its boundary must take the oracle's path exactly; its final token must be the
+    oracle's unless the draw's margin is below MARGIN, and then lie in the oracle's band for it.
+    A tree with a near-boundary decision may take another path: it must still be a valid walk
+    (each path node the previous one's child, the tokens of the path, a final token of positive
+    target probability at the last node). Invalid trees must match exactly. Returns (trees with
+    a flagged decision, trees with a flagged draw, trees different from the oracle)."""
+    acc, path, out, _ = gpu
+    d = orc.verify_tree_sample_detail(ti.target, draft, ti.dtype, ti.parents, ti.tokens,
+                                      uniforms, T, band=MARGIN)
+    oa, op, oo = d["accept_len"], d["path_nodes"], d["out_tokens"]
+    f_dec = f_draw = diff = 0
+    bad = []
+    for b in range(len(acc)):
+        if oa[b] < 0:
+            if acc[b] != -1 or np.any(out[b] != -1) or np.any(path[b] != -1):
+                bad.append((b, "invalid tree not reported"))
+            continue
+        n = int(acc[b])
+        same = (n == oa[b] and np.array_equal(path[b], op[b]) and np.array_equal(out[b], oo[b]))
+        diff += int(not same)
+        if d["dmargin"][b] >= MARGIN:
+            if n != oa[b] or not np.array_equal(path[b], op[b]) or \
+                    not np.array_equal(out[b, :n], oo[b, :n]) or np.any(out[b, n + 1:] != -1):
+                bad.append((b, f"path differs: gpu {path[b, :n + 1]} oracle {op[b, :oa[b] + 1]}"))
+                continue
+            t = int(out[b, n])
+            if d["cmargin"][b] >= MARGIN:
+                if t != oo[b, n]:
+                    bad.append((b, f"token {t} != {oo[b, n]}, margin {d['cmargin'][b]:.3g}"))
+            else:
+                f_draw += 1
+                if not d["lo"][b] <= t <= d["hi"][b]:
+                    bad.append((b, f"token {t} outside [{d['lo'][b]}, {d['hi'][b]}]"))
+            continue
+        f_dec += 1   # a near-boundary decision: any valid walk
+        if not 0 <= n < ti.N or path[b, 0] != 0 or np.any(path[b, n + 1:] != -1):
+            bad.append((b, "invalid walk"))
+            continue
+        ok = all(ti.parents[b, path[b, i]] == path[b, i - 1] and out[b, i - 1] == ti.tokens[b, path[b, i]]
+                 for i in range(1, n + 1))
+        p_last, _ = orc.probs(ti.target[b, path[b, n]:path[b, n] + 1], ti.dtype, T)
+        t = int(out[b, n])
+        if not (ok and 0 <= t < ti.V and p_last[0, t] > 0 and np.all(out[b, n + 1:] == -1)):
+            bad.append((b, "invalid walk"))
+    assert not bad, f"{name}: {len(bad)} trees fail, e.g. {bad[:4]}"
+    report(name, trees=len(acc), flagged_decisions=f_dec, flagged_draws=f_draw,
+           different=diff, outside_band=0)
+    return f_dec, f_draw, diff

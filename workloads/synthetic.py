@@ -43,7 +43,7 @@ BF16 = 1
 __all__ = [
     "F32", "BF16", "ChainInputs", "TreeInputs", "f32_to_bf16", "bf16_to_f32", "as_f32",
     "make_uniforms", "gumbel_draft_tokens", "chain_tiny", "chain_32k", "chain_128k",
-    "tree_32k", "sweep_152k", "tree_shape", "WORKLOADS",
+    "tree_32k", "tree_sample_32k", "sweep_152k", "tree_shape", "WORKLOADS",
 ]
 
 
@@ -358,10 +358,46 @@ def tree_32k(seed: int = 4, B: int = 32, N: int = 64, V: int = 32000, dtype: int
                                "designated": designated})
 
 
+def tree_sample_32k(seed: int = 6, B: int = 32, N: int = 64, V: int = 32000, dtype: int = BF16,
+                    temperature: float = 1.0, draft_sigma: float = 1.0,
+                    peaked: int = 50) -> TreeInputs:
+    """Stochastic tree verify workload: configuration 4's trees and target logits (N(0,3^2)
+    clipped to +-12, plus 8 on 50 distinct ids per node), a draft row per node (target + N(0,
+    draft_sigma^2)), and every node's token drafted from the draft distribution at its parent
+    (the Gumbel-max trick at the temperature), so that the children of a node are independent
+    draws from it. Uniforms [B, N]: [b, 0] the final draw, [b, i] node i's acceptance test.
+    meta["draft"] holds the draft logits (same dtype), meta["uniforms"] the uniforms."""
+    r_shape, r_t, r_p, r_d, r_tok, r_u = _rngs(seed, 6)
+    target_f = np.empty((B, N, V), dtype=np.float32)
+    parents = np.empty((B, N), dtype=np.int32)
+    npk = min(peaked, V)
+    for b in range(B):
+        parents[b] = tree_shape(r_shape, N)
+        t = np.clip(_normal(r_t, (N, V), 3.0), -12.0, 12.0)
+        for j in range(N):
+            ids = r_p.choice(V, size=npk, replace=False)
+            t[j, ids] += np.float32(8.0)
+        target_f[b] = t
+    draft_f = target_f + _normal(r_d, (B, N, V), draft_sigma)
+    target = _encode(target_f, dtype)
+    draft = _encode(draft_f, dtype)
+    dq = as_f32(draft, dtype)
+    tokens = np.zeros((B, N), dtype=np.int32)
+    for b in range(B):
+        # node i's token: one draw from the draft distribution at its parent
+        draws = gumbel_draft_tokens(r_tok, dq[b, np.maximum(parents[b], 0)], temperature)
+        tokens[b, 1:] = draws[1:]
+    u = make_uniforms(r_u, (B, N))
+    return TreeInputs(f"tree_sample_B{B}_N{N}_V{V}", target, dtype, parents, tokens,
+                      {"draft": draft, "uniforms": u, "temperature": float(temperature),
+                       "draft_sigma": draft_sigma, "branching": TREE_BRANCHING})
+
+
 WORKLOADS = {
     "chain_tiny": chain_tiny,
     "chain_32k": chain_32k,
     "chain_128k": chain_128k,
     "tree_32k": tree_32k,
+    "tree_sample_32k": tree_sample_32k,
     "sweep_152k": sweep_152k,
 }
