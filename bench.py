@@ -330,7 +330,8 @@ def time_calls(call, ncopies, stream, min_calls=50):
 
 ROW_NAMES = ("cfg1_chain_tiny", "cfg2_chain_32k", "cfg3_sigma0.25", "cfg3_sigma1", "cfg3_sigma4",
              "cfg4_tree_32k", "cfg5_B1_g3", "cfg5_B1_g7", "cfg5_B16_g3", "cfg5_B16_g7",
-             "cfg5_B128_g3", "cfg5_B128_g7", "cfg5_B1024_g3", "cfg5_B1024_g7", "probs_32k")
+             "cfg5_B128_g3", "cfg5_B128_g7", "cfg5_B1024_g3", "cfg5_B1024_g7", "probs_32k",
+             "tree_sample_32k")
 
 
 def _dev(a, device):
@@ -400,6 +401,32 @@ def measure_rows(names, lib, sv, device, stream, peak, min_calls):
                      vp(stream.cuda_stream)) for t in tt]
             call = lambda k: lib.spec_verify_tree(*args[k % nc])
             desc, pos = "32 trees x 64 nodes x 32000 bf16, greedy", ti.B * ti.N
+            torch.cuda.synchronize()
+        elif name == "tree_sample_32k":
+            from workloads import tree_sample_32k
+            ti = tree_sample_32k()
+            # target and draft logits, parents, tokens, uniforms, outputs: each once
+            nbytes = (2 * ti.B * ti.N * ti.V * 2 + 8 * ti.B * ti.N + 4 * ti.B * ti.N
+                      + 4 * ti.B * (2 * ti.N + 1))
+            nc = copies_for(ti.target.nbytes + ti.meta["draft"].nbytes)
+            tt = [_dev(ti.target, device) for _ in range(nc)]
+            dd = [_dev(ti.meta["draft"], device) for _ in range(nc)]
+            par, tok = _dev(ti.parents, device), _dev(ti.tokens, device)
+            uu = _dev(ti.meta["uniforms"], device)
+            acc = torch.empty(ti.B, dtype=torch.int32, device=device)
+            path = torch.empty((ti.B, ti.N), dtype=torch.int32, device=device)
+            out = torch.empty((ti.B, ti.N), dtype=torch.int32, device=device)
+            st = torch.zeros(1, dtype=torch.int32, device=device)
+            ws = sv.new_workspace(ti.B, 2 * ti.N, ti.V, BF16, device)
+            vp = ctypes.c_void_p
+            args = [(vp(tt[k].data_ptr()), vp(dd[k].data_ptr()), BF16, vp(par.data_ptr()),
+                     vp(tok.data_ptr()), vp(uu.data_ptr()), ti.B, ti.N, ti.V,
+                     ctypes.c_float(1.0), vp(acc.data_ptr()), vp(path.data_ptr()),
+                     vp(out.data_ptr()), vp(st.data_ptr()), vp(ws.data_ptr()), ws.numel(),
+                     vp(stream.cuda_stream)) for k in range(nc)]
+            call = lambda k: lib.spec_verify_tree_sample(*args[k % nc])
+            desc = "32 trees x 64 nodes x 32000 bf16, sampled drafts, T=1 (stochastic walk)"
+            pos = ti.B * ti.N
             torch.cuda.synchronize()
         elif name == "probs_32k":
             ci = chain_32k()

@@ -63,6 +63,9 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 #define SPEC_ERR_NONFINITE (-20) /* a logits row has NaN or +inf, or no finite entry          */
 #define SPEC_ERR_TOKEN (-21)     /* a draft / node token is outside [0, V)                    */
 #define SPEC_ERR_PARENT (-22)    /* parents[b,0] != -1 or parents[b,i] not in [0, i)          */
+#define SPEC_ERR_CHECK (-24)     /* checked build only (libspec_verify_checked.so): an index the
+                                    kernels computed fell outside its buffer; the access was
+                                    skipped. Never seen from a correct library.               */
 
 /* limits */
 #define SPEC_MAX_V (1 << 20)   /* vocabulary size                                            */

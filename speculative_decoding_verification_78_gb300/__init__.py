@@ -6,9 +6,9 @@ softmax helper. This package is its thin Python binding; see _binding.py.
 """
 
 from ._binding import (  # noqa: F401
-    EXPORTS, LIB_PATH, SPEC_BF16, SPEC_CALL_CHAIN, SPEC_CALL_PROBS, SPEC_CALL_TREE,
+    CHECKED_LIB_PATH, EXPORTS, LIB_PATH, SPEC_BF16, SPEC_CALL_CHAIN, SPEC_CALL_PROBS, SPEC_CALL_TREE,
     SPEC_ERR_ALIGN, SPEC_ERR_DTYPE, SPEC_ERR_LAUNCH, SPEC_ERR_NONFINITE, SPEC_ERR_NULL,
-    SPEC_ERR_PARENT, SPEC_ERR_SHAPE, SPEC_ERR_TEMP, SPEC_ERR_TOKEN, SPEC_ERR_WORKSPACE, SPEC_F32,
+    SPEC_ERR_CHECK, SPEC_ERR_PARENT, SPEC_ERR_SHAPE, SPEC_ERR_TEMP, SPEC_ERR_TOKEN, SPEC_ERR_WORKSPACE, SPEC_F32,
     SPEC_MAX_GAMMA, SPEC_MAX_NODES, SPEC_MAX_V, SPEC_OK, SPEC_STATIC_SCRATCH_BYTES, SpecError,
     SPEC_MAX_TOPK, check, dtype_flag, load_library, new_workspace, probs, sample,
     spec_launch_shape, spec_probs, spec_sample, spec_status_string, spec_topk, spec_tree_mask,

@@ -15,12 +15,14 @@ import torch
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libspec_verify.so")
+# the same kernels compiled with SPEC_CHECKED: computed indices range-checked (SPEC_ERR_CHECK)
+CHECKED_LIB_PATH = os.path.join(PKG, "libspec_verify_checked.so")
 
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_OK = 0
 SPEC_ERR_NULL, SPEC_ERR_SHAPE, SPEC_ERR_TEMP, SPEC_ERR_DTYPE = -1, -2, -3, -4
 SPEC_ERR_WORKSPACE, SPEC_ERR_ALIGN, SPEC_ERR_LAUNCH = -5, -6, -7
-SPEC_ERR_NONFINITE, SPEC_ERR_TOKEN, SPEC_ERR_PARENT = -20, -21, -22
+SPEC_ERR_NONFINITE, SPEC_ERR_TOKEN, SPEC_ERR_PARENT, SPEC_ERR_CHECK = -20, -21, -22, -24
 SPEC_MAX_V, SPEC_MAX_GAMMA, SPEC_MAX_NODES = 1 << 20, 255, 1024
 
 # every symbol include/spec_verify.h declares
@@ -34,6 +36,7 @@ SPEC_CALL_CHAIN, SPEC_CALL_TREE, SPEC_CALL_PROBS = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
+_checked_lib = None
 
 
 class SpecError(RuntimeError):
@@ -42,16 +45,18 @@ class SpecError(RuntimeError):
         super().__init__(f"{where}: {spec_status_string(code)} ({code})")
 
 
-def load_library():
-    """Loads libspec_verify.so (built in-tree by __graft_entry__.build())."""
-    global _lib
+def load_library(checked: bool = False):
+    """Loads libspec_verify.so (built in-tree by __graft_entry__.build()), or with
+    checked=True its checked build libspec_verify_checked.so."""
+    global _lib, _checked_lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        if not os.path.exists(LIB_PATH):
-            raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+        if (_checked_lib if checked else _lib) is not None:
+            return _checked_lib if checked else _lib
+        path = CHECKED_LIB_PATH if checked else LIB_PATH
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build the CUDA library first "
                               "(python -c 'import __graft_entry__ as g; g.build()')")
-        lib = ctypes.CDLL(LIB_PATH)
+        lib = ctypes.CDLL(path)
         vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.spec_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.spec_workspace_bytes.restype = sz
@@ -81,7 +86,10 @@ def load_library():
         lib.spec_topk.restype = i32
         lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
         lib.spec_tree_mask.restype = i32
-        _lib = lib
+        if checked:
+            _checked_lib = lib
+        else:
+            _lib = lib
         return lib
 
 

@@ -512,6 +512,7 @@ const char *spec_status_string(int code) {
     case SPEC_ERR_NONFINITE: return "a logits row holds NaN or +inf, or no finite value";
     case SPEC_ERR_TOKEN: return "a draft or node token is outside [0, V)";
     case SPEC_ERR_PARENT: return "a tree parent index is invalid";
+    case SPEC_ERR_CHECK: return "checked build: a computed index fell outside its buffer";
     default: return "unknown status";
   }
 }

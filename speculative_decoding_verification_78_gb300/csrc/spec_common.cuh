@@ -206,6 +206,21 @@ __device__ __forceinline__ void set_status(int32_t *status, int code) {
   atomicCAS(reinterpret_cast<int *>(status), 0, code);
 }
 
+// ------------------------------------------------------------------ the checked build
+//
+// SPEC_CHECK(p, cond) guards a memory access by an index the kernel computed. In the checked
+// build (compiled with SPEC_CHECKED, libspec_verify_checked.so) a false condition records
+// SPEC_ERR_CHECK in *status and the guarded access is skipped; in the normal build it is the
+// constant true and costs nothing.
+#ifdef SPEC_CHECKED
+static __device__ __noinline__ void spec_check_failed(int32_t *status) {
+  atomicCAS(reinterpret_cast<int *>(status), 0, SPEC_ERR_CHECK);
+}
+#define SPEC_CHECK(p, cond) ((cond) ? true : (spec_check_failed((p).status), false))
+#else
+#define SPEC_CHECK(p, cond) true
+#endif
+
 // ------------------------------------------------------------------ row geometry
 
 // A row's 16-byte aligned interior: `h` head elements before it, `nv` full vectors, `tl` tail
@@ -232,6 +247,7 @@ __device__ __forceinline__ RowGeom row_geom(const E *row, int V) {
 
 template <typename E>
 __device__ __forceinline__ const E *row_ptr(const Params &p, int b, int r) {
+  if (!SPEC_CHECK(p, b >= 0 && b < p.B && r >= 0 && r < p.R)) b = r = 0;
   if (r < p.Rt)
     return static_cast<const E *>(p.tgt) + (static_cast<long long>(b) * p.Rt + r) * p.V;
   return static_cast<const E *>(p.drf) + (static_cast<long long>(b) * p.Rd + (r - p.Rt)) * p.V;
@@ -243,6 +259,7 @@ struct UnitId {
 
 // unit -> (batch row, row, chunk), 32-bit unsigned division only
 __device__ __forceinline__ UnitId unit_id(const Params &p, int unit) {
+  if (!SPEC_CHECK(p, unit >= 0 && unit < p.units)) unit = 0;
   UnitId u;
   const unsigned uu = static_cast<unsigned>(unit);
   u.b = static_cast<int>(uu / static_cast<unsigned>(p.upb));

@@ -10,6 +10,7 @@ namespace specv {
 // ------------------------------------------------------------------ finishing helpers
 
 __device__ __forceinline__ void fail_chain_row(const Params &p, int b, int tid, int nthreads) {
+  if (!SPEC_CHECK(p, b >= 0 && b < p.B)) return;
   const int g1 = p.gamma + 1;
   for (int j = tid; j < g1; j += nthreads) p.out_tokens[static_cast<long long>(b) * g1 + j] = -1;
   if (tid == 0 && p.accept_len) p.accept_len[b] = -1;   // no accept_len when only sampling
@@ -54,6 +55,7 @@ __device__ __forceinline__ void combine_rows_stats(const Params &p, int b, float
   const int R = p.R, C = p.C;
   const int L = combine_lanes(C);
   const int sub = lane & (L - 1), rpw = 32 / L, pass = kWarps * rpw;
+  if (!SPEC_CHECK(p, b >= 0 && b < p.B)) b = 0;
   const uint2 *base = p.ws_part + static_cast<long long>(b) * R * C;
   const uint2 none = make_uint2(0xff800000u, 0u);
   for (int r0 = warp * rpw; r0 < R; r0 += 2 * pass) {
@@ -107,6 +109,7 @@ __device__ __forceinline__ void combine_rows_arg(const Params &p, int b, int *g,
   const int R = p.R, C = p.C;
   const int L = combine_lanes(C);
   const int sub = lane & (L - 1), rpw = 32 / L, pass = kWarps * rpw;
+  if (!SPEC_CHECK(p, b >= 0 && b < p.B)) b = 0;
   const uint2 *base = p.ws_part + static_cast<long long>(b) * R * C;
   const uint2 none = make_uint2(0xff800000u, 0x7fffffffu);
   for (int r0 = warp * rpw; r0 < R; r0 += 2 * pass) {
@@ -206,6 +209,8 @@ __device__ inline int chain_accept(const Params &p, int b, float *rowM, float *r
 // out_tokens[b] = x_0..x_{n-1}, tok, then -1; accept_len[b] = n. x: the step's drafts.
 __device__ __forceinline__ void emit_chain(const Params &p, int b, int n, int tok, const int *x,
                                            int tid, int nthreads) {
+  if (!SPEC_CHECK(p, b >= 0 && b < p.B && n >= 0 && n <= p.gamma)) return;
+  SPEC_CHECK(p, tok >= 0 && tok < p.V);
   const int g1 = p.gamma + 1;
   int32_t *o = p.out_tokens + static_cast<long long>(b) * g1;
   for (int j = tid; j < g1; j += nthreads) o[j] = (j < n) ? x[j] : (j == n ? tok : -1);
@@ -355,7 +360,8 @@ __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared
     for (int q = 0; q < kPer; ++q) {
       const int j = threadIdx.x + q * kThreads;
       if (j < N) {
-        const int a = anc[j];
+        int a = anc[j];
+        if (!SPEC_CHECK(p, a >= 0 && a < N)) a = 0;
         na[q] = anc[a];
         nc[q] = acc[j] & acc[a];
         nd[q] = dep[j] + dep[a];
@@ -380,9 +386,10 @@ __device__ inline void tail_tree(const Params &p, int b, float *smem, TailShared
     if (j > D) pn[j] = -1;
     if (j > D) ot[j] = -1;
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && SPEC_CHECK(p, best >= 0 && best < N && D >= 0 && D < N)) {
     int v = best;
     for (int d = D; d >= 0; --d) {
+      if (!SPEC_CHECK(p, v >= 0 && v < N)) break;
       pn[d] = v;
       if (d > 0) ot[d - 1] = tok[v];
       v = par[v];
@@ -483,7 +490,8 @@ __device__ inline void tail_tree_small(const Params &p, int b, float *smem) {
   // lane d writes the path node at depth d (and d + 32): D - d steps up from the deepest node
   for (int d = lane; d <= D; d += 32) {
     int v = best;
-    for (int k = d; k < D; ++k) v = par_s[v];
+    for (int k = d; k < D; ++k) v = SPEC_CHECK(p, v >= 0 && v < N) ? par_s[v] : 0;
+    if (!SPEC_CHECK(p, v >= 0 && v < N && d < N)) break;
     pn[d] = v;
     if (d > 0) ot[d - 1] = tok_s[v];
   }
@@ -551,6 +559,7 @@ __device__ void bonus_draw_units(const Params &p, int b, int n, float M, float Z
     uc_sel = max(uc_sel, 0);
   }
   // the element inside unit uc_sel: vectors j*32 + lane, elements in order
+  if (!SPEC_CHECK(p, uc_sel >= 0 && uc_sel < C)) uc_sel = 0;
   const E *row = row_ptr<E>(p, b, n);
   const RowGeom g = row_geom<E>(row, p.V);
   uint4 buf[kVPL];

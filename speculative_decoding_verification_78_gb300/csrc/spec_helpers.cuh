@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_stream_kernel(Params p) {
   }
   for (int unit = blockIdx.x * kWarps + warp; unit < p.units; unit += W) {
     const UnitId u = unit_id(p, unit);
+    if (!SPEC_CHECK(p, u.b < p.B && u.chunk < p.C)) continue;
     const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(u.b) * p.V;
     const RowGeom g = row_geom<E>(row, p.V);
     uint4 buf[kVPL];
@@ -236,7 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_finish(Params p) {
   // no element above -inf: no finite value in the row
   const bool invalid = row_bad || __uint_as_float(mine[0].x) == -INFINITY;
   if (invalid && lane == 0) set_status(p.status, SPEC_ERR_NONFINITE);
-  for (int r = lane; r < k; r += 32) out[r] = invalid ? -1 : static_cast<int>(mine[r].y);
+  for (int r = lane; r < k; r += 32) {
+    const int idx = invalid ? -1 : static_cast<int>(mine[r].y);
+    if (SPEC_CHECK(p, idx >= -1 && idx < p.V)) out[r] = idx;
+  }
 }
 
 // ------------------------------------------------------------------ tree-attention mask
@@ -276,7 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1) tree_mask_kernel(Params p) {
   uint32_t *mine = rows + tid * W;
   for (int i = tid; i < N; i += kThreads) {
     for (int w = 0; w < W; ++w) mine[w] = 0u;
-    for (int j = i; j >= 0; j = par[j]) mine[j >> 5] |= 1u << (j & 31);   // par[0] = -1 ends it
+    for (int j = i; j >= 0; j = par[j]) {   // par[0] = -1 ends it
+      if (!SPEC_CHECK(p, j < N && (j >> 5) < W)) break;
+      mine[j >> 5] |= 1u << (j & 31);
+    }
     for (int w = 0; w < W; ++w) out[static_cast<long long>(i) * W + w] = mine[w];
   }
 }

@@ -32,13 +32,13 @@ __device__ __forceinline__ void unit_work(const Params &p, int unit, const UnitI
     unit_argmax<E>(buf, eh, et, g, u.chunk * kUnitVecs, lane, v, i);
     part = make_uint2(__float_as_uint(v), static_cast<uint32_t>(i));
   }
-  if (lane == 0) p.ws_part[unit] = part;
+  if (lane == 0 && SPEC_CHECK(p, unit >= 0 && unit < p.units)) p.ws_part[unit] = part;
   if constexpr (MODE == kChainSample) {
     if (x >= 0 && x < p.V) {
       const int vb = u.chunk * kUnitVecs;
       float val = 0.f;
       if (span_logit<E>(row, g, vb, vb + kUnitVecs, u.chunk == 0, x, lane, buf, &val) &&
-          lane == 0)
+          lane == 0 && SPEC_CHECK(p, u.b < p.B && u.r < p.R))
         p.ws_xlogit[static_cast<long long>(u.b) * p.R + u.r] = val;
     }
   }
@@ -50,6 +50,7 @@ __device__ __forceinline__ int unit_token(const Params &p, const UnitId &u) {
   if constexpr (MODE == kChainSample) {
     if (u.r != p.gamma) {
       const int i = (u.r < p.Rt) ? u.r : u.r - p.Rt;
+      if (!SPEC_CHECK(p, u.b >= 0 && u.b < p.B && i >= 0 && i < p.gamma)) return -1;
       return __ldg(p.tokens + static_cast<long long>(u.b) * p.gamma + i);
     }
   }
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_kernel(Params p) {
   const int W = gridDim.x * kWarps;
   for (int unit = blockIdx.x * kWarps + (threadIdx.x >> 5); unit < p.units; unit += W) {
     const UnitId u = unit_id(p, unit);
+    if (!SPEC_CHECK(p, u.b < p.B && u.r < p.R && u.chunk < p.C)) continue;
     // the draft token of this row, fetched before the unit's data so both loads overlap
     const int x = unit_token<MODE>(p, u);
     const E *row = row_ptr<E>(p, u.b, u.r);
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
   const int b = blockIdx.x / S;
   cluster_started_arrive();   // the draw's exchange waits for it before touching peers
   wait_stream_kernel();
+  if (!SPEC_CHECK(p, b < p.B)) return;   // the same on every CTA of the cluster
   int n = 0;
   const int err = chain_accept(p, b, rowM, rowZ, xs, sh, &n, bonus_part);
   if (err) {   // the same on every CTA of the cluster: all of them leave here
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_probs(Params p) {
     // the unit's interior as groups of four: group q covers elements k0 + 4q .. k0 + 4q + 3
     const int k0 = g.h + u.chunk * kUnitVecs * kEPV;
     const int nq = min(kUnitVecs, g.nv - u.chunk * kUnitVecs) * kEPV / 4;
+    if (!SPEC_CHECK(p, u.b < p.B && nq >= 0 && k0 + 4 * nq <= V)) continue;
     const E *rq = row + k0;
     uint2 lo[kQuads], hi[kQuads];
 #pragma unroll
@@ -369,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 2) probs_resident(Params p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int V = p.V;
   const float c2 = p.c2;
-  const E *row = static_cast<const E *>(p.tgt) + static_cast<long long>(row_i) * V;
+  const E *row = static_cast<const E *>(p.tgt) +
+                 static_cast<long long>(SPEC_CHECK(p, row_i < p.B) ? row_i : 0) * V;
   const RowGeom g = row_geom<E>(row, V);
   const int nq = g.nv * kEPV / 4;                       // interior groups of four
   const int per = (nq + S - 1) / S;
@@ -583,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_cta(Params p) {
   __shared__ TailShared sh;
   wait_stream_kernel();
   const int b = blockIdx.x;
+  if (!SPEC_CHECK(p, b < p.B)) return;
   if constexpr (MODE == kChainGreedy) tail_chain_greedy(p, b, scratch, sh);
   else if (p.N <= 64) tail_tree_small(p, b, scratch);
   else tail_tree(p, b, scratch, sh);

@@ -254,7 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample(Params p) {
     __syncthreads();
     const int nc = sh.nchild;
     for (int i = tid; i < nc; i += kThreads) {
-      const int x = tok[ch[i]];
+      const int c = ch[i];
+      const int x = SPEC_CHECK(p, c > cur && c < N) ? tok[c] : 0;
+      if (!SPEC_CHECK(p, x >= 0 && x < V && i < SPEC_MAX_NODES)) continue;
       sh.lt[i] = ld_elem<E>(P + x);
       sh.ld[i] = ld_elem<E>(Q + x);
     }
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample(Params p) {
     __syncthreads();
     const int next = sh.next;
     if (next >= 0) {
-      if (tid == 0) {
+      if (tid == 0 && SPEC_CHECK(p, next < N && sh.depth + 1 < N)) {
         const int d = sh.depth + 1;
         pn[d] = next;
         ot[d - 1] = tok[next];
@@ -293,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample(Params p) {
       continue;
     }
     const int t = ts_draw<E>(P, Q, V, vec_ok, sh, c2, sh.u0, segsum);
-    if (tid == 0) {
+    if (tid == 0 && SPEC_CHECK(p, t >= 0 && t < V && sh.depth < N)) {
       pn[0] = 0;
       ot[sh.depth] = t;
       p.accept_len[b] = sh.depth;
