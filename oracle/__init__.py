@@ -5,7 +5,9 @@ may import this package. The product path (the CUDA library and its binding) nev
 this package imports nothing from it.
 
 The arithmetic lives in ``spec_oracle.c`` (plain single-threaded C in double precision); this
-module only compiles it with gcc and marshals numpy arrays through ctypes.
+module only compiles it with gcc and marshals numpy arrays through ctypes. The one exception is
+the LM-head product of ``lm_head_logits``, a float64 numpy matrix product (a library routine)
+whose results the C code rounds to bf16.
 """
 
 from __future__ import annotations
@@ -65,12 +67,13 @@ def _load():
             lib.oracle_sample.argtypes = [vp, i32, i64, i64, dbl, vp, vp, vp]
             lib.oracle_topk.argtypes = [vp, i32, i64, i64, i64, vp]
             lib.oracle_tree_mask.argtypes = [vp, i64, i64, vp]
+            lib.oracle_round_bf16.argtypes = [vp, i64, vp]
             for f in (lib.oracle_probs, lib.oracle_argmax, lib.oracle_verify_chain,
                       lib.oracle_verify_chain_detail,
                       lib.oracle_verify_tree, lib.oracle_verify_tree_sample,
                       lib.oracle_verify_tree_sample_detail,
                       lib.oracle_sample, lib.oracle_topk,
-                      lib.oracle_tree_mask):
+                      lib.oracle_tree_mask, lib.oracle_round_bf16):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -240,3 +243,36 @@ def tree_mask(parents):
     out = np.empty((B, N, W), dtype=np.uint32)
     rc = _load().oracle_tree_mask(_ptr(par), B, N, _ptr(out))
     return out, rc
+
+
+def round_bf16(x):
+    """float64 array -> bf16 bit patterns (uint16) of the nearest bf16 values, ties to even,
+    rounded once, straight from double."""
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    rc = _load().oracle_round_bf16(_ptr(v), v.size, _ptr(out))
+    if rc != OK:
+        raise ValueError(f"oracle_round_bf16: {rc}")
+    return out
+
+
+def _widen_bf16(bits):
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def lm_head_logits(hidden, head):
+    """LM-head logits of the fused producer ("Fast Inference from Transformers via Speculative
+    Decoding", pith.science review, "The pith": the target scores every drafted position in
+    one parallel pass, whose last layer maps each position's final hidden state to a logit
+    per vocabulary token).
+
+    hidden [M, H] and head [V, H] bf16 bit patterns -> (logits [M, V] as bf16 bit patterns,
+    the same logits in float64 before rounding): logits[m, v] = sum_k hidden[m, k] head[v, k],
+    each product and sum in float64 (a numpy matrix product), then rounded once to bf16."""
+    h = _widen_bf16(hidden)
+    w = _widen_bf16(head)
+    if h.ndim != 2 or w.ndim != 2 or h.shape[1] != w.shape[1]:
+        raise ValueError(f"lm_head_logits: shapes {h.shape} and {w.shape}")
+    exact = h @ w.T
+    return round_bf16(exact), exact

@@ -762,3 +762,38 @@ int oracle_tree_mask(const int32_t *parents, long B, long N, uint32_t *words) {
   }
   return rc;
 }
+
+/*
+ * LM-head logits as stored by the fused producer: the last layer of the target's (and the
+ * drafter's) scoring pass, logits = hidden . head^T ("Fast Inference from Transformers via
+ * Speculative Decoding", pith.science review, "The pith": the target scores every drafted
+ * position in one parallel pass), stored in bf16. The dot products are taken by the Python
+ * wrapper (a float64 matrix product); this is the rounding of each exact-or-nearly value to
+ * the nearest bf16, ties to the even significand (IEEE 754 roundTiesToEven), straight from
+ * double so that no intermediate float rounds it twice. NaN -> 0x7FC0; magnitudes at or above
+ * 2^128 after rounding -> infinity; below 2^-126 the spacing stays 2^-133 (bf16 subnormals).
+ */
+int oracle_round_bf16(const double *x, long n, uint16_t *out) {
+  if (n < 0 || (n > 0 && (!x || !out))) return ORC_ERR_ARG;
+  for (long i = 0; i < n; ++i) {
+    const double v = x[i];
+    if (isnan(v)) { out[i] = 0x7FC0; continue; }
+    const uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) { out[i] = sign; continue; }
+    if (isinf(a)) { out[i] = sign | 0x7F80; continue; }
+    int e;
+    frexp(a, &e);                 /* a = f 2^e, 0.5 <= f < 1: the leading bit is 2^(e-1) */
+    int q = e - 8;                /* 8 significant bits: the spacing is 2^(e-8) */
+    if (q < -133) q = -133;
+    a = ldexp(nearbyint(ldexp(a, -q)), q);   /* exact scalings; nearest, ties to even */
+    if (a >= ldexp(1.0, 128)) { out[i] = sign | 0x7F80; continue; }
+    /* a has at most 8 significant bits and lies in float's range: exact as a float, whose
+       upper 16 bits are then its bf16 pattern */
+    const float f = (float)a;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    out[i] = (uint16_t)(sign | (u >> 16));
+  }
+  return ORC_OK;
+}

@@ -43,7 +43,8 @@ BF16 = 1
 __all__ = [
     "F32", "BF16", "ChainInputs", "TreeInputs", "f32_to_bf16", "bf16_to_f32", "as_f32",
     "make_uniforms", "gumbel_draft_tokens", "chain_tiny", "chain_32k", "chain_128k",
-    "tree_32k", "tree_sample_32k", "sweep_152k", "tree_shape", "WORKLOADS",
+    "tree_32k", "tree_sample_32k", "sweep_152k", "tree_shape", "WORKLOADS", "LmHeadInputs",
+    "lmhead_grid", "lmhead_grid_scales",
 ]
 
 
@@ -267,6 +268,97 @@ def sweep_152k(seed: int = 5, B: int = 1, gamma: int = 3, V: int = 152064,
 # --------------------------------------------------------------------------- tree workload
 
 TREE_BRANCHING = (4, 3, 2, 2, 1, 1)
+
+
+@dataclass
+class LmHeadInputs:
+    """Inputs of one fused LM-head + chain verify call (host arrays, bf16 bit patterns).
+
+    hidden_t [B*(gamma+1), Ht]  final hidden states of the target at the gamma+1 positions
+    head_t   [V, Ht]            the target's LM head
+    hidden_d [B*gamma, Hd]      the drafter's final hidden states at its gamma positions
+    head_d   [V, Hd]            the drafter's LM head
+    uniforms [B, gamma+1]       float32, as for ChainInputs
+    (the draft tokens come from the drafter's own distribution, which needs its logits: the
+    caller draws them)
+    """
+    name: str
+    B: int
+    gamma: int
+    hidden_t: np.ndarray
+    head_t: np.ndarray
+    hidden_d: np.ndarray
+    head_d: np.ndarray
+    uniforms: np.ndarray
+    temperature: float
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def V(self) -> int:
+        return self.head_t.shape[0]
+
+
+def lmhead_grid_scales(Ht: int, Hd: int, target_sigma: float = 3.0,
+                       draft_sigma: float = 1.0) -> dict:
+    """Integer ranges of the LM-head recipe (see lmhead_grid): hidden entries a / 8 with a
+    uniform on [-4, 4]; head entries c / 64 with c uniform on [-m, m], m chosen per block of
+    columns so that the logits have the requested spread. s = min(Ht, Hd) columns are shared by
+    the two models; the rest belong to one model only."""
+    s = min(Ht, Hd)
+    var_h = 20.0 / 3.0 / 64.0                      # variance of a / 8, a uniform on [-4, 4]
+
+    def m_for(var_logit, cols):
+        if cols <= 0:
+            return 0
+        var_c = var_logit / (cols * var_h)          # variance of c / 64
+        return int(min(63, max(1, round(64.0 * np.sqrt(3.0 * var_c)))))
+
+    half = 0.5 * draft_sigma ** 2
+    return {"shared": s, "m_shared": m_for(target_sigma ** 2, s),
+            "m_target_only": m_for(half, Ht - s), "m_delta": m_for(half, s),
+            "m_draft_only": m_for(half, Hd - s)}
+
+
+def lmhead_grid(seed: int = 8, B: int = 30, gamma: int = 5, V: int = 4096, Ht: int = 640,
+                Hd: int = 256, temperature: float = 1.0, target_sigma: float = 3.0,
+                draft_sigma: float = 1.0) -> LmHeadInputs:
+    """LM-head workload on an integer grid: every hidden entry is a / 8 and every head entry
+    c / 64 with small integers a, c, so each logit is an integer multiple of 2^-9 below 2^15 in
+    magnitude: every partial sum of its dot product is exact in fp32, in any order, and the
+    stored bf16 logit is the correctly rounded exact value whichever way a kernel sums.
+
+    Structure (a drafter that resembles the target): the first s = min(Ht, Hd) hidden
+    components of a drafted position are the target's at that position, and the drafter's head
+    on them is the target's plus a small integer perturbation; the remaining components are
+    each model's own. The target logits spread about N(0, target_sigma^2) (a sum of many small
+    products), the draft logits differ from them by about N(0, draft_sigma^2)."""
+    r_h, r_w, r_d, r_u = _rngs(seed, 4)
+    sc = lmhead_grid_scales(Ht, Hd, target_sigma, draft_sigma)
+    s = sc["shared"]
+    Mt, Md = B * (gamma + 1), B * gamma
+
+    def ints(rng, shape, m):
+        return rng.integers(-m, m + 1, size=shape).astype(np.float32)
+
+    ht = ints(r_h, (Mt, Ht), 4) / 8
+    wt = np.empty((V, Ht), np.float32)
+    wt[:, :s] = ints(r_w, (V, s), sc["m_shared"]) / 64
+    if Ht > s:
+        wt[:, s:] = ints(r_w, (V, Ht - s), sc["m_target_only"]) / 64
+    rows_t = (np.arange(B)[:, None] * (gamma + 1) + np.arange(gamma)[None, :]).reshape(-1)
+    hd = np.empty((Md, Hd), np.float32)
+    hd[:, :s] = ht[rows_t, :s]
+    if Hd > s:
+        hd[:, s:] = ints(r_d, (Md, Hd - s), 4) / 8
+    wd = np.empty((V, Hd), np.float32)
+    wd[:, :s] = wt[:, :s] + ints(r_d, (V, s), sc["m_delta"]) / 64
+    if Hd > s:
+        wd[:, s:] = ints(r_d, (V, Hd - s), sc["m_draft_only"]) / 64
+    u = make_uniforms(r_u, (B, gamma + 1))
+    return LmHeadInputs(f"lmhead_grid_B{B}_g{gamma}_V{V}_Ht{Ht}_Hd{Hd}", B, gamma,
+                        f32_to_bf16(ht), f32_to_bf16(wt), f32_to_bf16(hd), f32_to_bf16(wd), u,
+                        float(temperature), dict(sc, target_sigma=target_sigma,
+                                                 draft_sigma=draft_sigma))
 
 
 def tree_shape(rng: np.random.Generator, n_nodes: int = 64,
