@@ -63,12 +63,15 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 #define SPEC_ERR_NONFINITE (-20) /* a logits row has NaN or +inf, or no finite entry          */
 #define SPEC_ERR_TOKEN (-21)     /* a draft / node token is outside [0, V)                    */
 #define SPEC_ERR_PARENT (-22)    /* parents[b,0] != -1 or parents[b,i] not in [0, i)          */
+#define SPEC_ERR_TIMEOUT (-23)   /* a bounded wait inside a kernel gave up (an on-chip copy or
+                                    tensor-core result did not arrive within 2 s)             */
 #define SPEC_ERR_CHECK (-24)     /* checked build only (libspec_verify_checked.so): an index the
                                     kernels computed fell outside its buffer; the access was
                                     skipped. Never seen from a correct library.               */
 
 /* limits */
 #define SPEC_MAX_V (1 << 20)   /* vocabulary size                                            */
+#define SPEC_LMHEAD_MAX_V (1 << 19)   /* vocabulary size of spec_verify_chain_lmhead          */
 #define SPEC_MAX_GAMMA 255     /* draft length of the chain                                  */
 #define SPEC_MAX_NODES 1024    /* nodes per candidate tree                                   */
 
@@ -135,6 +138,43 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
                      const int32_t *node_tokens, int B, int N, int V, int32_t *accept_len,
                      int32_t *path_nodes, int32_t *out_tokens, int32_t *status,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Chain verification (T > 0) fused with its logit producer: the target's and the drafter's LM
+ * heads evaluated on the 5th-generation tensor cores, logits = hidden states x head^T (bf16
+ * inputs, fp32 accumulation, logits stored as bf16), with the softmax reduction that verification
+ * starts with computed from the accumulators in the GEMM's epilogue, so that no pass reads the
+ * logits back for it. The target scores every drafted position in one parallel pass ("Fast
+ * Inference from Transformers via Speculative Decoding", pith.science review, "The pith"); this
+ * is that pass's last layer with verification's first step fused in. The verification itself is
+ * spec_verify_chain's, on the stored logits:
+ *   logits_t[b*(gamma+1) + i, :] = bf16(hidden_t[b*(gamma+1) + i, :] . head_t^T)  (i = 0 .. gamma)
+ *   logits_d[b*gamma + i, :]     = bf16(hidden_d[b*gamma + i, :] . head_d^T)      (i < gamma)
+ * (dot products accumulated in fp32, rounded to nearest-even bf16)
+ * then accept_len / out_tokens exactly as spec_verify_chain(logits_t, logits_d, ...) defines them.
+ *
+ *   hidden_t  [B*(gamma+1), Ht] bf16       hidden_d [B*gamma, Hd] bf16 (the positions' final
+ *                                          hidden states, row-major; Ht = hidden_t_size, Hd =
+ *                                          hidden_d_size: the drafter may be a smaller model)
+ *   head_t [V, Ht] bf16, head_d [V, Hd]    the two LM heads (row-major: one row per token)
+ *   logits_t  [B*(gamma+1), V] bf16 out    logits_d [B*gamma, V] bf16 out (also read back by
+ *                                          the draw)
+ *   draft_tokens, uniforms, accept_len, out_tokens, status: as for spec_verify_chain
+ *   workspace  at least spec_lmhead_workspace_bytes(B, gamma, V) bytes (scratch)
+ * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, V a multiple of 256 in [256, SPEC_LMHEAD_MAX_V], Ht and Hd
+ * positive multiples of 64, temperature in [FLT_MIN, FLT_MAX] (the greedy case is not offered here: use
+ * spec_verify_chain at T = 0 on the logits); every matrix 16-byte aligned. A non-finite hidden
+ * state or head row makes its logits rows non-finite: the batch row reports -1. A wait inside
+ * the GEMM that gives up (after 2 s) sets *status to SPEC_ERR_TIMEOUT.
+ */
+size_t spec_lmhead_workspace_bytes(int B, int gamma, int V);
+int spec_verify_chain_lmhead(const void *hidden_t, const void *head_t, int hidden_t_size,
+                             const void *hidden_d, const void *head_d, int hidden_d_size,
+                             const int32_t *draft_tokens,
+                             const float *uniforms, int B, int gamma, int V, float temperature,
+                             void *logits_t, void *logits_d, int32_t *accept_len,
+                             int32_t *out_tokens, int32_t *status, void *workspace,
+                             size_t workspace_bytes, void *stream);
 
 /*
  * Stochastic (T > 0) tree verification, batched over B candidate trees of N nodes: the walk of

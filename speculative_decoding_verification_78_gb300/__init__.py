@@ -9,9 +9,10 @@ from ._binding import (  # noqa: F401
     CHECKED_LIB_PATH, EXPORTS, LIB_PATH, SPEC_BF16, SPEC_CALL_CHAIN, SPEC_CALL_PROBS, SPEC_CALL_TREE,
     SPEC_ERR_ALIGN, SPEC_ERR_DTYPE, SPEC_ERR_LAUNCH, SPEC_ERR_NONFINITE, SPEC_ERR_NULL,
     SPEC_ERR_CHECK, SPEC_ERR_PARENT, SPEC_ERR_SHAPE, SPEC_ERR_TEMP, SPEC_ERR_TOKEN, SPEC_ERR_WORKSPACE, SPEC_F32,
-    SPEC_MAX_GAMMA, SPEC_MAX_NODES, SPEC_MAX_V, SPEC_OK, SPEC_STATIC_SCRATCH_BYTES, SpecError,
+    SPEC_MAX_GAMMA, SPEC_MAX_NODES, SPEC_MAX_V, SPEC_LMHEAD_MAX_V, SPEC_OK, SPEC_STATIC_SCRATCH_BYTES, SpecError,
     SPEC_MAX_TOPK, check, dtype_flag, load_library, new_workspace, probs, sample,
     spec_launch_shape, spec_probs, spec_sample, spec_status_string, spec_topk, spec_tree_mask,
     spec_verify_chain, spec_verify_chain_static, spec_verify_tree, spec_verify_tree_sample,
     spec_workspace_bytes,
-    spec_workspace_init, topk, tree_mask, verify_chain, verify_tree, verify_tree_sample)
+    spec_workspace_init, topk, tree_mask, verify_chain, verify_chain_lmhead, verify_tree,
+    verify_tree_sample, spec_verify_chain_lmhead, spec_lmhead_workspace_bytes, SPEC_ERR_TIMEOUT)

@@ -23,11 +23,14 @@ SPEC_OK = 0
 SPEC_ERR_NULL, SPEC_ERR_SHAPE, SPEC_ERR_TEMP, SPEC_ERR_DTYPE = -1, -2, -3, -4
 SPEC_ERR_WORKSPACE, SPEC_ERR_ALIGN, SPEC_ERR_LAUNCH = -5, -6, -7
 SPEC_ERR_NONFINITE, SPEC_ERR_TOKEN, SPEC_ERR_PARENT, SPEC_ERR_CHECK = -20, -21, -22, -24
+SPEC_ERR_TIMEOUT = -23
 SPEC_MAX_V, SPEC_MAX_GAMMA, SPEC_MAX_NODES = 1 << 20, 255, 1024
+SPEC_LMHEAD_MAX_V = 1 << 19
 
 # every symbol include/spec_verify.h declares
 EXPORTS = ("spec_workspace_bytes", "spec_workspace_init", "spec_verify_chain",
-           "spec_verify_tree", "spec_verify_tree_sample", "spec_probs", "spec_status_string",
+           "spec_verify_tree", "spec_verify_tree_sample", "spec_lmhead_workspace_bytes",
+           "spec_verify_chain_lmhead", "spec_probs", "spec_status_string",
            "spec_launch_shape", "spec_verify_chain_static", "spec_sample", "spec_topk",
            "spec_tree_mask")
 SPEC_MAX_TOPK = 16
@@ -71,6 +74,11 @@ def load_library(checked: bool = False):
         lib.spec_verify_tree_sample.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32,
                                                 vp, vp, vp, vp, vp, sz, vp]
         lib.spec_verify_tree_sample.restype = i32
+        lib.spec_lmhead_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.spec_lmhead_workspace_bytes.restype = sz
+        lib.spec_verify_chain_lmhead.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, i32, i32, i32,
+                                                 f32, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_chain_lmhead.restype = i32
         lib.spec_probs.argtypes = [vp, i32, i32, i32, f32, vp, vp, vp, sz, vp]
         lib.spec_probs.restype = i32
         lib.spec_status_string.argtypes = [i32]
@@ -232,6 +240,34 @@ def spec_verify_tree_sample(target_logits, draft_logits, parents, node_tokens, u
         _stream(stream))
 
 
+def spec_lmhead_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    return int(load_library().spec_lmhead_workspace_bytes(B, gamma, V))
+
+
+def spec_verify_chain_lmhead(hidden_t, head_t, hidden_d, head_d, draft_tokens, uniforms,
+                             temperature, logits_t, logits_d, accept_len, out_tokens, status,
+                             workspace, stream=None) -> int:
+    """hidden_t [B*(gamma+1), Ht], head_t [V, Ht], hidden_d [B*gamma, Hd], head_d [V, Hd] (bf16);
+    draft_tokens [B, gamma] int32, uniforms [B, gamma+1] fp32; logits_t / logits_d bf16 outputs;
+    accept_len [B], out_tokens [B, gamma+1] int32; status [1]; workspace uint8."""
+    B, gamma = draft_tokens.shape
+    V, Ht = head_t.shape
+    Hd = head_d.shape[1]
+    _expect(head_t, "head_t", V * Ht, (torch.bfloat16,))
+    _expect(head_d, "head_d", V * Hd, (torch.bfloat16,))
+    _expect(hidden_t, "hidden_t", B * (gamma + 1) * Ht, (torch.bfloat16,))
+    _expect(hidden_d, "hidden_d", B * gamma * Hd, (torch.bfloat16,))
+    _expect(logits_t, "logits_t", B * (gamma + 1) * V, (torch.bfloat16,))
+    _expect(logits_d, "logits_d", B * gamma * V, (torch.bfloat16,))
+    _expect(draft_tokens, "draft_tokens", B * gamma, (torch.int32,))
+    _expect(uniforms, "uniforms", B * (gamma + 1), (torch.float32,))
+    return load_library().spec_verify_chain_lmhead(
+        _ptr(hidden_t), _ptr(head_t), Ht, _ptr(hidden_d), _ptr(head_d), Hd, _ptr(draft_tokens),
+        _ptr(uniforms), B, gamma, V, float(temperature), _ptr(logits_t), _ptr(logits_d),
+        _ptr(accept_len), _ptr(out_tokens), _ptr(status), _ptr(workspace), _nbytes(workspace),
+        _stream(stream))
+
+
 def spec_probs(logits, temperature, out_probs, status, workspace, stream=None) -> int:
     """logits [..., V] -> out_probs [..., V] fp32."""
     V = logits.shape[-1]
@@ -347,6 +383,29 @@ def verify_tree_sample(target_logits, draft_logits, parents, node_tokens, unifor
                                   temperature, acc, path, out, st, workspace, stream),
           "spec_verify_tree_sample")
     return acc, path, out, st
+
+
+def verify_chain_lmhead(hidden_t, head_t, hidden_d, head_d, draft_tokens, uniforms,
+                        temperature, workspace=None, stream=None):
+    """Allocates the outputs and runs spec_verify_chain_lmhead. Returns (accept_len, out_tokens,
+    status, logits_t, logits_d) device tensors."""
+    B, gamma = draft_tokens.shape
+    V = head_t.shape[0]
+    dev = hidden_t.device
+    if workspace is None:
+        n = spec_lmhead_workspace_bytes(B, gamma, V)
+        if n == 0:
+            raise SpecError(SPEC_ERR_SHAPE, "spec_lmhead_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    lt = torch.empty((B * (gamma + 1), V), dtype=torch.bfloat16, device=dev)
+    ld = torch.empty((B * gamma, V), dtype=torch.bfloat16, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    check(spec_verify_chain_lmhead(hidden_t, head_t, hidden_d, head_d, draft_tokens, uniforms,
+                                   temperature, lt, ld, acc, out, st, workspace, stream),
+          "spec_verify_chain_lmhead")
+    return acc, out, st, lt, ld
 
 
 def probs(logits, temperature, workspace=None, stream=None):

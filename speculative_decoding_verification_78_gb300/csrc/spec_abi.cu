@@ -2,6 +2,7 @@
 // workspace layout, launch configuration, and dispatch to the kernel instances.
 #include <cuda_runtime.h>
 #include <float.h>
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -313,6 +314,59 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
+size_t spec_lmhead_workspace_bytes(int B, int gamma, int V) {
+  if (B < 0 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 256 || V % 256 ||
+      V > SPEC_LMHEAD_MAX_V)
+    return 0;
+  return layout(B, 2LL * gamma + 1, V / 256).total;
+}
+
+int spec_verify_chain_lmhead(const void *hidden_t, const void *head_t, int hidden_t_size,
+                             const void *hidden_d, const void *head_d, int hidden_d_size,
+                             const int32_t *draft_tokens,
+                             const float *uniforms, int B, int gamma, int V, float temperature,
+                             void *logits_t, void *logits_d, int32_t *accept_len,
+                             int32_t *out_tokens, int32_t *status, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+  if (B < 0 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 256 || V % 256 ||
+      V > SPEC_LMHEAD_MAX_V || hidden_t_size < 64 || hidden_t_size % 64 || hidden_d_size < 64 ||
+      hidden_d_size % 64 ||
+      static_cast<long long>(B) * (2 * gamma + 1) * (V / 256) > INT_MAX)
+    return SPEC_ERR_SHAPE;
+  if (!(temperature >= FLT_MIN && temperature <= FLT_MAX)) return SPEC_ERR_TEMP;
+  if (!hidden_t || !head_t || !hidden_d || !head_d || !draft_tokens || !uniforms || !logits_t ||
+      !logits_d || !accept_len || !out_tokens || !status || !workspace)
+    return SPEC_ERR_NULL;
+  if (!aligned(hidden_t, 16) || !aligned(head_t, 16) || !aligned(hidden_d, 16) ||
+      !aligned(head_d, 16) || !aligned(logits_t, 16) || !aligned(logits_d, 16) ||
+      !aligned(draft_tokens, 4) || !aligned(uniforms, 4) || !aligned(accept_len, 4) ||
+      !aligned(out_tokens, 4) || !aligned(status, 4) || !aligned(workspace, 16))
+    return SPEC_ERR_ALIGN;
+  if (B == 0) return SPEC_OK;
+  Params p = blank();
+  chain_shape(p, B, gamma, V, temperature);
+  p.tgt = logits_t;   // written by the producer, re-read by the draw
+  p.drf = logits_d;
+  p.tokens = draft_tokens;
+  p.uniforms = uniforms;
+  p.accept_len = accept_len;
+  p.out_tokens = out_tokens;
+  p.status = status;
+  p.tile_units = 1;
+  p.C = V / 256;   // one partial per 256-column tile of a row
+  p.upb = p.R * p.C;
+  p.units = static_cast<int>(static_cast<long long>(B) * p.upb);
+  const Layout L = layout(B, p.R, p.C);
+  if (workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  p.ws_part = reinterpret_cast<uint2 *>(static_cast<char *>(workspace) + L.part);
+  p.ws_xlogit = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.xlogit);
+  const FinishPlan f = chain_sample_plan(p, SPEC_BF16);
+  const cudaError_t e =
+      launch_lmhead(p, hidden_t, head_t, hidden_t_size, hidden_d, head_d, hidden_d_size, logits_t,
+                    logits_d, f, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
 int spec_verify_tree_sample(const void *target_logits, const void *draft_logits, int dtype,
                             const int32_t *parents, const int32_t *node_tokens,
                             const float *uniforms, int B, int N, int V, float temperature,
@@ -513,6 +567,7 @@ const char *spec_status_string(int code) {
     case SPEC_ERR_TOKEN: return "a draft or node token is outside [0, V)";
     case SPEC_ERR_PARENT: return "a tree parent index is invalid";
     case SPEC_ERR_CHECK: return "checked build: a computed index fell outside its buffer";
+    case SPEC_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
     default: return "unknown status";
   }
 }

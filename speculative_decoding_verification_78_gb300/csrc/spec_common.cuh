@@ -46,6 +46,8 @@ struct Params {
   int topk;                  // top-n: candidates per row (1..SPEC_MAX_TOPK)
   uint32_t *mask_words;      // tree mask output: [B, N, ceil(N / 32)] words
   float c2;                  // log2(e) / T
+  int tile_units;            // chain: units are 256-column tiles of the fused LM-head producer
+                             // (not 4 KB stream units), so the bonus draw takes the full pass
 };
 
 // ------------------------------------------------------------------ element access

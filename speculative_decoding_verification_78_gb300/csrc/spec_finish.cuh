@@ -210,7 +210,7 @@ __device__ inline int chain_accept(const Params &p, int b, float *rowM, float *r
 __device__ __forceinline__ void emit_chain(const Params &p, int b, int n, int tok, const int *x,
                                            int tid, int nthreads) {
   if (!SPEC_CHECK(p, b >= 0 && b < p.B && n >= 0 && n <= p.gamma)) return;
-  SPEC_CHECK(p, tok >= 0 && tok < p.V);
+  (void)SPEC_CHECK(p, tok >= 0 && tok < p.V);
   const int g1 = p.gamma + 1;
   int32_t *o = p.out_tokens + static_cast<long long>(b) * g1;
   for (int j = tid; j < g1; j += nthreads) o[j] = (j < n) ? x[j] : (j == n ? tok : -1);

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 2) finish_chain_sample(Params p) {
     // the bonus draw, from the unit partials when the row has no unaligned head or tail (the
     // same decision on every CTA of the cluster; no CTA has touched a peer's shared memory)
     const RowGeom g = row_geom<E>(row_ptr<E>(p, b, n), p.V);
-    if (g.h == 0 && g.tl == 0) {
+    if (g.h == 0 && g.tl == 0 && !p.tile_units) {
       if (rank == 0 && threadIdx.x < 32)
         bonus_draw_units<E>(p, b, n, rowM[n], rowZ[n], bonus_part, xs);
       return;

@@ -65,6 +65,11 @@ cudaError_t launch_chain(int mode, int dtype, const Params &p, int grid, const F
                          cudaStream_t stream);
 cudaError_t launch_tree(int dtype, const Params &p, int grid, const FinishPlan &f,
                         cudaStream_t stream);
+// Chain verification fused with its logit producer: the tensor-core LM-head GEMMs with the
+// softmax-partial epilogue, then the chain finisher (plan f).
+cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *head_t, int Kt,
+                          const void *hidden_d, const void *head_d, int Kd, void *logits_t,
+                          void *logits_d, const FinishPlan &f, cudaStream_t stream);
 // Stochastic tree verification: the stream kernel over every target and draft row, then one
 // finishing CTA per tree with `smem` bytes of dynamic shared memory.
 cudaError_t launch_tree_sample(int dtype, const Params &p, int grid, size_t smem,

@@ -38,7 +38,8 @@ def test_status_strings(lib):
     import speculative_decoding_verification_78_gb300 as sv
     for code in (sv.SPEC_OK, sv.SPEC_ERR_NULL, sv.SPEC_ERR_SHAPE, sv.SPEC_ERR_TEMP,
                  sv.SPEC_ERR_DTYPE, sv.SPEC_ERR_WORKSPACE, sv.SPEC_ERR_ALIGN, sv.SPEC_ERR_LAUNCH,
-                 sv.SPEC_ERR_NONFINITE, sv.SPEC_ERR_TOKEN, sv.SPEC_ERR_PARENT):
+                 sv.SPEC_ERR_NONFINITE, sv.SPEC_ERR_TOKEN, sv.SPEC_ERR_PARENT,
+                 sv.SPEC_ERR_TIMEOUT, sv.SPEC_ERR_CHECK):
         assert sv.spec_status_string(code) != "unknown status"
     assert sv.spec_status_string(12345) == "unknown status"
 
@@ -135,6 +136,47 @@ def test_tree_and_probs_host_validation(lib):
     assert pr(out=FAKE + 1) == sv.SPEC_ERR_ALIGN
     assert pr(wsb=16) == sv.SPEC_ERR_WORKSPACE
     assert pr(rows=0) == sv.SPEC_OK
+
+
+def test_lmhead_host_validation(lib):
+    """spec_verify_chain_lmhead rejects bad shapes, temperatures, pointers, alignment and short
+    workspaces on the host, before any CUDA call."""
+    import speculative_decoding_verification_78_gb300 as sv
+    vp = ctypes.c_void_p
+
+    def lm(**kw):
+        a = dict(ht=FAKE, wt=FAKE, Ht=256, hd=FAKE, wd=FAKE, Hd=128, tok=FAKE, uni=FAKE, B=4,
+                 g=3, V=1024, T=1.0, lt=FAKE, ld=FAKE, acc=FAKE, out=FAKE, st=FAKE, ws=FAKE,
+                 wsb=1 << 30)
+        a.update(kw)
+        return lib.spec_verify_chain_lmhead(
+            vp(a["ht"]), vp(a["wt"]), a["Ht"], vp(a["hd"]), vp(a["wd"]), a["Hd"], vp(a["tok"]),
+            vp(a["uni"]), a["B"], a["g"], a["V"], a["T"], vp(a["lt"]), vp(a["ld"]),
+            vp(a["acc"]), vp(a["out"]), vp(a["st"]), vp(a["ws"]), a["wsb"], None)
+
+    assert lm(V=1000) == sv.SPEC_ERR_SHAPE                 # not a multiple of 256
+    assert lm(V=0) == sv.SPEC_ERR_SHAPE
+    assert lm(V=sv.SPEC_LMHEAD_MAX_V + 256) == sv.SPEC_ERR_SHAPE
+    assert lm(Ht=100) == sv.SPEC_ERR_SHAPE                 # not a multiple of 64
+    assert lm(Hd=0) == sv.SPEC_ERR_SHAPE
+    assert lm(g=0) == sv.SPEC_ERR_SHAPE                    # nothing to verify
+    assert lm(g=sv.SPEC_MAX_GAMMA + 1) == sv.SPEC_ERR_SHAPE
+    assert lm(B=-1) == sv.SPEC_ERR_SHAPE
+    assert lm(T=0.0) == sv.SPEC_ERR_TEMP                   # greedy: spec_verify_chain
+    assert lm(T=float("nan")) == sv.SPEC_ERR_TEMP
+    for k in ("ht", "wt", "hd", "wd", "tok", "uni", "lt", "ld", "acc", "out", "st", "ws"):
+        assert lm(**{k: 0}) == sv.SPEC_ERR_NULL, k
+    for k in ("ht", "wt", "hd", "wd", "lt", "ld", "ws"):
+        assert lm(**{k: FAKE + 8}) == sv.SPEC_ERR_ALIGN, k   # 16-byte alignment
+    assert lm(tok=FAKE + 2) == sv.SPEC_ERR_ALIGN
+    need = sv.spec_lmhead_workspace_bytes(4, 3, 1024)
+    assert need > 0 and need % 256 == 0
+    assert lm(wsb=need - 1) == sv.SPEC_ERR_WORKSPACE
+    assert lm(B=0) == sv.SPEC_OK
+    assert sv.spec_lmhead_workspace_bytes(4, 3, 1000) == 0
+    assert sv.spec_lmhead_workspace_bytes(4, 0, 1024) == 0
+    # one partial per 256-column tile: more than the verify step's own workspace
+    assert need > sv.spec_workspace_bytes(4, 3, 1024, sv.SPEC_BF16)
 
 
 def test_helpers_host_validation(lib):

@@ -12,7 +12,7 @@ from __future__ import annotations
 
 import torch
 
-from .synthetic import BF16
+from .synthetic import BF16, lmhead_grid_scales
 
 
 def device_chain(B: int, gamma: int, V: int, dtype: int, temperature: float,
@@ -56,8 +56,58 @@ def device_chain(B: int, gamma: int, V: int, dtype: int, temperature: float,
     return tgt, drf, tok, uni
 
 
+def device_lmhead_grid(B: int, gamma: int, V: int, Ht: int, Hd: int, temperature: float,
+                       target_sigma: float = 3.0, draft_sigma: float = 1.0, seed: int = 0,
+                       device="cuda", block_rows: int = 512):
+    """workloads.synthetic.lmhead_grid's recipe drawn on `device`: integer-grid hidden states
+    (a / 8) and LM heads (c / 64) in bf16, the drafter sharing the first min(Ht, Hd) hidden
+    components with the target and perturbing its head there. Draft tokens are the drafter's
+    own samples: the Gumbel-max trick on its logits, which are formed here with a plain torch
+    matrix product (the drafter's last layer, upstream of verification), block_rows rows at a
+    time. Returns (hidden_t, head_t, hidden_d, head_d, tokens [B, gamma] int32, uniforms
+    [B, gamma+1] fp32) device tensors."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    sc = lmhead_grid_scales(Ht, Hd, target_sigma, draft_sigma)
+    s = sc["shared"]
+    Mt, Md = B * (gamma + 1), B * gamma
+    bf = torch.bfloat16
+
+    def ints(shape, m):
+        return torch.randint(-m, m + 1, shape, generator=g, device=device, dtype=torch.int32)
+
+    hidden_t = (ints((Mt, Ht), 4).float() / 8).to(bf)
+    head_t = torch.empty((V, Ht), dtype=bf, device=device)
+    head_t[:, :s] = (ints((V, s), sc["m_shared"]).float() / 64).to(bf)
+    if Ht > s:
+        head_t[:, s:] = (ints((V, Ht - s), sc["m_target_only"]).float() / 64).to(bf)
+    rows_t = (torch.arange(B, device=device)[:, None] * (gamma + 1) +
+              torch.arange(gamma, device=device)[None, :]).reshape(-1)
+    hidden_d = torch.empty((Md, Hd), dtype=bf, device=device)
+    hidden_d[:, :s] = hidden_t[rows_t, :s]
+    if Hd > s:
+        hidden_d[:, s:] = (ints((Md, Hd - s), 4).float() / 8).to(bf)
+    head_d = torch.empty((V, Hd), dtype=bf, device=device)
+    head_d[:, :s] = (head_t[:, :s].float() + ints((V, s), sc["m_delta"]).float() / 64).to(bf)
+    if Hd > s:
+        head_d[:, s:] = (ints((V, Hd - s), sc["m_draft_only"]).float() / 64).to(bf)
+    tok = torch.empty(Md, dtype=torch.int32, device=device)
+    wd = head_d.float()
+    for r0 in range(0, Md, block_rows):
+        r1 = min(Md, r0 + block_rows)
+        lg = hidden_d[r0:r1].float() @ wd.T
+        if temperature > 0:
+            u = torch.rand(lg.shape, generator=g, device=device).clamp_min_(1e-30)
+            lg = lg / temperature - torch.log(-torch.log(u))
+        tok[r0:r1] = torch.argmax(lg, dim=-1).to(torch.int32)
+    del wd
+    k = torch.randint(0, 1 << 23, (B, gamma + 1), generator=g, device=device)
+    uni = ((2 * k + 1).to(torch.float64) / float(1 << 24)).to(torch.float32)
+    return hidden_t, head_t, hidden_d, head_d, tok.view(B, gamma), uni
+
+
 def logits_bytes(B: int, rows: int, V: int, dtype: int) -> int:
     return B * rows * V * (2 if dtype == BF16 else 4)
 
 
-__all__ = ["device_chain", "logits_bytes"]
+__all__ = ["device_chain", "device_lmhead_grid", "logits_bytes"]
