@@ -154,6 +154,21 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+def measured_tensor_peaks():
+    """Dense bf16 tensor throughput (TFLOP/s) of this GPU model from MEASURED_PEAKS.json: the
+    burst figure (a cuBLAS GEMM timed alone) and the sustained one (back to back for seconds
+    under the power cap); the fallback figures when the file is absent."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"burst": float(d["bf16_tflops"]),
+                "sustained": float(d.get("bf16_tflops_sustained", 0.0)) or None,
+                "source": "measured (MEASURED_PEAKS.json, cuBLAS bf16 GEMM)"}
+    except Exception:
+        return {"burst": 1900.0, "sustained": 1700.0, "source": "fallback"}
+
+
 def kernel_source_hash():
     """Hash of the sources that define the kernels and their launches (the C ABI's host checks
     and the static-scratch entry point do not change what a kernel reads or writes)."""
@@ -331,7 +346,11 @@ def time_calls(call, ncopies, stream, min_calls=50):
 ROW_NAMES = ("cfg1_chain_tiny", "cfg2_chain_32k", "cfg3_sigma0.25", "cfg3_sigma1", "cfg3_sigma4",
              "cfg4_tree_32k", "cfg5_B1_g3", "cfg5_B1_g7", "cfg5_B16_g3", "cfg5_B16_g7",
              "cfg5_B128_g3", "cfg5_B128_g7", "cfg5_B1024_g3", "cfg5_B1024_g7", "probs_32k",
-             "tree_sample_32k")
+             "tree_sample_32k", "lmhead_cfg2", "lmhead_cfg3")
+
+# fused LM-head rows: (batch, gamma, V, target hidden size, drafter hidden size, temperature)
+LMHEAD_SHAPES = {"lmhead_cfg2": (64, 5, 32000, 4096, 1024, 1.0),
+                 "lmhead_cfg3": (256, 8, 128256, 4096, 2048, 0.7)}
 
 
 def _dev(a, device):
@@ -377,12 +396,89 @@ def row_inputs(name, device):
     raise KeyError(name)
 
 
+def lmhead_row(name, lib, sv, device, stream, min_calls):
+    """Chain verification with its logits produced by the LM heads: the fused path
+    (spec_verify_chain_lmhead: tcgen05 GEMMs whose epilogue emits the softmax partials, then the
+    chain finisher) against the unfused one (two cuBLAS bf16 GEMMs through torch.matmul writing
+    the logits, then spec_verify_chain reading them), and the two cuBLAS GEMMs alone. Integer-grid
+    inputs drawn on the device; the heads (about 1.5 GB at V=128256) exceed L2 many times over,
+    so every call reads them from HBM."""
+    import torch
+    from workloads.device import device_lmhead_grid
+    B, g, V, Ht, Hd, T = LMHEAD_SHAPES[name]
+    ht, wt, hd, wd, tok, uni = device_lmhead_grid(B, g, V, Ht, Hd, T, seed=900, device=device)
+    Mt, Md = B * (g + 1), B * g
+    lt = torch.empty((Mt, V), dtype=torch.bfloat16, device=device)
+    ld = torch.empty((Md, V), dtype=torch.bfloat16, device=device)
+    lt2, ld2 = torch.empty_like(lt), torch.empty_like(ld)
+    acc = torch.empty(B, dtype=torch.int32, device=device)
+    out = torch.empty((B, g + 1), dtype=torch.int32, device=device)
+    acc2, out2 = torch.empty_like(acc), torch.empty_like(out)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    ws = torch.empty(sv.spec_lmhead_workspace_bytes(B, g, V), dtype=torch.uint8, device=device)
+    ws2 = sv.new_workspace(B, 2 * g + 1, V, sv.SPEC_BF16, device)
+    vp = ctypes.c_void_p
+    sp = vp(stream.cuda_stream)
+    fused_args = (vp(ht.data_ptr()), vp(wt.data_ptr()), Ht, vp(hd.data_ptr()), vp(wd.data_ptr()),
+                  Hd, vp(tok.data_ptr()), vp(uni.data_ptr()), B, g, V, ctypes.c_float(T),
+                  vp(lt.data_ptr()), vp(ld.data_ptr()), vp(acc.data_ptr()), vp(out.data_ptr()),
+                  vp(st.data_ptr()), vp(ws.data_ptr()), ws.numel(), sp)
+    verify_args = (vp(lt2.data_ptr()), vp(ld2.data_ptr()), sv.SPEC_BF16, vp(tok.data_ptr()),
+                   vp(uni.data_ptr()), B, g, V, ctypes.c_float(T), vp(acc2.data_ptr()),
+                   vp(out2.data_ptr()), vp(st.data_ptr()), vp(ws2.data_ptr()), ws2.numel(), sp)
+    torch.cuda.synchronize()
+
+    def fused(k):
+        rc = lib.spec_verify_chain_lmhead(*fused_args)
+        if rc:
+            raise RuntimeError(f"spec_verify_chain_lmhead failed: {rc}")
+
+    def gemms(k):
+        torch.matmul(ht, wt.T, out=lt2)
+        torch.matmul(hd, wd.T, out=ld2)
+
+    def unfused(k):
+        gemms(k)
+        rc = lib.spec_verify_chain(*verify_args)
+        if rc:
+            raise RuntimeError(f"spec_verify_chain failed: {rc}")
+
+    flops = 2.0 * (Mt * Ht + Md * Hd) * V
+    peaks = measured_tensor_peaks()
+    res = {"shape": (f"B={B} gamma={g} V={V} bf16, target hidden {Ht}, drafter hidden {Hd}, "
+                     f"T={T}; integer-grid hidden states and heads drawn on the device"),
+           "gemm_flops_per_call": flops,
+           "tensor_peak_TFLOPs": peaks}
+    for arm, fn in (("fused", fused), ("cublas_gemms_plus_verify", unfused),
+                    ("cublas_gemms_only", gemms)):
+        med, lo, hi, n = time_calls(fn, 1, stream, min_calls)
+        tf = flops / med / 1e12
+        res[arm] = {"us_median": med * 1e6, "us_min": lo * 1e6, "us_max": hi * 1e6,
+                    "calls_timed": n, "TFLOPs": tf,
+                    "frac_of_burst_peak": tf / peaks["burst"] if peaks["burst"] else None,
+                    "frac_of_sustained_peak": (tf / peaks["sustained"] if peaks["sustained"]
+                                               else None)}
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"{name}: device-side error {int(st.item())}")
+    res["fused_logits_equal_cublas"] = bool(torch.equal(lt, lt2) and torch.equal(ld, ld2))
+    res["verified_positions_per_call"] = B * (g + 1)
+    res["positions_per_s_fused"] = B * (g + 1) / (res["fused"]["us_median"] * 1e-6)
+    res["step_stats"] = accept_stats(acc.cpu().numpy(), g)
+    return res
+
+
 def measure_rows(names, lib, sv, device, stream, peak, min_calls):
     import torch
     from workloads import BF16, chain_32k, tree_32k
     rows = {}
     for name in names:
         torch.cuda.nvtx.range_push(f"row {name}")
+        if name in LMHEAD_SHAPES:
+            rows[name] = lmhead_row(name, lib, sv, device, stream, min_calls)
+            torch.cuda.nvtx.range_pop()
+            torch.cuda.empty_cache()
+            continue
         if name == "cfg4_tree_32k":
             ti = tree_32k()
             nbytes = tree_bytes(ti.B, ti.N, ti.V, 2)

@@ -286,6 +286,15 @@ int spec_tree_mask(const int32_t *parents, int B, int N, uint32_t *mask_words, i
 const char *spec_status_string(int code);
 
 /*
+ * The CUDA runtime error (a cudaError_t value) behind the most recent SPEC_ERR_LAUNCH that a call
+ * of this library returned on the calling thread, 0 if there was none; and its text. Lets a
+ * caller tell a missing device, a launch the device cannot fit and an earlier sticky fault
+ * apart. Thread-local; never reset by a successful call.
+ */
+int spec_last_cuda_error(void);
+const char *spec_cuda_error_string(int cuda_error);
+
+/*
  * The kernel launches a call of the given shape makes on the current device; it enqueues
  * nothing and touches no memory (for tests and profiling; the pages have no counterpart).
  *   kind        SPEC_CALL_CHAIN (rows_per_b = 2*gamma+1, any temperature), SPEC_CALL_TREE

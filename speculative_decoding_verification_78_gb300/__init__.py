@@ -15,4 +15,5 @@ from ._binding import (  # noqa: F401
     spec_verify_chain, spec_verify_chain_static, spec_verify_tree, spec_verify_tree_sample,
     spec_workspace_bytes,
     spec_workspace_init, topk, tree_mask, verify_chain, verify_chain_lmhead, verify_tree,
-    verify_tree_sample, spec_verify_chain_lmhead, spec_lmhead_workspace_bytes, SPEC_ERR_TIMEOUT)
+    verify_tree_sample, spec_verify_chain_lmhead, spec_lmhead_workspace_bytes, SPEC_ERR_TIMEOUT,
+    spec_last_cuda_error, spec_cuda_error_string)

@@ -31,6 +31,7 @@ SPEC_LMHEAD_MAX_V = 1 << 19
 EXPORTS = ("spec_workspace_bytes", "spec_workspace_init", "spec_verify_chain",
            "spec_verify_tree", "spec_verify_tree_sample", "spec_lmhead_workspace_bytes",
            "spec_verify_chain_lmhead", "spec_probs", "spec_status_string",
+           "spec_last_cuda_error", "spec_cuda_error_string",
            "spec_launch_shape", "spec_verify_chain_static", "spec_sample", "spec_topk",
            "spec_tree_mask")
 SPEC_MAX_TOPK = 16
@@ -45,7 +46,12 @@ _checked_lib = None
 class SpecError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {spec_status_string(code)} ({code})")
+        msg = f"{where}: {spec_status_string(code)} ({code})"
+        if code == SPEC_ERR_LAUNCH:
+            ce = spec_last_cuda_error()
+            if ce:
+                msg += f"; CUDA error {ce}: {spec_cuda_error_string(ce)}"
+        super().__init__(msg)
 
 
 def load_library(checked: bool = False):
@@ -83,6 +89,10 @@ def load_library(checked: bool = False):
         lib.spec_probs.restype = i32
         lib.spec_status_string.argtypes = [i32]
         lib.spec_status_string.restype = ctypes.c_char_p
+        lib.spec_last_cuda_error.argtypes = []
+        lib.spec_last_cuda_error.restype = i32
+        lib.spec_cuda_error_string.argtypes = [i32]
+        lib.spec_cuda_error_string.restype = ctypes.c_char_p
         lib.spec_launch_shape.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp]
         lib.spec_launch_shape.restype = i32
         lib.spec_verify_chain_static.argtypes = [vp, vp, i32, vp, vp, i32, i32, i32, f32, vp, vp,
@@ -318,6 +328,18 @@ def spec_status_string(code: int) -> str:
         return load_library().spec_status_string(int(code)).decode()
     except ImportError:
         return f"status {code}"
+
+
+def spec_last_cuda_error() -> int:
+    """The cudaError_t behind this thread's last SPEC_ERR_LAUNCH (0 if none)."""
+    try:
+        return int(load_library().spec_last_cuda_error())
+    except ImportError:
+        return 0
+
+
+def spec_cuda_error_string(cuda_error: int) -> str:
+    return load_library().spec_cuda_error_string(int(cuda_error)).decode()
 
 
 # ------------------------------------------------------------------ conveniences (allocation)

@@ -211,6 +211,15 @@ FinishPlan probs_finish(const Params &p, int dtype) {
 
 namespace specv {
 
+// The CUDA error behind the last SPEC_ERR_LAUNCH returned on this thread (spec_last_cuda_error).
+thread_local int g_last_cuda_error = 0;
+
+int launch_result(cudaError_t e) {
+  if (e == cudaSuccess) return SPEC_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return SPEC_ERR_LAUNCH;
+}
+
 // The host checks of a chain call, in the order the header documents: dtype, shape,
 // temperature, null pointers, alignment. The workspace is checked only when asked (the
 // static-scratch entry point has none); nothing here needs a device.
@@ -249,10 +258,8 @@ size_t spec_workspace_bytes(int B, int rows_per_b, int V, int dtype) {
 int spec_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
   if (!workspace) return SPEC_ERR_NULL;
   if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
-  if (cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
-    return SPEC_ERR_LAUNCH;
-  return SPEC_OK;
+  return specv::launch_result(
+      cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 int spec_verify_chain(const void *target_logits, const void *draft_logits, int dtype,
@@ -280,7 +287,7 @@ int spec_verify_chain(const void *target_logits, const void *draft_logits, int d
   const FinishPlan f = chain_finish(p, greedy, dtype);
   const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
                                      f, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return specv::launch_result(e);
 }
 
 int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parents,
@@ -311,7 +318,7 @@ int spec_verify_tree(const void *target_logits, int dtype, const int32_t *parent
   if (rc != SPEC_OK) return rc;
   const FinishPlan f = tree_finish(p);
   const cudaError_t e = launch_tree(dtype, p, grid_for(p), f, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return specv::launch_result(e);
 }
 
 size_t spec_lmhead_workspace_bytes(int B, int gamma, int V) {
@@ -364,7 +371,7 @@ int spec_verify_chain_lmhead(const void *hidden_t, const void *head_t, int hidde
   const cudaError_t e =
       launch_lmhead(p, hidden_t, head_t, hidden_t_size, hidden_d, head_d, hidden_d_size, logits_t,
                     logits_d, f, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return specv::launch_result(e);
 }
 
 int spec_verify_tree_sample(const void *target_logits, const void *draft_logits, int dtype,
@@ -414,7 +421,7 @@ int spec_verify_tree_sample(const void *target_logits, const void *draft_logits,
                       sizeof(float) * static_cast<size_t>((V + kSeg - 1) / kSeg);
   const cudaError_t e = launch_tree_sample(dtype, p, grid_for(p), smem,
                                            static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return specv::launch_result(e);
 }
 
 int spec_probs(const void *logits, int dtype, int rows, int V, float temperature,
@@ -438,7 +445,7 @@ int spec_probs(const void *logits, int dtype, int rows, int V, float temperature
   if (rc != SPEC_OK) return rc;
   const cudaError_t e = launch_probs(greedy ? kProbsGreedy : kProbs, dtype, p, grid_for(p),
                                      probs_finish(p, dtype), static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return specv::launch_result(e);
 }
 
 int spec_sample(const void *logits, int dtype, int rows, int V, float temperature,
@@ -467,7 +474,7 @@ int spec_sample(const void *logits, int dtype, int rows, int V, float temperatur
   const FinishPlan f = chain_finish(p, greedy, dtype);
   const cudaError_t e = launch_chain(greedy ? kChainGreedy : kChainSample, dtype, p, grid_for(p),
                                      f, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return specv::launch_result(e);
 }
 
 int spec_topk(const void *logits, int dtype, int rows, int V, int k, int32_t *out_idx,
@@ -497,7 +504,7 @@ int spec_topk(const void *logits, int dtype, int rows, int V, int k, int32_t *ou
   const int grid = static_cast<int>(groups < cap ? groups : cap);
   const cudaError_t e = launch_topk(dtype, p, grid < 1 ? 1 : grid,
                                     static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return specv::launch_result(e);
 }
 
 int spec_tree_mask(const int32_t *parents, int B, int N, uint32_t *mask_words, int32_t *status,
@@ -514,7 +521,7 @@ int spec_tree_mask(const int32_t *parents, int B, int N, uint32_t *mask_words, i
   p.B = B;
   p.N = N;
   const cudaError_t e = launch_tree_mask(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+  return specv::launch_result(e);
 }
 
 int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float temperature,
@@ -551,6 +558,12 @@ int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float t
   *grid = f.grid;
   *cluster = f.cluster;
   return SPEC_OK;
+}
+
+int spec_last_cuda_error(void) { return specv::g_last_cuda_error; }
+
+const char *spec_cuda_error_string(int cuda_error) {
+  return cudaGetErrorString(static_cast<cudaError_t>(cuda_error));
 }
 
 const char *spec_status_string(int code) {

@@ -1,6 +1,6 @@
 // spec_kernels_tree.cu -- kernel instances for tree verification: greedy, and stochastic (the
 // walk by per-sibling rejection sampling).
-#include <atomic>
+#include <mutex>
 
 #include "spec_launch.h"
 
@@ -8,23 +8,26 @@ namespace specv {
 
 namespace {
 
-// The walk's finishing kernel needs more than the default 48 KB of dynamic shared memory for the
-// largest trees and vocabularies: its limit is raised to the device's opt-in maximum once per
-// device.
+// The walk's finishing kernel needs more than the default 48 KB of shared memory for the largest
+// trees and vocabularies. Its dynamic limit is raised only that far, to the largest size a call
+// has needed so far on the device (a kernel launched right after one whose limit sat at the
+// device maximum failed to launch in a measured experiment, so the limit is kept no higher than
+// it must be).
 template <typename E>
 cudaError_t tree_sample(const Params &p, int grid, size_t smem, cudaStream_t stream) {
-  static std::atomic<int> raised[64];
+  static std::mutex mu;
+  static size_t limit[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !raised[dev].load(std::memory_order_acquire)) {
-    int optin = 0;
-    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(finish_tree_sample<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             optin - static_cast<int>(sizeof(TsShared)));
-    if (e != cudaSuccess) return e;
-    if (dev < 64) raised[dev].store(1, std::memory_order_release);
+  if (smem + sizeof(TsShared) > 48 * 1024) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 64 || smem > limit[dev]) {
+      e = cudaFuncSetAttribute(finish_tree_sample<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      if (dev < 64) limit[dev] = smem;
+    }
   }
   e = launch_stream<E, kProbs>(p, grid, stream);
   if (e != cudaSuccess) return e;

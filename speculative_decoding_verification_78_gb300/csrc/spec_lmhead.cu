@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t full[kLmStages], empty[kLmStages], accum;
   __shared__ uint32_t tmem_slot;
+  // the finishing kernel may be scheduled once every CTA of this grid has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool draft = static_cast<int>(blockIdx.x) >= a.rt_t;
@@ -74,7 +75,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t taddr = tmem_slot;
-  // hidden states, heads and tokens may come from the kernel ahead of this one
+  // launched in stream order, so the kernel ahead has completed: this wait returns at once; it
+  // keeps the kernel correct if it is ever launched as a programmatic dependent
   asm volatile("griddepcontrol.wait;" ::: "memory");
   bool timed_out = false;
   if (warp == 0 && lane == 0) {   // producer: TMA loads into the ring
@@ -258,17 +260,17 @@ cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *hea
   a.Kd = Kd;
   a.rt_t = (Mt + kLmBM - 1) / kLmBM;
   const int rt_d = (Md + kLmBM - 1) / kLmBM;
-  // row tiles fastest: CTAs that read the same head tile run together, so it is read once
+  // row tiles fastest: CTAs that read the same head tile run together, so it is read once. A
+  // plain stream-ordered launch (not a programmatic dependent of the kernel before it): the GEMM
+  // is long, and a 193 KB kernel launched early beside a predecessor whose shared-memory limit
+  // had been raised to the device maximum failed to launch in a measured experiment.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.rt_t + rt_d), static_cast<unsigned>(p.V / kLmBN), 1);
   cfg.blockDim = dim3(kLmThreads, 1, 1);
   cfg.dynamicSmemBytes = kLmSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
   e = cudaLaunchKernelEx(&cfg, lmhead_stats_kernel, mht, mwt, mhd, mwd, p, a);
   if (e != cudaSuccess) return e;
   if (f.warp_tail)

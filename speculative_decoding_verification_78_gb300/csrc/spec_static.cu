@@ -17,6 +17,7 @@ int chain_args_check(const void *target_logits, const void *draft_logits, int dt
                      const int32_t *draft_tokens, const float *uniforms, int B, int gamma, int V,
                      float temperature, const int32_t *accept_len, const int32_t *out_tokens,
                      const int32_t *status, const void *workspace, bool need_workspace);
+int launch_result(cudaError_t e);   // SPEC_ERR_LAUNCH, recording e for spec_last_cuda_error
 }  // namespace specv
 
 namespace {
@@ -48,12 +49,16 @@ extern "C" int spec_verify_chain_static(const void *target_logits, const void *d
   if (spec_workspace_bytes(B, 2 * gamma + 1, V, dtype) > kStaticScratchBytes)
     return SPEC_ERR_WORKSPACE;
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return SPEC_ERR_LAUNCH;
+  const cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return specv::launch_result(de);
+  if (dev < 0) return SPEC_ERR_LAUNCH;
   // devices beyond the cache table look the address up on every call (same result, slower)
   const bool cached = dev < kMaxDevices;
   void *addr = cached ? g_scratch_addr[dev].load(std::memory_order_acquire) : nullptr;
   if (!addr) {
-    if (cudaGetSymbolAddress(&addr, g_scratch) != cudaSuccess || !addr) return SPEC_ERR_LAUNCH;
+    const cudaError_t se = cudaGetSymbolAddress(&addr, g_scratch);
+    if (se != cudaSuccess) return specv::launch_result(se);
+    if (!addr) return SPEC_ERR_LAUNCH;
     if (cached) g_scratch_addr[dev].store(addr, std::memory_order_release);
   }
   return spec_verify_chain(target_logits, draft_logits, dtype, draft_tokens, uniforms, B, gamma,

@@ -44,6 +44,22 @@ def test_status_strings(lib):
     assert sv.spec_status_string(12345) == "unknown status"
 
 
+def test_launch_failure_reports_cuda_error(lib):
+    """With arguments that pass every host check, a call on a machine without a usable device
+    fails at launch; the CUDA error behind it is kept for the caller."""
+    import torch
+    import speculative_decoding_verification_78_gb300 as sv
+    if torch.cuda.is_available():
+        pytest.skip("a device is present: the launch would run")
+    need = sv.spec_workspace_bytes(4, 7, 1000, 1)
+    assert _chain(lib, wsb=need) == sv.SPEC_ERR_LAUNCH
+    ce = sv.spec_last_cuda_error()
+    assert ce != 0
+    assert sv.spec_cuda_error_string(ce)
+    err = sv.SpecError(sv.SPEC_ERR_LAUNCH, "spec_verify_chain")
+    assert f"CUDA error {ce}" in str(err)
+
+
 def test_workspace_bytes(lib):
     import speculative_decoding_verification_78_gb300 as sv
     a = sv.spec_workspace_bytes(64, 11, 32000, sv.SPEC_BF16)

@@ -149,3 +149,30 @@ def test_lmhead_full_size(orc):
                      ld_ref.reshape(len(sel), g, V), BF16, tok.cpu().numpy()[sel],
                      uni.cpu().numpy()[sel], T)
     compare_chain(orc, ci, (acc.cpu().numpy()[sel], out.cpu().numpy()[sel], 0))
+
+
+def test_lmhead_after_large_tree_sample_on_one_stream():
+    """The GEMM (193 KB of shared memory per CTA) launched right after the stochastic-tree
+    finisher at its largest shared-memory size (N = 1024 nodes, V = 600064: the limit raised past
+    the default), and the other way round, on one stream: every call launches and succeeds."""
+    import speculative_decoding_verification_78_gb300 as sv
+    from workloads import tree_shape
+    rng = np.random.default_rng(41)
+    B, N, V = 1, 1024, 600064
+    g = torch.Generator(device="cuda")
+    g.manual_seed(41)
+    tgt = (torch.randn((B, N, V), generator=g, device="cuda") * 2).to(torch.bfloat16)
+    drf = (tgt.float() + torch.randn((B, N, V), generator=g, device="cuda")).to(torch.bfloat16)
+    par = torch.from_numpy(tree_shape(rng, N, branching=(4, 4, 4, 4, 4, 4))[None]).cuda()
+    tok = torch.randint(0, V, (B, N), generator=g, device="cuda", dtype=torch.int32)
+    uni = torch.rand((B, N), generator=g, device="cuda").clamp_(1e-6, 1 - 1e-6)
+    li = lmhead_grid(seed=2, B=8, gamma=3, V=1024, Ht=128, Hd=64)
+    toks = torch.from_numpy(rng.integers(0, 1024, (8, 3)).astype(np.int32)).cuda()
+    unis = torch.from_numpy(li.uniforms).cuda()
+    for _ in range(2):
+        acc, path, out, st = sv.verify_tree_sample(tgt, drf, par, tok, uni, 1.0)
+        r = sv.verify_chain_lmhead(dev(li.hidden_t), dev(li.head_t), dev(li.hidden_d),
+                                   dev(li.head_d), toks, unis, 1.0)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0 and int(acc[0].item()) >= 0
+        assert int(r[2].item()) == 0
