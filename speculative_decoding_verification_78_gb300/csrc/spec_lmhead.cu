@@ -6,15 +6,20 @@
 // Decoding", pith.science, "The pith") has the target score every drafted position in one
 // parallel pass; this is that pass's last layer, with the verify step's first reduction fused in.
 //
-// Tile: 128 rows x 256 vocabulary columns per CTA, K (the hidden size) in blocks of 64. Warp 0
-// issues TMA loads of the hidden-state and head tiles (128-byte swizzle) into a 4-stage ring;
-// warp 1 allocates 256 tensor-memory columns and issues the MMAs (one thread; 4 x K=16 per
-// block); warps 2-5 wait for the accumulator and read it back, one row per thread: each fp32
-// value is rounded to bf16 (the stored logit), the 256 stored values of the row give one (max,
-// sum of 2^((l - max) log2(e)/T)) partial, the row's drafted token's logit is recorded when it
-// falls in the tile, and the bf16 logits are written out (the draw of the finishing kernel
-// re-reads the two rows where each step stopped). The finishing kernel is the chain finisher,
-// with 256-column tiles as its units.
+// Persistent: one CTA per SM walks the output tiles blockIdx.x, blockIdx.x + G, ... (128 rows x
+// 256 vocabulary columns each, row tiles fastest so that the CTAs running at one time share
+// their head tiles in L2). Warp 0 streams the hidden-state and head tiles of every K block (64
+// wide) of every tile through a 4-stage TMA ring (128-byte swizzle) without draining it between
+// tiles; warp 1 owns 512 tensor-memory columns, two accumulators, and one of its threads issues
+// the MMAs (4 x K=16 per block) of tile i into accumulator i mod 2; warps 2-5 read tile i's
+// accumulator (one row per thread) while the MMAs of tile i+1 run in the other one: each fp32
+// value is rounded to bf16 (the stored logit), the row's 256 stored values give one (max, sum
+// of 2^((l - max) log2(e)/T)) partial, the drafted token's logit is kept when it falls in the
+// tile, and the bf16 logits are written out (the finishing kernel re-reads the two rows where
+// each step stopped). The finishing kernel is the chain finisher, with 256-column tiles as its
+// units.
+#include <limits.h>
+
 #include <atomic>
 
 #include <cudaTypedefs.h>
@@ -26,20 +31,117 @@ namespace specv {
 
 namespace {
 
-constexpr int kLmBM = 128, kLmBN = 256, kLmBK = 64, kLmStages = 4;
+constexpr int kLmBM = 128, kLmBN = 256, kLmBK = 64, kLmStages = 4, kLmAcc = 2;
 constexpr int kLmABytes = kLmBM * kLmBK * 2;
 constexpr int kLmBBytes = kLmBN * kLmBK * 2;
 constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
-constexpr int kLmThreads = 192;
+constexpr int kLmEpiWarps = 4;
+constexpr int kLmThreads = 32 * (2 + kLmEpiWarps);
 constexpr int kLmSmem = kLmStages * kLmStageBytes + 1024;   // + alignment of the ring to 1 KB
+constexpr uint32_t kLmTmemCols = kLmAcc * kLmBN;            // 512: all of an SM's tensor memory
 
 struct LmArgs {
   uint16_t *logits_t;   // [Mt, V] bf16 out
   uint16_t *logits_d;   // [Md, V] bf16 out
   int Mt, Md;           // B * (gamma + 1), B * gamma
   int Kt, Kd;           // hidden sizes of the target and of the drafter
-  int rt_t;             // row tiles of the target GEMM (the draft's follow)
+  int rt_t, rt;         // row tiles of the target GEMM; of both (the draft's follow)
+  int tiles;            // rt * (V / 256)
 };
+
+// Tile t: row tile t mod rt (the target's first, then the drafter's), column tile t / rt.
+struct LmTile {
+  bool draft;
+  int m0, M, ctile, KB;
+};
+
+__device__ __forceinline__ LmTile lm_tile(const LmArgs &a, int t) {
+  LmTile x;
+  const int r = t % a.rt;
+  x.ctile = t / a.rt;
+  x.draft = r >= a.rt_t;
+  x.m0 = (x.draft ? r - a.rt_t : r) * kLmBM;
+  x.M = x.draft ? a.Md : a.Mt;
+  x.KB = (x.draft ? a.Kd : a.Kt) / kLmBK;
+  return x;
+}
+
+// The epilogue of one accumulator row: thread `row` of the tile (tensor-memory lane q*32+lane).
+__device__ __forceinline__ void lm_epilogue_row(const Params &p, const LmArgs &a, const LmTile &x,
+                                                uint32_t tacc, int q, int lane) {
+  const int j = x.m0 + q * 32 + lane;
+  const bool valid = j < x.M;
+  const int g1 = p.gamma + 1;
+  int b = 0, r = 0, tok = -1;
+  if (valid) {
+    if (x.draft) {
+      b = j / p.gamma;
+      const int i = j - b * p.gamma;
+      r = g1 + i;
+      tok = __ldg(p.tokens + static_cast<long long>(b) * p.gamma + i);
+    } else {
+      b = j / g1;
+      const int i = j - b * g1;
+      r = i;
+      tok = i < p.gamma ? __ldg(p.tokens + static_cast<long long>(b) * p.gamma + i) : -1;
+    }
+  }
+  const int n0 = x.ctile * kLmBN;
+  const float c2 = p.c2;
+  uint16_t *out = (x.draft ? a.logits_d : a.logits_t) + static_cast<long long>(j) * p.V + n0;
+  float m = -INFINITY, s = 0.f, xval = 0.f;
+  bool has_x = false;
+#pragma unroll 1
+  for (int c = 0; c < kLmBN / 32; ++c) {
+    uint32_t v[32];
+    tc::tmem_load32(tacc + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 32),
+                    v);
+    // round to the stored bf16 logits; the statistics are taken on those values
+    uint32_t h[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * e])));
+      const uint32_t hi =
+          __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * e + 1])));
+      h[e] = lo | (hi << 16);
+    }
+    if (valid) {
+      uint4 *o = reinterpret_cast<uint4 *>(out + c * 32);
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        o[t] = make_uint4(h[4 * t], h[4 * t + 1], h[4 * t + 2], h[4 * t + 3]);
+    }
+    float cm = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) cm = fmax_nan(cm, fmax_nan(bf_lo(h[e]), bf_hi(h[e])));
+    float cs = 0.f;
+    if (cm != -INFINITY) {
+      f32x2 acc = pk2(0.f, 0.f);
+      const f32x2 m2 = pk2(cm, cm), c22 = pk2(c2, c2);
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        acc = add2(acc, ex2_shift2(pk2(bf_lo(h[e]), bf_hi(h[e])), m2, c22));
+      float a0, a1;
+      up2(acc, a0, a1);
+      cs = __fadd_rn(a0, a1);
+    }
+    stat_merge(m, s, cm, cs, c2);
+    const int rel = tok - (n0 + c * 32);
+    if (rel >= 0 && rel < 32) {
+      uint32_t w = h[0];
+#pragma unroll
+      for (int e = 1; e < 16; ++e)
+        if (e == (rel >> 1)) w = h[e];
+      xval = (rel & 1) ? bf_hi(w) : bf_lo(w);
+      has_x = true;
+    }
+  }
+  if (valid) {
+    const long long row = static_cast<long long>(b) * p.R + r;
+    p.ws_part[row * p.C + x.ctile] = make_uint2(__float_as_uint(m), __float_as_uint(s));
+    if (has_x) p.ws_xlogit[row] = xval;
+  }
+}
 
 __global__ void __launch_bounds__(kLmThreads, 1)
     lmhead_stats_kernel(const __grid_constant__ CUtensorMap map_ht,
@@ -49,28 +151,26 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t *ring = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full[kLmStages], empty[kLmStages], accum;
+  __shared__ __align__(8) uint64_t full[kLmStages], empty[kLmStages];
+  __shared__ __align__(8) uint64_t acc_full[kLmAcc], acc_empty[kLmAcc], mma_done;
   __shared__ uint32_t tmem_slot;
   // the finishing kernel may be scheduled once every CTA of this grid has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool draft = static_cast<int>(blockIdx.x) >= a.rt_t;
-  const int m0 = (draft ? static_cast<int>(blockIdx.x) - a.rt_t : static_cast<int>(blockIdx.x)) *
-                 kLmBM;
-  const int M = draft ? a.Md : a.Mt;
-  const int ctile = blockIdx.y, n0 = ctile * kLmBN;
-  const int KB = (draft ? a.Kd : a.Kt) / kLmBK;
-  const CUtensorMap *mh = draft ? &map_hd : &map_ht;
-  const CUtensorMap *mw = draft ? &map_wd : &map_wt;
+  const int G = static_cast<int>(gridDim.x);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLmStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(&accum, 1);
+    for (int b = 0; b < kLmAcc; ++b) {
+      tc::mbar_init(&acc_full[b], 1);
+      tc::mbar_init(&acc_empty[b], kLmEpiWarps);
+    }
+    tc::mbar_init(&mma_done, 1);
     tc::mbar_fence_init();
   }
-  if (warp == 1) tc::tmem_alloc(&tmem_slot, kLmBN);
+  if (warp == 1) tc::tmem_alloc(&tmem_slot, kLmTmemCols);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -79,117 +179,79 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   // keeps the kernel correct if it is ever launched as a programmatic dependent
   asm volatile("griddepcontrol.wait;" ::: "memory");
   bool timed_out = false;
-  if (warp == 0 && lane == 0) {   // producer: TMA loads into the ring
-    int issued = 0;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % kLmStages;
-      const uint32_t ph = (kb / kLmStages) & 1;
-      if (!tc::mbar_wait(&empty[s], ph ^ 1)) { timed_out = true; break; }
-      uint8_t *st = ring + s * kLmStageBytes;
-      tc::mbar_expect_tx(&full[s], kLmStageBytes);
-      tc::tma_load_2d(st, mh, kb * kLmBK, m0, &full[s]);
-      tc::tma_load_2d(st + kLmABytes, mw, kb * kLmBK, n0, &full[s]);
-      ++issued;
+  if (warp == 0 && lane == 0) {   // producer: TMA loads of every K block of every tile
+    int it = 0;   // K blocks issued so far (all tiles)
+    for (int t = blockIdx.x; t < a.tiles && !timed_out; t += G) {
+      const LmTile x = lm_tile(a, t);
+      const CUtensorMap *mh = x.draft ? &map_hd : &map_ht;
+      const CUtensorMap *mw = x.draft ? &map_wd : &map_wt;
+      for (int kb = 0; kb < x.KB; ++kb, ++it) {
+        const int s = it % kLmStages;
+        if (!tc::mbar_wait(&empty[s], ((it / kLmStages) & 1) ^ 1)) {
+          timed_out = true;
+          break;
+        }
+        uint8_t *st = ring + s * kLmStageBytes;
+        tc::mbar_expect_tx(&full[s], kLmStageBytes);
+        tc::tma_load_2d(st, mh, kb * kLmBK, x.m0, &full[s]);
+        tc::tma_load_2d(st + kLmABytes, mw, kb * kLmBK, x.ctile * kLmBN, &full[s]);
+      }
     }
     // no copy may still be landing in shared memory when the CTA exits: only the last load of
     // each stage can be (an earlier one was consumed before the stage was refilled)
-    for (int t = issued > kLmStages ? issued - kLmStages : 0; t < issued; ++t)
-      if (!tc::mbar_wait(&full[t % kLmStages], (t / kLmStages) & 1)) timed_out = true;
+    for (int q = it > kLmStages ? it - kLmStages : 0; q < it; ++q)
+      if (!tc::mbar_wait(&full[q % kLmStages], (q / kLmStages) & 1)) timed_out = true;
   } else if (warp == 1 && lane == 0) {   // the MMA thread
     constexpr uint32_t idesc = tc::bf16_f32_idesc(kLmBM, kLmBN);
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % kLmStages;
-      const uint32_t ph = (kb / kLmStages) & 1;
-      if (!tc::mbar_wait(&full[s], ph)) { timed_out = true; break; }
+    int it = 0, i = 0;   // K blocks consumed; tiles done
+    for (int t = blockIdx.x; t < a.tiles && !timed_out; t += G, ++i) {
+      const LmTile x = lm_tile(a, t);
+      const int buf = i & 1;
+      // the epilogue has read this accumulator's previous tile
+      if (!tc::mbar_wait(&acc_empty[buf], ((i >> 1) & 1) ^ 1)) {
+        timed_out = true;
+        break;
+      }
       tc::fence_after_sync();
-      const uint32_t sa = tc::saddr(ring + s * kLmStageBytes);
-      const uint64_t ad = tc::sw128_kmajor_desc(sa), bd = tc::sw128_kmajor_desc(sa + kLmABytes);
+      const uint32_t d = taddr + static_cast<uint32_t>(buf * kLmBN);
+      for (int kb = 0; kb < x.KB; ++kb, ++it) {
+        const int s = it % kLmStages;
+        if (!tc::mbar_wait(&full[s], (it / kLmStages) & 1)) {
+          timed_out = true;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t sa = tc::saddr(ring + s * kLmStageBytes);
+        const uint64_t ad = tc::sw128_kmajor_desc(sa), bd = tc::sw128_kmajor_desc(sa + kLmABytes);
 #pragma unroll
-      for (int k = 0; k < kLmBK / 16; ++k)
-        tc::mma_bf16(taddr, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k),
-                     idesc, (kb | k) != 0);
-      tc::mma_commit(&empty[s]);   // the stage is free once these MMAs have read it
+        for (int k = 0; k < kLmBK / 16; ++k)
+          tc::mma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k),
+                       idesc, (kb | k) != 0);
+        tc::mma_commit(&empty[s]);   // the stage is free once these MMAs have read it
+      }
+      if (timed_out) break;
+      tc::mma_commit(&acc_full[buf]);   // the tile's accumulator is complete
     }
-    // also after a timeout: the MMAs already issued complete before tensor memory is freed
-    tc::mma_commit(&accum);
-    if (!tc::mbar_wait(&accum, 0)) timed_out = true;
+    // every MMA issued has completed before tensor memory is freed (also after a timeout)
+    tc::mma_commit(&mma_done);
+    if (!tc::mbar_wait(&mma_done, 0)) timed_out = true;
   } else if (warp >= 2) {   // epilogue: one accumulator row per thread
     const int q = warp & 3;   // this warp's tensor-memory lanes: 32 q .. 32 q + 31
-    const int j = m0 + q * 32 + lane;
-    const bool valid = j < M;
-    const int g1 = p.gamma + 1;
-    int b = 0, r = 0, x = -1;
-    if (valid) {
-      if (draft) {
-        b = j / p.gamma;
-        const int i = j - b * p.gamma;
-        r = g1 + i;
-        x = __ldg(p.tokens + static_cast<long long>(b) * p.gamma + i);
-      } else {
-        b = j / g1;
-        const int i = j - b * g1;
-        r = i;
-        x = i < p.gamma ? __ldg(p.tokens + static_cast<long long>(b) * p.gamma + i) : -1;
+    int i = 0;
+    for (int t = blockIdx.x; t < a.tiles; t += G, ++i) {
+      const LmTile x = lm_tile(a, t);
+      const int buf = i & 1;
+      const bool ok = tc::mbar_wait(&acc_full[buf], (i >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        timed_out = true;
+        break;
       }
-    }
-    if (!tc::mbar_wait(&accum, 0)) {
-      timed_out = true;
-    } else {
       tc::fence_after_sync();
-      const float c2 = p.c2;
-      uint16_t *out = (draft ? a.logits_d : a.logits_t) + static_cast<long long>(j) * p.V + n0;
-      float m = -INFINITY, s = 0.f, xval = 0.f;
-      bool has_x = false;
-#pragma unroll 1
-      for (int c = 0; c < kLmBN / 32; ++c) {
-        uint32_t v[32];
-        tc::tmem_load32(taddr + (static_cast<uint32_t>(q * 32) << 16) +
-                            static_cast<uint32_t>(c * 32),
-                        v);
-        // round to the stored bf16 logits; the statistics are taken on those values
-        uint32_t h[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * e])));
-          const uint32_t hi =
-              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * e + 1])));
-          h[e] = lo | (hi << 16);
-        }
-        if (valid) {
-          uint4 *o = reinterpret_cast<uint4 *>(out + c * 32);
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            o[t] = make_uint4(h[4 * t], h[4 * t + 1], h[4 * t + 2], h[4 * t + 3]);
-        }
-        float cm = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) cm = fmax_nan(cm, fmax_nan(bf_lo(h[e]), bf_hi(h[e])));
-        float cs = 0.f;
-        if (cm != -INFINITY) {
-          f32x2 acc = pk2(0.f, 0.f);
-          const f32x2 m2 = pk2(cm, cm), c22 = pk2(c2, c2);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) acc = add2(acc, ex2_shift2(pk2(bf_lo(h[e]), bf_hi(h[e])), m2, c22));
-          float a0, a1;
-          up2(acc, a0, a1);
-          cs = __fadd_rn(a0, a1);
-        }
-        stat_merge(m, s, cm, cs, c2);
-        const int rel = x - (n0 + c * 32);
-        if (rel >= 0 && rel < 32) {
-          uint32_t w = h[0];
-#pragma unroll
-          for (int e = 1; e < 16; ++e)
-            if (e == (rel >> 1)) w = h[e];
-          xval = (rel & 1) ? bf_hi(w) : bf_lo(w);
-          has_x = true;
-        }
-      }
-      if (valid) {
-        const long long row = static_cast<long long>(b) * p.R + r;
-        p.ws_part[row * p.C + ctile] = make_uint2(__float_as_uint(m), __float_as_uint(s));
-        if (has_x) p.ws_xlogit[row] = xval;
-      }
+      lm_epilogue_row(p, a, x, taddr + static_cast<uint32_t>(buf * kLmBN), q, lane);
+      // this warp's reads of the accumulator are complete: the MMAs may overwrite it
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
     }
   }
   if (timed_out) set_status(p.status, SPEC_ERR_TIMEOUT);
@@ -197,7 +259,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_free(taddr, kLmBN);
+    tc::tmem_free(taddr, kLmTmemCols);
   }
 }
 
@@ -237,6 +299,7 @@ cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *hea
                           const void *hidden_d, const void *head_d, int Kd, void *logits_t,
                           void *logits_d, const FinishPlan &f, cudaStream_t stream) {
   static std::atomic<int> raised[64];
+  static std::atomic<int> sms[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -245,6 +308,12 @@ cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *hea
                              kLmSmem);
     if (e != cudaSuccess) return e;
     if (dev < 64) raised[dev].store(1, std::memory_order_release);
+  }
+  int n_sm = dev < 64 ? sms[dev].load(std::memory_order_acquire) : 0;
+  if (n_sm <= 0) {
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) sms[dev].store(n_sm, std::memory_order_release);
   }
   const int Mt = p.B * (p.gamma + 1), Md = p.B * p.gamma;
   CUtensorMap mht, mwt, mhd, mwd;
@@ -259,13 +328,17 @@ cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *hea
   a.Kt = Kt;
   a.Kd = Kd;
   a.rt_t = (Mt + kLmBM - 1) / kLmBM;
-  const int rt_d = (Md + kLmBM - 1) / kLmBM;
-  // row tiles fastest: CTAs that read the same head tile run together, so it is read once. A
-  // plain stream-ordered launch (not a programmatic dependent of the kernel before it): the GEMM
-  // is long, and a 193 KB kernel launched early beside a predecessor whose shared-memory limit
-  // had been raised to the device maximum failed to launch in a measured experiment.
+  a.rt = a.rt_t + (Md + kLmBM - 1) / kLmBM;
+  const long long tiles = static_cast<long long>(a.rt) * (p.V / kLmBN);
+  if (tiles > INT_MAX) return cudaErrorInvalidValue;
+  a.tiles = static_cast<int>(tiles);
+  // One persistent CTA per SM. A plain stream-ordered launch (not a programmatic dependent of
+  // the kernel before it): the GEMM is long, and a 193 KB kernel launched early beside a
+  // predecessor whose shared-memory limit had been raised to the device maximum failed to
+  // launch in a measured experiment.
+  const int grid = a.tiles < n_sm ? a.tiles : n_sm;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(a.rt_t + rt_d), static_cast<unsigned>(p.V / kLmBN), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(grid < 1 ? 1 : grid), 1, 1);
   cfg.blockDim = dim3(kLmThreads, 1, 1);
   cfg.dynamicSmemBytes = kLmSmem;
   cfg.stream = stream;

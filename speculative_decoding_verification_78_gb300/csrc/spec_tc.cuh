@@ -53,6 +53,11 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
   return true;
 }
 
+// A plain arrival (no transaction count) on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+
 // A 2-D tile of a tensor map (box given by the map) into shared memory; completion counted on
 // `bar`. c0: innermost coordinate (elements; a multiple of 16 bytes), c1: row.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
