@@ -6,18 +6,23 @@
 // Decoding", pith.science, "The pith") has the target score every drafted position in one
 // parallel pass; this is that pass's last layer, with the verify step's first reduction fused in.
 //
-// Persistent: one CTA per SM walks the output tiles blockIdx.x, blockIdx.x + G, ... (128 rows x
-// 256 vocabulary columns each, row tiles fastest so that the CTAs running at one time share
-// their head tiles in L2). Warp 0 streams the hidden-state and head tiles of every K block (64
-// wide) of every tile through a 4-stage TMA ring (128-byte swizzle) without draining it between
-// tiles; warp 1 owns 512 tensor-memory columns, two accumulators, and one of its threads issues
-// the MMAs (4 x K=16 per block) of tile i into accumulator i mod 2; warps 2-5 read tile i's
-// accumulator (one row per thread) while the MMAs of tile i+1 run in the other one: each fp32
-// value is rounded to bf16 (the stored logit), the row's 256 stored values give one (max, sum
-// of 2^((l - max) log2(e)/T)) partial, the drafted token's logit is kept when it falls in the
-// tile, and the bf16 logits are written out (the finishing kernel re-reads the two rows where
-// each step stopped). The finishing kernel is the chain finisher, with 256-column tiles as its
-// units.
+// Persistent CTA pairs. A cluster of two CTAs (on two SMs) walks the output tiles c, c + NC, ...
+// (NC clusters), each tile 256 rows x 256 vocabulary columns, row tiles fastest so that the
+// clusters running at one time share their head tiles in L2. One 5th-generation MMA
+// (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16) spans the pair: each CTA holds its own
+// 128 hidden-state rows and half of the head tile's 256 rows in shared memory, so an SM loads
+// 32 KB per 64-wide K block instead of the 48 KB a single-CTA 128 x 256 tile needs, and the
+// 192 KB ring holds six stages. Per CTA: warp 0 streams its halves of every K block of every
+// tile through the TMA ring (128-byte swizzle) without draining it between tiles; warp 1 owns
+// 512 tensor-memory columns (two accumulators, allocated by the pair together) — in the even
+// CTA one of its threads issues the pair's MMAs of tile i into accumulator i mod 2 once both
+// CTAs' stages have landed (the odd CTA's copies count their bytes on the even CTA's stage
+// barrier); warps 2-5 read tile i's accumulator (one of the CTA's 128 rows per thread) while the
+// MMAs of tile i+1 run in the other one: each fp32 value is rounded to bf16 (the stored logit),
+// the row's 256 stored values give one (max, sum of 2^((l - max) log2(e)/T)) partial, the
+// drafted token's logit is kept when it falls in the tile, and the bf16 logits are written out
+// (the finishing kernel re-reads the two rows where each step stopped). The finishing kernel is
+// the chain finisher, with 256-column tiles as its units.
 #include <limits.h>
 
 #include <atomic>
@@ -31,36 +36,43 @@ namespace specv {
 
 namespace {
 
-constexpr int kLmBM = 128, kLmBN = 256, kLmBK = 64, kLmStages = 4, kLmAcc = 2;
+constexpr int kLmBM = 128;     // rows of a CTA (the pair's tile: 256)
+constexpr int kLmBN = 256;     // vocabulary columns of a tile (each CTA loads 128 head rows)
+constexpr int kLmBK = 64, kLmStages = 6, kLmAcc = 2;
 constexpr int kLmABytes = kLmBM * kLmBK * 2;
-constexpr int kLmBBytes = kLmBN * kLmBK * 2;
+constexpr int kLmBBytes = (kLmBN / 2) * kLmBK * 2;
 constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
 constexpr int kLmEpiWarps = 4;
 constexpr int kLmThreads = 32 * (2 + kLmEpiWarps);
 constexpr int kLmSmem = kLmStages * kLmStageBytes + 1024;   // + alignment of the ring to 1 KB
 constexpr uint32_t kLmTmemCols = kLmAcc * kLmBN;            // 512: all of an SM's tensor memory
+constexpr uint16_t kLmPairMask = 3;                         // both CTAs of the cluster
 
 struct LmArgs {
   uint16_t *logits_t;   // [Mt, V] bf16 out
   uint16_t *logits_d;   // [Md, V] bf16 out
   int Mt, Md;           // B * (gamma + 1), B * gamma
   int Kt, Kd;           // hidden sizes of the target and of the drafter
-  int rt_t, rt;         // row tiles of the target GEMM; of both (the draft's follow)
+  int rt_t, rt;         // 256-row tiles of the target GEMM; of both (the draft's follow)
   int tiles;            // rt * (V / 256)
 };
 
-// Tile t: row tile t mod rt (the target's first, then the drafter's), column tile t / rt.
+// Tile t: column tile t / rt and, within it, row tile (t + t / rt) mod rt (the target's row
+// tiles first, then the drafter's). The skew keeps a cluster that walks t = c, c + NC, ... from
+// landing on the same row tile every time when NC is a multiple of rt (the target's and the
+// drafter's tiles differ in K, so a fixed row tile would unbalance the clusters). m0 is this
+// CTA's first row (the pair's tile starts 128 rows earlier in the odd CTA).
 struct LmTile {
   bool draft;
   int m0, M, ctile, KB;
 };
 
-__device__ __forceinline__ LmTile lm_tile(const LmArgs &a, int t) {
+__device__ __forceinline__ LmTile lm_tile(const LmArgs &a, int t, int rank) {
   LmTile x;
-  const int r = t % a.rt;
   x.ctile = t / a.rt;
+  const int r = (t - x.ctile * a.rt + x.ctile) % a.rt;
   x.draft = r >= a.rt_t;
-  x.m0 = (x.draft ? r - a.rt_t : r) * kLmBM;
+  x.m0 = (x.draft ? r - a.rt_t : r) * (2 * kLmBM) + rank * kLmBM;
   x.M = x.draft ? a.Md : a.Mt;
   x.KB = (x.draft ? a.Kd : a.Kt) / kLmBK;
   return x;
@@ -157,7 +169,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   // the finishing kernel may be scheduled once every CTA of this grid has started
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = static_cast<int>(gridDim.x);
+  const int rank = static_cast<int>(tc::cluster_rank());
+  const bool leader = rank == 0;
+  const int NC = static_cast<int>(gridDim.x) / 2, c = static_cast<int>(blockIdx.x) / 2;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLmStages; ++s) {
       tc::mbar_init(&full[s], 1);
@@ -165,26 +179,33 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     }
     for (int b = 0; b < kLmAcc; ++b) {
       tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], kLmEpiWarps);
+      tc::mbar_init(&acc_empty[b], 2 * kLmEpiWarps);   // the epilogue warps of both CTAs
     }
     tc::mbar_init(&mma_done, 1);
     tc::mbar_fence_init();
   }
-  if (warp == 1) tc::tmem_alloc(&tmem_slot, kLmTmemCols);
+  if (warp == 1) tc::tmem_alloc_pair(&tmem_slot, kLmTmemCols);
   tc::fence_before_sync();
   __syncthreads();
+  // both CTAs' barriers are initialised and the pair's tensor memory allocated before any
+  // thread touches the other CTA
+  tc::cluster_sync_all();
   tc::fence_after_sync();
   const uint32_t taddr = tmem_slot;
   // launched in stream order, so the kernel ahead has completed: this wait returns at once; it
   // keeps the kernel correct if it is ever launched as a programmatic dependent
   asm volatile("griddepcontrol.wait;" ::: "memory");
   bool timed_out = false;
-  if (warp == 0 && lane == 0) {   // producer: TMA loads of every K block of every tile
+  if (warp == 0 && lane == 0) {   // producer: this CTA's halves of every K block of every tile
+    // both CTAs' copies of a stage count their bytes on the even CTA's barrier of that stage,
+    // which expects the pair's bytes
+    const uint32_t full0 = tc::mapa(tc::saddr(&full[0]), 0);
     int it = 0;   // K blocks issued so far (all tiles)
-    for (int t = blockIdx.x; t < a.tiles && !timed_out; t += G) {
-      const LmTile x = lm_tile(a, t);
+    for (int t = c; t < a.tiles && !timed_out; t += NC) {
+      const LmTile x = lm_tile(a, t, rank);
       const CUtensorMap *mh = x.draft ? &map_hd : &map_ht;
       const CUtensorMap *mw = x.draft ? &map_wd : &map_wt;
+      const int n0 = x.ctile * kLmBN + rank * (kLmBN / 2);
       for (int kb = 0; kb < x.KB; ++kb, ++it) {
         const int s = it % kLmStages;
         if (!tc::mbar_wait(&empty[s], ((it / kLmStages) & 1) ^ 1)) {
@@ -192,23 +213,33 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           break;
         }
         uint8_t *st = ring + s * kLmStageBytes;
-        tc::mbar_expect_tx(&full[s], kLmStageBytes);
-        tc::tma_load_2d(st, mh, kb * kLmBK, x.m0, &full[s]);
-        tc::tma_load_2d(st + kLmABytes, mw, kb * kLmBK, x.ctile * kLmBN, &full[s]);
+        if (leader) tc::mbar_expect_tx(&full[s], 2 * kLmStageBytes);
+        const uint32_t bar = full0 + static_cast<uint32_t>(s * sizeof(uint64_t));
+        tc::tma_load_2d_pair(st, mh, kb * kLmBK, x.m0, bar);
+        tc::tma_load_2d_pair(st + kLmABytes, mw, kb * kLmBK, n0, bar);
       }
     }
-    // no copy may still be landing in shared memory when the CTA exits: only the last load of
-    // each stage can be (an earlier one was consumed before the stage was refilled)
-    for (int q = it > kLmStages ? it - kLmStages : 0; q < it; ++q)
-      if (!tc::mbar_wait(&full[q % kLmStages], (q / kLmStages) & 1)) timed_out = true;
-  } else if (warp == 1 && lane == 0) {   // the MMA thread
-    constexpr uint32_t idesc = tc::bf16_f32_idesc(kLmBM, kLmBN);
+    // no copy may still be landing in shared memory when either CTA exits. The even CTA waits
+    // for the last phase of each stage (the pair's copies); only the last copy of each stage can
+    // be in flight (an earlier one was consumed before the stage was refilled). The odd CTA
+    // cannot wait on those barriers: it stays until the even CTA has (the final cluster barrier),
+    // and after a timeout it also lets any copy it issued past the even CTA's land.
+    if (leader) {
+      for (int q = it > kLmStages ? it - kLmStages : 0; q < it; ++q)
+        if (!tc::mbar_wait(&full[q % kLmStages], (q / kLmStages) & 1)) timed_out = true;
+    } else if (timed_out) {
+      const unsigned long long t0 = tc::now_ns();
+      while (tc::now_ns() - t0 < 100000ull) {
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {   // the pair's MMA thread
+    constexpr uint32_t idesc = tc::bf16_f32_idesc(2 * kLmBM, kLmBN);
     int it = 0, i = 0;   // K blocks consumed; tiles done
-    for (int t = blockIdx.x; t < a.tiles && !timed_out; t += G, ++i) {
-      const LmTile x = lm_tile(a, t);
+    for (int t = c; t < a.tiles && !timed_out; t += NC, ++i) {
+      const LmTile x = lm_tile(a, t, rank);
       const int buf = i & 1;
-      // the epilogue has read this accumulator's previous tile
-      if (!tc::mbar_wait(&acc_empty[buf], ((i >> 1) & 1) ^ 1)) {
+      // both CTAs' epilogues have read this accumulator's previous tile
+      if (!tc::mbar_wait_cluster(&acc_empty[buf], ((i >> 1) & 1) ^ 1)) {
         timed_out = true;
         break;
       }
@@ -216,7 +247,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       const uint32_t d = taddr + static_cast<uint32_t>(buf * kLmBN);
       for (int kb = 0; kb < x.KB; ++kb, ++it) {
         const int s = it % kLmStages;
-        if (!tc::mbar_wait(&full[s], (it / kLmStages) & 1)) {
+        const uint32_t ph = (it / kLmStages) & 1;
+        // both CTAs' halves of the stage have landed
+        if (!tc::mbar_wait(&full[s], ph)) {
           timed_out = true;
           break;
         }
@@ -225,22 +258,31 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         const uint64_t ad = tc::sw128_kmajor_desc(sa), bd = tc::sw128_kmajor_desc(sa + kLmABytes);
 #pragma unroll
         for (int k = 0; k < kLmBK / 16; ++k)
-          tc::mma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k),
-                       idesc, (kb | k) != 0);
-        tc::mma_commit(&empty[s]);   // the stage is free once these MMAs have read it
+          tc::mma_bf16_pair(d, ad + static_cast<uint64_t>(2 * k),
+                            bd + static_cast<uint64_t>(2 * k), idesc, (kb | k) != 0);
+        // both CTAs' stages are free once these MMAs have read them
+        tc::mma_commit_pair(&empty[s], kLmPairMask);
       }
       if (timed_out) break;
-      tc::mma_commit(&acc_full[buf]);   // the tile's accumulator is complete
+      tc::mma_commit_pair(&acc_full[buf], kLmPairMask);   // the tile's accumulators are complete
     }
-    // every MMA issued has completed before tensor memory is freed (also after a timeout)
-    tc::mma_commit(&mma_done);
+    // every MMA issued has completed before either CTA frees its tensor memory or exits (also
+    // after a timeout)
+    tc::mma_commit_pair(&mma_done, kLmPairMask);
+    if (!tc::mbar_wait(&mma_done, 0)) timed_out = true;
+  } else if (warp == 1 && lane == 0) {
+    // odd CTA: the pair's MMAs (which read this CTA's shared memory and write its tensor memory)
+    // are complete before it frees its tensor memory or exits
     if (!tc::mbar_wait(&mma_done, 0)) timed_out = true;
   } else if (warp >= 2) {   // epilogue: one accumulator row per thread
     const int q = warp & 3;   // this warp's tensor-memory lanes: 32 q .. 32 q + 31
+    const uint32_t empty0 = tc::mapa(tc::saddr(&acc_empty[0]), 0);
     int i = 0;
-    for (int t = blockIdx.x; t < a.tiles; t += G, ++i) {
-      const LmTile x = lm_tile(a, t);
+    for (int t = c; t < a.tiles; t += NC, ++i) {
+      const LmTile x = lm_tile(a, t, rank);
       const int buf = i & 1;
+      // the arrival is the MMA unit's (a commit from the even CTA); this CTA then reads only its
+      // own tensor memory, so a CTA-scope wait suffices (and polls far more cheaply)
       const bool ok = tc::mbar_wait(&acc_full[buf], (i >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         timed_out = true;
@@ -251,15 +293,17 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       // this warp's reads of the accumulator are complete: the MMAs may overwrite it
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) tc::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(buf * sizeof(uint64_t)));
     }
   }
   if (timed_out) set_status(p.status, SPEC_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
+  // neither CTA leaves while the other may still arrive on its barriers
+  tc::cluster_sync_all();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_free(taddr, kLmTmemCols);
+    tc::tmem_free_pair(taddr, kLmTmemCols);
   }
 }
 
@@ -298,27 +342,14 @@ bool make_map(CUtensorMap *m, const void *base, int rows, int K, int box_rows) {
 cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *head_t, int Kt,
                           const void *hidden_d, const void *head_d, int Kd, void *logits_t,
                           void *logits_d, const FinishPlan &f, cudaStream_t stream) {
-  static std::atomic<int> raised[64];
-  static std::atomic<int> sms[64];
+  static std::atomic<int> clusters[64];   // co-resident CTA pairs per device (0: not known yet)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !raised[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(lmhead_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kLmSmem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) raised[dev].store(1, std::memory_order_release);
-  }
-  int n_sm = dev < 64 ? sms[dev].load(std::memory_order_acquire) : 0;
-  if (n_sm <= 0) {
-    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) sms[dev].store(n_sm, std::memory_order_release);
-  }
   const int Mt = p.B * (p.gamma + 1), Md = p.B * p.gamma;
   CUtensorMap mht, mwt, mhd, mwd;
-  if (!make_map(&mht, hidden_t, Mt, Kt, kLmBM) || !make_map(&mwt, head_t, p.V, Kt, kLmBN) ||
-      !make_map(&mhd, hidden_d, Md, Kd, kLmBM) || !make_map(&mwd, head_d, p.V, Kd, kLmBN))
+  if (!make_map(&mht, hidden_t, Mt, Kt, kLmBM) || !make_map(&mwt, head_t, p.V, Kt, kLmBN / 2) ||
+      !make_map(&mhd, hidden_d, Md, Kd, kLmBM) || !make_map(&mwd, head_d, p.V, Kd, kLmBN / 2))
     return cudaErrorInvalidValue;
   LmArgs a;
   a.logits_t = static_cast<uint16_t *>(logits_t);
@@ -327,23 +358,44 @@ cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *hea
   a.Md = Md;
   a.Kt = Kt;
   a.Kd = Kd;
-  a.rt_t = (Mt + kLmBM - 1) / kLmBM;
-  a.rt = a.rt_t + (Md + kLmBM - 1) / kLmBM;
+  a.rt_t = (Mt + 2 * kLmBM - 1) / (2 * kLmBM);
+  a.rt = a.rt_t + (Md + 2 * kLmBM - 1) / (2 * kLmBM);
   const long long tiles = static_cast<long long>(a.rt) * (p.V / kLmBN);
   if (tiles > INT_MAX) return cudaErrorInvalidValue;
   a.tiles = static_cast<int>(tiles);
-  // One persistent CTA per SM. A plain stream-ordered launch (not a programmatic dependent of
-  // the kernel before it): the GEMM is long, and a 193 KB kernel launched early beside a
-  // predecessor whose shared-memory limit had been raised to the device maximum failed to
-  // launch in a measured experiment.
-  const int grid = a.tiles < n_sm ? a.tiles : n_sm;
+
+  // Clusters of two CTAs, as many as can be resident at once (a persistent grid must not wait
+  // for a slot). A plain stream-ordered launch (not a programmatic dependent of the kernel before
+  // it): the GEMM is long, and a 193 KB kernel launched early beside a predecessor whose
+  // shared-memory limit had been raised to the device maximum failed to launch in a measured
+  // experiment.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid < 1 ? 1 : grid), 1, 1);
   cfg.blockDim = dim3(kLmThreads, 1, 1);
   cfg.dynamicSmemBytes = kLmSmem;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int ncl = dev < 64 ? clusters[dev].load(std::memory_order_acquire) : 0;
+  if (ncl <= 0) {
+    e = cudaFuncSetAttribute(lmhead_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kLmSmem);
+    if (e != cudaSuccess) return e;
+    int n_sm = 0;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (n_sm / 2)), 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&ncl, lmhead_stats_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (ncl <= 0) return cudaErrorInvalidConfiguration;
+    if (dev < 64) clusters[dev].store(ncl, std::memory_order_release);
+  }
+  const int npair = a.tiles < ncl ? a.tiles : ncl;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (npair < 1 ? 1 : npair)), 1, 1);
   e = cudaLaunchKernelEx(&cfg, lmhead_stats_kernel, mht, mwt, mhd, mwd, p, a);
   if (e != cudaSuccess) return e;
   if (f.warp_tail)
