@@ -12,7 +12,7 @@
 // (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16) spans the pair: each CTA holds its own
 // 128 hidden-state rows and half of the head tile's 256 rows in shared memory, so an SM loads
 // 32 KB per 64-wide K block instead of the 48 KB a single-CTA 128 x 256 tile needs, and the
-// 192 KB ring holds six stages. Per CTA: warp 0 streams its halves of every K block of every
+// 224 KB ring holds seven stages. Per CTA: warp 0 streams its halves of every K block of every
 // tile through the TMA ring (128-byte swizzle) without draining it between tiles; warp 1 owns
 // 512 tensor-memory columns (two accumulators, allocated by the pair together) — in the even
 // CTA one of its threads issues the pair's MMAs of tile i into accumulator i mod 2 once both
@@ -38,7 +38,7 @@ namespace {
 
 constexpr int kLmBM = 128;     // rows of a CTA (the pair's tile: 256)
 constexpr int kLmBN = 256;     // vocabulary columns of a tile (each CTA loads 128 head rows)
-constexpr int kLmBK = 64, kLmStages = 6, kLmAcc = 2;
+constexpr int kLmBK = 64, kLmStages = 7, kLmAcc = 2;
 constexpr int kLmABytes = kLmBM * kLmBK * 2;
 constexpr int kLmBBytes = (kLmBN / 2) * kLmBK * 2;
 constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
