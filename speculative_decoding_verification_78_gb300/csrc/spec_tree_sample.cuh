@@ -14,6 +14,8 @@
 // statistics (rows 0 .. N-1 target, N .. 2N-1 draft); one CTA per tree combines them and walks.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "spec_finish.cuh"
 
 namespace specv {
@@ -299,6 +301,323 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample(Params p) {
       pn[0] = 0;
       ot[sh.depth] = t;
       p.accept_len[b] = sh.depth;
+    }
+    return;
+  }
+}
+
+// ------------------------------------------------------------------ the walk over a cluster
+
+// The walk with one thread-block cluster of S CTAs per tree (blockIdx.x = b * S + rank): every
+// CTA runs the walk's control (the same decisions: they combine the same statistics, load the
+// same children's logits and reduce the same totals in the same order), and CTA `rank` owns
+// the vocabulary slice of segments [rank * nsl, (rank + 1) * nsl). At each visited node a CTA
+// computes p and q of its slice once into shared memory (fp32); every pass after that (each
+// rejection's residual mass, the final draw's segment sums) reads them there. A pass's slice
+// totals are pushed into every CTA of the cluster (two alternating slot arrays, so one cluster
+// barrier per pass) and summed in rank order. The final draw's crossing is found from the
+// slice totals; the CTA holding it picks the token. Rank 0 writes the path and the outputs.
+// Dynamic shared memory: rowM, rowZ [2N]; parents, tokens, children [N]; the slice's segment
+// sums [nsl]; then (16-byte aligned) p and q of the slice, nsl * kSeg floats each.
+struct TsClusterShared {
+  float tot[2][kMaxCluster];   // slice totals of the last two passes, by rank
+};
+
+// p and q of this CTA's slice [k_lo, k_lo + 8 * ngroups) into shared memory (0 past V): groups of
+// 8 elements, four groups per thread in flight.
+template <typename E>
+__device__ __forceinline__ void tsc_stage(const E *P, const E *Q, int V, int k_lo, int ngroups,
+                                          float Mt, float iZt, float Md, float iZd, float c2,
+                                          float *ps, float *qs) {
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(P) | reinterpret_cast<uintptr_t>(Q)) & 15u) == 0;
+  for (int g0 = threadIdx.x; g0 < ngroups; g0 += 4 * kThreads) {
+    uint4 wp[4][2], wq[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * kThreads;
+      const int k0 = g < ngroups ? k_lo + 8 * g : V;   // past V: -inf, p = q = 0
+      load8_raw<E>(P, k0, V, vec_ok, wp[u]);
+      load8_raw<E>(Q, k0, V, vec_ok, wq[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = g0 + u * kThreads;
+      if (g >= ngroups) continue;
+      float pv[8], qv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        pv[e] = __fmul_rn(ex2_shift(raw8_elem<E>(wp[u], e), Mt, c2), iZt);
+        qv[e] = __fmul_rn(ex2_shift(raw8_elem<E>(wq[u], e), Md, c2), iZd);
+      }
+      float4 *pd = reinterpret_cast<float4 *>(ps + 8 * g);
+      float4 *qd = reinterpret_cast<float4 *>(qs + 8 * g);
+      pd[0] = make_float4(pv[0], pv[1], pv[2], pv[3]);
+      pd[1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
+      qd[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+      qd[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
+    }
+  }
+}
+
+// This CTA's slice total of the pass's weight (the update max(0, r - q), or r itself), in a fixed
+// order: a lane's 8 elements, the warp's segments (segment j of the slice: warp j % kWarps),
+// then the warps in order. With `segsum`, each segment's sum is stored too.
+__device__ __forceinline__ float tsc_slice_pass(const float *ps, const float *qs, int nsl,
+                                                const TsShared &sh, bool update, float *segsum,
+                                                float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float wsum = 0.f;
+  for (int j = warp; j < nsl; j += kWarps) {
+    const float4 *pa = reinterpret_cast<const float4 *>(ps + j * kSeg + lane * 8);
+    const float4 *qa = reinterpret_cast<const float4 *>(qs + j * kSeg + lane * 8);
+    const float4 p0 = pa[0], p1 = pa[1], q0 = qa[0], q1 = qa[1];
+    const float pp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    float ls = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float r = ts_weight(pp[e], qq[e], sh.invS, sh.nS);
+      ls = __fadd_rn(ls, update ? fmaxf(__fsub_rn(r, qq[e]), 0.f) : r);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ls = __fadd_rn(ls, __shfl_xor_sync(0xffffffffu, ls, off));
+    if (segsum && lane == 0) segsum[j] = ls;
+    wsum = __fadd_rn(wsum, ls);
+  }
+  if (lane == 0) red[warp] = wsum;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < kWarps; ++w) tot = __fadd_rn(tot, red[w]);
+  __syncthreads();   // red is reused by the next pass
+  return tot;
+}
+
+// Pushes this CTA's slice total into slot array `buf` of every CTA of the cluster, then one
+// cluster barrier; returns the S totals' sum in rank order, and (in `before`) the sum of the
+// totals of the ranks below this one.
+__device__ __forceinline__ float tsc_allreduce(float mine, int buf, TsClusterShared &cs, int S,
+                                               int rank) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  if (threadIdx.x < static_cast<unsigned>(S)) {
+    float *dst = cl.map_shared_rank(&cs.tot[buf][rank], static_cast<int>(threadIdx.x));
+    *dst = mine;
+  }
+  cl.sync();
+  float t = 0.f;
+  for (int r = 0; r < S; ++r) t = __fadd_rn(t, cs.tot[buf][r]);
+  return t;
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kThreads, 1) finish_tree_sample_cluster(Params p) {
+  namespace cg = cooperative_groups;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  cg::cluster_group cl = cg::this_cluster();
+  const int S = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int N = p.N, V = p.V, R = p.R;
+  const int nseg = (V + kSeg - 1) / kSeg;
+  const int nsl = (nseg + S - 1) / S;
+  const int k_lo = rank * nsl * kSeg;
+  float *rowM = reinterpret_cast<float *>(smem_raw);
+  float *rowZ = rowM + R;
+  int *par = reinterpret_cast<int *>(rowZ + R);
+  int *tok = par + N;
+  int *ch = tok + N;
+  float *segsum = reinterpret_cast<float *>(ch + N);
+  float *ps = reinterpret_cast<float *>(
+      (reinterpret_cast<uintptr_t>(segsum + nsl) + 15) & ~static_cast<uintptr_t>(15));
+  float *qs = ps + nsl * kSeg;
+  __shared__ TsShared sh;
+  __shared__ TsClusterShared cs;
+  cluster_started_arrive();   // the first push waits for it before touching peers
+  wait_stream_kernel();
+  const int b = blockIdx.x / S;
+  if (!SPEC_CHECK(p, b < p.B)) return;   // the same on every CTA of the cluster
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long bN = static_cast<long long>(b) * N;
+  const float c2 = p.c2;
+  if (tid == 0) sh.u0 = p.uniforms[bN];
+  for (int j = tid; j < N; j += kThreads) {
+    par[j] = p.parents[bN + j];
+    tok[j] = j == 0 ? 0 : p.tokens[bN + j];
+  }
+  combine_rows_stats(p, b, rowM, rowZ);
+  __syncthreads();
+  // the oracle's order of checks: parents, then tokens, then rows
+  int e1 = 0, e2 = 0, e3 = 0;
+  for (int j = tid; j < N; j += kThreads) {
+    if (j == 0 ? par[j] != -1 : (par[j] < 0 || par[j] >= j)) e1 = 1;
+    if (j > 0 && (tok[j] < 0 || tok[j] >= V)) e2 = 1;
+  }
+  for (int r = tid; r < R; r += kThreads)
+    if (!stats_ok(rowM[r], rowZ[r])) e3 = 1;
+  e1 = __syncthreads_or(e1);
+  e2 = __syncthreads_or(e2);
+  e3 = __syncthreads_or(e3);
+  int32_t *pn = p.path_nodes + bN;
+  int32_t *ot = p.out_tokens + bN;
+  const int err = e1 ? SPEC_ERR_PARENT : e2 ? SPEC_ERR_TOKEN : e3 ? SPEC_ERR_NONFINITE : 0;
+  if (rank == 0)
+    for (int j = tid; j < N; j += kThreads) { pn[j] = -1; ot[j] = -1; }
+  if (err) {   // the same on every CTA of the cluster: all of them leave here
+    if (rank == 0 && tid == 0) { set_status(p.status, err); p.accept_len[b] = -1; }
+    return;
+  }
+  cluster_started_wait();
+  if (tid == 0) { sh.cur = 0; sh.depth = 0; }
+  __syncthreads();
+  int pass = 0;   // cluster passes so far: selects the slot array
+  for (;;) {
+    const int cur = sh.cur;
+    const E *P = row_ptr<E>(p, b, cur);
+    const E *Q = row_ptr<E>(p, b, N + cur);
+    // the children of cur in index order (a block-wide compaction)
+    {
+      int base = 0;
+      for (int j0 = 0; j0 < N; j0 += kThreads) {
+        const int j = j0 + tid;
+        const int is_child = (j < N && j > cur && par[j] == cur) ? 1 : 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, is_child);
+        if (lane == 0) sh.red[warp] = __int_as_float(__popc(bal));
+        __syncthreads();
+        int before = base;
+        for (int w = 0; w < warp; ++w) before += __float_as_int(sh.red[w]);
+        const int rank_in = before + __popc(bal & ((1u << lane) - 1u));
+        if (is_child && SPEC_CHECK(p, rank_in < N)) ch[rank_in] = j;
+        int total = 0;
+        for (int w = 0; w < kWarps; ++w) total += __float_as_int(sh.red[w]);
+        base += total;
+        __syncthreads();
+      }
+      if (tid == 0) {
+        sh.nchild = base;
+        sh.next = -1;
+        sh.nS = 0;
+        sh.Mt = rowM[cur];
+        sh.iZt = __frcp_rn(rowZ[cur]);
+        sh.Md = rowM[N + cur];
+        sh.iZd = __frcp_rn(rowZ[N + cur]);
+      }
+    }
+    __syncthreads();
+    tsc_stage<E>(P, Q, V, k_lo, nsl * (kSeg / 8), sh.Mt, sh.iZt, sh.Md, sh.iZd, c2, ps, qs);
+    const int nc = sh.nchild;
+    for (int i = tid; i < nc; i += kThreads) {
+      const int c = ch[i];
+      const int x = SPEC_CHECK(p, c > cur && c < N) ? tok[c] : 0;
+      if (!SPEC_CHECK(p, x >= 0 && x < V && i < SPEC_MAX_NODES)) continue;
+      sh.lt[i] = ld_elem<E>(P + x);
+      sh.ld[i] = ld_elem<E>(Q + x);
+    }
+    __syncthreads();
+    for (int i = 0; i < nc; ++i) {
+      // the test of child i (the same on every thread of every CTA)
+      const int c = ch[i];
+      const float px = __fmul_rn(ex2_shift(sh.lt[i], sh.Mt, c2), sh.iZt);
+      const float qx = __fmul_rn(ex2_shift(sh.ld[i], sh.Md, c2), sh.iZd);
+      const float rx = ts_weight(px, qx, sh.invS, sh.nS);
+      const float ratio = qx > 0.f ? __fdiv_rn(rx, qx) : (rx > 0.f ? INFINITY : 0.f);
+      const float uc = p.uniforms[bN + c];
+      if (uc <= ratio) {
+        if (tid == 0) sh.next = c;
+        break;
+      }
+      // rejected: the mass of max(0, r - q) over the vocabulary, for the next sibling's test
+      const float mine = tsc_slice_pass(ps, qs, nsl, sh, true, nullptr, sh.red);
+      const float St = tsc_allreduce(mine, pass & 1, cs, S, rank);
+      ++pass;
+      if (St > 0.f && tid == 0 && sh.nS < kTsMaxUpdates) {
+        sh.invS[sh.nS] = __frcp_rn(St);
+        sh.nS = sh.nS + 1;
+      }
+      __syncthreads();
+    }
+    __syncthreads();
+    const int next = sh.next;
+    if (next >= 0) {
+      if (tid == 0 && SPEC_CHECK(p, next < N && sh.depth + 1 < N)) {
+        const int d = sh.depth + 1;
+        if (rank == 0) {
+          pn[d] = next;
+          ot[d - 1] = tok[next];
+        }
+        sh.depth = d;
+        sh.cur = next;
+      }
+      __syncthreads();
+      continue;
+    }
+    // the draw from r with u0: slice totals and segment sums, the slices' prefix in rank order
+    const float mine = tsc_slice_pass(ps, qs, nsl, sh, false, segsum, sh.red);
+    const int buf = pass & 1;
+    const float Stot = tsc_allreduce(mine, buf, cs, S, rank);
+    float off = 0.f;
+    for (int r = 0; r < rank; ++r) off = __fadd_rn(off, cs.tot[buf][r]);
+    const float t = __fmul_rn(sh.u0, Stot);
+    // the CTA whose slice holds the crossing (ex <= t < in), else (rounding: no crossing) the
+    // highest rank with mass, which takes the last element with r > 0
+    int owner = -1, mode = 0;
+    {
+      float acc = 0.f;
+      for (int r = 0; r < S; ++r) {
+        const float nx = __fadd_rn(acc, cs.tot[buf][r]);
+        if (t < Stot && acc <= t && t < nx) { owner = r; break; }
+        acc = nx;
+      }
+      if (owner < 0) {
+        mode = 1;
+        for (int r = S - 1; r >= 0; --r)
+          if (cs.tot[buf][r] > 0.f) { owner = r; break; }
+        if (owner < 0) owner = 0;
+      }
+    }
+    if (rank != owner) return;
+    // the segment of the crossing within this slice (one thread scans the segment sums)
+    if (tid == 0) {
+      int seg = -1;
+      float base = off;
+      if (mode == 0) {
+        float acc = off;
+        for (int j = 0; j < nsl; ++j) {
+          const float nx = __fadd_rn(acc, segsum[j]);
+          if (nx > t) { seg = j; base = acc; break; }
+          acc = nx;
+        }
+      }
+      if (seg < 0) {
+        mode = 1;
+        for (int j = nsl - 1; j >= 0; --j)
+          if (segsum[j] > 0.f) { seg = j; break; }
+        if (seg < 0) seg = 0;
+      }
+      sh.seg = seg;
+      sh.base = base;
+      sh.mode = mode;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int seg = sh.seg;
+      const float4 *pa = reinterpret_cast<const float4 *>(ps + seg * kSeg + lane * 8);
+      const float4 *qa = reinterpret_cast<const float4 *>(qs + seg * kSeg + lane * 8);
+      const float4 p0 = pa[0], p1 = pa[1], q0 = qa[0], q1 = qa[1];
+      const float pp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      float r[8], ls = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        r[e] = ts_weight(pp[e], qq[e], sh.invS, sh.nS);
+        ls = __fadd_rn(ls, r[e]);
+      }
+      const int k0 = k_lo + seg * kSeg + lane * 8;
+      int tk = segment_pick(r, ls, k0, sh.base, t, sh.mode, lane);
+      if (tk < 0 || tk >= V) tk = V - 1;   // unreachable: the segment holds mass
+      if (lane == 0 && SPEC_CHECK(p, sh.depth < N)) {
+        pn[0] = 0;
+        ot[sh.depth] = tk;
+        p.accept_len[b] = sh.depth;
+      }
     }
     return;
   }

@@ -46,9 +46,12 @@ def test_tree_sample_32k_full_size(orc, offset):
     assert gpu[0].max() >= 1
 
 
+# V = 300001 fp32: a vocabulary slice per CTA no longer fits in shared memory even across a
+# cluster of eight, so the walk runs one CTA per tree reading the rows from L2 (the other cases
+# take the cluster walk with p and q in shared memory)
 @pytest.mark.parametrize("dtype,V,N,T", [(F32, 1000, 12, 0.8), (BF16, 4099, 64, 1.0),
                                          (F32, 7, 30, 2.0), (BF16, 70001, 20, 0.6),
-                                         (F32, 1, 5, 1.0)])
+                                         (F32, 1, 5, 1.0), (F32, 300001, 6, 1.0)])
 def test_tree_sample_shapes(orc, dtype, V, N, T):
     ti = tree_sample_32k(seed=7 + V, B=24, N=N, V=V, dtype=dtype, temperature=T,
                          peaked=min(50, max(1, V // 4)))
