@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // both CTAs' copies of a stage count their bytes on the even CTA's barrier of that stage,
     // which expects the pair's bytes
     const uint32_t full0 = tc::mapa(tc::saddr(&full[0]), 0);
+    // the hidden states are read by every column tile: keep them in L2
+    const uint64_t keep = tc::l2_policy_evict_last();
     int it = 0;   // K blocks issued so far (all tiles)
     for (int t = c; t < a.tiles && !timed_out; t += NC) {
       const LmTile x = lm_tile(a, t, rank);
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         uint8_t *st = ring + s * kLmStageBytes;
         if (leader) tc::mbar_expect_tx(&full[s], 2 * kLmStageBytes);
         const uint32_t bar = full0 + static_cast<uint32_t>(s * sizeof(uint64_t));
-        tc::tma_load_2d_pair(st, mh, kb * kLmBK, x.m0, bar);
+        tc::tma_load_2d_pair_hint(st, mh, kb * kLmBK, x.m0, bar, keep);
         tc::tma_load_2d_pair(st + kLmABytes, mw, kb * kLmBK, n0, bar);
       }
     }

@@ -194,6 +194,26 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
       : "memory");
 }
+// tma_load_2d_pair with an L2 cache-policy hint (a policy from l2_policy_evict_last / _first).
+__device__ __forceinline__ void tma_load_2d_pair_hint(void *dst, const CUtensorMap *map, int c0,
+                                                      int c1, uint32_t bar_cluster,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(saddr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 // Tensor memory of a CTA pair: one warp of each of the two CTAs executes these together; both
 // CTAs get the same columns of their own SM's tensor memory.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
