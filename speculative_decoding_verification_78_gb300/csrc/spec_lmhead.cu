@@ -82,7 +82,7 @@ __device__ __forceinline__ LmTile lm_tile(const LmArgs &a, int t, int rank) {
 __device__ __forceinline__ void lm_epilogue_row(const Params &p, const LmArgs &a, const LmTile &x,
                                                 uint32_t tacc, int q, int lane) {
   const int j = x.m0 + q * 32 + lane;
-  const bool valid = j < x.M;
+  const bool valid = j < x.M && SPEC_CHECK(p, j >= 0 && x.ctile >= 0 && x.ctile < p.C);
   const int g1 = p.gamma + 1;
   int b = 0, r = 0, tok = -1;
   if (valid) {
@@ -148,7 +148,7 @@ __device__ __forceinline__ void lm_epilogue_row(const Params &p, const LmArgs &a
       has_x = true;
     }
   }
-  if (valid) {
+  if (valid && SPEC_CHECK(p, b < p.B && r < p.R)) {
     const long long row = static_cast<long long>(b) * p.R + r;
     p.ws_part[row * p.C + x.ctile] = make_uint2(__float_as_uint(m), __float_as_uint(s));
     if (has_x) p.ws_xlogit[row] = xval;

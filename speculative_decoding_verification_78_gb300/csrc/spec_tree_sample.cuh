@@ -419,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample_cluster(Params
   const int N = p.N, V = p.V, R = p.R;
   const int nseg = (V + kSeg - 1) / kSeg;
   const int nsl = (nseg + S - 1) / S;
+  if (!SPEC_CHECK(p, S >= 1 && S <= kMaxCluster)) return;   // the same on every CTA
   const int k_lo = rank * nsl * kSeg;
   float *rowM = reinterpret_cast<float *>(smem_raw);
   float *rowZ = rowM + R;
@@ -597,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample_cluster(Params
       sh.mode = mode;
     }
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 0 && SPEC_CHECK(p, sh.seg >= 0 && sh.seg < nsl)) {
       const int seg = sh.seg;
       const float4 *pa = reinterpret_cast<const float4 *>(ps + seg * kSeg + lane * 8);
       const float4 *qa = reinterpret_cast<const float4 *>(qs + seg * kSeg + lane * 8);

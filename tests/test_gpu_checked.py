@@ -101,3 +101,21 @@ def test_checked_probs_sample_topk(both, dtype, V, T):
         got = _np(_run(bnd, clib, fn, *args))
         assert int(got[-1][0]) == 0, (fn.__name__, int(got[-1][0]))
         np.testing.assert_array_equal(got[0], want[0])
+
+
+def test_checked_lmhead(both, orc):
+    """The fused LM-head call (tensor-core GEMM epilogue, then the chain finisher) through the
+    checked build: no check fires and every output, logits included, equals the plain build's."""
+    from workloads import lmhead_grid
+    bnd, lib, clib = both
+    li = lmhead_grid(seed=9, B=6, gamma=3, V=768, Ht=128, Hd=64)
+    rng = np.random.default_rng(9)
+    tok = dev(rng.integers(0, 768, (6, 3)).astype(np.int32))
+    args = (dev(li.hidden_t), dev(li.head_t), dev(li.hidden_d), dev(li.head_d), tok,
+            dev(li.uniforms), 1.0)
+    bits = lambda ts: [t.view(torch.int16) if t.dtype == torch.bfloat16 else t for t in ts]
+    want = _np(bits(_run(bnd, lib, bnd.verify_chain_lmhead, *args)))
+    got = _np(bits(_run(bnd, clib, bnd.verify_chain_lmhead, *args)))
+    assert int(got[2][0]) == 0 and int(want[2][0]) == 0
+    for g, w in zip(got, want):
+        np.testing.assert_array_equal(g, w)
