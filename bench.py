@@ -170,12 +170,14 @@ def measured_tensor_peaks():
 
 
 def kernel_source_hash():
-    """Hash of the sources that define the kernels and their launches (the C ABI's host checks
-    and the static-scratch entry point do not change what a kernel reads or writes)."""
+    """Hash of the sources that define the verify kernels and their launches (the C ABI's host
+    checks, the static-scratch entry point and the LM-head GEMM's tensor-core helpers do not
+    change what those kernels read or write)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_78_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith(".cuh") or f == "spec_launch.h" or f.startswith("spec_kernels_"):
+        if (f.endswith(".cuh") and f != "spec_tc.cuh") or f == "spec_launch.h" or \
+                f.startswith("spec_kernels_"):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

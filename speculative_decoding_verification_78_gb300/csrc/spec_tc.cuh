@@ -53,22 +53,6 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
   return true;
 }
 
-// A plain arrival (no transaction count) on a barrier of this CTA.
-__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
-}
-
-// A 2-D tile of a tensor map (box given by the map) into shared memory; completion counted on
-// `bar`. c0: innermost coordinate (elements; a multiple of 16 bytes), c1: row.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
-                                            uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
-      "{%2, %3}], [%4];" ::"r"(saddr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(saddr(bar))
-      : "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major operand tile written by a TMA load with 128-byte
 // swizzling: rows of 128 bytes (64 bf16), 8-row atoms of 1024 bytes (the stride between atoms),
 // the tile 1024-byte aligned. Fields: start address / 16 (bits 0-13), leading byte offset / 16
@@ -92,38 +76,11 @@ __host__ __device__ constexpr uint32_t bf16_f32_idesc(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread; accumulate when acc != 0
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc));
-}
-// `bar` receives one arrival once every MMA this thread issued before has completed
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          saddr(bar))
-      : "memory");
-}
 __device__ __forceinline__ void fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// Tensor-memory allocation by one whole warp: the column base address is written to *slot.
-__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   saddr(slot)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
 }
 // 32 consecutive fp32 columns of this thread's lane (warp w reads lanes 32 (w % 4) .. + 31)
 __device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&v)[32]) {
@@ -194,7 +151,7 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
       : "memory");
 }
-// tma_load_2d_pair with an L2 cache-policy hint (a policy from l2_policy_evict_last / _first).
+// tma_load_2d_pair with an L2 cache-policy hint (a policy from l2_policy_evict_last).
 __device__ __forceinline__ void tma_load_2d_pair_hint(void *dst, const CUtensorMap *map, int c0,
                                                       int c1, uint32_t bar_cluster,
                                                       uint64_t policy) {
@@ -207,11 +164,6 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(void *dst, const CUtensorM
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 // Tensor memory of a CTA pair: one warp of each of the two CTAs executes these together; both
