@@ -62,6 +62,16 @@ def test_tree_sample_shapes(orc, dtype, V, N, T):
         compare_tree_sample(orc, ti, draft, u, T, gpu, name=ti.name)
 
 
+def test_tree_sample_many_trees(orc):
+    """300 trees of 16 nodes over V=32000 bf16: more trees than SMs, so the walk's clusters shrink
+    to the two CTAs a slice of p and q needs to fit, in several waves."""
+    ti = tree_sample_32k(seed=88, B=300, N=16, V=32000)
+    draft, u = ti.meta["draft"], ti.meta["uniforms"]
+    gpu = run_tree_sample(ti, draft, u, 1.0)
+    assert gpu[3] == 0
+    compare_tree_sample(orc, ti, draft, u, 1.0, gpu, name=ti.name)
+
+
 @pytest.mark.parametrize("kind", ["star", "chain", "wide_deep"])
 def test_tree_sample_structures(orc, kind):
     """A star of 200 children of the root (up to 199 residual updates at one node), a 300-node
