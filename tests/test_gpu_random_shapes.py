@@ -2,7 +2,9 @@
 lengths, vocabularies (ragged, unaligned row bases, single- and multi-unit rows, cluster and
 CTA draws), dtypes and temperatures drawn from a fixed seed, so that the launch plans and their
 boundaries (one-warp finishers, clusters of 1-8 CTAs, lane groups of 1-32 per row, trees of
-1-64 nodes and deeper CTA trees) are all exercised with inputs no hand-written case chose."""
+1-64 nodes and deeper CTA trees, the stochastic walk's cluster and single-CTA forms, the fused
+LM head's tile counts and hidden sizes) are all exercised with inputs no hand-written case
+chose."""
 
 import numpy as np
 import pytest
@@ -113,3 +115,56 @@ def test_random_probs_sample_topk(orc, seed):
     iw, rc = orc.topk(lg, dtype, k)
     assert int(st.item()) == 0 and rc == 0
     np.testing.assert_array_equal(idx.cpu().numpy(), iw)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_tree_sample(orc, seed):
+    """Stochastic tree walks over seeded shapes: tree sizes, vocabularies (clusters of 1-8 CTAs,
+    slices that fit in shared memory or not), batch sizes, dtypes, temperatures and draft
+    distances, with ragged and unaligned rows."""
+    from gpu_util import compare_tree_sample, run_tree_sample
+    from workloads import tree_sample_32k
+    rng = np.random.default_rng(4000 + seed)
+    dtype = BF16 if rng.random() < 0.5 else F32
+    V = int(rng.choice([2, 300, 1031, 32000, 65536, 250007]))
+    N = int(rng.choice([2, 9, 33, 64]))
+    B = int(rng.choice([1, 7, 40, 160]))
+    B = max(1, min(B, 40_000_000 // (2 * N * V)))
+    T = float(rng.choice([0.4, 1.0, 2.0]))
+    ti = tree_sample_32k(seed=5000 + seed, B=B, N=N, V=V, dtype=dtype, temperature=T,
+                         draft_sigma=float(rng.choice([0.3, 1.0, 3.0])),
+                         peaked=min(50, max(1, V // 4)))
+    draft, u = ti.meta["draft"], ti.meta["uniforms"]
+    gpu = run_tree_sample(ti, draft, u, T, offset_elems=int(rng.integers(0, 2)))
+    assert gpu[3] == 0
+    compare_tree_sample(orc, ti, draft, u, T, gpu, name=f"rtree_sample{seed}")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_lmhead(orc, seed):
+    """The fused LM-head call over seeded shapes (batch, draft length, vocabulary, both hidden
+    sizes, temperature) on integer-grid inputs: logits bit-exact, verification draw by draw."""
+    import speculative_decoding_verification_78_gb300 as sv
+    from workloads import bf16_to_f32, lmhead_grid
+    rng = np.random.default_rng(6000 + seed)
+    B = int(rng.choice([1, 3, 20, 70]))
+    gamma = int(rng.choice([1, 2, 5, 9, 16]))
+    V = 256 * int(rng.choice([1, 3, 8, 33, 130]))
+    Ht = 64 * int(rng.choice([1, 2, 5, 12]))
+    Hd = 64 * int(rng.choice([1, 3, 7]))
+    T = float(rng.choice([0.3, 1.0, 1.7]))
+    li = lmhead_grid(seed=7000 + seed, B=B, gamma=gamma, V=V, Ht=Ht, Hd=Hd, temperature=T)
+    lt_ref, _ = orc.lm_head_logits(li.hidden_t, li.head_t)
+    ld_ref, _ = orc.lm_head_logits(li.hidden_d, li.head_d)
+    tok = gumbel_draft_tokens(rng, bf16_to_f32(ld_ref).reshape(B, gamma, V), T).astype(np.int32)
+    acc, out, st, lt, ld = sv.verify_chain_lmhead(dev(li.hidden_t), dev(li.head_t),
+                                                  dev(li.hidden_d), dev(li.head_d), dev(tok),
+                                                  dev(li.uniforms), T)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(bits(lt), lt_ref)
+    np.testing.assert_array_equal(bits(ld), ld_ref)
+    ci = ChainInputs(f"rlmhead{seed}", lt_ref.reshape(B, gamma + 1, V),
+                     ld_ref.reshape(B, gamma, V), BF16, tok, li.uniforms, T)
+    compare_chain(orc, ci, (acc.cpu().numpy(), out.cpu().numpy(), 0))
