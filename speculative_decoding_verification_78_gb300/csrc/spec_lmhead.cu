@@ -53,15 +53,16 @@ struct LmArgs {
   uint16_t *logits_d;   // [Md, V] bf16 out
   int Mt, Md;           // B * (gamma + 1), B * gamma
   int Kt, Kd;           // hidden sizes of the target and of the drafter
-  int rt_t, rt;         // 256-row tiles of the target GEMM; of both (the draft's follow)
-  int tiles;            // rt * (V / 256)
+  int rt_t, rt_d;       // 256-row tiles of the target GEMM and of the drafter's
+  int tiles_t;          // rt_t * (V / 256): the target's tiles come first
+  int tiles;            // (rt_t + rt_d) * (V / 256)
 };
 
-// Tile t: column tile t / rt and, within it, row tile (t + t / rt) mod rt (the target's row
-// tiles first, then the drafter's). The skew keeps a cluster that walks t = c, c + NC, ... from
-// landing on the same row tile every time when NC is a multiple of rt (the target's and the
-// drafter's tiles differ in K, so a fixed row tile would unbalance the clusters). m0 is this
-// CTA's first row (the pair's tile starts 128 rows earlier in the odd CTA).
+// Tile t: the target GEMM's tiles first, then the drafter's; within each, column tile-major with
+// the row tiles fastest. All tiles of one GEMM cost the same (one K), so the clusters walking
+// t = c, c + NC, ... stay in step within a GEMM, and the tiles they run at one time are a
+// contiguous window: each head tile is read by its row tiles' clusters together, from L2 after
+// the first. m0 is this CTA's first row (the pair's tile starts 128 rows earlier in the odd CTA).
 struct LmTile {
   bool draft;
   int m0, M, ctile, KB;
@@ -69,10 +70,12 @@ struct LmTile {
 
 __device__ __forceinline__ LmTile lm_tile(const LmArgs &a, int t, int rank) {
   LmTile x;
-  x.ctile = t / a.rt;
-  const int r = (t - x.ctile * a.rt + x.ctile) % a.rt;
-  x.draft = r >= a.rt_t;
-  x.m0 = (x.draft ? r - a.rt_t : r) * (2 * kLmBM) + rank * kLmBM;
+  x.draft = t >= a.tiles_t;
+  const int u = x.draft ? t - a.tiles_t : t;
+  const int rt = x.draft ? a.rt_d : a.rt_t;
+  x.ctile = u / rt;
+  const int r = u - x.ctile * rt;
+  x.m0 = r * (2 * kLmBM) + rank * kLmBM;
   x.M = x.draft ? a.Md : a.Mt;
   x.KB = (x.draft ? a.Kd : a.Kt) / kLmBK;
   return x;
@@ -361,8 +364,9 @@ cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *hea
   a.Kt = Kt;
   a.Kd = Kd;
   a.rt_t = (Mt + 2 * kLmBM - 1) / (2 * kLmBM);
-  a.rt = a.rt_t + (Md + 2 * kLmBM - 1) / (2 * kLmBM);
-  const long long tiles = static_cast<long long>(a.rt) * (p.V / kLmBN);
+  a.rt_d = (Md + 2 * kLmBM - 1) / (2 * kLmBM);
+  a.tiles_t = a.rt_t * (p.V / kLmBN);
+  const long long tiles = static_cast<long long>(a.rt_t + a.rt_d) * (p.V / kLmBN);
   if (tiles > INT_MAX) return cudaErrorInvalidValue;
   a.tiles = static_cast<int>(tiles);
 
