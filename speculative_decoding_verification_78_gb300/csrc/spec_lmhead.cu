@@ -11,18 +11,20 @@
 // clusters running at one time share their head tiles in L2. One 5th-generation MMA
 // (tcgen05.mma.cta_group::2, M = 256, N = 256, K = 16) spans the pair: each CTA holds its own
 // 128 hidden-state rows and half of the head tile's 256 rows in shared memory, so an SM loads
-// 32 KB per 64-wide K block instead of the 48 KB a single-CTA 128 x 256 tile needs, and the
-// 224 KB ring holds seven stages. Per CTA: warp 0 streams its halves of every K block of every
-// tile through the TMA ring (128-byte swizzle) without draining it between tiles; warp 1 owns
-// 512 tensor-memory columns (two accumulators, allocated by the pair together) — in the even
-// CTA one of its threads issues the pair's MMAs of tile i into accumulator i mod 2 once both
-// CTAs' stages have landed (the odd CTA's copies count their bytes on the even CTA's stage
-// barrier); warps 2-5 read tile i's accumulator (one of the CTA's 128 rows per thread) while the
-// MMAs of tile i+1 run in the other one: each fp32 value is rounded to bf16 (the stored logit),
-// the row's 256 stored values give one (max, sum of 2^((l - max) log2(e)/T)) partial, the
-// drafted token's logit is kept when it falls in the tile, and the bf16 logits are written out
-// (the finishing kernel re-reads the two rows where each step stopped). The finishing kernel is
-// the chain finisher, with 256-column tiles as its units.
+// 32 KB per 64 of K instead of the 48 KB a single-CTA 128 x 256 tile needs. The K blocks are
+// 128 wide (two 64-wide TMA boxes per operand, 64 KB per CTA) and the 192 KB ring holds three:
+// on GB300 fewer, larger stages stream faster than the same bytes in more, smaller ones (seven
+// 32 KB stages of 64-wide blocks were 10 % slower). Per CTA: warp 0 streams its halves of every
+// K block of every tile through the TMA ring (128-byte swizzle) without draining it between
+// tiles; warp 1 owns 512 tensor-memory columns (two accumulators, allocated by the pair
+// together) — in the even CTA one of its threads issues the pair's MMAs of tile i into
+// accumulator i mod 2 once both CTAs' stages have landed (the odd CTA's copies count their bytes
+// on the even CTA's stage barrier); warps 2-5 read tile i's accumulator (one of the CTA's 128
+// rows per thread) while the MMAs of tile i+1 run in the other one: each fp32 value is rounded
+// to bf16 (the stored logit), the row's 256 stored values give one (max, sum of
+// 2^((l - max) log2(e)/T)) partial, the drafted token's logit is kept when it falls in the tile,
+// and the bf16 logits are written out (the finishing kernel re-reads the two rows where each step
+// stopped). The finishing kernel is the chain finisher, with 256-column tiles as its units.
 #include <limits.h>
 
 #include <atomic>
@@ -38,9 +40,11 @@ namespace {
 
 constexpr int kLmBM = 128;     // rows of a CTA (the pair's tile: 256)
 constexpr int kLmBN = 256;     // vocabulary columns of a tile (each CTA loads 128 head rows)
-constexpr int kLmBK = 64, kLmStages = 7, kLmAcc = 2;
+constexpr int kLmBK = 128, kLmStages = 3, kLmAcc = 2;
+constexpr int kLmBox = 64;   // K width of one TMA box: the 128-byte swizzle span of bf16
 constexpr int kLmABytes = kLmBM * kLmBK * 2;
 constexpr int kLmBBytes = (kLmBN / 2) * kLmBK * 2;
+static_assert(kLmABytes == kLmBBytes, "one descriptor offset serves both operands' boxes");
 constexpr int kLmStageBytes = kLmABytes + kLmBBytes;
 constexpr int kLmEpiWarps = 4;
 constexpr int kLmThreads = 32 * (2 + kLmEpiWarps);
@@ -77,7 +81,9 @@ __device__ __forceinline__ LmTile lm_tile(const LmArgs &a, int t, int rank) {
   const int r = u - x.ctile * rt;
   x.m0 = r * (2 * kLmBM) + rank * kLmBM;
   x.M = x.draft ? a.Md : a.Mt;
-  x.KB = (x.draft ? a.Kd : a.Kt) / kLmBK;
+  // a hidden size that is an odd multiple of 64 ends in half a block: the TMA fills the box past
+  // K with zeros, which add nothing to the products
+  x.KB = ((x.draft ? a.Kd : a.Kt) + kLmBK - 1) / kLmBK;
   return x;
 }
 
@@ -220,8 +226,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         uint8_t *st = ring + s * kLmStageBytes;
         if (leader) tc::mbar_expect_tx(&full[s], 2 * kLmStageBytes);
         const uint32_t bar = full0 + static_cast<uint32_t>(s * sizeof(uint64_t));
-        tc::tma_load_2d_pair_hint(st, mh, kb * kLmBK, x.m0, bar, keep);
-        tc::tma_load_2d_pair(st + kLmABytes, mw, kb * kLmBK, n0, bar);
+        for (int h = 0; h < kLmBK / kLmBox; ++h) {
+          const int k0 = kb * kLmBK + h * kLmBox;
+          tc::tma_load_2d_pair_hint(st + h * (kLmABytes / 2), mh, k0, x.m0, bar, keep);
+          tc::tma_load_2d_pair(st + kLmABytes + h * (kLmBBytes / 2), mw, k0, n0, bar);
+        }
       }
     }
     // no copy may still be landing in shared memory when either CTA exits. The even CTA waits
@@ -262,9 +271,12 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         const uint32_t sa = tc::saddr(ring + s * kLmStageBytes);
         const uint64_t ad = tc::sw128_kmajor_desc(sa), bd = tc::sw128_kmajor_desc(sa + kLmABytes);
 #pragma unroll
-        for (int k = 0; k < kLmBK / 16; ++k)
-          tc::mma_bf16_pair(d, ad + static_cast<uint64_t>(2 * k),
-                            bd + static_cast<uint64_t>(2 * k), idesc, (kb | k) != 0);
+        for (int k = 0; k < kLmBK / 16; ++k) {
+          // K step k: box k / 4 of each operand (the boxes lie 16 KB apart: 1024 units of 16
+          // bytes), 32 bytes (2 units) per 16 elements within it
+          const uint64_t off = static_cast<uint64_t>((k >> 2) * (kLmABytes / 2 / 16) + 2 * (k & 3));
+          tc::mma_bf16_pair(d, ad + off, bd + off, idesc, (kb | k) != 0);
+        }
         // both CTAs' stages are free once these MMAs have read them
         tc::mma_commit_pair(&empty[s], kLmPairMask);
       }
@@ -328,13 +340,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return f;
 }
 
-// a [rows, K] bf16 row-major matrix, boxes of box_rows x 64 with 128-byte swizzle
+// a [rows, K] bf16 row-major matrix, boxes of box_rows x 64 with 128-byte swizzle (K a multiple of
+// 64, so that every box starts on a 16-byte boundary)
 bool make_map(CUtensorMap *m, const void *base, int rows, int K, int box_rows) {
   const auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  cuuint32_t box[2] = {kLmBK, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {kLmBox, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
