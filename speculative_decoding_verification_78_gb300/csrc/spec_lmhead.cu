@@ -64,6 +64,8 @@ struct LmArgs {
   int ct;               // 512-column tiles: ceil(V / 512) (the last one may hold one half)
   int tiles_t;          // rt_t * ct: the target's tiles come first
   int tiles;            // (rt_t + rt_d) * ct
+  int even;             // drafter tiles a cluster with one target tile fewer takes first (see
+                        // lm_sched): Kt / Kd rounded down, 0 when the drafter's K is larger
 };
 
 // Tile t: the target GEMM's tiles first, then the drafter's; within each, column tile-major with
@@ -89,6 +91,29 @@ __device__ __forceinline__ LmTile lm_tile(const Params &p, const LmArgs &a, int 
   x.nh = p.C - 2 * x.ctile < 2 ? 1 : 2;
   x.KB = (x.draft ? a.Kd : a.Kt) / kLmBK;   // hidden sizes are multiples of 64
   return x;
+}
+
+// The i-th tile of cluster c of NC, or -1 when it has no more. The target's tiles go round robin
+// (cluster c takes c, c + NC, ...), so the clusters c >= T mod NC hold one target tile fewer; they
+// first take `even` drafter tiles each (round robin among them), which the drafter's shorter K
+// makes worth about one target tile, and the remaining drafter tiles go round robin over all
+// clusters. Every thread of both CTAs of a cluster computes the same sequence.
+__device__ __forceinline__ int lm_sched(const LmArgs &a, int c, int NC, int i) {
+  const int T = a.tiles_t, D = a.tiles - a.tiles_t;
+  const int h = T % NC;
+  const int nT = T / NC + (c < h ? 1 : 0);
+  if (i < nT) return c + i * NC;
+  i -= nT;
+  const int light = NC - h;
+  const int p1 = h > 0 ? min(D, light * a.even) : 0;   // drafter tiles of the first round
+  if (h > 0 && c >= h) {
+    const int first = c - h;   // this cluster's first tile of that round
+    const int n1 = p1 > first ? (p1 - first + light - 1) / light : 0;
+    if (i < n1) return T + first + i * light;
+    i -= n1;
+  }
+  const int j = p1 + c + i * NC;
+  return j < D ? T + j : -1;
 }
 
 // Chunk C (columns 32 C .. 32 C + 31 of the half, bf16 pairs h[16 C ..]) merged into the row's
@@ -250,7 +275,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // the hidden states are read by every column tile: keep them in L2
     const uint64_t keep = tc::l2_policy_evict_last();
     int it = 0;   // stages filled so far (all tiles)
-    for (int t = c; t < a.tiles && !timed_out; t += NC) {
+    for (int i = 0, t; !timed_out && (t = lm_sched(a, c, NC, i)) >= 0; ++i) {
       const LmTile x = lm_tile(p, a, t, rank);
       const CUtensorMap *mh = x.draft ? &map_hd : &map_ht;
       const CUtensorMap *mw = x.draft ? &map_wd : &map_wt;
@@ -287,7 +312,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   } else if (warp == 1 && lane == 0 && leader) {   // the pair's MMA thread
     constexpr uint32_t idesc = tc::bf16_f32_idesc(2 * kLmBM, kLmHalf);
     int it = 0, i = 0;   // stages consumed; tiles done
-    for (int t = c; t < a.tiles && !timed_out; t += NC, ++i) {
+    for (int t; !timed_out && (t = lm_sched(a, c, NC, i)) >= 0; ++i) {
       const LmTile x = lm_tile(p, a, t, rank);
       // both CTAs' epilogues have read the previous tile's accumulators
       if (!tc::mbar_wait_cluster(&acc_empty, (i & 1) ^ 1)) {
@@ -332,7 +357,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int hf = (warp - 2) >> 2;    // warps 2-5 read the first half, 6-9 the second
     const uint32_t release = tc::mapa(tc::saddr(&acc_empty), 0);
     int i = 0;
-    for (int t = c; t < a.tiles; t += NC, ++i) {
+    for (int t; (t = lm_sched(a, c, NC, i)) >= 0; ++i) {
       const LmTile x = lm_tile(p, a, t, rank);
       // the arrival is the MMA unit's (a commit from the even CTA); this CTA then reads only its
       // own tensor memory, so a CTA-scope wait suffices (and polls far more cheaply)
@@ -418,6 +443,7 @@ cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *hea
   const long long tiles = static_cast<long long>(a.rt_t + a.rt_d) * a.ct;
   if (tiles > INT_MAX) return cudaErrorInvalidValue;
   a.tiles = static_cast<int>(tiles);
+  a.even = Kd > 0 && Kt >= Kd ? Kt / Kd : 0;
 
   // Clusters of two CTAs, as many as can be resident at once (a persistent grid must not wait
   // for a slot). A plain stream-ordered launch (not a programmatic dependent of the kernel before
