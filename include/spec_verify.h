@@ -295,6 +295,22 @@ int spec_last_cuda_error(void);
 const char *spec_cuda_error_string(int cuda_error);
 
 /*
+ * Self-check of the bounded waits (not an operation of the method). The LM-head GEMM's roles
+ * wait on shared-memory barriers (copy completion, MMA completion, the other CTA's epilogue);
+ * each wait gives up after a limit (2 s in the kernels), writes SPEC_ERR_TIMEOUT to *status and
+ * lets the kernel finish, so that a lost arrival ends the call with an error instead of hanging
+ * the GPU. This call launches one cluster of two CTAs that waits, through the same wait
+ * routines, on barriers nothing ever arrives on, with the given limit: a CTA-scope wait in each
+ * CTA and a cluster-scope wait in the even one.
+ *   status         [1] int32 device word; receives SPEC_ERR_TIMEOUT when the waits give up (the
+ *                  caller zeroes it first; the first nonzero code written is kept)
+ *   limit_seconds  how long each wait tries, 1e-6 .. 10
+ * Returns SPEC_OK once enqueued (the kernel then runs for about two limits), or
+ * SPEC_ERR_NULL / ALIGN / SHAPE (limit out of range) / LAUNCH.
+ */
+int spec_selftest_bounded_wait(int32_t *status, double limit_seconds, void *stream);
+
+/*
  * The kernel launches a call of the given shape makes on the current device; it enqueues
  * nothing and touches no memory (for tests and profiling; the pages have no counterpart).
  *   kind        SPEC_CALL_CHAIN (rows_per_b = 2*gamma+1, any temperature), SPEC_CALL_TREE

@@ -16,4 +16,4 @@ from ._binding import (  # noqa: F401
     spec_workspace_bytes,
     spec_workspace_init, topk, tree_mask, verify_chain, verify_chain_lmhead, verify_tree,
     verify_tree_sample, spec_verify_chain_lmhead, spec_lmhead_workspace_bytes, SPEC_ERR_TIMEOUT,
-    spec_last_cuda_error, spec_cuda_error_string)
+    spec_last_cuda_error, spec_cuda_error_string, spec_selftest_bounded_wait)

@@ -33,7 +33,7 @@ EXPORTS = ("spec_workspace_bytes", "spec_workspace_init", "spec_verify_chain",
            "spec_verify_chain_lmhead", "spec_probs", "spec_status_string",
            "spec_last_cuda_error", "spec_cuda_error_string",
            "spec_launch_shape", "spec_verify_chain_static", "spec_sample", "spec_topk",
-           "spec_tree_mask")
+           "spec_tree_mask", "spec_selftest_bounded_wait")
 SPEC_MAX_TOPK = 16
 SPEC_STATIC_SCRATCH_BYTES = 4 << 20
 SPEC_CALL_CHAIN, SPEC_CALL_TREE, SPEC_CALL_PROBS = 0, 1, 2
@@ -104,6 +104,8 @@ def load_library(checked: bool = False):
         lib.spec_topk.restype = i32
         lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
         lib.spec_tree_mask.restype = i32
+        lib.spec_selftest_bounded_wait.argtypes = [vp, ctypes.c_double, vp]
+        lib.spec_selftest_bounded_wait.restype = i32
         if checked:
             _checked_lib = lib
         else:
@@ -340,6 +342,14 @@ def spec_last_cuda_error() -> int:
 
 def spec_cuda_error_string(cuda_error: int) -> str:
     return load_library().spec_cuda_error_string(int(cuda_error)).decode()
+
+
+def spec_selftest_bounded_wait(status, limit_seconds: float, stream=None) -> int:
+    """The bounded-wait self-check (see include/spec_verify.h): returns the SPEC_* code of the
+    call; the kernel writes SPEC_ERR_TIMEOUT into status[0] when its waits give up."""
+    _expect(status, "status", 1, (torch.int32,))
+    return int(load_library().spec_selftest_bounded_wait(_ptr(status), float(limit_seconds),
+                                                         _stream(stream)))
 
 
 # ------------------------------------------------------------------ conveniences (allocation)

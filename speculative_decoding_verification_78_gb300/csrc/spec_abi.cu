@@ -560,6 +560,15 @@ int spec_launch_shape(int kind, int B, int rows_per_b, int V, int dtype, float t
   return SPEC_OK;
 }
 
+int spec_selftest_bounded_wait(int32_t *status, double limit_seconds, void *stream) {
+  if (!status) return SPEC_ERR_NULL;
+  if (!aligned(status, 4)) return SPEC_ERR_ALIGN;
+  if (!(limit_seconds >= 1e-6 && limit_seconds <= 10.0)) return SPEC_ERR_SHAPE;
+  const auto ns = static_cast<unsigned long long>(limit_seconds * 1e9);
+  return specv::launch_result(
+      specv::launch_wait_selftest(status, ns, static_cast<cudaStream_t>(stream)));
+}
+
 int spec_last_cuda_error(void) { return specv::g_last_cuda_error; }
 
 const char *spec_cuda_error_string(int cuda_error) {

@@ -385,6 +385,29 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   }
 }
 
+// Self-check of the bounded waits: a cluster of two CTAs whose first threads wait, through the
+// same routines the GEMM's roles use, on barriers that nothing ever arrives on (a CTA-scope wait in
+// each CTA, then a cluster-scope one in the even CTA). Each wait must give up after limit_ns and
+// report SPEC_ERR_TIMEOUT; the kernel then returns normally.
+__global__ void __cluster_dims__(2, 1, 1)
+    wait_selftest_kernel(int32_t *status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t never[2];
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&never[0], 1);
+    tc::mbar_init(&never[1], 1);
+    tc::mbar_fence_init();
+  }
+  __syncthreads();
+  tc::cluster_sync_all();
+  if (threadIdx.x == 0) {
+    if (!tc::mbar_wait(&never[0], 0, limit_ns)) set_status(status, SPEC_ERR_TIMEOUT);
+    if (tc::cluster_rank() == 0 && !tc::mbar_wait_cluster(&never[1], 0, limit_ns))
+      set_status(status, SPEC_ERR_TIMEOUT);
+  }
+  __syncthreads();
+  tc::cluster_sync_all();
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
   PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
@@ -483,6 +506,12 @@ cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *hea
     return launch_dependent(finish_chain_sample_warp<uint16_t>, p, f.grid, 1, 0, stream,
                             32 * kTailWarpsPerCta);
   return launch_dependent(finish_chain_sample<uint16_t>, p, f.grid, f.cluster, f.smem, stream);
+}
+
+cudaError_t launch_wait_selftest(int32_t *status, unsigned long long limit_ns,
+                                 cudaStream_t stream) {
+  wait_selftest_kernel<<<2, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
 }
 
 }  // namespace specv

@@ -43,13 +43,14 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits until the phase of parity `parity` has completed, for at most kWaitNs; false if it gave
+// Waits until the phase of parity `parity` has completed, for at most limit_ns; false if it gave
 // up. (A fresh barrier is in phase 0, so waiting on parity 1 returns at once.)
-static __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity,
+                                              unsigned long long limit_ns = kWaitNs) {
   if (mbar_try(b, parity)) return true;
   const unsigned long long t0 = now_ns();
   while (!mbar_try(b, parity))
-    if (now_ns() - t0 > kWaitNs) return false;
+    if (now_ns() - t0 > limit_ns) return false;
   return true;
 }
 
@@ -129,12 +130,13 @@ __device__ __forceinline__ bool mbar_try_cluster(uint64_t *b, uint32_t parity) {
   return ok != 0;
 }
 // mbar_wait for a barrier that threads of other CTAs of the cluster arrive on (acquire at cluster
-// scope), at most kWaitNs; false if it gave up.
-static __device__ __noinline__ bool mbar_wait_cluster(uint64_t *b, uint32_t parity) {
+// scope), at most limit_ns; false if it gave up.
+static __device__ __noinline__ bool mbar_wait_cluster(uint64_t *b, uint32_t parity,
+                                                      unsigned long long limit_ns = kWaitNs) {
   if (mbar_try_cluster(b, parity)) return true;
   const unsigned long long t0 = now_ns();
   while (!mbar_try_cluster(b, parity))
-    if (now_ns() - t0 > kWaitNs) return false;
+    if (now_ns() - t0 > limit_ns) return false;
   return true;
 }
 // A 2-D tile of a tensor map into this CTA's shared memory whose completion is counted on a

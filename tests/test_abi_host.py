@@ -195,6 +195,18 @@ def test_lmhead_host_validation(lib):
     assert need > sv.spec_workspace_bytes(4, 3, 1024, sv.SPEC_BF16)
 
 
+def test_selftest_bounded_wait_host_validation(lib):
+    """The bounded-wait self-check rejects a NULL or misaligned status and a limit outside
+    1e-6 .. 10 s on the host, before any CUDA call."""
+    import speculative_decoding_verification_78_gb300 as sv
+    vp = ctypes.c_void_p
+    f = lib.spec_selftest_bounded_wait
+    assert f(None, 0.01, None) == sv.SPEC_ERR_NULL
+    assert f(vp(FAKE + 2), 0.01, None) == sv.SPEC_ERR_ALIGN
+    for bad in (0.0, -1.0, 1e-7, 10.5, float("nan"), float("inf")):
+        assert f(vp(FAKE), bad, None) == sv.SPEC_ERR_SHAPE, bad
+
+
 def test_helpers_host_validation(lib):
     """spec_sample, spec_topk, spec_tree_mask and spec_verify_chain_static reject bad arguments
     on the host, before anything is enqueued (the fake device addresses are never touched)."""

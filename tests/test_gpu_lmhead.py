@@ -179,3 +179,27 @@ def test_lmhead_after_large_tree_sample_on_one_stream():
         torch.cuda.synchronize()
         assert int(st.item()) == 0 and int(acc[0].item()) >= 0
         assert int(r[2].item()) == 0
+
+
+def test_bounded_waits_give_up_and_report(orc):
+    """The kernel's waits end: waiting (through the GEMM's own wait routines) on barriers nothing
+    arrives on gives up after the limit, writes SPEC_ERR_TIMEOUT, and the kernel returns; the
+    context stays usable (an LM-head call right after succeeds and matches the oracle's logits)."""
+    import time
+    import speculative_decoding_verification_78_gb300 as sv
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    assert sv.spec_selftest_bounded_wait(st, 0.02) == sv.SPEC_OK
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st.item()) == sv.SPEC_ERR_TIMEOUT
+    assert 0.02 <= dt < 5.0, dt      # two waits of 20 ms in the even CTA
+    li = lmhead_grid(seed=9, B=4, gamma=2, V=512, Ht=128, Hd=64)
+    tok = np.random.default_rng(9).integers(0, 512, (4, 2)).astype(np.int32)
+    acc, out, st2, lt, ld = _run(li.hidden_t, li.head_t, li.hidden_d, li.head_d, tok,
+                                 li.uniforms, 1.0)
+    assert st2 == 0
+    np.testing.assert_array_equal(lt, orc.lm_head_logits(li.hidden_t, li.head_t)[0])
+    np.testing.assert_array_equal(ld, orc.lm_head_logits(li.hidden_d, li.head_d)[0])
+
