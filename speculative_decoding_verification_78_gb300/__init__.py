@@ -1,8 +1,10 @@
 """GB300 (sm_103a) speculative-decoding verify step.
 
 The C library libspec_verify.so (csrc/, declared in include/spec_verify.h) holds the kernels:
-batched chain verification by rejection sampling, greedy tree verification and a temperature
-softmax helper. This package is its thin Python binding; see _binding.py.
+batched chain verification by rejection sampling, greedy and stochastic tree verification, the
+temperature softmax, the drafter-side sampler and top-k, the tree-attention mask, and chain
+verification fused with its LM-head GEMMs on the tensor cores. This package is its thin Python
+binding (argument marshalling only); see _binding.py.
 """
 
 from ._binding import (  # noqa: F401

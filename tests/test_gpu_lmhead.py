@@ -56,11 +56,10 @@ def _oracle_case(orc, li, seed):
     return ci, lt, ld
 
 
-# B, gamma, V, Ht, Hd, T: ragged row tiles on both GEMMs and a K ring that wraps (640 / 128 = 5
-# blocks over 3 stages); one 256-column tile per row (the warp-level finisher) and hidden sizes
-# of half a K block (64: the TMA zero-fills the second box); a drafter wider than the target
-# whose hidden size ends in half a block (320 = 2.5 blocks); row tiles that end exactly on a tile
-# boundary; gamma at its largest; the largest vocabulary
+# B, gamma, V, Ht, Hd, T: ragged row tiles on both GEMMs and a K ring that wraps (640 / 64 = 10
+# blocks over 4 stages); one 256-column half per row (the warp-level finisher) and a one-block K;
+# a drafter wider than the target and a last column tile with one half (V / 256 = 9); row tiles
+# that end exactly on a tile boundary; gamma at its largest; the largest vocabulary
 SHAPES = [(30, 5, 4096, 640, 256, 1.0), (1, 1, 256, 64, 64, 0.7), (9, 8, 2304, 128, 320, 1.3),
           (128, 3, 1024, 256, 128, 1.0), (4, 32, 512, 64, 128, 1.0),
           (2, 2, 1 << 19, 64, 64, 0.3)]   # the largest vocabulary the call accepts, low T
