@@ -245,6 +245,10 @@ int chain_args_check(const void *target_logits, const void *draft_logits, int dt
   return SPEC_OK;
 }
 
+// The bounded-wait self-check kernel's launcher (spec_lmhead.cu, beside the kernel whose waits it
+// exercises): one cluster of two CTAs.
+cudaError_t launch_wait_selftest(int32_t *status, unsigned long long limit_ns,
+                                 cudaStream_t stream);
 }  // namespace specv
 
 extern "C" {

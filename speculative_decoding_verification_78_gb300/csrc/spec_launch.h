@@ -70,9 +70,6 @@ cudaError_t launch_tree(int dtype, const Params &p, int grid, const FinishPlan &
 cudaError_t launch_lmhead(const Params &p, const void *hidden_t, const void *head_t, int Kt,
                           const void *hidden_d, const void *head_d, int Kd, void *logits_t,
                           void *logits_d, const FinishPlan &f, cudaStream_t stream);
-// The bounded-wait self-check (spec_selftest_bounded_wait): one cluster of two CTAs.
-cudaError_t launch_wait_selftest(int32_t *status, unsigned long long limit_ns,
-                                 cudaStream_t stream);
 // Stochastic tree verification: the stream kernel over every target and draft row, then one
 // finishing CTA per tree with `smem` bytes of dynamic shared memory.
 cudaError_t launch_tree_sample(int dtype, const Params &p, int grid, size_t smem,
