@@ -359,6 +359,16 @@ __device__ __forceinline__ void tsc_stage(const E *P, const E *Q, int V, int k_l
   }
 }
 
+// Asks L2 for this CTA's slice [k_lo, k_lo + n) of one row, one 128-byte line per thread and
+// step (a hint: nothing waits for it), so that a later tsc_stage of the row finds it there.
+template <typename E>
+__device__ __forceinline__ void tsc_prefetch(const E *row, int V, int k_lo, int n) {
+  constexpr int kLine = 128 / static_cast<int>(sizeof(E));
+  const int hi = min(V, k_lo + n);
+  for (int k = k_lo + static_cast<int>(threadIdx.x) * kLine; k < hi; k += kThreads * kLine)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + k));
+}
+
 // This CTA's slice total of the pass's weight (the update max(0, r - q), or r itself), in a fixed
 // order: a lane's 8 elements, the warp's segments (segment j of the slice: warp j % kWarps),
 // then the warps in order. With `segsum`, each segment's sum is stored too.
@@ -433,8 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample_cluster(Params
   __shared__ TsShared sh;
   __shared__ TsClusterShared cs;
   cluster_started_arrive();   // the first push waits for it before touching peers
-  wait_stream_kernel();
   const int b = blockIdx.x / S;
+  // the root's rows are inputs (the stream kernel only reads them): ask L2 for this CTA's slices
+  // while the stream kernel drains
+  if (b < p.B) {
+    tsc_prefetch<E>(row_ptr<E>(p, b, 0), V, k_lo, nsl * kSeg);
+    tsc_prefetch<E>(row_ptr<E>(p, b, N), V, k_lo, nsl * kSeg);
+  }
+  wait_stream_kernel();
   if (!SPEC_CHECK(p, b < p.B)) return;   // the same on every CTA of the cluster
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long bN = static_cast<long long>(b) * N;
@@ -503,6 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample_cluster(Params
       }
     }
     __syncthreads();
+    // the walk moves to one of these children (or stops here): ask L2 for their slices now, so
+    // that the next node's staging finds them there
     tsc_stage<E>(P, Q, V, k_lo, nsl * (kSeg / 8), sh.Mt, sh.iZt, sh.Md, sh.iZd, c2, ps, qs);
     const int nc = sh.nchild;
     for (int i = tid; i < nc; i += kThreads) {
