@@ -519,11 +519,26 @@ __global__ void __launch_bounds__(kThreads, 1) finish_tree_sample_cluster(Params
       }
     }
     __syncthreads();
-    // the walk moves to one of these children (or stops here): ask L2 for their slices now, so
-    // that the next node's staging finds them there
-    tsc_stage<E>(P, Q, V, k_lo, nsl * (kSeg / 8), sh.Mt, sh.iZt, sh.Md, sh.iZd, c2, ps, qs);
+    // the children's token logits: the first kThreads into registers before the slice is staged,
+    // so that their loads overlap the staging's, stored once it is done
     const int nc = sh.nchild;
-    for (int i = tid; i < nc; i += kThreads) {
+    float lt0 = 0.f, ld0 = 0.f;
+    bool have0 = false;
+    if (tid < nc) {
+      const int c = ch[tid];
+      const int x = SPEC_CHECK(p, c > cur && c < N) ? tok[c] : 0;
+      if (SPEC_CHECK(p, x >= 0 && x < V && tid < SPEC_MAX_NODES)) {
+        lt0 = ld_elem<E>(P + x);
+        ld0 = ld_elem<E>(Q + x);
+        have0 = true;
+      }
+    }
+    tsc_stage<E>(P, Q, V, k_lo, nsl * (kSeg / 8), sh.Mt, sh.iZt, sh.Md, sh.iZd, c2, ps, qs);
+    if (have0) {
+      sh.lt[tid] = lt0;
+      sh.ld[tid] = ld0;
+    }
+    for (int i = tid + kThreads; i < nc; i += kThreads) {
       const int c = ch[i];
       const int x = SPEC_CHECK(p, c > cur && c < N) ? tok[c] : 0;
       if (!SPEC_CHECK(p, x >= 0 && x < V && i < SPEC_MAX_NODES)) continue;
