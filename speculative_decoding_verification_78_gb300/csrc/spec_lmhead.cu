@@ -105,7 +105,10 @@ __device__ __forceinline__ int lm_sched(const LmArgs &a, int c, int NC, int i) {
   if (i < nT) return c + i * NC;
   i -= nT;
   const int light = NC - h;
-  const int p1 = h > 0 ? min(D, light * a.even) : 0;   // drafter tiles of the first round
+  // drafter tiles of the first round (the product in 64 bits: even can be large)
+  const int p1 = h > 0 ? static_cast<int>(min(static_cast<long long>(D),
+                                              static_cast<long long>(light) * a.even))
+                       : 0;
   if (h > 0 && c >= h) {
     const int first = c - h;   // this cluster's first tile of that round
     const int n1 = p1 > first ? (p1 - first + light - 1) / light : 0;
