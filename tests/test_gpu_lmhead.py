@@ -59,10 +59,13 @@ def _oracle_case(orc, li, seed):
 # B, gamma, V, Ht, Hd, T: ragged row tiles on both GEMMs and a K ring that wraps (640 / 64 = 10
 # blocks over 4 stages); one 256-column half per row (the warp-level finisher) and a one-block K;
 # a drafter wider than the target and a last column tile with one half (V / 256 = 9); row tiles
-# that end exactly on a tile boundary; gamma at its largest; the largest vocabulary
+# that end exactly on a tile boundary; gamma at its largest; the largest vocabulary; more tiles
+# than clusters with a drafter 16 times narrower (48 target and 32 drafter tiles: the clusters
+# one target tile short take every drafter tile, some of them two)
 SHAPES = [(30, 5, 4096, 640, 256, 1.0), (1, 1, 256, 64, 64, 0.7), (9, 8, 2304, 128, 320, 1.3),
           (128, 3, 1024, 256, 128, 1.0), (4, 32, 512, 64, 128, 1.0),
-          (2, 2, 1 << 19, 64, 64, 0.3)]   # the largest vocabulary the call accepts, low T
+          (2, 2, 1 << 19, 64, 64, 0.3),   # the largest vocabulary the call accepts, low T
+          (128, 4, 8192, 1024, 64, 1.0)]
 
 
 @pytest.mark.parametrize("B,gamma,V,Ht,Hd,T", SHAPES)
