@@ -65,7 +65,8 @@ def _oracle_case(orc, li, seed):
 SHAPES = [(30, 5, 4096, 640, 256, 1.0), (1, 1, 256, 64, 64, 0.7), (9, 8, 2304, 128, 320, 1.3),
           (128, 3, 1024, 256, 128, 1.0), (4, 32, 512, 64, 128, 1.0),
           (2, 2, 1 << 19, 64, 64, 0.3),   # the largest vocabulary the call accepts, low T
-          (128, 4, 8192, 1024, 64, 1.0)]
+          (128, 4, 8192, 1024, 64, 1.0),
+          (8, 3, 1024, 128, 64, 0.01), (8, 3, 1024, 128, 64, 100.0)]   # extreme temperatures
 
 
 @pytest.mark.parametrize("B,gamma,V,Ht,Hd,T", SHAPES)
