@@ -497,3 +497,36 @@ def test_chain_invalid_rows_and_repeats(orc):
         again = run_chain(ci)
         np.testing.assert_array_equal(again[0], first[0])
         np.testing.assert_array_equal(again[1], first[1])
+
+
+def test_concurrent_calls_on_separate_streams(orc):
+    """Two chain calls and a greedy-tree call in flight at once on three streams, each with its
+    own workspace and outputs, launched back to back three times over: every result equals the
+    oracle's (no state is shared between calls beyond cached device attributes)."""
+    import speculative_decoding_verification_78_gb300 as sv
+    a = chain_32k(seed=61, B=48, gamma=5, V=32000)
+    c = chain_tiny(seed=62, B=400, gamma=4)
+    t = tree_32k(seed=63, B=16, N=64, V=32000)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    ins_a = (dev(a.target), dev(a.draft), dev(a.tokens), dev(a.uniforms))
+    ins_c = (dev(c.target), dev(c.draft), dev(c.tokens), dev(c.uniforms))
+    ins_t = (dev(t.target), dev(t.parents), dev(t.tokens))
+    torch.cuda.synchronize()
+    results = []
+    for _ in range(3):
+        with torch.cuda.stream(streams[0]):
+            ra = sv.verify_chain(*ins_a, a.temperature, stream=streams[0])
+        with torch.cuda.stream(streams[1]):
+            rc = sv.verify_chain(*ins_c, c.temperature, stream=streams[1])
+        with torch.cuda.stream(streams[2]):
+            rt = sv.verify_tree(*ins_t, stream=streams[2])
+        results.append((ra, rc, rt))
+    torch.cuda.synchronize()
+    oa = orc.verify_tree(t.target, BF16, t.parents, t.tokens)
+    for ra, rc, rt in results:
+        for ci, r in ((a, ra), (c, rc)):
+            assert int(r[2].item()) == 0
+            compare_chain(orc, ci, (r[0].cpu().numpy(), r[1].cpu().numpy(), 0))
+        assert int(rt[3].item()) == 0 and oa[3] == 0
+        for got, want in zip(rt[:3], oa[:3]):
+            np.testing.assert_array_equal(got.cpu().numpy(), want)
